@@ -1,0 +1,338 @@
+/*
+ * oracle.c -- TEST INFRASTRUCTURE, NOT PRODUCT CODE.
+ *
+ * A plain, slow, fp64 CPU oracle for causal linear attention and its chunkwise,
+ * normalised, feature-mapped and log-linear variants.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg load it.  It includes nothing from
+ * the CUDA library and the CUDA library never links, loads or calls it.
+ *
+ * Every routine is single-threaded, loops in the order its source describes, and
+ * accumulates in double.  Callers pass float64 arrays holding the stored input
+ * values exactly (bf16 and fp32 values are doubles), row-major, one (b,h) head:
+ *   q, k : [L, d_in]   v : [L, dv]   feature-mapped rows : [L, D]
+ *
+ * Sources (page title, then section / equation / listing):
+ *   [chunked]   "attention と線形の間" (sharin-2a1.pages.dev, parts/chunked.html):
+ *               section 1 (ScoresFirst / StateFirst, the state-size table),
+ *               section 2 (Chunked, CausalScoresFirst, CausalStateFirst, tril),
+ *               section 3 (the Shape cost model and its two tables).
+ *   [perf]      "Linear Attention / Performerの理論と実装" (disassemble-channel.com):
+ *               ELU feature map, FAVOR+ positive random features, the normalised
+ *               output equation, "再帰的な状態更新" (S_t, z_t recurrence).
+ *   [loglinear] "論文紹介：Log Linear Attention" (docswell slides): Fenwick tree
+ *               partition (slides 15-16, 20-21), level weights (slide 17), decoding
+ *               update rule (slide 22).
+ *
+ * Parity status: every routine here is pinned by CPU tests against printed values,
+ * closed forms, library routines or brute force (tests/test_oracle_*.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* feature maps phi                                                           */
+/* ------------------------------------------------------------------------- */
+
+/* Identity: phi(x) = x (plain linear attention, [chunked] section 1). */
+void orc_phi_identity(const double *x, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = x[i];
+}
+
+/* [perf] ELU feature map: phi(x) = elu(x) + 1, i.e. x + 1 where x >= 0, e^x below. */
+void orc_phi_elu1(const double *x, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = (x[i] >= 0.0) ? x[i] + 1.0 : exp(x[i]);
+}
+
+/* [perf] FAVOR+ positive random features.  The inputs are first scaled by d^{-1/4}
+ * (the Performer implementation scales both q and k), then
+ *     phi(x) = exp(omega x - |x|^2 / 2) / sqrt(m),  omega: [m, d] (rows omega_l).
+ * rows x: [rows, d] -> out: [rows, m]. */
+void orc_phi_favor(const double *x, long rows, int d, const double *omega, int m, double *out)
+{
+    const double s = pow((double)d, -0.25);
+    double *xs = (double *)malloc(sizeof(double) * (size_t)d);
+    for (long r = 0; r < rows; ++r) {
+        double nrm2 = 0.0;
+        for (int j = 0; j < d; ++j) {
+            xs[j] = x[r * d + j] * s;
+            nrm2 += xs[j] * xs[j];
+        }
+        for (int l = 0; l < m; ++l) {
+            double p = 0.0;
+            for (int j = 0; j < d; ++j) p += omega[(long)l * d + j] * xs[j];
+            out[r * m + l] = exp(p - 0.5 * nrm2) / sqrt((double)m);
+        }
+    }
+    free(xs);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Fenwick level of a (query t, key s) pair                                   */
+/* ------------------------------------------------------------------------- */
+
+/* [loglinear] slides 16 and 20-21: for query t the past splits into buckets of sizes
+ * 1, 1, 2, 4, ...; level 0 is t itself and level l >= 1 holds the keys s < t whose
+ * highest bit differing from t is bit l-1.  So level = 0 if s == t, else
+ * 1 + floor(log2(t XOR s)).  Worked case t = 7: {7}, {6}, {4,5}, {0,1,2,3}. */
+int orc_fenwick_level(long t, long s)
+{
+    if (s == t) return 0;
+    uint64_t x = (uint64_t)(t ^ s);
+    int lg = 0;
+    while (x >>= 1) ++lg;
+    return 1 + lg;
+}
+
+static double dot(const double *a, const double *b, int n)
+{
+    double acc = 0.0;
+    for (int i = 0; i < n; ++i) acc += a[i] * b[i];
+    return acc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Definition, scores first                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* The plain definition, one output row at a time:
+ *   num_t = sum_{s<=t} M[t,s] (phi(q_t) . phi(k_s)) v_s
+ *   den_t = sum_{s<=t} M[t,s] (phi(q_t) . phi(k_s))
+ *   out_t = normalize ? num_t / den_t : num_t
+ * with M[t,s] = 1, or lam[t, level(t,s)] when lam is given (log-linear mask).
+ * [chunked] CausalScoresFirst and tril (the diagonal is kept: s <= t);
+ * [perf] normalised output equation y_t (sums over j = 1..t);
+ * [loglinear] slide 17 (M built from per-level weights lambda_t^(l)).
+ * causal = 0 gives the non-causal ScoresFirst order ([chunked] section 1), s over all L.
+ * rows: the output rows to compute (NULL = all L, in order); out: [nrows, dv].
+ * Returns 0, or -1 when a needed level is >= nl. */
+int orc_scores_first(const double *fq, const double *fk, const double *v, long L, int D, int dv,
+                     int causal, int normalize, const double *lam, int nl,
+                     const long *rows, long nrows, double *out)
+{
+    double *num = (double *)malloc(sizeof(double) * (size_t)dv);
+    long n = rows ? nrows : L;
+    for (long r = 0; r < n; ++r) {
+        long t = rows ? rows[r] : r;
+        long smax = causal ? t : L - 1;
+        double den = 0.0;
+        for (int j = 0; j < dv; ++j) num[j] = 0.0;
+        for (long s = 0; s <= smax; ++s) {
+            double a = dot(fq + t * D, fk + s * D, D);
+            if (lam) {
+                int l = orc_fenwick_level(t, s);
+                if (l >= nl) { free(num); return -1; }
+                a *= lam[t * nl + l];
+            }
+            for (int j = 0; j < dv; ++j) num[j] += a * v[s * dv + j];
+            den += a;
+        }
+        for (int j = 0; j < dv; ++j) out[r * dv + j] = normalize ? num[j] / den : num[j];
+    }
+    free(num);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Non-causal state first                                                      */
+/* ------------------------------------------------------------------------- */
+
+/* [chunked] section 1, StateFirst: out = phi(Q) (phi(K)^T V); the state phi(K)^T V is
+ * D x dv whatever L is.  With normalize, [perf]'s non-causal normalised form
+ * out_i = phi(q_i)^T S / phi(q_i)^T z with z = sum_j phi(k_j).
+ * S_out (D x dv) and z_out (D) receive the state if non-NULL. */
+void orc_state_first(const double *fq, const double *fk, const double *v, long L, int D, int dv,
+                     int normalize, double *out, double *S_out, double *z_out)
+{
+    double *S = (double *)calloc((size_t)D * dv, sizeof(double));
+    double *z = (double *)calloc((size_t)D, sizeof(double));
+    for (long s = 0; s < L; ++s)
+        for (int i = 0; i < D; ++i) {
+            z[i] += fk[s * D + i];
+            for (int j = 0; j < dv; ++j) S[i * dv + j] += fk[s * D + i] * v[s * dv + j];
+        }
+    for (long t = 0; t < L; ++t) {
+        double den = dot(fq + t * D, z, D);
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < D; ++i) acc += fq[t * D + i] * S[i * dv + j];
+            out[t * dv + j] = normalize ? acc / den : acc;
+        }
+    }
+    if (S_out) memcpy(S_out, S, sizeof(double) * (size_t)D * dv);
+    if (z_out) memcpy(z_out, z, sizeof(double) * (size_t)D);
+    free(S);
+    free(z);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Causal state recurrence (chunk size 1)                                      */
+/* ------------------------------------------------------------------------- */
+
+/* [chunked] CausalStateFirst and [perf] "再帰的な状態更新":
+ *   S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ *   out_t = phi(q_t)^T S_t  (/ phi(q_t)^T z_t when normalize).
+ * S0 (D x dv) / z0 (D): optional starting state (NULL = zero); S_out / z_out: optional
+ * final state S_L, z_L. */
+void orc_state_recurrence(const double *fq, const double *fk, const double *v, long L, int D,
+                          int dv, int normalize, const double *S0, const double *z0,
+                          double *out, double *S_out, double *z_out)
+{
+    double *S = (double *)calloc((size_t)D * dv, sizeof(double));
+    double *z = (double *)calloc((size_t)D, sizeof(double));
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)D * dv);
+    if (z0) memcpy(z, z0, sizeof(double) * (size_t)D);
+    for (long t = 0; t < L; ++t) {
+        const double *kt = fk + t * D, *vt = v + t * dv, *qt = fq + t * D;
+        for (int i = 0; i < D; ++i) {
+            z[i] += kt[i];
+            for (int j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * vt[j];
+        }
+        double den = dot(qt, z, D);
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < D; ++i) acc += qt[i] * S[i * dv + j];
+            out[t * dv + j] = normalize ? acc / den : acc;
+        }
+    }
+    if (S_out) memcpy(S_out, S, sizeof(double) * (size_t)D * dv);
+    if (z_out) memcpy(z_out, z, sizeof(double) * (size_t)D);
+    free(S);
+    free(z);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chunked form (self-check of the chunk-size invariant only)                  */
+/* ------------------------------------------------------------------------- */
+
+/* [chunked] section 2, Chunked(q, k, v, c): chunk size c <= 0 becomes 1; the sequence
+ * is cut into chunks of c rows (the last may be shorter).  Per chunk, the part of the
+ * past before the chunk is read from the carried state (inter = q_c . state), the part
+ * inside the chunk from the causally masked scores (tril(q_c k_c^T) v_c), the two are
+ * added, and then the state takes the chunk's k_c^T v_c.  The normaliser rides along
+ * the same way (z carried, masked score row sums inside the chunk).
+ * unmasked_intra = 1 plants the mistake the page reports making first (no mask inside
+ * the chunk); it exists only so a test can show that the checks catch it. */
+void orc_chunked(const double *fq, const double *fk, const double *v, long L, int D, int dv,
+                 long C, int normalize, int unmasked_intra, double *out)
+{
+    if (C <= 0) C = 1;
+    double *S = (double *)calloc((size_t)D * dv, sizeof(double));
+    double *z = (double *)calloc((size_t)D, sizeof(double));
+    double *num = (double *)malloc(sizeof(double) * (size_t)dv);
+    for (long start = 0; start < L; start += C) {
+        long end = start + C < L ? start + C : L;
+        for (long t = start; t < end; ++t) {
+            const double *qt = fq + t * D;
+            /* inter: from the carried state */
+            double den = dot(qt, z, D);
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < D; ++i) acc += qt[i] * S[i * dv + j];
+                num[j] = acc;
+            }
+            /* intra: masked scores inside the chunk */
+            for (long s = start; s < end; ++s) {
+                if (s > t && !unmasked_intra) continue;
+                double a = dot(qt, fk + s * D, D);
+                for (int j = 0; j < dv; ++j) num[j] += a * v[s * dv + j];
+                den += a;
+            }
+            for (int j = 0; j < dv; ++j) out[t * dv + j] = normalize ? num[j] / den : num[j];
+        }
+        /* carry the chunk into the state */
+        for (long s = start; s < end; ++s)
+            for (int i = 0; i < D; ++i) {
+                z[i] += fk[s * D + i];
+                for (int j = 0; j < dv; ++j) S[i * dv + j] += fk[s * D + i] * v[s * dv + j];
+            }
+    }
+    free(S);
+    free(z);
+    free(num);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Log-linear Fenwick recurrence (chunk size 1)                                 */
+/* ------------------------------------------------------------------------- */
+
+/* [loglinear] slides 18-22, read so that it produces the mask of orc_fenwick_level.
+ * Level states S^(l), l = 1..nl-1, each hold sum phi(k_s) v_s^T over the keys of
+ * bucket l of the current query (z^(l) likewise for the normaliser).  At step t:
+ *   out_t = lam[t,0] (phi(q_t).phi(k_t)) v_t + sum_{l>=1} lam[t,l] phi(q_t)^T S^(l)
+ * then, with r = number of trailing zero bits of t+1 (slide 22's lssb):
+ *   level 0 takes the current token, levels 1..r are emptied into level r+1,
+ *   S^(r+1) = phi(k_t) v_t^T + sum_{l=1..r} S^(l),  S^(1..r) = 0,
+ *   higher levels are kept as they are.
+ * Returns 0, or -1 if a level >= nl would be needed before the end of the sequence. */
+int orc_loglinear_recurrence(const double *fq, const double *fk, const double *v, long L, int D,
+                             int dv, const double *lam, int nl, int normalize, double *out)
+{
+    size_t sz = (size_t)D * dv;
+    double *S = (double *)calloc(sz * (size_t)nl, sizeof(double));
+    double *z = (double *)calloc((size_t)D * nl, sizeof(double));
+    double *num = (double *)malloc(sizeof(double) * (size_t)dv);
+    int rc = 0;
+    for (long t = 0; t < L; ++t) {
+        const double *qt = fq + t * D, *kt = fk + t * D, *vt = v + t * dv;
+        const double *lt = lam + t * nl;
+        double a0 = lt[0] * dot(qt, kt, D);
+        double den = a0;
+        for (int j = 0; j < dv; ++j) num[j] = a0 * vt[j];
+        for (int l = 1; l < nl; ++l) {
+            const double *Sl = S + sz * l;
+            den += lt[l] * dot(qt, z + (size_t)D * l, D);
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < D; ++i) acc += qt[i] * Sl[i * dv + j];
+                num[j] += lt[l] * acc;
+            }
+        }
+        for (int j = 0; j < dv; ++j) out[t * dv + j] = normalize ? num[j] / den : num[j];
+        if (t + 1 == L) break;
+        int r = 0;
+        while ((((uint64_t)(t + 1)) >> r & 1u) == 0) ++r;
+        if (r + 1 >= nl) { rc = -1; break; }
+        double *Sn = S + sz * (r + 1), *zn = z + (size_t)D * (r + 1);
+        for (int i = 0; i < D; ++i) {
+            zn[i] = kt[i];
+            for (int j = 0; j < dv; ++j) Sn[i * dv + j] = kt[i] * vt[j];
+        }
+        for (int l = 1; l <= r; ++l) {
+            double *Sl = S + sz * l, *zl = z + (size_t)D * l;
+            for (size_t e = 0; e < sz; ++e) { Sn[e] += Sl[e]; Sl[e] = 0.0; }
+            for (int i = 0; i < D; ++i) { zn[i] += zl[i]; zl[i] = 0.0; }
+        }
+    }
+    free(S);
+    free(z);
+    free(num);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Cost model                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* [chunked] section 3, Shape{L, D, C}: multiply-add counts.
+ *   state: writing and reading the d x d state, C d^2 each per chunk, L/C chunks
+ *          -> 2 L d^2, independent of C;
+ *   score: making the scores and mixing the values, C^2 d each per chunk
+ *          -> 2 L C d, proportional to C;
+ *   intra memory: the C x C score block. */
+long long orc_state_flops(long long L, long long D, long long C) { (void)C; return 2 * L * D * D; }
+long long orc_score_flops(long long L, long long D, long long C) { return 2 * L * C * D; }
+long long orc_total_flops(long long L, long long D, long long C)
+{
+    return orc_state_flops(L, D, C) + orc_score_flops(L, D, C);
+}
+long long orc_intra_memory(long long C) { return C * C; }
+int orc_is_full_attention(long long L, long long C) { return C >= L; }
+int orc_is_linear(long long C) { return C == 1; }
+
+/* [chunked] section 1 table: the d x d state against a KV cache holding k and v rows. */
+long long orc_state_elems(long long L, long long d) { (void)L; return d * d; }
+long long orc_kv_cache_elems(long long L, long long d) { return 2 * L * d; }
