@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunkwise causal linear attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--C C]
+                    [--impl ours|reference] [--path auto|simt|tc]
+
+One step = one la_chunked_fwd call over the whole workload (feature map, chunk states,
+chunk scan, intra/inter outputs, normaliser, store).  Default workload: elu+1 features
+with the normaliser, B=8 H=16 L=8192 d_k=d_v=128, bf16, C=64 (the L=8192, d=128 case the
+throughput target is stated on).  Prints one JSON line on rank 0.
+
+Multi-GPU (torchrun): (b, h) heads are independent problems, so every rank runs its own
+copy of the workload (weak scaling, no collective on the data path); the barrier and the
+max over ranks only frame the timing.
+
+--impl reference times the CPU oracle (chunk-size-1 recurrence, fp64) on the host cores,
+each step a bounded sample of heads of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "tokens/sec (B·H·L/s) chunked causal linear-attn fwd; % of bf16 TC roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="elu1-norm-d128-L8192", choices=list(synth.WORKLOADS))
+    ap.add_argument("--C", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--seed", type=int, default=11)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(name, w, C):
+    return {"workload": name, "B": w["B"], "H": w["H"], "L": w["L"], "dk": w["dk"],
+            "dv": w["dv"], "C": C, "feature_map": w["fm"], "m": w["m"],
+            "normalize": bool(w["normalize"]), "loglinear": bool(w.get("loglinear")),
+            "storage": w["dtype"]}
+
+
+def bytes_per_token(w):
+    es = 2 if w["dtype"] == "bf16" else 4
+    b = es * (2 * w["dk"] + 2 * w["dv"])
+    if w.get("loglinear"):
+        b += 4 * synth.num_levels(w["L"])
+    return b
+
+
+def flops_per_token(w, C):
+    """Chunked-order FLOPs per token: 2x the chunked page's multiply-add counts
+    (state write + read 2 D dv, scores + value mixing C (D + dv)) plus the FAVOR+
+    projection of q and k (2 * 2 dk m)."""
+    D = w["m"] if w["fm"] == "favor" else w["dk"]
+    f = 2 * (2 * D * w["dv"] + C * (D + w["dv"]))
+    if w["fm"] == "favor":
+        f += 2 * 2 * w["dk"] * w["m"]
+    return f
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def cpu_baseline(w, inp_heads, heads_used, threads):
+    """Times the oracle's chunk-size-1 recurrence (Fenwick recurrence for the log-linear
+    mask) on the given heads, one head per host thread."""
+    import oracle
+    q = synth.as_f64(inp_heads["q"], w["dtype"])
+    k = synth.as_f64(inp_heads["k"], w["dtype"])
+    v = synth.as_f64(inp_heads["v"], w["dtype"])
+    lam = None if inp_heads["lam"] is None else inp_heads["lam"].astype(np.float64)
+    om = None if inp_heads["omega"] is None else inp_heads["omega"].astype(np.float64)
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, fm=w["fm"], omega=om, normalize=w["normalize"], lam=lam,
+                   method="recurrence", threads=threads)
+    dt = time.perf_counter() - t0
+    toks = heads_used * w["L"]
+    return toks / dt, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def sample_heads(w, cores):
+    """A bounded sample: about one head per core, at most all heads."""
+    n = w["B"] * w["H"]
+    per_head = w["L"] * flops_per_token(w, 1)
+    want = max(1, min(n, cores, int(4e10 // max(per_head, 1)) or 1))
+    return list(range(want))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = dict(synth.WORKLOADS[args.workload])
+    C = args.C if args.C is not None else w["C"]
+    cores = host_cores()
+    heads = sample_heads(w, cores)
+    inp = synth.make_inputs(w, args.seed, heads=heads)
+    for _ in range(max(0, args.warmup)):
+        cpu_baseline(w, inp, len(heads), cores)
+        break  # one warm-up pass is enough for a CPU loop; the rest would only burn time
+    times = []
+    for _ in range(args.steps):
+        _, dt = cpu_baseline(w, inp, len(heads), cores)
+        times.append(dt)
+    tot = sum(times)
+    value = args.steps * len(heads) * w["L"] / tot
+    sample = f"{len(heads)} of {w['B'] * w['H']} heads x L={w['L']} per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args.workload, w, C),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    from chunkwise_causal_linear_gb300 import build as la_build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not la_build.up_to_date():
+        la_build.build()
+    if dist:
+        dist.barrier()
+
+    w = dict(synth.WORKLOADS[args.workload])
+    C = args.C if args.C is not None else w["C"]
+    B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
+    path = {"auto": la.LA_PATH_AUTO, "simt": la.LA_PATH_SIMT, "tc": la.LA_PATH_TC}[args.path]
+    dtype = la.LA_BF16 if w["dtype"] == "bf16" else la.LA_F32
+    tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+
+    inp = synth.make_inputs(w, args.seed)
+
+    def host_tensor(x, shape):
+        if w["dtype"] == "bf16":
+            t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(x)
+        return t.reshape(shape).pin_memory()
+
+    qh, kh, vh = (host_tensor(inp["q"], (B, H, L, dk)), host_tensor(inp["k"], (B, H, L, dk)),
+                  host_tensor(inp["v"], (B, H, L, dv)))
+    q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
+    out = torch.empty((B, H, L, dv), dtype=tdt, device="cuda")
+    outh = torch.empty((B, H, L, dv), dtype=tdt).pin_memory()
+    omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
+    lam = None if inp["lam"] is None else torch.from_numpy(inp["lam"]).reshape(
+        B, H, L, -1).cuda()
+    nl = 0 if lam is None else lam.shape[-1]
+    fm = la.make_feature_map(w["fm"], w["m"], omega.data_ptr() if omega is not None else 0)
+    wsb = la.la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), nl, dtype)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    rc, plan = la.la_chunked_plan(B, H, L, dk, dv, C, fm, int(w["normalize"]), int(lam is not None),
+                                  nl, dtype, path, 0)
+    if rc != la.LA_OK:
+        raise la.LAError(rc, "la_chunked_plan")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    lam_ptr = lam.data_ptr() if lam is not None else None
+
+    def step():
+        r = la.la_chunked_fwd_path(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
+                                   H, L, dk, dv, C, fm, int(w["normalize"]), lam_ptr, nl, dtype,
+                                   ws.data_ptr(), wsb, sptr, path)
+        if r != la.LA_OK:
+            raise la.LAError(r, "la_chunked_fwd")
+
+    io_bytes = B * H * L * bytes_per_token(w)
+    flush = None
+    if io_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    st = la.la_last_device_status(sptr)
+    if st != la.LA_OK:
+        raise la.LAError(st, "device status after warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    times = [a.elapsed_time(b) for a, b in evs]
+    t_ms = sum(times)
+    st = la.la_last_device_status(sptr)
+    if st != la.LA_OK:
+        raise la.LAError(st, "device status after the timed steps")
+    if dist:
+        tt = torch.tensor([t_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+
+    tokens_per_step = B * H * L
+    value = world * tokens_per_step * args.steps / (t_ms / 1e3)
+    ms_per_step = t_ms / args.steps
+
+    # ---- end to end through the host-buffer entry point (copies inside the region)
+    e2e = None
+    if not args.no_e2e:
+        h2d = int(qh.numel() * qh.element_size() * 2 + vh.numel() * vh.element_size())
+        d2h = int(outh.numel() * outh.element_size())
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            r = la.la_chunked_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(),
+                                       outh.data_ptr(), qd.data_ptr(), kd.data_ptr(),
+                                       vd.data_ptr(), out.data_ptr(), B, H, L, dk, dv, C, fm,
+                                       int(w["normalize"]), lam_ptr, nl, dtype, ws.data_ptr(),
+                                       wsb, sptr)
+            if r != la.LA_OK:
+                raise la.LAError(r, "la_chunked_fwd_host")
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        te = e0.elapsed_time(e1)
+        if dist:
+            tt = torch.tensor([te], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e2e = {"value": world * tokens_per_step * n_e2e / (te / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    kernel_s = (t_ms / args.steps) / 1e3
+    achieved = io_bytes / kernel_s / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            key = f"{args.workload}/C{C}/{plan['path']}"
+            traffic = tr.get(key)
+        except Exception:
+            traffic = None
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": traffic,
+            "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+            "algorithmic_bytes_per_launch": io_bytes,
+            "tensor_tflops": tokens_per_step * flops_per_token(w, C) / kernel_s / 1e12,
+            "tensor_peak_tflops": float(peaks.get("bf16_tflops", 1900.0))}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cores = host_cores()
+        heads = sample_heads(w, cores)
+        sub = {kk: (vv[heads] if kk in ("q", "k", "v", "lam") and vv is not None else vv)
+               for kk, vv in inp.items()}
+        val, dt = cpu_baseline(w, sub, len(heads), cores)
+        cpu = {"value": val, "unit": "tokens/s", "cores": min(cores, len(heads)),
+               "kind": "oracle",
+               "sample": f"{len(heads)} of {B * H} heads x L={L}, chunk-size-1 recurrence in "
+                         f"fp64, {dt:.1f} s wall"}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w["dtype"] == "bf16" else "f32", "data": "synthetic",
+            "config": dict(workload_config(args.workload, w, C),
+                           l2="inputs larger than L2" if flush is None else
+                           "L2 flushed between steps (2x L2 buffer written)",
+                           path={1: "simt", 2: "tc"}.get(plan["path"], plan["path"]),
+                           parallelism=f"heads independent; weak scaling over {world} GPU(s)"),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": plan["n_launches"] * args.steps}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

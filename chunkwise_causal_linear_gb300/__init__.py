@@ -1,0 +1,212 @@
+"""Python binding of liblachunked -- chunkwise-parallel causal linear attention on GB300.
+
+Argument marshalling only: every step of the forward pass runs in the library's CUDA
+kernels.  The functions named ``la_*`` mirror the C ABI in ``include/la_chunked.h`` one to
+one (pointers are passed as integers).  ``chunked_fwd`` is a convenience wrapper taking
+torch tensors; torch provides the device memory and the stream, nothing else.
+
+There is no fallback: if ``liblachunked.so`` is missing or fails to load, every call
+raises.  Build it with ``python -m chunkwise_causal_linear_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblachunked.so")
+
+LA_OK = 0
+LA_ERR_NULL = -1
+LA_ERR_SHAPE = -2
+LA_ERR_UNSUPPORTED = -3
+LA_ERR_WORKSPACE = -4
+LA_ERR_CUDA = -5
+LA_ERR_TIMEOUT = -6
+LA_ERR_DEVICE = -7
+
+LA_FM_IDENTITY, LA_FM_ELU1, LA_FM_FAVOR = 0, 1, 2
+LA_BF16, LA_F32 = 0, 1
+LA_PATH_AUTO, LA_PATH_SIMT, LA_PATH_TC = 0, 1, 2
+
+FEATURE_MAPS = {"identity": LA_FM_IDENTITY, "elu1": LA_FM_ELU1, "favor": LA_FM_FAVOR}
+
+# every function the header declares (checked by the tests against include/la_chunked.h)
+EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
+           "la_chunked_workspace_bytes", "la_chunked_plan", "la_last_device_status",
+           "la_status_string", "la_cost_model", "la_version")
+
+
+class la_feature_map(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("m", ctypes.c_int), ("omega", ctypes.c_void_p)]
+
+
+class la_plan_info(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("chunk", ctypes.c_int), ("n_chunks", ctypes.c_int),
+                ("feature_dim", ctypes.c_int), ("grid_x", ctypes.c_int),
+                ("grid_y", ctypes.c_int), ("block", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("n_launches", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class LAError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {la_status_string(status)} ({status})" if what else
+                         f"{la_status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it is missing: there is no fallback path)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing; build it with "
+                    "`python -m chunkwise_causal_linear_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            i, p, sz, ll = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong
+            fmp = ctypes.POINTER(la_feature_map)
+            common = [i, i, i, i, i, i, fmp, i, p, i, i, p, sz, p]
+            L.la_chunked_fwd.argtypes = [p, p, p, p, *common]
+            L.la_chunked_fwd.restype = i
+            L.la_chunked_fwd_path.argtypes = [p, p, p, p, *common, i]
+            L.la_chunked_fwd_path.restype = i
+            L.la_chunked_fwd_host.argtypes = [p, p, p, p, p, p, p, p, *common]
+            L.la_chunked_fwd_host.restype = i
+            L.la_chunked_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i, i]
+            L.la_chunked_workspace_bytes.restype = sz
+            L.la_chunked_plan.argtypes = [i, i, i, i, i, i, fmp, i, i, i, i, i, i,
+                                          ctypes.POINTER(la_plan_info)]
+            L.la_chunked_plan.restype = i
+            L.la_last_device_status.argtypes = [p]
+            L.la_last_device_status.restype = i
+            L.la_status_string.argtypes = [i]
+            L.la_status_string.restype = ctypes.c_char_p
+            L.la_cost_model.argtypes = [ll, ll, ll, ctypes.POINTER(ll), ctypes.POINTER(ll)]
+            L.la_cost_model.restype = i
+            L.la_version.argtypes = []
+            L.la_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def make_feature_map(kind="identity", m=0, omega_ptr=0) -> la_feature_map:
+    if isinstance(kind, str):
+        kind = FEATURE_MAPS[kind]
+    return la_feature_map(int(kind), int(m), ctypes.c_void_p(int(omega_ptr) or None))
+
+
+def _fm(fm):
+    return None if fm is None else ctypes.byref(fm)
+
+
+# ---- one-to-one wrappers of the C ABI ------------------------------------------------
+def la_chunked_fwd(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, level_weights,
+                   num_levels, dtype, workspace, workspace_bytes, stream) -> int:
+    return lib().la_chunked_fwd(q, k, v, out, B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                level_weights, num_levels, dtype, workspace, workspace_bytes,
+                                stream)
+
+
+def la_chunked_fwd_path(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize,
+                        level_weights, num_levels, dtype, workspace, workspace_bytes, stream,
+                        path) -> int:
+    return lib().la_chunked_fwd_path(q, k, v, out, B, H, L, dk, dv, C, _fm(feature_map),
+                                     normalize, level_weights, num_levels, dtype, workspace,
+                                     workspace_bytes, stream, path)
+
+
+def la_chunked_fwd_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, B, H,
+                        L, dk, dv, C, feature_map, normalize, level_weights, num_levels, dtype,
+                        workspace, workspace_bytes, stream) -> int:
+    return lib().la_chunked_fwd_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev,
+                                     out_dev, B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                     level_weights, num_levels, dtype, workspace,
+                                     workspace_bytes, stream)
+
+
+def la_chunked_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, num_levels,
+                               dtype) -> int:
+    return lib().la_chunked_workspace_bytes(B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                            num_levels, dtype)
+
+
+def la_chunked_plan(B, H, L, dk, dv, C, feature_map, normalize, loglinear, num_levels, dtype,
+                    path=LA_PATH_AUTO, num_sms=0):
+    info = la_plan_info()
+    rc = lib().la_chunked_plan(B, H, L, dk, dv, C, _fm(feature_map), normalize, loglinear,
+                               num_levels, dtype, path, num_sms, ctypes.byref(info))
+    return rc, info.as_dict()
+
+
+def la_last_device_status(stream=0) -> int:
+    return lib().la_last_device_status(stream)
+
+
+def la_status_string(status: int) -> str:
+    return lib().la_status_string(status).decode()
+
+
+def la_cost_model(L, D, C):
+    st, sc = ctypes.c_longlong(), ctypes.c_longlong()
+    rc = lib().la_cost_model(L, D, C, ctypes.byref(st), ctypes.byref(sc))
+    if rc != LA_OK:
+        raise LAError(rc, "la_cost_model")
+    return st.value, sc.value
+
+
+def la_version() -> str:
+    return lib().la_version().decode()
+
+
+# ---- torch-tensor convenience ----------------------------------------------------------
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    if t.dtype == torch.float32:
+        return LA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def chunked_fwd(q, k, v, C=64, feature_map="identity", omega=None, normalize=False,
+                level_weights=None, out=None, workspace=None, stream=None, path=LA_PATH_AUTO):
+    """out[B,H,L,dv] = chunkwise causal linear attention of CUDA tensors q,k [B,H,L,dk],
+    v [B,H,L,dv] (bf16 or fp32, contiguous).  omega: [m, dk] fp32 CUDA tensor for
+    feature_map="favor".  level_weights: [B,H,L,NL] fp32 CUDA tensor for the log-linear
+    mask.  out / workspace are allocated with torch when not given."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, L, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    nl = level_weights.shape[-1] if level_weights is not None else 0
+    need = la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), nl, dtype)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_chunked_fwd_path(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L,
+                             dk, dv, C, fm, int(normalize),
+                             level_weights.data_ptr() if level_weights is not None else None,
+                             nl, dtype, workspace.data_ptr() if need else None,
+                             need, stream, path)
+    if rc != LA_OK:
+        raise LAError(rc, "la_chunked_fwd")
+    return out

@@ -1,0 +1,311 @@
+// api.cu -- the C ABI of liblachunked: argument checks, planning, dispatch.
+//
+// Declarations and the meaning of every argument: include/la_chunked.h.
+#include <limits.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace la {
+
+// kernels in other translation units
+size_t simt_smem_bytes(int D, int dk, int fm);
+int simt_inter_levels(int L, int C);
+size_t simt_workspace_bytes(int B, int H, int L, int D, int dv, int C, bool loglinear);
+int simt_launch(const Problem &p, int n_inter, int log2C);
+bool tc_supported(const Problem &p, int num_sms);
+int tc_plan(const Problem &p, int num_sms, la_plan_info *info);
+int tc_launch(const Problem &p, int num_sms);
+
+int required_levels(int L)
+{
+    if (L <= 1) return 1;
+    return 2 + ilog2(L - 1);
+}
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x)
+{
+    int r = 0;
+    while (x >>= 1) ++r;
+    return r;
+}
+
+// ---- device error word (one per device) -------------------------------------------
+__device__ int g_la_err = 0;
+
+static int *err_ptr()
+{
+    static int *ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_la_err) != cudaSuccess) return nullptr;
+        ptrs[dev] = (int *)p;
+    }
+    return ptrs[dev];
+}
+
+static int device_sms()
+{
+    static int sms[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+static bool trace_enabled()
+{
+    static int t = -1;
+    if (t < 0) {
+        const char *e = getenv("LA_TRACE");
+        t = (e && *e && *e != '0') ? 1 : 0;
+    }
+    return t == 1;
+}
+
+// Shape / argument checks shared by every entry point; fills *p (pointers untouched).
+static int check_problem(int B, int H, int L, int dk, int dv, int C, const la_feature_map *fm,
+                         int normalize, bool loglinear, int num_levels, int dtype, Problem *p)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || dk <= 0 || dv <= 0) return LA_ERR_SHAPE;
+    if ((long long)B * H * L * (dk > dv ? dk : dv) > (long long)INT_MAX * 64) return LA_ERR_SHAPE;
+    if ((long long)B * H > INT_MAX / 2) return LA_ERR_SHAPE;
+    if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_UNSUPPORTED;
+    const int kind = fm ? fm->kind : LA_FM_IDENTITY;
+    if (kind != LA_FM_IDENTITY && kind != LA_FM_ELU1 && kind != LA_FM_FAVOR)
+        return LA_ERR_UNSUPPORTED;
+    int D = dk;
+    if (kind == LA_FM_FAVOR) {
+        if (fm->m <= 0) return LA_ERR_SHAPE;
+        D = fm->m;
+    }
+    if (D > 512 || dk > 512) return LA_ERR_UNSUPPORTED;
+    // chunk size: C <= 0 means 1; C >= L means a single chunk
+    if (C <= 0) C = 1;
+    if (C > L) C = L;
+    const int nch = (L + C - 1) / C;
+    if (loglinear) {
+        if (nch > 1 && !is_pow2(C)) return LA_ERR_UNSUPPORTED;
+        if (num_levels < required_levels(L)) return LA_ERR_SHAPE;
+    }
+    memset(p, 0, sizeof(*p));
+    p->B = B; p->H = H; p->L = L; p->dk = dk; p->dv = dv; p->C = C; p->D = D;
+    p->fm = kind;
+    p->m = (kind == LA_FM_FAVOR) ? fm->m : 0;
+    p->omega = (kind == LA_FM_FAVOR) ? fm->omega : nullptr;
+    p->normalize = normalize ? 1 : 0;
+    p->nl = loglinear ? num_levels : 0;
+    p->dtype = dtype;
+    return LA_OK;
+}
+
+static size_t simt_ws(const Problem &p, bool loglinear)
+{
+    return simt_workspace_bytes(p.B, p.H, p.L, p.D, p.dv, p.C, loglinear);
+}
+
+static int plan_problem(const Problem &p, bool loglinear, int path, int num_sms,
+                        la_plan_info *info)
+{
+    memset(info, 0, sizeof(*info));
+    info->chunk = p.C;
+    info->n_chunks = (p.L + p.C - 1) / p.C;
+    info->feature_dim = p.D;
+    Problem q = p;
+    if (loglinear) q.lam = (const float *)1;  // marks the log-linear mask for the planner
+    if (path == LA_PATH_AUTO) path = tc_supported(q, num_sms) ? LA_PATH_TC : LA_PATH_SIMT;
+    if (path == LA_PATH_TC) {
+        if (!tc_supported(q, num_sms)) return LA_ERR_UNSUPPORTED;
+        int rc = tc_plan(q, num_sms, info);
+        info->path = LA_PATH_TC;
+        return rc;
+    }
+    if (path != LA_PATH_SIMT) return LA_ERR_UNSUPPORTED;
+    info->path = LA_PATH_SIMT;
+    info->grid_x = p.B * p.H;
+    info->grid_y = (p.dv + 31) / 32;
+    info->block = 256;
+    info->smem_bytes = (int)simt_smem_bytes(p.D, p.dk, p.fm);
+    info->n_launches = 1;
+    info->workspace_bytes = simt_ws(p, loglinear);
+    return LA_OK;
+}
+
+static int run(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+               int dk, int dv, int C, const la_feature_map *fm, int normalize,
+               const float *lam, int num_levels, int dtype, void *ws, size_t ws_bytes,
+               void *stream, int path)
+{
+    if (!q || !k || !v || !out) return LA_ERR_NULL;
+    const bool ll = lam != nullptr;
+    Problem p;
+    int rc = check_problem(B, H, L, dk, dv, C, fm, normalize, ll, num_levels, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
+    const int sms = device_sms();
+    if (sms <= 0) return LA_ERR_CUDA;
+    la_plan_info info;
+    rc = plan_problem(p, ll, path, sms, &info);
+    if (rc != LA_OK) return rc;
+    if (info.workspace_bytes > 0 && (!ws || ws_bytes < info.workspace_bytes))
+        return LA_ERR_WORKSPACE;
+    p.q = q; p.k = k; p.v = v; p.out = out;
+    p.lam = lam;
+    p.workspace = ws;
+    p.workspace_bytes = ws_bytes;
+    p.stream = (cudaStream_t)stream;
+    p.err = err_ptr();
+    if (!p.err) return LA_ERR_CUDA;
+    if (trace_enabled())
+        fprintf(stderr,
+                "[la] B=%d H=%d L=%d dk=%d dv=%d C=%d D=%d fm=%d norm=%d ll=%d dtype=%d -> "
+                "path=%d grid=(%d,%d) block=%d smem=%d ws=%zu launches=%d\n",
+                B, H, L, dk, dv, p.C, p.D, p.fm, p.normalize, (int)ll, dtype, info.path,
+                info.grid_x, info.grid_y, info.block, info.smem_bytes, info.workspace_bytes,
+                info.n_launches);
+    if (info.path == LA_PATH_TC) return tc_launch(p, sms);
+    int log2C = ll ? ilog2(p.C) : 0;
+    int n_inter = ll ? simt_inter_levels(p.L, p.C) : 0;
+    return simt_launch(p, n_inter, log2C);
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+int la_chunked_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                   int dk, int dv, int C, const la_feature_map *feature_map, int normalize,
+                   const float *level_weights, int num_levels, int dtype, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    return run(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, level_weights,
+               num_levels, dtype, workspace, workspace_bytes, stream, LA_PATH_AUTO);
+}
+
+int la_chunked_fwd_path(const void *q, const void *k, const void *v, void *out, int B, int H,
+                        int L, int dk, int dv, int C, const la_feature_map *feature_map,
+                        int normalize, const float *level_weights, int num_levels, int dtype,
+                        void *workspace, size_t workspace_bytes, void *stream, int path)
+{
+    return run(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, level_weights,
+               num_levels, dtype, workspace, workspace_bytes, stream, path);
+}
+
+int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                        void *out_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,
+                        int B, int H, int L, int dk, int dv, int C,
+                        const la_feature_map *feature_map, int normalize,
+                        const float *level_weights, int num_levels, int dtype, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    if (!q_host || !k_host || !v_host || !out_host) return LA_ERR_NULL;
+    if (!q_dev || !k_dev || !v_dev || !out_dev) return LA_ERR_NULL;
+    Problem p;
+    int rc = check_problem(B, H, L, dk, dv, C, feature_map, normalize, level_weights != nullptr,
+                           num_levels, dtype, &p);
+    if (rc != LA_OK) return rc;
+    const size_t es = dtype == LA_F32 ? 4 : 2;
+    const size_t nqk = (size_t)B * H * L * dk * es, nv = (size_t)B * H * L * dv * es;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(q_dev, q_host, nqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev, k_host, nqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev, v_host, nv, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return LA_ERR_CUDA;
+    rc = la_chunked_fwd(q_dev, k_dev, v_dev, out_dev, B, H, L, dk, dv, C, feature_map,
+                        normalize, level_weights, num_levels, dtype, workspace, workspace_bytes,
+                        stream);
+    if (rc != LA_OK) return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, nv, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+size_t la_chunked_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                  const la_feature_map *feature_map, int normalize,
+                                  int num_levels, int dtype)
+{
+    Problem p;
+    const bool ll = num_levels > 0;
+    if (check_problem(B, H, L, dk, dv, C, feature_map, normalize, ll, num_levels, dtype, &p) !=
+        LA_OK)
+        return 0;
+    const int sms = device_sms();
+    la_plan_info info;
+    if (plan_problem(p, ll, LA_PATH_AUTO, sms > 0 ? sms : 152, &info) != LA_OK) return 0;
+    // enough for either path, so a caller may force a path with the same buffer
+    size_t a = info.workspace_bytes, b = simt_ws(p, ll);
+    return a > b ? a : b;
+}
+
+int la_chunked_plan(int B, int H, int L, int dk, int dv, int C,
+                    const la_feature_map *feature_map, int normalize, int loglinear,
+                    int num_levels, int dtype, int path, int num_sms, la_plan_info *info)
+{
+    if (!info) return LA_ERR_NULL;
+    Problem p;
+    int rc = check_problem(B, H, L, dk, dv, C, feature_map, normalize, loglinear != 0,
+                           num_levels, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if (num_sms <= 0) num_sms = device_sms();
+    if (num_sms <= 0) return LA_ERR_CUDA;
+    return plan_problem(p, loglinear != 0, path, num_sms, info);
+}
+
+int la_last_device_status(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return LA_ERR_CUDA;
+    int *ep = err_ptr();
+    if (!ep) return LA_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, ep, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (h != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(ep, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return LA_ERR_CUDA;
+    }
+    return h;
+}
+
+const char *la_status_string(int status)
+{
+    switch (status) {
+    case LA_OK: return "ok";
+    case LA_ERR_NULL: return "a required pointer is NULL";
+    case LA_ERR_SHAPE: return "invalid or inconsistent sizes";
+    case LA_ERR_UNSUPPORTED: return "unsupported combination of dtype, sizes, feature map or C";
+    case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LA_ERR_CUDA: return "a CUDA runtime call failed";
+    case LA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case LA_ERR_DEVICE: return "a device-side check failed";
+    default: return "unknown status";
+    }
+}
+
+int la_cost_model(long long L, long long D, long long C, long long *state_macs,
+                  long long *score_macs)
+{
+    if (L < 0 || D < 0 || C < 0) return LA_ERR_SHAPE;
+    // "attention と線形の間", section 3: per chunk, writing and reading the state cost
+    // C D^2 each (L/C chunks -> 2 L D^2); making the scores and mixing the values cost
+    // C^2 D each (-> 2 L C D).
+    if (state_macs) *state_macs = 2 * L * D * D;
+    if (score_macs) *score_macs = 2 * L * C * D;
+    return LA_OK;
+}
+
+const char *la_version(void) { return "0.1.0"; }
+
+}  // extern "C"

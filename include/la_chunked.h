@@ -1,0 +1,188 @@
+/*
+ * la_chunked.h -- C ABI of the chunkwise-parallel causal linear attention forward pass
+ * (GB300, sm_103a).  Library: chunkwise_causal_linear_gb300/liblachunked.so.
+ *
+ * What is computed (per (b, h) head, rows t = 0..L-1, phi applied row-wise):
+ *
+ *     num_t = sum_{s <= t} M[t,s] (phi(q_t) . phi(k_s)) v_s
+ *     den_t = sum_{s <= t} M[t,s] (phi(q_t) . phi(k_s))
+ *     out_t = normalize ? num_t / den_t : num_t
+ *
+ * with M[t,s] = 1 (causal linear attention), or M[t,s] = lambda_t^(l(t,s)),
+ * l = 0 if s == t else 1 + floor(log2(t XOR s)) (Fenwick-level log-linear mask).
+ *
+ * Sources:
+ *   "attention と線形の間" (sharin-2a1.pages.dev, parts/chunked.html), section 2:
+ *       Chunked(q, k, v, c) -- chunks of c rows; inside a chunk the causally masked
+ *       scores (diagonal kept), across chunks a d_k x d_v state carried forward;
+ *       c <= 0 means 1; a partial last chunk is allowed.  Section 3: Shape cost model.
+ *   "Linear Attention / Performerの理論と実装" (disassemble-channel.com): the ELU
+ *       feature map, FAVOR+ positive random features, the normalised output y_t and the
+ *       (S_t, z_t) recurrence.
+ *   "論文紹介：Log Linear Attention" (docswell slides): Fenwick buckets (slides 15-21),
+ *       level weights lambda (slide 17), chunkwise level-0 block plus per-level
+ *       inter-chunk states (slides 34-35).
+ *
+ * Conventions for every entry point:
+ *   - Layout: q, k [B, H, L, dk]; v, out [B, H, L, dv]; contiguous row-major.
+ *   - All tensor pointers are DEVICE pointers unless the name says _host.  The caller
+ *     owns every buffer; the library allocates no device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream) and return after the launches are queued.
+ *   - Host-detectable errors return a negative la_status before anything is launched.
+ *     Errors found on the device (a bounded wait that timed out, an index check) are
+ *     recorded in a device error word that la_last_device_status() reads.
+ *   - Concurrent calls on different streams are safe if they use different workspaces
+ *     (the device error word is shared by all calls).
+ */
+#ifndef LA_CHUNKED_H
+#define LA_CHUNKED_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------- */
+enum la_status {
+    LA_OK = 0,
+    LA_ERR_NULL = -1,        /* a required pointer is NULL                               */
+    LA_ERR_SHAPE = -2,       /* a dimension is <= 0, or sizes overflow                   */
+    LA_ERR_UNSUPPORTED = -3, /* combination not supported (dtype, dims, feature map, C)  */
+    LA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than la_chunked_workspace_bytes */
+    LA_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, copy, attribute)      */
+    LA_ERR_TIMEOUT = -6,     /* device: a bounded wait gave up (read via la_last_device_status) */
+    LA_ERR_DEVICE = -7       /* device: an index or shape check failed inside a kernel    */
+};
+
+/* ---- feature maps phi -------------------------------------------------------------- */
+enum la_fm_kind {
+    LA_FM_IDENTITY = 0, /* phi(x) = x                                                     */
+    LA_FM_ELU1 = 1,     /* phi(x) = elu(x) + 1 = (x >= 0 ? x + 1 : e^x)                   */
+    LA_FM_FAVOR = 2     /* FAVOR+: x^ = x / dk^(1/4); phi(x) = exp(omega x^ - |x^|^2/2)/sqrt(m) */
+};
+
+typedef struct la_feature_map {
+    int kind;            /* enum la_fm_kind                                              */
+    int m;               /* FAVOR+: number of random features (the feature dimension);
+                            other kinds: ignored (the feature dimension is dk)            */
+    const float *omega;  /* FAVOR+: device [m, dk] fp32 row-major random matrix, owned by
+                            the caller and read during the call; other kinds: ignored     */
+} la_feature_map;
+
+/* ---- storage dtypes of q, k, v, out ---------------------------------------------- */
+enum la_dtype {
+    LA_BF16 = 0,  /* bfloat16 storage; arithmetic in fp32 with bf16 tensor-core operands  */
+    LA_F32 = 1    /* fp32 storage; arithmetic in fp32 (exact on small-integer inputs)     */
+};
+
+/* ---- execution paths ---------------------------------------------------------------- */
+enum la_path {
+    LA_PATH_AUTO = 0,    /* the library picks (see la_chunked_plan)                       */
+    LA_PATH_SIMT = 1,    /* generic fp32 CUDA-core path: any C, any supported dims         */
+    LA_PATH_TC = 2       /* tcgen05/TMEM tensor-core single-pass path (subset of shapes)   */
+};
+
+/*
+ * la_chunked_fwd -- the forward pass.
+ *
+ *   q, k          device [B, H, L, dk], dtype `dtype`
+ *   v             device [B, H, L, dv], dtype `dtype`
+ *   out           device [B, H, L, dv], dtype `dtype`; fully overwritten
+ *   C             chunk size: C <= 0 means 1, C >= L means one chunk ("attention and
+ *                 linear order meet at the two ends", chunked page section 2)
+ *   feature_map   NULL means identity
+ *   normalize     0: out = num; 1: out = num / den
+ *   level_weights NULL, or device [B, H, L, num_levels] fp32 lambda_t^(l) (log-linear).
+ *                 num_levels must cover 1 + ceil(log2 L) levels, and with more than one
+ *                 chunk C must be a power of two (chunk edges are then Fenwick edges).
+ *   workspace     device scratch of at least la_chunked_workspace_bytes(...) bytes (may
+ *                 be NULL when that is 0); contents on entry are ignored.
+ *   stream        cudaStream_t as void*.
+ * Returns LA_OK or a negative la_status (nothing launched on error).
+ */
+int la_chunked_fwd(const void *q, const void *k, const void *v, void *out,
+                   int B, int H, int L, int dk, int dv, int C,
+                   const la_feature_map *feature_map, int normalize,
+                   const float *level_weights, int num_levels,
+                   int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* As la_chunked_fwd, with an explicit execution path (enum la_path).  LA_PATH_TC returns
+ * LA_ERR_UNSUPPORTED for shapes the tensor-core path does not cover. */
+int la_chunked_fwd_path(const void *q, const void *k, const void *v, void *out,
+                        int B, int H, int L, int dk, int dv, int C,
+                        const la_feature_map *feature_map, int normalize,
+                        const float *level_weights, int num_levels,
+                        int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                        int path);
+
+/*
+ * la_chunked_fwd_host -- the same forward pass from HOST buffers: copies q, k, v (and
+ * nothing else: omega and level_weights stay device pointers) from host memory into the
+ * caller's device buffers q_dev, k_dev, v_dev, runs la_chunked_fwd on them into out_dev,
+ * copies out_dev back into out_host, all queued on `stream`.  Host buffers should be
+ * pinned (cudaHostAlloc / page-locked) for the copies to be asynchronous; the host
+ * buffers must stay valid until the stream reaches the end of the call.  Sizes and error
+ * behaviour as la_chunked_fwd.
+ */
+int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                        void *out_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,
+                        int B, int H, int L, int dk, int dv, int C,
+                        const la_feature_map *feature_map, int normalize,
+                        const float *level_weights, int num_levels,
+                        int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace la_chunked_fwd needs for this problem on the current device
+ * (0 when none).  Returns 0 also for invalid arguments (la_chunked_fwd reports those). */
+size_t la_chunked_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                  const la_feature_map *feature_map, int normalize,
+                                  int num_levels, int dtype);
+
+/* ---- plan introspection (host only; no device call when num_sms > 0) --------------- */
+typedef struct la_plan_info {
+    int path;              /* enum la_path actually chosen                               */
+    int chunk;             /* effective chunk size after clamping                         */
+    int n_chunks;          /* ceil(L / chunk)                                             */
+    int feature_dim;       /* D: dk, or m for FAVOR+                                      */
+    int grid_x, grid_y;    /* main kernel grid                                            */
+    int block;             /* threads per CTA of the main kernel                          */
+    int smem_bytes;        /* dynamic shared memory per CTA of the main kernel            */
+    int n_launches;        /* kernel launches per call                                    */
+    size_t workspace_bytes;
+} la_plan_info;
+
+/* Fills *info with the plan for the problem as la_chunked_fwd_path(path) would run it.
+ * num_sms: SM count to plan for (0 = query the current device).  Returns LA_OK or the
+ * status la_chunked_fwd_path would return for these arguments (pointers are not
+ * checked). */
+int la_chunked_plan(int B, int H, int L, int dk, int dv, int C,
+                    const la_feature_map *feature_map, int normalize, int loglinear,
+                    int num_levels, int dtype, int path, int num_sms, la_plan_info *info);
+
+/* Waits for `stream`, then returns and clears the device error word: LA_OK, or the
+ * first device-side error (LA_ERR_TIMEOUT, LA_ERR_DEVICE) recorded since the last call,
+ * or LA_ERR_CUDA if the stream itself reports an error. */
+int la_last_device_status(void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *la_status_string(int status);
+
+/*
+ * la_cost_model -- "attention と線形の間", section 3, Shape{L, D, C}: multiply-add counts
+ * of the chunked order.  *state_macs = 2 L D^2 (writing and reading the D x D state, the
+ * same for every C); *score_macs = 2 L C D (making the in-chunk scores and mixing the
+ * values, proportional to C).  Either output pointer may be NULL.  Returns LA_OK, or
+ * LA_ERR_SHAPE for negative sizes.
+ */
+int la_cost_model(long long L, long long D, long long C, long long *state_macs,
+                  long long *score_macs);
+
+/* Library version string, e.g. "0.1.0". */
+const char *la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_CHUNKED_H */

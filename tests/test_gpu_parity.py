@@ -1,0 +1,137 @@
+"""GPU parity: the library (through its C ABI) against the CPU oracle, element by element.
+
+Small cases compare every output; full-size workloads compare sampled heads and rows
+(first and last 2C rows of each sampled head plus random rows), computed by the oracle's
+scores-first definition one row at a time.  The integer case must be bit-exact; bf16
+cases must satisfy max|err| <= 2e-2 max|ref| and ||err||/||ref|| <= 5e-3.
+"""
+import numpy as np
+import pytest
+
+import synth
+from parity_util import (assert_close, oracle_heads, run_gpu, sample_rows, workload)
+
+pytestmark = pytest.mark.gpu
+
+SIMT, TC, AUTO = 1, 2, 0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunkwise_causal_linear_gb300 import build
+    build.build()
+
+
+def tc_supported(w, C):
+    import chunkwise_causal_linear_gb300 as la
+    fm = la.make_feature_map(w["fm"], w["m"], 1 if w["fm"] == "favor" else 0)
+    nl = synth.num_levels(w["L"]) if w.get("loglinear") else 0
+    rc, _ = la.la_chunked_plan(w["B"], w["H"], w["L"], w["dk"], w["dv"], C, fm,
+                               int(w["normalize"]), int(bool(w.get("loglinear"))), nl,
+                               la.LA_BF16 if w["dtype"] == "bf16" else la.LA_F32, TC, 0)
+    return rc == la.LA_OK
+
+
+def paths_for(w, C):
+    return [SIMT] + ([TC] if tc_supported(w, C) else [])
+
+
+# ---------------------------------------------------------------------------
+# exactness case: integers in {-3..3}, fp32, identity, no normaliser
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("C", [1, 4, 16, 64, 0, -5, 3, 7, 100])
+@pytest.mark.parametrize("path", [SIMT, AUTO])
+def test_tiny_integer_case_bit_exact(C, path):
+    w = workload("tiny-int-exact")
+    inp = synth.make_inputs(w, seed=1)
+    out, _ = run_gpu(w, inp, C, path)
+    ref = oracle_heads(w, inp, [0], method="scores_first")
+    assert np.array_equal(out, ref), np.abs(out - ref).max()
+
+
+@pytest.mark.parametrize("L,C", [(50, 16), (50, 7), (1, 1), (1, 64), (129, 64), (64, 65)])
+def test_integer_ragged_bit_exact(L, C):
+    w = workload("tiny-int-exact", B=2, H=3, L=L, dk=8, dv=40)
+    inp = synth.make_inputs(w, seed=2)
+    out, _ = run_gpu(w, inp, C, SIMT)
+    ref = oracle_heads(w, inp, list(range(6)), method="scores_first")
+    assert np.array_equal(out, ref)
+
+
+# ---------------------------------------------------------------------------
+# reduced-size versions of each workload: full outputs against the oracle recurrence
+# ---------------------------------------------------------------------------
+SMALL = [
+    ("identity-d64-L2048", dict(B=1, H=3, L=333), 64),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 16),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 32),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 64),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 128),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 256),
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=600), 64),
+    ("loglinear-d64-L65536", dict(B=1, H=2, L=1000), 64),
+    ("loglinear-d64-L65536", dict(B=1, H=1, L=300), 16),
+    ("loglinear-d64-L65536", dict(B=1, H=1, L=200), 1),
+    ("elu1-norm-d128-L8192", dict(B=1, H=1, L=1, ), 64),
+    ("elu1-norm-d128-L8192", dict(B=1, H=1, L=100, dk=32, dv=48), 64),
+    ("identity-d64-L2048", dict(B=1, H=1, L=200, dk=16, dv=16), 64),
+]
+
+
+@pytest.mark.parametrize("base,over,C", SMALL)
+def test_small_workloads_match_oracle(base, over, C):
+    w = workload(base, **over)
+    inp = synth.make_inputs(w, seed=3)
+    n = w["B"] * w["H"]
+    ref = oracle_heads(w, inp, list(range(n)), method="recurrence")
+    for path in paths_for(w, C):
+        out, _ = run_gpu(w, inp, C, path)
+        assert_close(out, ref, f"{base} {over} C={C} path={path}")
+
+
+def test_loglinear_all_ones_equals_plain():
+    """Slide 17 of the log-linear deck: lambda == 1 gives linear attention."""
+    w = workload("loglinear-d64-L65536", B=1, H=2, L=500)
+    inp = synth.make_inputs(w, seed=4)
+    inp["lam"] = np.ones_like(inp["lam"])
+    out_ll, _ = run_gpu(w, inp, 64, SIMT)
+    wp = dict(w, loglinear=False)
+    inp_p = dict(inp, lam=None)
+    out_p, _ = run_gpu(wp, inp_p, 64, SIMT)
+    assert_close(out_ll, out_p, "lambda=1 vs plain")
+    ref = oracle_heads(wp, inp_p, [0, 1])
+    assert_close(out_ll, ref, "lambda=1 vs oracle")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the configuration the benchmark times (automatic path)
+# ---------------------------------------------------------------------------
+FULL = [("identity-d64-L2048", 64), ("favor-m256-d64-L16384", 64),
+        ("loglinear-d64-L65536", 64)] + [("elu1-norm-d128-L8192", C) for C in
+                                         (16, 32, 64, 128, 256)]
+
+_cache = {}
+
+
+def full_inputs(name):
+    if name not in _cache:
+        _cache.clear()
+        w = workload(name)
+        _cache[name] = (w, synth.make_inputs(w, seed=11))
+    return _cache[name]
+
+
+@pytest.mark.parametrize("name,C", FULL)
+def test_full_size_sampled_rows(name, C):
+    w, inp = full_inputs(name)
+    out, _ = run_gpu(w, inp, C, AUTO)
+    n = w["B"] * w["H"]
+    heads = [0, n - 1]
+    rows = sample_rows(w["L"], C, 48, seed=C)
+    ref = oracle_heads(w, inp, heads, method="scores_first", rows=rows)
+    assert_close(out[heads][:, rows], ref, f"{name} C={C}")
+    # whole-output sanity: finite everywhere
+    assert np.isfinite(out).all()
