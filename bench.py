@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=11)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--B", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     return ap.parse_args()
 
 
@@ -171,11 +173,24 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def sample_heads(w, cores):
-    """A bounded sample: about one head per core, at most all heads."""
+def oracle_flops_per_token(w):
+    """FLOPs per token of the oracle's chunk-size-1 recurrence (state update + read, one
+    state per Fenwick level for the log-linear mask, plus the FAVOR+ projections)."""
+    D = w["m"] if w["fm"] == "favor" else w["dk"]
+    n_states = synth.num_levels(w["L"]) if w.get("loglinear") else 1
+    f = 2 * D * w["dv"] * (1 + n_states)
+    if w["fm"] == "favor":
+        f += 2 * 2 * w["dk"] * w["m"]
+    return f
+
+
+def sample_heads(w, cores, core_seconds=20.0, flops_per_core=2.5e9):
+    """A bounded sample of heads: about `core_seconds` of oracle work on the host cores,
+    at least one head per core when that is cheaper, at most all heads."""
     n = w["B"] * w["H"]
-    per_head = w["L"] * flops_per_token(w, 1)
-    want = max(1, min(n, cores, int(4e10 // max(per_head, 1)) or 1))
+    per_head = w["L"] * oracle_flops_per_token(w) / flops_per_core
+    want = int(core_seconds // max(per_head, 1e-9))
+    want = max(1, min(n, max(want, min(cores, n)) if per_head * cores < core_seconds else want))
     return list(range(want))
 
 
@@ -184,6 +199,10 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = dict(synth.WORKLOADS[args.workload])
+    if args.B:
+        w["B"] = args.B
+    if args.H:
+        w["H"] = args.H
     C = args.C if args.C is not None else w["C"]
     cores = host_cores()
     heads = sample_heads(w, cores)
@@ -231,6 +250,10 @@ def run_ours(args):
         dist.barrier()
 
     w = dict(synth.WORKLOADS[args.workload])
+    if args.B:
+        w["B"] = args.B
+    if args.H:
+        w["H"] = args.H
     C = args.C if args.C is not None else w["C"]
     B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
     path = {"auto": la.LA_PATH_AUTO, "simt": la.LA_PATH_SIMT, "tc": la.LA_PATH_TC}[args.path]
