@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/la_chunked.h"
+#include "la_chunked.h"
 
 namespace la {
 

@@ -4,28 +4,31 @@
 // section 2, Chunked): for chunk c the output is the carried state read by the chunk's
 // queries (inter) plus the causally masked in-chunk scores times the chunk's values
 // (intra); then the chunk's phi(K)^T V joins the state.  The normaliser of "Linear
-// Attention / Performerの理論と実装" (y_t = phi(q_t)^T S_t / phi(q_t)^T z_t) is carried in
-// fp32 beside it.
+// Attention / Performerの理論と実装" (y_t = phi(q_t)^T S_t / phi(q_t)^T z_t) is carried
+// beside it: z_c = sum of phi(k) over the chunks before c, kept in fp32.
 //
 // GB300 mapping (everything stays on chip except q, k, v in and out):
 //   * warp 0       TMA producer: Q_c, K_c, V_c tiles (128-byte swizzled) into a 3-stage ring.
 //   * warp 1       one thread issues every tcgen05.mma; the warp owns the TMEM allocation.
-//   * warps 4-7    feature map phi applied in place in shared memory; fp32 normaliser
-//                  terms: z += colsum(phi(K_c)) and phi(q_t).z for the chunk's rows.
-//   * warps 8-11   scores -> P: read phi(Q_c)phi(K_c)^T from TMEM, causal mask (diagonal
-//                  kept), fp32 row sums for the normaliser, bf16 P into shared memory; and
-//                  after each state update, S^T (fp32 in TMEM) -> bf16 copy in TMEM.
-//   * warps 12-15  output epilogue: O^T from TMEM, normaliser division, bf16, swizzled
-//                  shared-memory tile, TMA store.
+//   * warps 4-11   feature map phi applied in place in shared memory; with the normaliser,
+//                  the fp32 column sums of phi(K_c) update z, and z_c is written (as a bf16
+//                  hi/lo pair) into two extra rows after the chunk's 64 key rows, so the
+//                  scores MMA also returns phi(q_t).z_c in fp32.
+//   * warps 12-15  scores -> P: read the scores row from TMEM, causal mask (diagonal kept),
+//                  fp32 row sum, 1 / (phi(q_t).z_c + row sum) for the normaliser, bf16 P
+//                  into shared memory; after each state update, S^T (fp32 in TMEM) -> its
+//                  bf16 copy in TMEM.
+//   * warps 16-19  output epilogue: O^T from TMEM, normaliser, bf16, swizzled shared-memory
+//                  tile, TMA store.
 // TMEM (512 columns): S^T fp32 [dv lanes x D] | S^T bf16 [dv x D/2] | O^T x2 [dv x C] |
-// scores x2 [C x C].  The state is accumulated in fp32 by the MMA and never leaves TMEM;
-// the inter-chunk product reads its bf16 copy as the A operand straight from TMEM.
+// scores x2 [C x (C + 8)].  The state is accumulated in fp32 by the MMA and never leaves
+// TMEM; the inter-chunk product reads its bf16 copy as the A operand straight from TMEM.
 //
 // MMAs per chunk (bf16 in, fp32 accumulate), D = feature dim, C = chunk:
-//   scores  A_c   = phi(Q_c) phi(K_c)^T         M=C   N=C  K=D
-//   inter   O^T   = bf16(S)^T phi(Q_c)^T        M=dv  N=C  K=D   (A from TMEM)
-//   state   S^T  += V_c^T phi(K_c)              M=dv  N=D  K=C
-//   intra   O^T  += V_c^T P_c^T                 M=dv  N=C  K=C
+//   scores  A_c   = phi(Q_c) [phi(K_c); z_c]^T   M=C   N=C(+8)  K=D
+//   inter   O^T   = bf16(S)^T phi(Q_c)^T         M=dv  N=C      K=D   (A from TMEM)
+//   state   S^T  += V_c^T phi(K_c)               M=dv  N=D      K=C
+//   intra   O^T  += V_c^T P_c^T                  M=dv  N=C      K=C
 //
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA records
 // LA_ERR_TIMEOUT in the device error word, raises a shared abort flag that the other roles
@@ -42,8 +45,10 @@ using namespace ptx;
 
 namespace {
 
-constexpr int TC_THREADS = 512;
+constexpr int TC_THREADS = 640;
+constexpr int TC_FWARPS = 8;  // warps in the feature-map group
 constexpr int TC_STAGES = 3;
+constexpr int TC_DEN = 4;  // ring of per-chunk 1/den vectors
 
 struct TcArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
@@ -53,29 +58,36 @@ struct TcArgs {
     int debug_stall;  // test knob: the feature-map group never signals (forces a timeout)
 };
 
-template <int D, int DV, int C>
+template <int D, int DV, int C, bool NORM>
 struct TcLayout {
+    static constexpr int KROWS = NORM ? C + 8 : C;    // key rows (+ z hi/lo + zero rows)
+    static constexpr int NSC = KROWS;                 // N of the scores MMA
+    static constexpr int K_BLK = KROWS * 128;         // one 64-feature block of the K tile
     static constexpr int Q_BYTES = C * D * 2;
-    static constexpr int K_BYTES = C * D * 2;
+    static constexpr int K_BYTES = (D / 64) * K_BLK;
     static constexpr int V_BYTES = C * DV * 2;
     static constexpr int STAGE_BYTES = Q_BYTES + K_BYTES + V_BYTES;
+    static constexpr int STAGE_TX = Q_BYTES + C * D * 2 + V_BYTES;  // bytes TMA delivers
     static constexpr int P_BYTES = C * C * 2;
     static constexpr int O_BYTES = C * DV * 2;
+    // P and the output tile are single-buffered: MMAs complete in issue order, so the
+    // scores of chunk c+1 finishing implies the intra product of chunk c has read P.
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_P = TC_STAGES * STAGE_BYTES;
-    static constexpr int OFF_O = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_F32 = OFF_O + 2 * O_BYTES;              // float area
-    // floats: den_inter[2][C], den_intra[2][C], rden[C], z[D], zpart[4][D]
-    static constexpr int N_F32 = 2 * C + 2 * C + C + D + 4 * D;
+    static constexpr int OFF_O = OFF_P + P_BYTES;
+    static constexpr int OFF_F32 = OFF_O + O_BYTES;
+    // floats: rden[TC_DEN][C], z[D], zpart[TC_FWARPS][D]
+    static constexpr int N_F32 = TC_DEN * C + D + TC_FWARPS * D;
     static constexpr int OFF_BAR = OFF_F32 + ((N_F32 * 4 + 15) / 16) * 16;
-    static constexpr int N_BAR = 3 * TC_STAGES + 2 * 6 + 2 + 2 * 2;
+    static constexpr int N_BAR = 3 * TC_STAGES + 2 * 5 + 2 * TC_DEN + 3;
     static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
     // TMEM columns
-    static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 256, T_A = 384;
+    static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 192, T_A = 320, A_STRIDE = 80;
     static_assert(D <= 128 && DV == 128, "tensor-core path: D <= 128, dv == 128");
     static_assert(C == 64, "tensor-core path: C == 64");
+    static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
     static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
@@ -91,17 +103,31 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, const
 {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 255) == 0) {
-            if (*ctl.abort) return false;
-            if (globaltimer() - t0 > ctl.timeout_ns) {
-                *ctl.abort = 1;
-                record_error(ctl.err, LA_ERR_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        // sleeps (up to 0.2 ms) until the phase completes; no busy probing
+        if (mbar_try_sleep(bar, parity, 200000u)) return true;
+        if (*ctl.abort) return false;
+        if (globaltimer() - t0 > ctl.timeout_ns) {
+            *ctl.abort = 1;
+            record_error(ctl.err, LA_ERR_TIMEOUT);
+            return false;
         }
     }
+}
+
+// Group wait: only the group's leader polls the mbarrier(s); the others park on the
+// hardware named barrier, which also hands every thread the same decision.  The leader's
+// acquire plus the barrier order the other threads' later reads after the awaited writes.
+__device__ __forceinline__ bool group_wait(bool leader, int bar_id, uint64_t *b1, uint32_t p1,
+                                           uint64_t *b2, uint32_t p2, bool use2, const Ctl &ctl,
+                                           int nthreads = 128)
+{
+    bool ok = true;
+    if (leader) {
+        ok = wait_phase(b1, p1, ctl);
+        if (ok && use2) ok = wait_phase(b2, p2, ctl);
+    }
+    return named_bar_and(bar_id, nthreads, ok);
 }
 
 // bf16 (raw 16-bit) -> fp32 for the two halves of a 32-bit word
@@ -111,36 +137,40 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 template <int FM>
 __device__ __forceinline__ float phi1(float x)
 {
-    if (FM == LA_FM_ELU1) return x >= 0.f ? x + 1.f : __expf(x);
+    if (FM == LA_FM_ELU1) {
+        // e^x = 2^(x log2 e) on the SFU (hardware ex2, flush-to-zero); x >= 0 takes x + 1
+        float e;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+        return x >= 0.f ? x + 1.f : e;
+    }
     return x;
 }
 
 template <int D, int DV, int C, int FM, bool NORM>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_constant__ TcArgs a)
 {
-    using Lay = TcLayout<D, DV, C>;
+    using Lay = TcLayout<D, DV, C, NORM>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base for the 128B-swizzled tiles (offset taken in the shared window)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *f32 = (float *)(sm + Lay::OFF_F32);
-    float *den_inter = f32;              // [2][C]
-    float *den_intra = den_inter + 2 * C;  // [2][C]
-    float *rden = den_intra + 2 * C;     // [C]
-    float *zs = rden + C;                // [D]
-    float *zpart = zs + D;               // [4][D]
+    float *rden = f32;                   // [TC_DEN][C]  1 / den per row of a chunk
+    float *zs = rden + TC_DEN * C;       // [D]
+    float *zpart = zs + D;               // [TC_FWARPS][D]
     uint64_t *bars = (uint64_t *)(sm + Lay::OFF_BAR);
-    uint64_t *full = bars;                       // [S] TMA -> feature map
-    uint64_t *phi_ready = full + TC_STAGES;      // [S] feature map -> MMA
-    uint64_t *stage_free = phi_ready + TC_STAGES;  // [S] MMA -> TMA
+    uint64_t *full = bars;                           // [S] TMA -> feature map
+    uint64_t *phi_ready = full + TC_STAGES;          // [S] feature map -> MMA
+    uint64_t *stage_free = phi_ready + TC_STAGES;    // [S] MMA -> TMA
     uint64_t *scores_done = stage_free + TC_STAGES;  // [2]
-    uint64_t *a_free = scores_done + 2;          // [2]
-    uint64_t *p_ready = a_free + 2;              // [2]
-    uint64_t *o_done = p_ready + 2;              // [2]
-    uint64_t *o_free = o_done + 2;               // [2]
-    uint64_t *den_full = o_free + 2;             // [2]
-    uint64_t *state_done = den_full + 2;         // [1]
-    uint64_t *s_ready = state_done + 1;          // [1]
-    uint64_t *den_empty = s_ready + 1;           // [2]
-    uint64_t *drain = den_empty + 2;             // [1] abort path: MMA drain
+    uint64_t *a_free = scores_done + 2;              // [2]
+    uint64_t *p_ready = a_free + 2;                  // [2]
+    uint64_t *o_done = p_ready + 2;                  // [2]
+    uint64_t *o_free = o_done + 2;                   // [2]
+    uint64_t *den_full = o_free + 2;                 // [TC_DEN]
+    uint64_t *den_empty = den_full + TC_DEN;         // [TC_DEN]
+    uint64_t *state_done = den_empty + TC_DEN;       // [1]
+    uint64_t *s_ready = state_done + 1;              // [1]
+    uint64_t *drain = s_ready + 1;                   // [1] abort path: MMA drain
     uint32_t *tmem_slot = (uint32_t *)(sm + Lay::OFF_MISC);
     volatile int *abort_flag = (volatile int *)(sm + Lay::OFF_MISC + 4);
 
@@ -148,6 +178,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     const int head = blockIdx.x;
     const int nch = a.nch;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
+
+    auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
+    auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
+    auto stage_v = [&](int s) { return stage_k(s) + Lay::K_BYTES; };
+    uint8_t *const p_tile = sm + Lay::OFF_P;
+    uint8_t *const o_tile = sm + Lay::OFF_O;
 
     if (tid == 0) {
         for (int i = 0; i < TC_STAGES; ++i) {
@@ -161,7 +197,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             mbar_init(&p_ready[i], 1);
             mbar_init(&o_done[i], 1);
             mbar_init(&o_free[i], 4);
-            mbar_init(&den_full[i], 2);
+        }
+        for (int i = 0; i < TC_DEN; ++i) {
+            mbar_init(&den_full[i], 1);
             mbar_init(&den_empty[i], 1);
         }
         mbar_init(state_done, 1);
@@ -170,18 +208,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         *abort_flag = 0;
         mbar_init_fence();
     }
+    if (NORM) {
+        // the z rows of every stage's K tile: rows C, C+1 rewritten per chunk, the rest zero
+        for (int e = tid; e < TC_STAGES * (D / 64) * 8 * 8; e += TC_THREADS) {
+            const int st = e / ((D / 64) * 64), r = e % ((D / 64) * 64);
+            const int kb = r / 64, row = C + (r % 64) / 8, chn = r % 8;
+            *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
+        }
+        for (int i = tid; i < D; i += TC_THREADS) zs[i] = 0.f;
+    }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB;
-
-    auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
-    auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
-    auto stage_v = [&](int s) { return stage_k(s) + Lay::K_BYTES; };
-    auto p_buf = [&](int b) { return sm + Lay::OFF_P + b * Lay::P_BYTES; };
-    auto o_buf = [&](int b) { return sm + Lay::OFF_O + b * Lay::O_BYTES; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -191,10 +233,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const int s = c % TC_STAGES;
                 if (c >= TC_STAGES && !wait_phase(&stage_free[s], ((c / TC_STAGES) - 1) & 1, ctl))
                     break;
-                mbar_arrive_expect_tx(&full[s], Lay::STAGE_BYTES);
+                mbar_arrive_expect_tx(&full[s], Lay::STAGE_TX);
                 for (int kb = 0; kb < D / 64; ++kb) {
                     tma_load_3d(stage_q(s) + kb * C * 128, &a.tm_q, kb * 64, c * C, head, &full[s]);
-                    tma_load_3d(stage_k(s) + kb * C * 128, &a.tm_k, kb * 64, c * C, head, &full[s]);
+                    tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, c * C, head, &full[s]);
                 }
                 for (int jb = 0; jb < DV / 64; ++jb)
                     tma_load_3d(stage_v(s) + jb * C * 128, &a.tm_v, jb * 64, c * C, head, &full[s]);
@@ -204,14 +246,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             for (int c = (issued > TC_STAGES ? issued - TC_STAGES : 0); c < issued; ++c) {
                 const int s = c % TC_STAGES;
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try(&full[s], (c / TC_STAGES) & 1))
+                while (!mbar_try_sleep(&full[s], (c / TC_STAGES) & 1, 200000u))
                     if (globaltimer() - t0 > ctl.timeout_ns) break;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_SC = idesc_bf16_f32(C, C, 0, 0);
+            constexpr uint32_t ID_SC = idesc_bf16_f32(C, Lay::NSC, 0, 0);
             constexpr uint32_t ID_INTER = idesc_bf16_f32(DV, C, 0, 0);
             constexpr uint32_t ID_STATE = idesc_bf16_f32(DV, D, 1, 1);
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(DV, C, 1, 0);
@@ -222,14 +264,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 if (c >= 2 && !wait_phase(&a_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
-                               va = smem_u32(stage_v(s)), pa = smem_u32(p_buf(b));
-                const uint32_t tA = tmem + Lay::T_A + b * C, tO = tmem + Lay::T_O + b * C;
-                // scores: phi(Q_c) phi(K_c)^T, both K-major, K = D in steps of 16
+                               va = smem_u32(stage_v(s)), pa = smem_u32(p_tile);
+                const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
+                // scores: phi(Q_c) [phi(K_c); z_c]^T, both K-major, K = D in steps of 16
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C * 128 + (ks & 3) * 32;
-                    mma_ss(tA, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), ID_SC,
-                           ks > 0);
+                    const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32;
+                    const uint32_t ko = (ks >> 2) * Lay::K_BLK + (ks & 3) * 32;
+                    mma_ss(tA, smem_desc(qa + qo, 16, 1024), smem_desc(ka + ko, 16, 1024), ID_SC, ks > 0);
                 }
                 mma_commit(&scores_done[b]);
                 if (c >= 1 && !wait_phase(s_ready, (c - 1) & 1, ctl)) break;
@@ -239,8 +281,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 if (c >= 1) {
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * C * 128 + (ks & 3) * 32;
-                        mma_ts(tO, tSB + ks * 8, smem_desc(qa + off, 16, 1024), ID_INTER, ks > 0);
+                        const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32;
+                        mma_ts(tO, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
                     }
                 }
                 // state: S^T += V_c^T phi(K_c), both MN-major, K = C in steps of 16 rows
@@ -248,7 +290,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks)
                         mma_ss(tS, smem_desc(va + ks * 2048, C * 128, 1024),
-                               smem_desc(ka + ks * 2048, C * 128, 1024), ID_STATE, (c > 0) || (ks > 0));
+                               smem_desc(ka + ks * 2048, Lay::K_BLK, 1024), ID_STATE, (c > 0) || (ks > 0));
                     mma_commit(state_done);
                 }
                 if (!wait_phase(&p_ready[b], (c >> 1) & 1, ctl)) break;
@@ -264,143 +306,166 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // drain: every MMA issued above has completed before TMEM is released
             mma_commit(drain);
             const uint64_t t0 = globaltimer();
-            while (!mbar_try(drain, 0))
+            while (!mbar_try_sleep(drain, 0, 200000u))
                 if (globaltimer() - t0 > ctl.timeout_ns) break;
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ feature map / normaliser
+    } else if (warp >= 4 && warp < 4 + TC_FWARPS) {
+        // ------------------------------------------------------------ feature map / z
+        // Thread (rg, g) owns 16-byte chunk g (8 features) of rows rg, rg + RG, ...: it
+        // loads all its Q and K chunks at once, transforms them in registers and stores
+        // them back in place (same swizzled slot).
         const int ft = tid - 128;
-        constexpr int G = D / 8;          // 16-byte chunks per row
-        constexpr int RG = 128 / G;       // row groups
+        constexpr int NF = 32 * TC_FWARPS;  // threads in the group
+        constexpr int G = D / 8;            // 16-byte chunks per row
+        constexpr int RG = NF / G;          // row groups
+        constexpr int NR = C / RG;          // rows per thread
         const int g = ft % G, rg = ft / G;
         const int kb = g >> 3, ch = g & 7;
-        const int swz = ((ch ^ (rg & 7)) << 4);
-        if (NORM)
-            for (int i = ft; i < D; i += 128) zs[i] = 0.f;
-        named_bar(1, 128);
+        const int q_swz = kb * C * 128 + ((ch ^ (rg & 7)) << 4) + rg * 128;
+        const int k_swz = kb * Lay::K_BLK + ((ch ^ (rg & 7)) << 4) + rg * 128;
         if (FM != LA_FM_IDENTITY || NORM) {
             for (int c = 0; c < nch; ++c) {
-                const int s = c % TC_STAGES, slot = c & 1;
-                bool ok = wait_phase(&full[s], (c / TC_STAGES) & 1, ctl);
-                if (NORM && c >= 2) ok = ok && wait_phase(&den_empty[slot], ((c >> 1) - 1) & 1, ctl);
-                if (!named_bar_and(1, 128, ok)) break;  // one decision for the whole group
-                float zc[8];
-                if (NORM) {
+                const int s = c % TC_STAGES;
+                if (!group_wait(ft == 0, 1, &full[s], (c / TC_STAGES) & 1, nullptr, 0, false, ctl,
+                                NF))
+                    break;
+                uint4 *qp = (uint4 *)(stage_q(s) + q_swz);
+                uint4 *kp = (uint4 *)(stage_k(s) + k_swz);
+                uint4 wq[NR], wk[NR];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) zc[e] = zs[8 * g + e];
+                for (int n = 0; n < NR; ++n) {
+                    if (FM != LA_FM_IDENTITY) wq[n] = qp[n * RG * 8];
+                    wk[n] = kp[n * RG * 8];
                 }
-                // Q: phi in place, phi(q_t).z for the normaliser
-                uint8_t *qb = stage_q(s) + kb * C * 128 + swz;
-#pragma unroll 2
-                for (int n = 0; n < C / RG; ++n) {
-                    const int t = rg + RG * n;
-                    uint4 *p = (uint4 *)(qb + t * 128);
-                    uint4 w = *p;
-                    uint32_t *wv = (uint32_t *)&w;
-                    float dpart = 0.f;
+                if (NORM && ft < 8 * (D / 64) * 2) {
+                    // z_c (before this chunk) as a bf16 hi/lo pair in key rows C and C+1
+                    const int zkb = ft / 16, zr = (ft / 8) & 1, zch = ft & 7;
+                    const float4 z0 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4];
+                    const float4 z1 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4 + 1];
+                    const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+                    uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
-                        if (NORM) dpart += x0 * zc[2 * e] + x1 * zc[2 * e + 1];
-                        if (FM != LA_FM_IDENTITY) wv[e] = pack_bf16x2(x0, x1);
+                        float h0 = __bfloat162float(__float2bfloat16_rn(zz[2 * e]));
+                        float h1 = __bfloat162float(__float2bfloat16_rn(zz[2 * e + 1]));
+                        pk[e] = zr ? pack_bf16x2(zz[2 * e] - h0, zz[2 * e + 1] - h1) : pack_bf16x2(h0, h1);
                     }
-                    if (FM != LA_FM_IDENTITY) *p = w;
-                    if (NORM) {
+                    const int row = C + zr;
+                    *(uint4 *)(stage_k(s) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                if (FM != LA_FM_IDENTITY) {
 #pragma unroll
-                        for (int o = G / 2; o > 0; o >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, o);
-                        if (g == 0) den_inter[slot * C + t] = dpart;
+                    for (int n = 0; n < NR; ++n) {
+                        uint32_t *wv = (uint32_t *)&wq[n];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(phi1<FM>(bf_lo(wv[e])), phi1<FM>(bf_hi(wv[e])));
                     }
                 }
-                // K: phi in place, column sums for z
                 float colsum[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) colsum[e] = 0.f;
-                uint8_t *kbp = stage_k(s) + kb * C * 128 + swz;
-#pragma unroll 2
-                for (int n = 0; n < C / RG; ++n) {
-                    const int t = rg + RG * n;
-                    uint4 *p = (uint4 *)(kbp + t * 128);
-                    uint4 w = *p;
-                    uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+                for (int n = 0; n < NR; ++n) {
+                    uint32_t *wv = (uint32_t *)&wk[n];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
-                        colsum[2 * e] += x0;
-                        colsum[2 * e + 1] += x1;
+                        const float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
+                        if (NORM) {
+                            colsum[2 * e] += x0;
+                            colsum[2 * e + 1] += x1;
+                        }
                         if (FM != LA_FM_IDENTITY) wv[e] = pack_bf16x2(x0, x1);
                     }
-                    if (FM != LA_FM_IDENTITY) *p = w;
+                }
+                if (FM != LA_FM_IDENTITY) {
+#pragma unroll
+                    for (int n = 0; n < NR; ++n) {
+                        qp[n * RG * 8] = wq[n];
+                        kp[n * RG * 8] = wk[n];
+                    }
                 }
                 fence_async_smem();
                 if (NORM && c + 1 < nch) {
-                    // reduce the column sums over the row groups: lanes g, g+G, ... of a
-                    // warp, then the four warps through shared memory
+                    // column sums over the row groups: lanes g, g+G, ... of a warp, then the
+                    // group's warps through shared memory
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        for (int o = G; o < 32; o <<= 1) colsum[e] += __shfl_xor_sync(0xffffffffu, colsum[e], o);
-                    if (lane < G)
+                    for (int o = G; o < 32; o <<= 1)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) zpart[(ft >> 5) * D + 8 * g + e] = colsum[e];
+                        for (int e = 0; e < 8; ++e) colsum[e] += __shfl_xor_sync(0xffffffffu, colsum[e], o);
+                    if (lane < G) {
+                        float4 *zp = (float4 *)(zpart + (ft >> 5) * D + 8 * g);
+                        zp[0] = make_float4(colsum[0], colsum[1], colsum[2], colsum[3]);
+                        zp[1] = make_float4(colsum[4], colsum[5], colsum[6], colsum[7]);
+                    }
                 }
-                named_bar(1, 128);
-                if (ft == 0 && !a.debug_stall) {
-                    mbar_arrive(&phi_ready[s]);
-                    if (NORM) mbar_arrive(&den_full[slot]);
-                }
+                named_bar(1, NF);
+                if (ft == 0 && !a.debug_stall) mbar_arrive(&phi_ready[s]);
                 if (NORM && c + 1 < nch) {
-                    for (int i = ft; i < D; i += 128)
-                        zs[i] += zpart[i] + zpart[D + i] + zpart[2 * D + i] + zpart[3 * D + i];
-                    named_bar(1, 128);
+                    for (int i = ft; i < D; i += NF) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int w = 0; w < TC_FWARPS; ++w) acc += zpart[w * D + i];
+                        zs[i] += acc;
+                    }
+                    named_bar(1, NF);
                 }
             }
         }
-    } else if (warp >= 8 && warp < 12) {
+    } else if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
         // ------------------------------------------------------------ scores -> P, S readback
         const int q4 = warp & 3;
-        const int pt = tid - 256;
+        const int pt = tid - 32 * (4 + TC_FWARPS);
         const int t = 16 * q4 + (lane & 15);  // M = 64 TMEM layout: row t at lane t%16 of quadrant t/16
         const bool row_lane = lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         for (int c = 0; c < nch; ++c) {
-            const int b = c & 1, slot = c & 1;
-            bool ok = wait_phase(&scores_done[b], (c >> 1) & 1, ctl);
-            if (NORM && c >= 2) ok = ok && wait_phase(&den_empty[slot], ((c >> 1) - 1) & 1, ctl);
-            if (!named_bar_and(2, 128, ok)) break;
+            const int b = c & 1, slot = c % TC_DEN;
+            if (!group_wait(pt == 0, 2, &scores_done[b], (c >> 1) & 1, &den_empty[slot],
+                            ((c / TC_DEN) - 1) & 1, NORM && c >= TC_DEN, ctl))
+                break;
             tc_fence_after();
-            uint32_t r0[32], r1[32];
-            const uint32_t tA = tmem + Lay::T_A + b * C + lane_off;
-            tmem_ld32(tA, r0);
-            tmem_ld32(tA + 32, r1);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_free[b]);
-            if (row_lane) {
-                float rs = 0.f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int s0 = 2 * e, s1 = 2 * e + 1;
-                    float v0 = s0 <= t ? __uint_as_float(r0[s0]) : 0.f;
-                    float v1 = s1 <= t ? __uint_as_float(r0[s1]) : 0.f;
-                    rs += v0 + v1;
-                    pk[e] = pack_bf16x2(v0, v1);
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int s0 = 32 + 2 * e, s1 = 33 + 2 * e;
-                    float v0 = s0 <= t ? __uint_as_float(r1[2 * e]) : 0.f;
-                    float v1 = s1 <= t ? __uint_as_float(r1[2 * e + 1]) : 0.f;
-                    rs += v0 + v1;
-                    pk[16 + e] = pack_bf16x2(v0, v1);
-                }
-                uint8_t *prow = p_buf(b) + t * 128;
-#pragma unroll
-                for (int chn = 0; chn < 8; ++chn)
-                    *(uint4 *)(prow + ((chn ^ (t & 7)) << 4)) =
-                        make_uint4(pk[4 * chn], pk[4 * chn + 1], pk[4 * chn + 2], pk[4 * chn + 3]);
-                if (NORM) den_intra[slot * C + t] = rs;
+            // one 32-column half of the scores row at a time (register budget)
+            const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off;
+            float rs = 0.f, dz = 0.f;
+            if (NORM) {
+                uint32_t rz[8];
+                tmem_ld8(tA + C, rz);
+                tmem_wait_ld();
+                dz = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);  // phi(q_t).z_c (hi + lo)
             }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_ld32(tA + 32 * h, r);
+                tmem_wait_ld();
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_free[b]);
+                }
+                if (row_lane) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
+                        const float v0 = s0 <= t ? __uint_as_float(r[2 * e]) : 0.f;
+                        const float v1 = s1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
+                        rs += v0 + v1;
+                        pk[e] = pack_bf16x2(v0, v1);
+                    }
+                    uint8_t *prow = p_tile + t * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chn = 4 * h + q;
+                        *(uint4 *)(prow + ((chn ^ (t & 7)) << 4)) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
+                }
+            }
+            // den = phi(q_t).z_c + masked row sum
+            if (NORM && row_lane) rden[slot * C + t] = __frcp_rn(dz + rs);
             fence_async_smem();
             named_bar(2, 128);
             if (pt == 0) {
@@ -409,7 +474,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             }
             // bf16 copy of the state for the next chunk's inter product
             if (c + 1 < nch) {
-                if (!named_bar_and(2, 128, wait_phase(state_done, c & 1, ctl))) break;
+                if (!group_wait(pt == 0, 2, state_done, c & 1, nullptr, 0, false, ctl)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
@@ -427,51 +492,66 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 if (lane == 0) mbar_arrive(s_ready);
             }
         }
-        (void)pt;
-    } else if (warp >= 12) {
+    } else if (warp >= 8 + TC_FWARPS) {
         // ------------------------------------------------------------ output epilogue
         const int q4 = warp & 3;
-        const int ot = tid - 384;
-        const int j = 32 * q4 + lane;  // M = dv = 128: row j at lane j
+        const int ot = tid - 32 * (8 + TC_FWARPS);
+        const int j = 32 * q4 + lane;  // M = dv = 128: row j of O^T at lane j
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const bool odd = lane & 1;
+        uint8_t *const ob = o_tile + (j >> 6) * C * 128 + (((j & 7) & ~1) << 1);
+        const int jc = (j & 63) >> 3;
         for (int c = 0; c < nch; ++c) {
-            const int b = c & 1, slot = c & 1;
-            bool ok = wait_phase(&o_done[b], (c >> 1) & 1, ctl);
-            if (NORM) ok = ok && wait_phase(&den_full[slot], (c >> 1) & 1, ctl);
-            if (!named_bar_and(3, 128, ok)) break;
+            const int b = c & 1, slot = c % TC_DEN;
+            if (!group_wait(ot == 0, 3, &o_done[b], (c >> 1) & 1, &den_full[slot], (c / TC_DEN) & 1,
+                            NORM, ctl))
+                break;
             tc_fence_after();
-            uint32_t r0[32], r1[32];
-            const uint32_t tO = tmem + Lay::T_O + b * C + lane_off;
-            tmem_ld32(tO, r0);
-            tmem_ld32(tO + 32, r1);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[b]);
-            if (NORM && ot < C) rden[ot] = 1.f / (den_inter[slot * C + ot] + den_intra[slot * C + ot]);
-            // the staging buffer of chunk c-2 must have been read by its TMA store
-            if (ot == 0 && c >= 2) tma_wait_read_le1();
+            // the output tile must have been read by the previous chunk's TMA store
+            if (ot == 0 && c >= 1) tma_wait_read_all();
             named_bar(3, 128);
-            if (NORM && ot == 0) mbar_arrive(&den_empty[slot]);
-            uint8_t *ob = o_buf(b) + (j >> 6) * C * 128 + ((j & 7) << 1);
-            const int jc = (j & 63) >> 3;
+            const uint32_t tO = tmem + Lay::T_O + b * C + lane_off;
 #pragma unroll
-            for (int tt = 0; tt < 32; ++tt) {
-                float v0 = __uint_as_float(r0[tt]), v1 = __uint_as_float(r1[tt]);
-                if (NORM) {
-                    v0 *= rden[tt];
-                    v1 *= rden[tt + 32];
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_ld32(tO + 32 * h, r);
+                tmem_wait_ld();
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&o_free[b]);
                 }
-                *(__nv_bfloat16 *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = __float2bfloat16_rn(v0);
-                *(__nv_bfloat16 *)(ob + (tt + 32) * 128 + ((jc ^ (tt & 7)) << 4)) =
-                    __float2bfloat16_rn(v1);
+                float rd[32];
+                if (NORM) {
+                    const float4 *rp = (const float4 *)(rden + slot * C + 32 * h);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 v = rp[q];
+                        rd[4 * q] = v.x; rd[4 * q + 1] = v.y; rd[4 * q + 2] = v.z; rd[4 * q + 3] = v.w;
+                    }
+                }
+                // Lanes j, j^1 swap one value per pair of rows so that each writes two
+                // neighbouring columns of one row as a single 32-bit word.
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
+                    if (NORM) {
+                        a0 *= rd[2 * u];
+                        a1 *= rd[2 * u + 1];
+                    }
+                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+                    const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
+                    const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
+                    *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
+                }
             }
             fence_async_smem();
             named_bar(3, 128);
             if (ot == 0) {
                 for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_store_3d(&a.tm_o, o_buf(b) + jb * C * 128, jb * 64, c * C, head);
+                    tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, c * C, head);
                 tma_commit_group();
+                if (NORM) mbar_arrive(&den_empty[slot]);
             }
         }
         if (ot == 0) tma_wait_all();
@@ -525,7 +605,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int BH, int L, int d, int C)
 template <int D, int DV, int C, int FM, bool NORM>
 int launch_t(const Problem &p)
 {
-    using Lay = TcLayout<D, DV, C>;
+    using Lay = TcLayout<D, DV, C, NORM>;
     TcArgs a;
     memset(&a, 0, sizeof(a));
     const int BH = p.B * p.H;
@@ -579,7 +659,8 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
     info->grid_x = p.B * p.H;
     info->grid_y = 1;
     info->block = TC_THREADS;
-    info->smem_bytes = p.D == 128 ? TcLayout<128, 128, 64>::ALLOC : TcLayout<64, 128, 64>::ALLOC;
+    info->smem_bytes = p.D == 128 ? (p.normalize ? TcLayout<128, 128, 64, true>::ALLOC : TcLayout<128, 128, 64, false>::ALLOC)
+                                   : (p.normalize ? TcLayout<64, 128, 64, true>::ALLOC : TcLayout<64, 128, 64, false>::ALLOC);
     info->n_launches = 1;
     info->workspace_bytes = 0;
     return LA_OK;

@@ -46,6 +46,60 @@ LA_DEV bool mbar_try(uint64_t *b, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp sleeps until the phase completes or the hint
+// (in ns) runs out, instead of re-issuing probes that take issue slots from working warps.
+LA_DEV bool mbar_try_sleep(uint64_t *b, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// ---- shared memory by 32-bit shared-window address ---------------------------------------
+LA_DEV uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+LA_DEV void sts128(uint32_t a, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+LA_DEV void sts32(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+LA_DEV float2 lds64f(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+    return v;
+}
+LA_DEV void sts16(uint32_t a, uint16_t v)
+{
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
+LA_DEV float ldsf(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+LA_DEV void stsf(uint32_t a, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
 // ---- proxies / named barriers -------------------------------------------------------------
 LA_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 LA_DEV void named_bar(int id, int nthreads)
@@ -81,6 +135,7 @@ LA_DEV void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, 
 }
 LA_DEV void tma_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LA_DEV void tma_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+LA_DEV void tma_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 LA_DEV void tma_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---- tcgen05 -------------------------------------------------------------------------------
@@ -138,6 +193,13 @@ LA_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+LA_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
 }
 LA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
