@@ -82,6 +82,27 @@ def flops_per_token(w, C):
     return f
 
 
+def kernel_sha1():
+    import hashlib
+    d = os.path.join(ROOT, "chunkwise_causal_linear_gb300", "csrc")
+    return hashlib.sha1(open(os.path.join(d, "tc.cu"), "rb").read() +
+                        open(os.path.join(d, "tc_ptx.cuh"), "rb").read()).hexdigest()
+
+
+def ncu_traffic(workload, C, path, B, H):
+    """DRAM bytes per launch from the committed ncu capture (profiles/traffic.json), or None
+    when there is none for this workload or the kernel changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{workload}/C{C}/{path}")
+    except Exception:
+        return None
+    w = synth.WORKLOADS[workload]
+    if not rec or rec.get("kernel_sha1") != kernel_sha1() or (B, H) != (w["B"], w["H"]):
+        return None
+    return rec["bytes_per_launch"]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -385,16 +406,7 @@ def run_ours(args):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     kernel_s = (t_ms / args.steps) / 1e3
     achieved = io_bytes / kernel_s / 1e9
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                tr = json.load(f)
-            key = f"{args.workload}/C{C}/{plan['path']}"
-            traffic = tr.get(key)
-        except Exception:
-            traffic = None
+    traffic = ncu_traffic(args.workload, C, plan["path"], B, H)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "traffic": traffic,
             "peak_kind": f"{peak_kind} hbm_gbs (copy)",
