@@ -25,6 +25,7 @@ LA_ERR_WORKSPACE = -4
 LA_ERR_CUDA = -5
 LA_ERR_TIMEOUT = -6
 LA_ERR_DEVICE = -7
+LA_ERR_SCRATCH_LIMIT = -8
 
 LA_FM_IDENTITY, LA_FM_ELU1, LA_FM_FAVOR = 0, 1, 2
 LA_BF16, LA_F32 = 0, 1
@@ -34,8 +35,8 @@ FEATURE_MAPS = {"identity": LA_FM_IDENTITY, "elu1": LA_FM_ELU1, "favor": LA_FM_F
 
 # every function the header declares (checked by the tests against include/la_chunked.h)
 EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
-           "la_chunked_workspace_bytes", "la_chunked_plan", "la_last_device_status",
-           "la_status_string", "la_cost_model", "la_version")
+           "la_chunked_fwd_noalloc", "la_chunked_workspace_bytes", "la_chunked_plan",
+           "la_last_device_status", "la_status_string", "la_cost_model", "la_version")
 
 
 class la_feature_map(ctypes.Structure):
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
             L.la_chunked_fwd_path.restype = i
             L.la_chunked_fwd_host.argtypes = [p, p, p, p, p, p, p, p, *common]
             L.la_chunked_fwd_host.restype = i
+            L.la_chunked_fwd_noalloc.argtypes = [p, p, p, p, i, i, i, i, i, i, fmp, i, p, i, i, p]
+            L.la_chunked_fwd_noalloc.restype = i
             L.la_chunked_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i, i]
             L.la_chunked_workspace_bytes.restype = sz
             L.la_chunked_plan.argtypes = [i, i, i, i, i, i, fmp, i, i, i, i, i, i,
@@ -133,6 +136,15 @@ def la_chunked_fwd_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, o
                                      out_dev, B, H, L, dk, dv, C, _fm(feature_map), normalize,
                                      level_weights, num_levels, dtype, workspace,
                                      workspace_bytes, stream)
+
+
+def la_chunked_fwd_noalloc(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize,
+                           level_weights, num_levels, dtype, stream) -> int:
+    """Forward pass that allocates nothing (for callers that cannot allocate device
+    memory); scratch, where needed, comes from a fixed 8 MiB buffer inside the library.
+    Calls that may overlap on the GPU must be serialised by the caller."""
+    return lib().la_chunked_fwd_noalloc(q, k, v, out, B, H, L, dk, dv, C, _fm(feature_map),
+                                        normalize, level_weights, num_levels, dtype, stream)
 
 
 def la_chunked_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, num_levels,

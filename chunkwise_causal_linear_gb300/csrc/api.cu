@@ -290,6 +290,7 @@ const char *la_status_string(int status)
     case LA_ERR_CUDA: return "a CUDA runtime call failed";
     case LA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
     case LA_ERR_DEVICE: return "a device-side check failed";
+    case LA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed no-alloc buffer (8 MiB) holds";
     default: return "unknown status";
     }
 }

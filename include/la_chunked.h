@@ -53,7 +53,9 @@ enum la_status {
     LA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than la_chunked_workspace_bytes */
     LA_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, copy, attribute)      */
     LA_ERR_TIMEOUT = -6,     /* device: a bounded wait gave up (read via la_last_device_status) */
-    LA_ERR_DEVICE = -7       /* device: an index or shape check failed inside a kernel    */
+    LA_ERR_DEVICE = -7,      /* device: an index or shape check failed inside a kernel    */
+    LA_ERR_SCRATCH_LIMIT = -8 /* la_chunked_fwd_noalloc: the problem needs more scratch than
+                                 its fixed buffer holds (8 MiB)                           */
 };
 
 /* ---- feature maps phi -------------------------------------------------------------- */
@@ -132,6 +134,30 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
                         const la_feature_map *feature_map, int normalize,
                         const float *level_weights, int num_levels,
                         int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * la_chunked_fwd_noalloc -- the same forward pass, for callers that cannot allocate device
+ * memory (code running inside an allocator or a memory-pool callback, plugins whose host
+ * application owns every device allocation, real-time loops that must never call
+ * cudaMalloc / cudaFree).  No counterpart on the pages: it is a deployment variant.
+ *
+ * It allocates nothing.  Where the problem needs scratch (the log-linear mask's per-level
+ * chunk states), it uses a fixed 8 MiB array compiled into the library; every GPU that
+ * loads the library holds those 8 MiB until the process exits.  Problems that need more
+ * return LA_ERR_SCRATCH_LIMIT before anything is launched (la_chunked_workspace_bytes tells
+ * how much a problem needs).
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; the kernel
+ *     clears what it needs at the start of every call.  Calls that may overlap on the GPU
+ *     (different streams, or different host threads) race on it: serialise them.
+ * Arguments, layout and the other errors are those of la_chunked_fwd (no workspace).
+ */
+int la_chunked_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
+                           int B, int H, int L, int dk, int dv, int C,
+                           const la_feature_map *feature_map, int normalize,
+                           const float *level_weights, int num_levels,
+                           int dtype, void *stream);
 
 /* Bytes of device workspace la_chunked_fwd needs for this problem on the current device
  * (0 when none).  Returns 0 also for invalid arguments (la_chunked_fwd reports those). */
