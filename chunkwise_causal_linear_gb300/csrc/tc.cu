@@ -24,11 +24,17 @@
 // scores x2 [C x (C + 8)].  The state is accumulated in fp32 by the MMA and never leaves
 // TMEM; the inter-chunk product reads its bf16 copy as the A operand straight from TMEM.
 //
-// MMAs per chunk (bf16 in, fp32 accumulate), D = feature dim, C = chunk:
-//   scores  A_c   = phi(Q_c) [phi(K_c); z_c]^T   M=C   N=C(+8)  K=D
-//   inter   O^T   = bf16(S)^T phi(Q_c)^T         M=dv  N=C      K=D   (A from TMEM)
-//   state   S^T  += V_c^T phi(K_c)               M=dv  N=D      K=C
-//   intra   O^T  += V_c^T P_c^T                  M=dv  N=C      K=C
+// Rows move in 64-row tiles (TMA box, MMA tile).  The chunk size CH is 16, 32 or 64: a tile
+// holds 64/CH chunks, each with its own inter product (from the state at the chunk's start),
+// its own state update and its own bf16 state copy, while the intra part of the tile uses
+// a block-diagonal causal mask at CH granularity.  The normaliser does not depend on CH: it
+// is phi(q_t).z at the tile start plus the causal row sum inside the tile.
+//
+// MMAs per tile (bf16 in, fp32 accumulate), D = feature dim, T = 64:
+//   scores  A     = phi(Q_T) [phi(K_T); z]^T     M=T   N=T(+8)  K=D   once per tile
+//   inter   O^T_j = bf16(S_j)^T phi(Q_j)^T       M=dv  N=CH     K=D   per chunk j (A in TMEM)
+//   state   S^T  += V_j^T phi(K_j)               M=dv  N=D      K=CH  per chunk j
+//   intra   O^T  += V_T^T P_T^T                  M=dv  N=T      K=T   once per tile
 //
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA records
 // LA_ERR_TIMEOUT in the device error word, raises a shared abort flag that the other roles
@@ -52,7 +58,8 @@ constexpr int TC_DEN = 4;  // ring of per-chunk 1/den vectors
 
 struct TcArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
-    int L, nch;
+    int L, nch;  // nch: number of 64-row tiles
+    int nsub;    // number of chunks of CH rows
     int *err;
     unsigned long long timeout_ns;
     int debug_stall;  // test knob: the feature-map group never signals (forces a timeout)
@@ -86,7 +93,7 @@ struct TcLayout {
     // TMEM columns
     static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 192, T_A = 320, A_STRIDE = 80;
     static_assert(D <= 128 && DV == 128, "tensor-core path: D <= 128, dv == 128");
-    static_assert(C == 64, "tensor-core path: C == 64");
+    static_assert(C == 64, "tensor-core path: 64-row tiles");
     static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
     static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -146,9 +153,11 @@ __device__ __forceinline__ float phi1(float x)
     return x;
 }
 
-template <int D, int DV, int C, int FM, bool NORM>
+template <int D, int DV, int CH, int FM, bool NORM>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_constant__ TcArgs a)
 {
+    constexpr int C = 64;           // rows per tile
+    constexpr int NSUB = C / CH;    // chunks per tile
     using Lay = TcLayout<D, DV, C, NORM>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles (offset taken in the shared window)
@@ -224,6 +233,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB;
+    if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
+        // the state and its bf16 copy start at zero (the first chunk's inter product is 0)
+        const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t zero[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int col = 0; col < D; col += 16) tmem_st16(tS + lo + col, zero);
+#pragma unroll
+        for (int col = 0; col < D / 2; col += 16) tmem_st16(tSB + lo + col, zero);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -254,10 +276,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t ID_SC = idesc_bf16_f32(C, Lay::NSC, 0, 0);
-            constexpr uint32_t ID_INTER = idesc_bf16_f32(DV, C, 0, 0);
+            constexpr uint32_t ID_INTER = idesc_bf16_f32(DV, CH, 0, 0);
             constexpr uint32_t ID_STATE = idesc_bf16_f32(DV, D, 1, 1);
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(DV, C, 1, 0);
-            for (int c = 0; c < nch; ++c) {
+            const int nsub = a.nsub;
+            bool ok = true;
+            for (int c = 0; ok && c < nch; ++c) {
                 const int s = c % TC_STAGES, b = c & 1;
                 uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM) ? &full[s] : &phi_ready[s];
                 if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
@@ -266,7 +290,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
                                va = smem_u32(stage_v(s)), pa = smem_u32(p_tile);
                 const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
-                // scores: phi(Q_c) [phi(K_c); z_c]^T, both K-major, K = D in steps of 16
+                // scores of the tile: phi(Q) [phi(K); z]^T, both K-major, K = D in steps of 16
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32;
@@ -274,32 +298,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     mma_ss(tA, smem_desc(qa + qo, 16, 1024), smem_desc(ka + ko, 16, 1024), ID_SC, ks > 0);
                 }
                 mma_commit(&scores_done[b]);
-                if (c >= 1 && !wait_phase(s_ready, (c - 1) & 1, ctl)) break;
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
-                tc_fence_after();
-                // inter: bf16(S)^T (TMEM) x phi(Q_c)^T (K-major B), K = D
-                if (c >= 1) {
+                for (int j = 0; j < NSUB; ++j) {
+                    const int g = c * NSUB + j;  // chunk index in the sequence
+                    if (g >= nsub) break;
+                    if (g >= 1 && !wait_phase(s_ready, (g - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // inter: bf16(S_g)^T (TMEM) x phi(Q_g)^T, the chunk's CH rows, K = D
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32;
-                        mma_ts(tO, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
+                        const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32 + j * CH * 128;
+                        mma_ts(tO + j * CH, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
+                    }
+                    // state: S^T += V_g^T phi(K_g), both MN-major, K = CH in steps of 16 rows
+                    if (g + 1 < nsub) {
+#pragma unroll
+                        for (int ks = 0; ks < CH / 16; ++ks) {
+                            const uint32_t ro = (j * CH + 16 * ks) * 128;
+                            mma_ss(tS, smem_desc(va + ro, C * 128, 1024),
+                                   smem_desc(ka + ro, Lay::K_BLK, 1024), ID_STATE, 1);
+                        }
+                        mma_commit(state_done);
                     }
                 }
-                // state: S^T += V_c^T phi(K_c), both MN-major, K = C in steps of 16 rows
-                if (c + 1 < nch) {
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_ss(tS, smem_desc(va + ks * 2048, C * 128, 1024),
-                               smem_desc(ka + ks * 2048, Lay::K_BLK, 1024), ID_STATE, (c > 0) || (ks > 0));
-                    mma_commit(state_done);
-                }
+                if (!ok) break;
                 if (!wait_phase(&p_ready[b], (c >> 1) & 1, ctl)) break;
                 tc_fence_after();
-                // intra: V_c^T (MN-major A) x P_c^T (K-major B), K = C
+                // intra: V^T (MN-major A) x P^T (K-major B) over the tile, K = 64
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ss(tO, smem_desc(va + ks * 2048, C * 128, 1024),
-                           smem_desc(pa + ks * 32, 16, 1024), ID_INTRA, (c > 0) || (ks > 0));
+                           smem_desc(pa + ks * 32, 16, 1024), ID_INTRA, 1);
                 mma_commit(&o_done[b]);
                 mma_commit(&stage_free[s]);
             }
@@ -449,11 +481,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
+                        // P keeps s in t's chunk with s <= t (block-diagonal causal mask at
+                        // CH); the normaliser's row sum keeps every s <= t of the tile
                         const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
                         const float v0 = s0 <= t ? __uint_as_float(r[2 * e]) : 0.f;
                         const float v1 = s1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
                         rs += v0 + v1;
-                        pk[e] = pack_bf16x2(v0, v1);
+                        if (CH == C) {
+                            pk[e] = pack_bf16x2(v0, v1);
+                        } else {
+                            const int tlo = t & ~(CH - 1);
+                            pk[e] = pack_bf16x2(s0 >= tlo ? v0 : 0.f, s1 >= tlo ? v1 : 0.f);
+                        }
                     }
                     uint8_t *prow = p_tile + t * 128;
 #pragma unroll
@@ -472,9 +511,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 mbar_arrive(&p_ready[b]);
                 if (NORM) mbar_arrive(&den_full[slot]);
             }
-            // bf16 copy of the state for the next chunk's inter product
-            if (c + 1 < nch) {
-                if (!group_wait(pt == 0, 2, state_done, c & 1, nullptr, 0, false, ctl)) break;
+            // bf16 copy of the state for each next chunk's inter product
+            bool rb_ok = true;
+            for (int j = 0; j < NSUB; ++j) {
+                const int g = c * NSUB + j;
+                if (g + 1 >= a.nsub) break;  // no state update after the last chunk
+                if (!group_wait(pt == 0, 2, state_done, g & 1, nullptr, 0, false, ctl)) {
+                    rb_ok = false;
+                    break;
+                }
                 tc_fence_after();
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
@@ -491,6 +536,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_ready);
             }
+            if (!rb_ok) break;
         }
     } else if (warp >= 8 + TC_FWARPS) {
         // ------------------------------------------------------------ output epilogue
@@ -602,9 +648,10 @@ bool make_map(CUtensorMap *m, const void *ptr, int BH, int L, int d, int C)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int DV, int C, int FM, bool NORM>
+template <int D, int DV, int CH, int FM, bool NORM>
 int launch_t(const Problem &p)
 {
+    constexpr int C = 64;  // rows per tile
     using Lay = TcLayout<D, DV, C, NORM>;
     TcArgs a;
     memset(&a, 0, sizeof(a));
@@ -614,13 +661,14 @@ int launch_t(const Problem &p)
         return LA_ERR_CUDA;
     a.L = p.L;
     a.nch = (p.L + C - 1) / C;
+    a.nsub = (p.L + CH - 1) / CH;
     a.err = p.err;
     a.timeout_ns = 2000000000ull;
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");
     if (e && *e) a.timeout_ns = strtoull(e, nullptr, 10);
     const char *st = getenv("LA_DEBUG_STALL");
     a.debug_stall = (st && *st && *st != '0') ? 1 : 0;
-    auto kern = tc_chunked_kernel<D, DV, C, FM, NORM>;
+    auto kern = tc_chunked_kernel<D, DV, CH, FM, NORM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
         cudaSuccess)
         return LA_ERR_CUDA;
@@ -628,14 +676,22 @@ int launch_t(const Problem &p)
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-template <int D>
-int launch_d(const Problem &p)
+template <int D, int CH>
+int launch_dc(const Problem &p)
 {
     const bool n = p.normalize != 0;
     if (p.fm == LA_FM_IDENTITY)
-        return n ? launch_t<D, 128, 64, LA_FM_IDENTITY, true>(p)
-                 : launch_t<D, 128, 64, LA_FM_IDENTITY, false>(p);
-    return n ? launch_t<D, 128, 64, LA_FM_ELU1, true>(p) : launch_t<D, 128, 64, LA_FM_ELU1, false>(p);
+        return n ? launch_t<D, 128, CH, LA_FM_IDENTITY, true>(p)
+                 : launch_t<D, 128, CH, LA_FM_IDENTITY, false>(p);
+    return n ? launch_t<D, 128, CH, LA_FM_ELU1, true>(p) : launch_t<D, 128, CH, LA_FM_ELU1, false>(p);
+}
+
+template <int D>
+int launch_d(const Problem &p)
+{
+    if (p.C == 16) return launch_dc<D, 16>(p);
+    if (p.C == 32) return launch_dc<D, 32>(p);
+    return launch_dc<D, 64>(p);
 }
 
 }  // namespace
@@ -648,7 +704,7 @@ bool tc_supported(const Problem &p, int num_sms)
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     if (p.dk != p.D) return false;
     if (!(p.D == 64 || p.D == 128) || p.dv != 128) return false;
-    if (p.C != 64) return false;
+    if (p.C != 16 && p.C != 32 && p.C != 64) return false;
     if (p.L < 2 * 64) return false;  // short sequences: the generic path is as fast
     return true;
 }
