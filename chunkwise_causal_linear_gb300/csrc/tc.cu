@@ -20,6 +20,8 @@
 //                  bf16 copy in TMEM.
 //   * warps 16-19  output epilogue: O^T from TMEM, normaliser, bf16, swizzled shared-memory
 //                  tile, TMA store.
+// With dv = 64 the dv-row accumulators use the M = 64 lane layout (row m in lane
+// m%16 + 32*(m/16)), which is also where an M = 64 A operand is read from in TMEM.
 // TMEM (512 columns): S^T fp32 [dv lanes x D] | S^T bf16 [dv x D/2] | O^T x2 [dv x C] |
 // scores x2 [C x (C + 8)].  The state is accumulated in fp32 by the MMA and never leaves
 // TMEM; the inter-chunk product reads its bf16 copy as the A operand straight from TMEM.
@@ -41,6 +43,8 @@
 // poll, drains its own async copies / MMAs, frees TMEM and exits.
 #include <stdio.h>
 #include <stdlib.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -92,7 +96,7 @@ struct TcLayout {
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
     // TMEM columns
     static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 192, T_A = 320, A_STRIDE = 80;
-    static_assert(D <= 128 && DV == 128, "tensor-core path: D <= 128, dv == 128");
+    static_assert(D <= 128 && (DV == 64 || DV == 128), "tensor-core path: D <= 128, dv 64 or 128");
     static_assert(C == 64, "tensor-core path: 64-row tiles");
     static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
     static_assert(ALLOC <= 232448, "shared memory budget");
@@ -542,7 +546,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         // ------------------------------------------------------------ output epilogue
         const int q4 = warp & 3;
         const int ot = tid - 32 * (8 + TC_FWARPS);
-        const int j = 32 * q4 + lane;  // M = dv = 128: row j of O^T at lane j
+        // row j of O^T: lane j (dv = 128), or lane j%16 of quadrant j/16 (dv = 64)
+        const int j = (DV == 128) ? 32 * q4 + lane : 16 * q4 + (lane & 15);
+        const bool live = (DV == 128) || lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const bool odd = lane & 1;
         uint8_t *const ob = o_tile + (j >> 6) * C * 128 + (((j & 7) & ~1) << 1);
@@ -588,7 +594,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
                     const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
                     const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-                    *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
+                    if (live) *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
                 }
             }
             fence_async_smem();
@@ -676,22 +682,22 @@ int launch_t(const Problem &p)
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-template <int D, int CH>
+template <int D, int DV, int CH>
 int launch_dc(const Problem &p)
 {
     const bool n = p.normalize != 0;
     if (p.fm == LA_FM_IDENTITY)
-        return n ? launch_t<D, 128, CH, LA_FM_IDENTITY, true>(p)
-                 : launch_t<D, 128, CH, LA_FM_IDENTITY, false>(p);
-    return n ? launch_t<D, 128, CH, LA_FM_ELU1, true>(p) : launch_t<D, 128, CH, LA_FM_ELU1, false>(p);
+        return n ? launch_t<D, DV, CH, LA_FM_IDENTITY, true>(p)
+                 : launch_t<D, DV, CH, LA_FM_IDENTITY, false>(p);
+    return n ? launch_t<D, DV, CH, LA_FM_ELU1, true>(p) : launch_t<D, DV, CH, LA_FM_ELU1, false>(p);
 }
 
-template <int D>
+template <int D, int DV>
 int launch_d(const Problem &p)
 {
-    if (p.C == 16) return launch_dc<D, 16>(p);
-    if (p.C == 32) return launch_dc<D, 32>(p);
-    return launch_dc<D, 64>(p);
+    if (p.C == 16) return launch_dc<D, DV, 16>(p);
+    if (p.C == 32) return launch_dc<D, DV, 32>(p);
+    return launch_dc<D, DV, 64>(p);
 }
 
 }  // namespace
@@ -703,7 +709,8 @@ bool tc_supported(const Problem &p, int num_sms)
     if (p.lam) return false;
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     if (p.dk != p.D) return false;
-    if (!(p.D == 64 || p.D == 128) || p.dv != 128) return false;
+    // (D, dv) in {(64, 64), (64, 128), (128, 128)}
+    if (!((p.D == 64 && (p.dv == 64 || p.dv == 128)) || (p.D == 128 && p.dv == 128))) return false;
     if (p.C != 16 && p.C != 32 && p.C != 64) return false;
     if (p.L < 2 * 64) return false;  // short sequences: the generic path is as fast
     return true;
@@ -715,8 +722,13 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
     info->grid_x = p.B * p.H;
     info->grid_y = 1;
     info->block = TC_THREADS;
-    info->smem_bytes = p.D == 128 ? (p.normalize ? TcLayout<128, 128, 64, true>::ALLOC : TcLayout<128, 128, 64, false>::ALLOC)
-                                   : (p.normalize ? TcLayout<64, 128, 64, true>::ALLOC : TcLayout<64, 128, 64, false>::ALLOC);
+    auto alloc = [&](auto d, auto dv) {
+        constexpr int D = decltype(d)::value, DV = decltype(dv)::value;
+        return p.normalize ? TcLayout<D, DV, 64, true>::ALLOC : TcLayout<D, DV, 64, false>::ALLOC;
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    info->smem_bytes = p.D == 128 ? alloc(I128{}, I128{}) : (p.dv == 128 ? alloc(I64{}, I128{}) : alloc(I64{}, I64{}));
     info->n_launches = 1;
     info->workspace_bytes = 0;
     return LA_OK;
@@ -725,7 +737,8 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
 int tc_launch(const Problem &p, int num_sms)
 {
     if (!tc_supported(p, num_sms)) return LA_ERR_UNSUPPORTED;
-    return p.D == 128 ? launch_d<128>(p) : launch_d<64>(p);
+    if (p.D == 128) return launch_d<128, 128>(p);
+    return p.dv == 128 ? launch_d<64, 128>(p) : launch_d<64, 64>(p);
 }
 
 }  // namespace la
