@@ -56,6 +56,22 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(dist, value, device="cpu"):
+    """The largest `value` over all ranks (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank_step, steps, max_ms):
+    """Whole-job units per second under weak scaling: every rank runs its own copy of the
+    workload, so the job processes world x units per step in the slowest rank's time."""
+    return world * units_per_rank_step * steps / (max_ms / 1e3)
+
+
 def workload_config(name, w, C):
     return {"workload": name, "B": w["B"], "H": w["H"], "L": w["L"], "dk": w["dk"],
             "dv": w["dv"], "C": C, "feature_map": w["fm"], "m": w["m"],
@@ -352,13 +368,10 @@ def run_ours(args):
     st = la.la_last_device_status(sptr)
     if st != la.LA_OK:
         raise la.LAError(st, "device status after the timed steps")
-    if dist:
-        tt = torch.tensor([t_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(dist, t_ms, "cuda")
 
     tokens_per_step = B * H * L
-    value = world * tokens_per_step * args.steps / (t_ms / 1e3)
+    value = job_throughput(world, tokens_per_step, args.steps, t_ms)
     ms_per_step = t_ms / args.steps
 
     # ---- end to end through the host-buffer entry point (copies inside the region)
@@ -389,12 +402,8 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        te = e0.elapsed_time(e1)
-        if dist:
-            tt = torch.tensor([te], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
-        e2e = {"value": world * tokens_per_step * n_e2e / (te / 1e3), "unit": "tokens/s",
+        te = max_over_ranks(dist, e0.elapsed_time(e1), "cuda")
+        e2e = {"value": job_throughput(world, tokens_per_step, n_e2e, te), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     if rank != 0:
