@@ -62,8 +62,17 @@ constexpr int TC_DEN = 4;  // ring of per-chunk 1/den vectors
 
 struct TcArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
-    int L, nch;  // nch: number of 64-row tiles
-    int nsub;    // number of chunks of CH rows
+    int L, nch;  // nch: number of 64-row tiles of a head
+    int nsub;    // number of chunks of CH rows of a head
+    // Sequence split: a head's tiles are cut into segments of seg_tiles tiles, one CTA each.
+    // The totals pass writes each segment's sum of phi(K)^T V (as S^T rows) and of phi(K);
+    // the main pass starts segment g from the sum of the totals of segments 0..g-1.
+    int seg_tiles;
+    int grid_seg;    // segments per head in this launch's grid
+    int totals;      // 1: totals pass
+    int BH;
+    float *ws_T;     // [segments-1][BH][dv][D]
+    float *ws_z;     // [segments-1][BH][D]
     int *err;
     unsigned long long timeout_ns;
     int debug_stall;  // test knob: the feature-map group never signals (forces a timeout)
@@ -188,8 +197,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     volatile int *abort_flag = (volatile int *)(sm + Lay::OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int head = blockIdx.x;
-    const int nch = a.nch;
+    const int head = blockIdx.x / a.grid_seg, seg = blockIdx.x % a.grid_seg;
+    const int tile0 = seg * a.seg_tiles;                 // first tile of this CTA
+    const int nch = min(a.seg_tiles, a.nch - tile0);     // tiles of this CTA
+    const bool totals = a.totals != 0;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
 
     auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
@@ -228,7 +239,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             const int kb = r / 64, row = C + (r % 64) / 8, chn = r % 8;
             *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
         }
-        for (int i = tid; i < D; i += TC_THREADS) zs[i] = 0.f;
+        for (int i = tid; i < D; i += TC_THREADS) {
+            float z0 = 0.f;
+            if (!totals)
+                for (int g = 0; g < seg; ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
+            zs[i] = z0;
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_async_smem();
@@ -238,13 +254,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB;
     if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
-        // the state and its bf16 copy start at zero (the first chunk's inter product is 0)
+        // the state and its bf16 copy start at the sum of the earlier segments' totals (zero
+        // for the first segment and for the totals pass)
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t zero[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+        const int jr = (DV == 128) ? 32 * (warp & 3) + lane : 16 * (warp & 3) + (lane & 15);
+        const bool live = (DV == 128) || lane < 16;
+        const int nprev = totals ? 0 : seg;
+#pragma unroll 1
+        for (int col = 0; col < D; col += 16) {
+            float acc[16];
 #pragma unroll
-        for (int col = 0; col < D; col += 16) tmem_st16(tS + lo + col, zero);
+            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+            if (live)
+                for (int g = 0; g < nprev; ++g) {
+                    const float4 *src = (const float4 *)(a.ws_T + (((size_t)g * a.BH + head) * DV + jr) * D + col);
 #pragma unroll
-        for (int col = 0; col < D / 2; col += 16) tmem_st16(tSB + lo + col, zero);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v4 = src[q];
+                        acc[4 * q] += v4.x; acc[4 * q + 1] += v4.y; acc[4 * q + 2] += v4.z; acc[4 * q + 3] += v4.w;
+                    }
+                }
+            uint32_t w32[16], w16[8];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w32[e] = __float_as_uint(acc[e]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w16[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+            tmem_st16(tS + lo + col, w32);
+            tmem_st8(tSB + lo + col / 2, w16);
+        }
         tmem_wait_st();
     }
     tc_fence_before();
@@ -259,13 +296,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const int s = c % TC_STAGES;
                 if (c >= TC_STAGES && !wait_phase(&stage_free[s], ((c / TC_STAGES) - 1) & 1, ctl))
                     break;
-                mbar_arrive_expect_tx(&full[s], Lay::STAGE_TX);
+                const int row = (tile0 + c) * C;
+                mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES : Lay::STAGE_TX);
                 for (int kb = 0; kb < D / 64; ++kb) {
-                    tma_load_3d(stage_q(s) + kb * C * 128, &a.tm_q, kb * 64, c * C, head, &full[s]);
-                    tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, c * C, head, &full[s]);
+                    if (!totals)
+                        tma_load_3d(stage_q(s) + kb * C * 128, &a.tm_q, kb * 64, row, head, &full[s]);
+                    tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &full[s]);
                 }
                 for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_load_3d(stage_v(s) + jb * C * 128, &a.tm_v, jb * 64, c * C, head, &full[s]);
+                    tma_load_3d(stage_v(s) + jb * C * 128, &a.tm_v, jb * 64, row, head, &full[s]);
                 issued = c + 1;
             }
             // never leave the CTA with loads in flight: wait for every issued stage to land
@@ -285,6 +324,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(DV, C, 1, 0);
             const int nsub = a.nsub;
             bool ok = true;
+            if (totals) {
+                // totals pass: only the state, over whole tiles
+                for (int c = 0; c < nch; ++c) {
+                    const int s = c % TC_STAGES;
+                    uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM) ? &full[s] : &phi_ready[s];
+                    if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_ss(tS, smem_desc(va + ks * 2048, C * 128, 1024),
+                               smem_desc(ka + ks * 2048, Lay::K_BLK, 1024), ID_STATE, 1);
+                    mma_commit(&stage_free[s]);
+                }
+                if (ok) mma_commit(state_done);
+                ok = false;  // skip the main loop
+            }
             for (int c = 0; ok && c < nch; ++c) {
                 const int s = c % TC_STAGES, b = c & 1;
                 uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM) ? &full[s] : &phi_ready[s];
@@ -304,9 +363,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 mma_commit(&scores_done[b]);
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 for (int j = 0; j < NSUB; ++j) {
-                    const int g = c * NSUB + j;  // chunk index in the sequence
+                    const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
+                    const int lg = c * NSUB + j;           // chunk index in this CTA
                     if (g >= nsub) break;
-                    if (g >= 1 && !wait_phase(s_ready, (g - 1) & 1, ctl)) {
+                    if (lg >= 1 && !wait_phase(s_ready, (lg - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -370,10 +430,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 uint4 wq[NR], wk[NR];
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
-                    if (FM != LA_FM_IDENTITY) wq[n] = qp[n * RG * 8];
+                    if (FM != LA_FM_IDENTITY && !totals) wq[n] = qp[n * RG * 8];
                     wk[n] = kp[n * RG * 8];
                 }
-                if (NORM && ft < 8 * (D / 64) * 2) {
+                if (NORM && !totals && ft < 8 * (D / 64) * 2) {
                     // z_c (before this chunk) as a bf16 hi/lo pair in key rows C and C+1
                     const int zkb = ft / 16, zr = (ft / 8) & 1, zch = ft & 7;
                     const float4 z0 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4];
@@ -390,7 +450,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     *(uint4 *)(stage_k(s) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                if (FM != LA_FM_IDENTITY) {
+                if (FM != LA_FM_IDENTITY && !totals) {
 #pragma unroll
                     for (int n = 0; n < NR; ++n) {
                         uint32_t *wv = (uint32_t *)&wq[n];
@@ -418,12 +478,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 if (FM != LA_FM_IDENTITY) {
 #pragma unroll
                     for (int n = 0; n < NR; ++n) {
-                        qp[n * RG * 8] = wq[n];
+                        if (!totals) qp[n * RG * 8] = wq[n];
                         kp[n * RG * 8] = wk[n];
                     }
                 }
                 fence_async_smem();
-                if (NORM && c + 1 < nch) {
+                const bool zupd = NORM && (c + 1 < nch || totals);
+                if (zupd) {
                     // column sums over the row groups: lanes g, g+G, ... of a warp, then the
                     // group's warps through shared memory
 #pragma unroll
@@ -438,7 +499,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
                 named_bar(1, NF);
                 if (ft == 0 && !a.debug_stall) mbar_arrive(&phi_ready[s]);
-                if (NORM && c + 1 < nch) {
+                if (zupd) {
                     for (int i = ft; i < D; i += NF) {
                         float acc = 0.f;
 #pragma unroll
@@ -448,6 +509,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     named_bar(1, NF);
                 }
             }
+            if (totals && NORM)
+                for (int i = ft; i < D; i += NF) a.ws_z[((size_t)seg * a.BH + head) * D + i] = zs[i];
         }
     } else if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
         // ------------------------------------------------------------ scores -> P, S readback
@@ -456,7 +519,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const int t = 16 * q4 + (lane & 15);  // M = 64 TMEM layout: row t at lane t%16 of quadrant t/16
         const bool row_lane = lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        for (int c = 0; c < nch; ++c) {
+        if (totals) {
+            // this segment's total: S^T rows (fp32) to the workspace
+            const int jr = (DV == 128) ? 32 * q4 + lane : 16 * q4 + (lane & 15);
+            const bool live = (DV == 128) || lane < 16;
+            if (group_wait(pt == 0, 2, state_done, 0, nullptr, 0, false, ctl)) {
+                tc_fence_after();
+                float *dst = a.ws_T + (((size_t)seg * a.BH + head) * DV + jr) * D;
+#pragma unroll 1
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    uint32_t sv[32];
+                    tmem_ld32(tS + lane_off + cb * 32, sv);
+                    tmem_wait_ld();
+                    if (live) {
+                        float4 *d4 = (float4 *)(dst + cb * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                                                __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+                    }
+                }
+            }
+        }
+        for (int c = 0; c < nch && !totals; ++c) {
             const int b = c & 1, slot = c % TC_DEN;
             if (!group_wait(pt == 0, 2, &scores_done[b], (c >> 1) & 1, &den_empty[slot],
                             ((c / TC_DEN) - 1) & 1, NORM && c >= TC_DEN, ctl))
@@ -518,9 +603,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // bf16 copy of the state for each next chunk's inter product
             bool rb_ok = true;
             for (int j = 0; j < NSUB; ++j) {
-                const int g = c * NSUB + j;
+                const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
+                const int lg = c * NSUB + j;           // chunk index in this CTA
                 if (g + 1 >= a.nsub) break;  // no state update after the last chunk
-                if (!group_wait(pt == 0, 2, state_done, g & 1, nullptr, 0, false, ctl)) {
+                if (!group_wait(pt == 0, 2, state_done, lg & 1, nullptr, 0, false, ctl)) {
                     rb_ok = false;
                     break;
                 }
@@ -553,7 +639,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const bool odd = lane & 1;
         uint8_t *const ob = o_tile + (j >> 6) * C * 128 + (((j & 7) & ~1) << 1);
         const int jc = (j & 63) >> 3;
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 0; c < nch && !totals; ++c) {
             const int b = c & 1, slot = c % TC_DEN;
             if (!group_wait(ot == 0, 3, &o_done[b], (c >> 1) & 1, &den_full[slot], (c / TC_DEN) & 1,
                             NORM, ctl))
@@ -601,7 +687,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             named_bar(3, 128);
             if (ot == 0) {
                 for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, c * C, head);
+                    tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, (tile0 + c) * C, head);
                 tma_commit_group();
                 if (NORM) mbar_arrive(&den_empty[slot]);
             }
@@ -654,8 +740,26 @@ bool make_map(CUtensorMap *m, const void *ptr, int BH, int L, int d, int C)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Segments per head: split the sequence when the heads alone leave most SMs idle, keeping
+// at least 4 tiles (256 rows) per segment.
+int tc_segments(const Problem &p, int num_sms, int *seg_tiles)
+{
+    const int BH = p.B * p.H, tiles = (p.L + 63) / 64;
+    int g = 1;
+    if (BH < num_sms / 2) g = max(1, min(num_sms / BH, tiles / 4));
+    const int st = (tiles + g - 1) / g;
+    if (seg_tiles) *seg_tiles = st;
+    return (tiles + st - 1) / st;
+}
+
+size_t tc_workspace(const Problem &p, int nseg)
+{
+    if (nseg <= 1) return 0;
+    return (size_t)(nseg - 1) * p.B * p.H * ((size_t)p.dv * p.D + p.D) * sizeof(float);
+}
+
 template <int D, int DV, int CH, int FM, bool NORM>
-int launch_t(const Problem &p)
+int launch_t(const Problem &p, int num_sms)
 {
     constexpr int C = 64;  // rows per tile
     using Lay = TcLayout<D, DV, C, NORM>;
@@ -668,6 +772,13 @@ int launch_t(const Problem &p)
     a.L = p.L;
     a.nch = (p.L + C - 1) / C;
     a.nsub = (p.L + CH - 1) / CH;
+    const int nseg = tc_segments(p, num_sms, &a.seg_tiles);
+    a.BH = BH;
+    if (nseg > 1) {
+        if (!p.workspace || p.workspace_bytes < tc_workspace(p, nseg)) return LA_ERR_WORKSPACE;
+        a.ws_T = (float *)p.workspace;
+        a.ws_z = a.ws_T + (size_t)(nseg - 1) * BH * DV * D;
+    }
     a.err = p.err;
     a.timeout_ns = 2000000000ull;
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");
@@ -678,26 +789,35 @@ int launch_t(const Problem &p)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
         cudaSuccess)
         return LA_ERR_CUDA;
-    kern<<<BH, TC_THREADS, Lay::ALLOC, p.stream>>>(a);
+    if (nseg > 1) {
+        // totals of segments 0..nseg-2, then the main pass over all segments
+        a.totals = 1;
+        a.grid_seg = nseg - 1;
+        kern<<<BH * (nseg - 1), TC_THREADS, Lay::ALLOC, p.stream>>>(a);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    }
+    a.totals = 0;
+    a.grid_seg = nseg;
+    kern<<<BH * nseg, TC_THREADS, Lay::ALLOC, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
 template <int D, int DV, int CH>
-int launch_dc(const Problem &p)
+int launch_dc(const Problem &p, int sms)
 {
     const bool n = p.normalize != 0;
     if (p.fm == LA_FM_IDENTITY)
-        return n ? launch_t<D, DV, CH, LA_FM_IDENTITY, true>(p)
-                 : launch_t<D, DV, CH, LA_FM_IDENTITY, false>(p);
-    return n ? launch_t<D, DV, CH, LA_FM_ELU1, true>(p) : launch_t<D, DV, CH, LA_FM_ELU1, false>(p);
+        return n ? launch_t<D, DV, CH, LA_FM_IDENTITY, true>(p, sms)
+                 : launch_t<D, DV, CH, LA_FM_IDENTITY, false>(p, sms);
+    return n ? launch_t<D, DV, CH, LA_FM_ELU1, true>(p, sms) : launch_t<D, DV, CH, LA_FM_ELU1, false>(p, sms);
 }
 
 template <int D, int DV>
-int launch_d(const Problem &p)
+int launch_d(const Problem &p, int sms)
 {
-    if (p.C == 16) return launch_dc<D, DV, 16>(p);
-    if (p.C == 32) return launch_dc<D, DV, 32>(p);
-    return launch_dc<D, DV, 64>(p);
+    if (p.C == 16) return launch_dc<D, DV, 16>(p, sms);
+    if (p.C == 32) return launch_dc<D, DV, 32>(p, sms);
+    return launch_dc<D, DV, 64>(p, sms);
 }
 
 }  // namespace
@@ -718,8 +838,9 @@ bool tc_supported(const Problem &p, int num_sms)
 
 int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
 {
-    (void)num_sms;
-    info->grid_x = p.B * p.H;
+    int seg_tiles = 0;
+    const int nseg = tc_segments(p, num_sms, &seg_tiles);
+    info->grid_x = p.B * p.H * nseg;
     info->grid_y = 1;
     info->block = TC_THREADS;
     auto alloc = [&](auto d, auto dv) {
@@ -729,16 +850,16 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;
     info->smem_bytes = p.D == 128 ? alloc(I128{}, I128{}) : (p.dv == 128 ? alloc(I64{}, I128{}) : alloc(I64{}, I64{}));
-    info->n_launches = 1;
-    info->workspace_bytes = 0;
+    info->n_launches = nseg > 1 ? 2 : 1;
+    info->workspace_bytes = tc_workspace(p, nseg);
     return LA_OK;
 }
 
 int tc_launch(const Problem &p, int num_sms)
 {
     if (!tc_supported(p, num_sms)) return LA_ERR_UNSUPPORTED;
-    if (p.D == 128) return launch_d<128, 128>(p);
-    return p.dv == 128 ? launch_d<64, 128>(p) : launch_d<64, 64>(p);
+    if (p.D == 128) return launch_d<128, 128>(p, num_sms);
+    return p.dv == 128 ? launch_d<64, 128>(p, num_sms) : launch_d<64, 64>(p, num_sms);
 }
 
 }  // namespace la
