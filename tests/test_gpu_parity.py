@@ -72,6 +72,9 @@ SMALL = [
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 128),
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777), 256),
     ("favor-m256-d64-L16384", dict(B=1, H=2, L=600), 64),
+    ("favor-m256-d64-L16384", dict(B=1, H=1, L=777, normalize=False), 64),
+    # few heads: the tensor-core path splits each sequence into segments
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=4096), 64),
     ("loglinear-d64-L65536", dict(B=1, H=2, L=1000), 64),
     ("loglinear-d64-L65536", dict(B=1, H=1, L=300), 16),
     ("loglinear-d64-L65536", dict(B=1, H=1, L=200), 1),
