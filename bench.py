@@ -98,11 +98,17 @@ def flops_per_token(w, C):
     return f
 
 
-def kernel_sha1():
+def kernel_sha1(feature_map="elu1"):
+    """Hash of the tensor-core kernel source that serves `feature_map` (plus the shared
+    headers): a committed DRAM-traffic figure is only used while this is unchanged."""
     import hashlib
     d = os.path.join(ROOT, "chunkwise_causal_linear_gb300", "csrc")
-    return hashlib.sha1(open(os.path.join(d, "tc.cu"), "rb").read() +
-                        open(os.path.join(d, "tc_ptx.cuh"), "rb").read()).hexdigest()
+    main = "tc_favor.cu" if feature_map == "favor" else "tc.cu"
+    h = hashlib.sha1()
+    for name in (main, "tc_ptx.cuh", "tc_common.cuh"):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def ncu_traffic(workload, C, path, B, H):
@@ -114,7 +120,7 @@ def ncu_traffic(workload, C, path, B, H):
     except Exception:
         return None
     w = synth.WORKLOADS[workload]
-    if not rec or rec.get("kernel_sha1") != kernel_sha1() or (B, H) != (w["B"], w["H"]):
+    if not rec or rec.get("kernel_sha1") != kernel_sha1(w["fm"]) or (B, H) != (w["B"], w["H"]):
         return None
     return rec["bytes_per_launch"]
 

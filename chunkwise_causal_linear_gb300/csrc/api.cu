@@ -156,6 +156,12 @@ static int run(const void *q, const void *k, const void *v, void *out, int B, in
     la_plan_info info;
     rc = plan_problem(p, ll, path, sms, &info);
     if (rc != LA_OK) return rc;
+    // the tensor-core log-linear kernel copies lambda rows in bulk (16-byte aligned)
+    if (info.path == LA_PATH_TC && ll && ((uintptr_t)lam & 15) != 0) {
+        if (path != LA_PATH_AUTO) return LA_ERR_UNSUPPORTED;
+        rc = plan_problem(p, ll, LA_PATH_SIMT, sms, &info);
+        if (rc != LA_OK) return rc;
+    }
     if (info.workspace_bytes > 0 && (!ws || ws_bytes < info.workspace_bytes))
         return LA_ERR_WORKSPACE;
     p.q = q; p.k = k; p.v = v; p.out = out;

@@ -133,6 +133,15 @@ LA_DEV void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, 
                  "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
+// plain bulk copy global -> shared (both addresses and the size multiples of 16 bytes)
+LA_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 LA_DEV void tma_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LA_DEV void tma_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 LA_DEV void tma_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

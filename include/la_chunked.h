@@ -111,7 +111,16 @@ int la_chunked_fwd(const void *q, const void *k, const void *v, void *out,
                    int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* As la_chunked_fwd, with an explicit execution path (enum la_path).  LA_PATH_TC returns
- * LA_ERR_UNSUPPORTED for shapes the tensor-core path does not cover. */
+ * LA_ERR_UNSUPPORTED for shapes the tensor-core path does not cover.  It covers bf16
+ * storage, L >= 128, and:
+ *   - identity / elu+1 features, with or without the normaliser, dk = D, (dk, dv) in
+ *     {(64, 64), (64, 128), (128, 128)}, C in {16, 32, 64};
+ *   - FAVOR+ features, dk = 64, m = 256, dv = 64, C = 64, with or without the normaliser;
+ *   - the log-linear mask: identity features, no normaliser, dk = dv = 64, C = 64, at most
+ *     4096 chunks, num_levels <= 32, L * num_levels a multiple of 4 and level_weights
+ *     16-byte aligned (LA_PATH_AUTO falls back to LA_PATH_SIMT when it is not).
+ * Few-head problems are split along the sequence into segments; their plan reports two
+ * launches and a workspace for the segment totals. */
 int la_chunked_fwd_path(const void *q, const void *k, const void *v, void *out,
                         int B, int H, int L, int dk, int dv, int C,
                         const la_feature_map *feature_map, int normalize,

@@ -76,6 +76,9 @@ SMALL = [
     # few heads: the tensor-core path splits each sequence into segments
     ("favor-m256-d64-L16384", dict(B=1, H=2, L=4096), 64),
     ("loglinear-d64-L65536", dict(B=1, H=2, L=1000), 64),
+    # few heads: the tensor-core path splits the sequence; ragged last chunk
+    ("loglinear-d64-L65536", dict(B=1, H=3, L=4096), 64),
+    ("loglinear-d64-L65536", dict(B=2, H=2, L=2000), 64),
     ("loglinear-d64-L65536", dict(B=1, H=1, L=300), 16),
     ("loglinear-d64-L65536", dict(B=1, H=1, L=200), 1),
     ("elu1-norm-d128-L8192", dict(B=1, H=1, L=1, ), 64),
@@ -95,12 +98,13 @@ def test_small_workloads_match_oracle(base, over, C):
         assert_close(out, ref, f"{base} {over} C={C} path={path}")
 
 
-def test_loglinear_all_ones_equals_plain():
+@pytest.mark.parametrize("path", [SIMT, TC])
+def test_loglinear_all_ones_equals_plain(path):
     """Slide 17 of the log-linear deck: lambda == 1 gives linear attention."""
     w = workload("loglinear-d64-L65536", B=1, H=2, L=500)
     inp = synth.make_inputs(w, seed=4)
     inp["lam"] = np.ones_like(inp["lam"])
-    out_ll, _ = run_gpu(w, inp, 64, SIMT)
+    out_ll, _ = run_gpu(w, inp, 64, path)
     wp = dict(w, loglinear=False)
     inp_p = dict(inp, lam=None)
     out_p, _ = run_gpu(wp, inp_p, 64, SIMT)
