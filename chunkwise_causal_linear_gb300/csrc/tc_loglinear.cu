@@ -20,14 +20,17 @@
 // The fp32 snapshots PS(x) at the binary prefixes x of the current position form a stack
 // (depth = popcount(x)) kept in the workspace, where it stays in L2.
 //
-// Per chunk (all MMAs M = 64, N = 64, K = 64 as 4 x K16; bf16 in, fp32 accumulate):
-//   scores  A   = Q K^T                      (A K-major, B K-major)
-//   state   PS += K^T V                      (A = K MN-major, B = V MN-major)
-//   inter   O  += (lambda^(7+j) . Q) T_j     per set bit j (A K-major from a ring, B MN-major)
-//   intra   O  += P V,  P = lambda-masked A  (A K-major, B = V MN-major)
-// Warps: 0 TMA producer, 1 MMA issuer, 2-3 write the lambda-scaled copies of Q into a ring
-// of 4 tiles, 4-7 turn scores into P, 8-11 close the Fenwick blocks, 12-15 store output
-// rows.  A group of four consecutive warps covers the four TMEM lane quadrants (warp % 4).
+// Per chunk (all MMAs M = 64 rows, K = 64 as 4 x K16; bf16 in, fp32 accumulate):
+//   scores  A   = Q K^T                 (A K-major, B K-major)
+//   state   PS += K^T V                 (A = K MN-major, B = V MN-major)
+//   intra   O   = P V,  P = lambda-masked A
+//   levels  R_j = Q T_j                 per set bit j
+// Both kinds of product go, in that order, through one ring of 6 TMEM slots, and the output
+// rows o_t = O[t] + sum_j lambda_t^(7+j) R_j[t] are formed in fp32 by the output warps, so
+// the level weights never pass through a bf16 operand.
+// Warps: 0 TMA producer, 1 MMA issuer, 4-7 turn scores into P, 8-11 close the Fenwick
+// blocks, 12-15 combine and store the output rows.  A group of four consecutive warps
+// covers the four TMEM lane quadrants (warp % 4).
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -43,32 +46,34 @@ using namespace tcc;
 namespace {
 
 constexpr int LL_THREADS = 512;  // 16 warps
-constexpr int LL_STAGES = 2;
 constexpr int LL_D = 64, LL_C = 64, LL_LOG2C = 6;
-constexpr int LL_RING = 4;
-constexpr int LL_MAXLEV = 12;   // inter levels: up to 4096 chunks per head
-constexpr int LL_MAXNL = 32;    // lambda entries per row held in shared memory
+constexpr int LL_RING = 6;       // TMEM slots for the products P V and R_j
+constexpr int LL_MAXLEV = 12;    // inter levels: up to 4096 chunks per head
+constexpr int LL_MAXNL = 32;     // lambda entries per row held in shared memory
 constexpr int LL_TILE = LL_C * 128;
-constexpr int LL_LAMBUF = LL_C * LL_MAXNL * 4;            // 8 KB
-constexpr int LL_STAGE_BYTES = 3 * LL_TILE + LL_LAMBUF;   // Q, K, V, lambda
-constexpr int LL_N_BAR = 2 * LL_STAGES + 2 * LL_RING + 12;
+constexpr int LL_STAGES_MAIN = 3;   // Q, K, V, lambda (32 KB each)
+constexpr int LL_STAGES_TOT = 6;    // K, V (16 KB each)
+constexpr int LL_STAGE_AREA = LL_STAGES_MAIN * 4 * LL_TILE;
+static_assert(LL_STAGES_TOT * 2 * LL_TILE <= LL_STAGE_AREA, "stage area");
+static_assert(LL_C * LL_MAXNL * 4 <= LL_TILE, "lambda tile");
+constexpr int LL_N_BAR = 2 * LL_STAGES_TOT + 2 * LL_RING + 16;
 
 // TMEM columns (M = 64 layout: row m at lane (m % 16) + 32 (m / 16))
 constexpr uint32_t LT_PS = 0;     // running segment state PS [d_k rows][d_v]
 constexpr uint32_t LT_A = 64;     // scores
-constexpr uint32_t LT_O = 128;    // output, two buffers of 64 columns
+constexpr uint32_t LT_R = 128;    // products P V and R_j, LL_RING slots of 64 columns
+static_assert(LT_R + 64 * LL_RING <= 512, "TMEM columns");
 
 struct LlLayout {
-    int off_T, off_ring, off_P, off_bar, bytes, alloc;
+    int off_T, off_P, off_bar, bytes, alloc;
 };
 
 inline LlLayout ll_layout(int nlev)
 {
     LlLayout l;
-    l.off_T = LL_STAGES * LL_STAGE_BYTES;
-    l.off_ring = l.off_T + nlev * LL_TILE;
-    l.off_P = l.off_ring + LL_RING * LL_TILE;
-    l.off_bar = l.off_P + LL_TILE;
+    l.off_T = LL_STAGE_AREA;
+    l.off_P = l.off_T + nlev * LL_TILE;   // two P tiles (chunk parity)
+    l.off_bar = l.off_P + 2 * LL_TILE;
     l.bytes = l.off_bar + LL_N_BAR * 8 + 16;
     l.alloc = l.bytes + 1024;
     return l;
@@ -93,19 +98,20 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = (uint64_t *)(sm + a.lay.off_bar);
-    uint64_t *full = bars;                        // [STAGES]
-    uint64_t *stage_free = full + LL_STAGES;      // [STAGES]
-    uint64_t *ring_full = stage_free + LL_STAGES; // [RING]
-    uint64_t *ring_free = ring_full + LL_RING;    // [RING]
-    uint64_t *scores_done = ring_free + LL_RING;
+    uint64_t *full = bars;                           // [stages]
+    uint64_t *stage_free = full + LL_STAGES_TOT;     // [stages]
+    uint64_t *r_full = stage_free + LL_STAGES_TOT;   // [RING]
+    uint64_t *r_free = r_full + LL_RING;             // [RING]
+    uint64_t *scores_done = r_free + LL_RING;
     uint64_t *a_free = scores_done + 1;
-    uint64_t *p_ready = a_free + 1;
-    uint64_t *state_done = p_ready + 1;
-    uint64_t *ps_read = state_done + 1;           // PS copied out by the block-closing group
-    uint64_t *t_formed = ps_read + 1;             // the block closed after a chunk is in smem
-    uint64_t *o_done = t_formed + 1;              // [2]
-    uint64_t *o_free = o_done + 2;                // [2]
-    uint64_t *drain = o_free + 2;
+    // p_ready and t_formed alternate by chunk parity: their producers may finish chunk i + 1
+    // before the MMA issuer waits for chunk i, and one barrier would then be two phases ahead
+    uint64_t *p_ready = a_free + 1;                  // [2]
+    uint64_t *state_done = p_ready + 2;
+    uint64_t *ps_read = state_done + 1;              // PS copied out by the block-closing warps
+    uint64_t *t_formed = ps_read + 1;                // [2] the block closed after a chunk is in smem
+    uint64_t *c_done = t_formed + 2;                 // [2] every product of a chunk is in TMEM
+    uint64_t *drain = c_done + 2;
     uint64_t *totals_done = drain + 1;
     uint32_t *tmem_slot = (uint32_t *)(sm + a.lay.off_bar + LL_N_BAR * 8);
     volatile int *abort_flag = (volatile int *)(sm + a.lay.off_bar + LL_N_BAR * 8 + 4);
@@ -116,39 +122,41 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     const int nloc = min(a.seg_chunks, a.nch - tile0);  // chunks in this segment
     const bool totals = a.totals != 0;
     const int NL = a.NL;
+    const int nst = totals ? LL_STAGES_TOT : LL_STAGES_MAIN;
+    const int sbytes = totals ? 2 * LL_TILE : 4 * LL_TILE;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
-    auto stage_q = [&](int s) { return sm + s * LL_STAGE_BYTES; };
-    auto stage_k = [&](int s) { return stage_q(s) + LL_TILE; };
-    auto stage_v = [&](int s) { return stage_q(s) + 2 * LL_TILE; };
-    auto stage_l = [&](int s) { return (const float *)(stage_q(s) + 3 * LL_TILE); };
+    // stage layout: main [Q | K | V | lambda], totals [K | V]
+    auto stage_q = [&](int s) { return sm + s * sbytes; };
+    auto stage_k = [&](int s) { return sm + s * sbytes + (totals ? 0 : LL_TILE); };
+    auto stage_v = [&](int s) { return stage_k(s) + LL_TILE; };
+    auto stage_l = [&](int s) { return (const float *)(sm + s * sbytes + 3 * LL_TILE); };
     auto tbuf = [&](int j) { return sm + a.lay.off_T + j * LL_TILE; };
-    auto ring = [&](int r) { return sm + a.lay.off_ring + r * LL_TILE; };
 
     if (tid == 0) {
-        for (int i = 0; i < LL_STAGES; ++i) {
+        for (int i = 0; i < nst; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&stage_free[i], 1);
+            mbar_init(&stage_free[i], totals ? 1 : 2);  // MMA commit (+ output warps, main)
         }
         for (int i = 0; i < LL_RING; ++i) {
-            mbar_init(&ring_full[i], 1);
-            mbar_init(&ring_free[i], 1);
+            mbar_init(&r_full[i], 1);
+            mbar_init(&r_free[i], 4);
         }
         mbar_init(scores_done, 1);
         mbar_init(a_free, 4);
-        mbar_init(p_ready, 1);
+        mbar_init(&p_ready[0], 1);
+        mbar_init(&p_ready[1], 1);
         mbar_init(state_done, 1);
         mbar_init(ps_read, 4);
-        mbar_init(t_formed, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&o_done[i], 1);
-            mbar_init(&o_free[i], 4);
-        }
+        mbar_init(&t_formed[0], 1);
+        mbar_init(&t_formed[1], 1);
+        mbar_init(&c_done[0], 1);
+        mbar_init(&c_done[1], 1);
         mbar_init(drain, 1);
         mbar_init(totals_done, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
 
     // ---- fixed levels j >= p: sums of whole earlier segments (main pass) ----
     if (!totals && warp >= 8 && warp < 12) {
@@ -187,10 +195,9 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, s = 0, ph = 0;
             for (int i = 0; i < nloc; ++i) {
-                const int s = i % LL_STAGES;
-                if (i >= LL_STAGES && !wait_phase(&stage_free[s], ((i / LL_STAGES) - 1) & 1, ctl)) break;
+                if (i >= nst && !wait_phase(&stage_free[s], ph ^ 1, ctl)) break;
                 const int row = (tile0 + i) * LL_C;
                 const int rows = min(LL_C, a.L - row);
                 const uint32_t lam_bytes = totals ? 0u : (uint32_t)(rows * NL * 4);
@@ -202,129 +209,113 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 tma_load_3d(stage_k(s), &a.tm_k, 0, row, head, &full[s]);
                 tma_load_3d(stage_v(s), &a.tm_v, 0, row, head, &full[s]);
                 issued = i + 1;
+                if (++s == nst) { s = 0; ph ^= 1; }
             }
-            for (int i = (issued > LL_STAGES ? issued - LL_STAGES : 0); i < issued; ++i) {
+            for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) {
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_sleep(&full[i % LL_STAGES], (i / LL_STAGES) & 1, 200000u))
+                while (!mbar_try_sleep(&full[i % nst], (i / nst) & 1, 200000u))
                     if (globaltimer() - t0 > ctl.timeout_ns) break;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Main pass, software-pipelined by one chunk: iteration i issues the scores and the
+        // state update of chunk i + 1 before the level products and P V of chunk i, so the
+        // P and block-closing warps work a chunk ahead of the output warps.
         if (lane == 0) {
             constexpr uint32_t ID_SC = idesc_bf16_f32(64, 64, 0, 0);
             constexpr uint32_t ID_ST = idesc_bf16_f32(64, 64, 1, 1);
             constexpr uint32_t ID_AB = idesc_bf16_f32(64, 64, 0, 1);
-            const uint32_t pa = smem_u32(sm + a.lay.off_P);
-            int kq = 0;  // ring uses so far
-            for (int i = 0; i < nloc; ++i) {
-                const int s = i % LL_STAGES, b = i & 1;
-                if (!wait_phase(&full[s], (i / LL_STAGES) & 1, ctl)) break;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
-                if (!totals) {
-                    if (i >= 1 && !wait_phase(a_free, (i - 1) & 1, ctl)) break;
+            const uint64_t dP0 = smem_desc(smem_u32(sm + a.lay.off_P), 16, 1024);
+            const uint64_t dT0 = smem_desc(smem_u32(tbuf(0)), LL_TILE, 1024);
+            // descriptor start addresses advance 16 bytes per unit: +2 is one K16 step of a
+            // K-major tile (32 bytes), +128 one of an MN-major tile (2048 bytes)
+            auto dK_k = [&](int s) { return smem_desc(smem_u32(stage_k(s)), 16, 1024); };
+            auto dK_m = [&](int s) { return smem_desc(smem_u32(stage_k(s)), LL_TILE, 1024); };
+            auto dV_m = [&](int s) { return smem_desc(smem_u32(stage_v(s)), LL_TILE, 1024); };
+            auto dQ_k = [&](int s) { return smem_desc(smem_u32(stage_q(s)), 16, 1024); };
+            bool ok = true;
+            if (totals) {
+                int s = 0, ph = 0;
+                for (int i = 0; i < nloc && ok; ++i) {
+                    if (!wait_phase(&full[s], ph, ctl)) { ok = false; break; }
                     tc_fence_after();
+                    const uint64_t dKm = dK_m(s), dVm = dV_m(s);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tmem + LT_A, smem_desc(qa + ks * 32, 16, 1024), smem_desc(ka + ks * 32, 16, 1024),
-                               ID_SC, ks > 0);
-                    mma_commit(scores_done);
-                    if (i >= 1 && !wait_phase(ps_read, (i - 1) & 1, ctl)) break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tmem + LT_PS, smem_desc(ka + ks * 2048, LL_TILE, 1024),
-                           smem_desc(va + ks * 2048, LL_TILE, 1024), ID_ST, (i > 0) || (ks > 0));
-                if (totals) {
+                        mma_ss(tmem + LT_PS, dKm + 128 * ks, dVm + 128 * ks, ID_ST, (i > 0) || (ks > 0));
                     mma_commit(&stage_free[s]);
-                    continue;
+                    if (++s == nst) { s = 0; ph ^= 1; }
                 }
-                mma_commit(state_done);
-                if (i >= 1 && !wait_phase(t_formed, (i - 1) & 1, ctl)) break;
-                if (i >= 2 && !wait_phase(&o_free[b], ((i >> 1) - 1) & 1, ctl)) break;
-                tc_fence_after();
-                const uint32_t tO = tmem + LT_O + 64 * b;
-                const int c = tile0 + i;
-                bool first = true, ok = true;
-                for (int j = 0; j < a.nlev; ++j) {
-                    if (!((c >> j) & 1)) continue;
-                    const int slot = kq % LL_RING;
-                    if (!wait_phase(&ring_full[slot], (kq / LL_RING) & 1, ctl)) { ok = false; break; }
+                mma_commit(totals_done);
+            } else {
+                // scores and state of chunk i (stage sl, phase pl)
+                auto front = [&](int i, int sl, int pl) -> bool {
+                    if (!wait_phase(&full[sl], pl, ctl)) return false;
                     tc_fence_after();
-                    const uint32_t ra = smem_u32(ring(slot)), tb = smem_u32(tbuf(j));
+                    const uint64_t dQ = dQ_k(sl), dKk = dK_k(sl), dKm = dK_m(sl), dVm = dV_m(sl);
+                    if (i >= 1 && !wait_phase(a_free, (i - 1) & 1, ctl)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) mma_ss(tmem + LT_A, dQ + 2 * ks, dKk + 2 * ks, ID_SC, ks > 0);
+                    mma_commit(scores_done);
+                    if (i >= 1 && !wait_phase(ps_read, (i - 1) & 1, ctl)) return false;
+                    tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tO, smem_desc(ra + ks * 32, 16, 1024), smem_desc(tb + ks * 2048, LL_TILE, 1024),
-                               ID_AB, (!first) || (ks > 0));
-                    mma_commit(&ring_free[slot]);
-                    ++kq;
-                    first = false;
-                }
-                if (!ok) break;
-                if (!wait_phase(p_ready, i & 1, ctl)) break;
-                tc_fence_after();
+                        mma_ss(tmem + LT_PS, dKm + 128 * ks, dVm + 128 * ks, ID_ST, (i > 0) || (ks > 0));
+                    mma_commit(state_done);
+                    return true;
+                };
+                int s = 0;                           // stage of chunk i
+                int s1 = 1 % nst, ph1 = (1 == nst) ? 1 : 0;  // stage of chunk i + 1
+                int kr = 0, slot = 0, rph = 0;       // ring uses so far, next slot and its phase
+                // one product into the next ring slot: 4 x K16 MMAs
+                auto product = [&](uint64_t dA, uint64_t dB) -> bool {
+                    if (kr >= LL_RING && !wait_phase(&r_free[slot], rph ^ 1, ctl)) return false;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tO, smem_desc(pa + ks * 32, 16, 1024), smem_desc(va + ks * 2048, LL_TILE, 1024), ID_AB,
-                           (!first) || (ks > 0));
-                mma_commit(&o_done[b]);
-                mma_commit(&stage_free[s]);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(tmem + LT_R + 64 * slot, dA + 2 * ks, dB + 128 * ks, ID_AB, ks > 0);
+                    mma_commit(&r_full[slot]);
+                    ++kr;
+                    if (++slot == LL_RING) { slot = 0; rph ^= 1; }
+                    return true;
+                };
+                ok = front(0, 0, 0);
+                for (int i = 0; i < nloc && ok; ++i) {
+                    const int b = i & 1;
+                    if (i + 1 < nloc && !front(i + 1, s1, ph1)) { ok = false; break; }
+                    const uint64_t dQ = dQ_k(s), dVm = dV_m(s);
+                    // P V first: its P was written a chunk ahead
+                    if (!wait_phase(&p_ready[b], (i >> 1) & 1, ctl)) { ok = false; break; }
+                    if (!product(dP0 + (uint64_t)(b * (LL_TILE >> 4)), dVm)) { ok = false; break; }
+                    if (i >= 1 && !wait_phase(&t_formed[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl)) { ok = false; break; }
+                    // set bits of the chunk index, lowest first (one product each)
+                    for (uint32_t bits = (uint32_t)(tile0 + i) & ((1u << a.nlev) - 1u); bits && ok; bits &= bits - 1u)
+                        ok = product(dQ, dT0 + (uint64_t)((__ffs(bits) - 1) * (LL_TILE >> 4)));
+                    if (!ok) break;
+                    mma_commit(&c_done[b]);
+                    mma_commit(&stage_free[s]);
+                    s = s1;
+                    if (++s1 == nst) { s1 = 0; ph1 ^= 1; }
+                }
             }
-            if (totals) mma_commit(totals_done);
             mma_commit(drain);
             const uint64_t t0 = globaltimer();
             while (!mbar_try_sleep(drain, 0, 200000u))
                 if (globaltimer() - t0 > ctl.timeout_ns) break;
         }
-    } else if (warp >= 2 && warp < 4 && !totals) {
-        // ------------------------------------------------------------ lambda-scaled copies of Q
-        const int st = tid - 64, t = st;  // one row per thread
-        int kq = 0;
-        for (int i = 0; i < nloc; ++i) {
-            const int c = tile0 + i, s = i % LL_STAGES;
-            if (c == 0) continue;  // chunk 0 has no earlier blocks
-            if (!group_wait(st == 0, 5, &full[s], (i / LL_STAGES) & 1, nullptr, 0, false, ctl, 64)) break;
-            const bool valid = c * LL_C + t < a.L;
-            const uint8_t *qrow = stage_q(s) + t * 128;
-            const float *lrow = stage_l(s) + t * NL;
-            bool ok = true;
-            for (int j = 0; j < a.nlev; ++j) {
-                if (!((c >> j) & 1)) continue;
-                const int slot = kq % LL_RING;
-                if (kq >= LL_RING &&
-                    !group_wait(st == 0, 5, &ring_free[slot], ((kq / LL_RING) - 1) & 1, nullptr, 0, false, ctl, 64)) {
-                    ok = false;
-                    break;
-                }
-                const float w = valid ? lrow[1 + LL_LOG2C + j] : 0.f;
-                uint8_t *dst = ring(slot) + t * 128;
-#pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    const int off = (ck ^ (t & 7)) << 4;
-                    const uint4 x = *(const uint4 *)(qrow + off);
-                    *(uint4 *)(dst + off) = make_uint4(pack_bf16x2(bf_lo(x.x) * w, bf_hi(x.x) * w),
-                                                       pack_bf16x2(bf_lo(x.y) * w, bf_hi(x.y) * w),
-                                                       pack_bf16x2(bf_lo(x.z) * w, bf_hi(x.z) * w),
-                                                       pack_bf16x2(bf_lo(x.w) * w, bf_hi(x.w) * w));
-                }
-                fence_async_smem();
-                named_bar(5, 64);
-                if (st == 0) mbar_arrive(&ring_full[slot]);
-                ++kq;
-            }
-            if (!ok) break;
-        }
     } else if (warp >= 4 && warp < 8 && !totals) {
         // ------------------------------------------------------------ scores -> P (intra mask)
         const int q4 = warp & 3, pt = tid - 128;
         const int t = 16 * q4 + (lane & 15);
+        const int t8 = t >> 3, t7 = t & 7;
         const bool row_lane = lane < 16;
         const uint32_t tA = tmem + LT_A + ((uint32_t)(32 * q4) << 16);
+        int s = 0, ph = 0;
         for (int i = 0; i < nloc; ++i) {
-            const int s = i % LL_STAGES;
-            if (!group_wait(pt == 0, 2, scores_done, i & 1, &full[s], (i / LL_STAGES) & 1, true, ctl)) break;
+            if (!group_wait(pt == 0, 2, scores_done, i & 1, &full[s], ph, true, ctl)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tA, r0);
@@ -334,27 +325,45 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
             __syncwarp();
             if (lane == 0) mbar_arrive(a_free);
             if (row_lane) {
+                // lambda_t^(l) for the intra levels 0..6.  Column block ck (8 keys) against
+                // row block t8: below the diagonal the level is 4 + floor(log2(ck ^ t8)),
+                // on it 1 + floor(log2(e ^ t7)) (0 on the diagonal element).
                 const bool valid = (tile0 + i) * LL_C + t < a.L;
-                const float *lrow = stage_l(s) + t * NL;  // lambda_t^(0..6) by level
-                uint8_t *prow = sm + a.lay.off_P + t * 128;
+                const float *lrow = stage_l(s) + t * NL;
+                float lw[LL_LOG2C + 1];
+#pragma unroll
+                for (int l = 0; l <= LL_LOG2C; ++l) lw[l] = valid ? lrow[l] : 0.f;
+                uint8_t *prow = sm + a.lay.off_P + (i & 1) * LL_TILE + t * 128;
 #pragma unroll
                 for (int ck = 0; ck < 8; ++ck) {
-                    uint32_t w[4];
+                    const uint32_t *rr = ck < 4 ? r0 : r1;
+                    const int i0 = (8 * ck) & 31;
+                    float v[8];
+                    if (ck < t8) {
+                        const int x = ck ^ t8;
+                        const float w = x >= 4 ? lw[6] : (x >= 2 ? lw[5] : lw[4]);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = 8 * ck + 2 * e, s1 = s0 + 1;
-                        const uint32_t *rr = s0 < 32 ? r0 : r1;
-                        const float l0 = lrow[fenwick_level(t, s0)], l1 = lrow[fenwick_level(t, s1)];
-                        const float v0 = (valid && s0 <= t) ? __uint_as_float(rr[s0 & 31]) * l0 : 0.f;
-                        const float v1 = (valid && s1 <= t) ? __uint_as_float(rr[s1 & 31]) * l1 : 0.f;
-                        w[e] = pack_bf16x2(v0, v1);
+                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i0 + e]) * w;
+                    } else if (ck == t8) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int y = e ^ t7;
+                            const float w = y == 0 ? lw[0] : (y >= 4 ? lw[3] : (y >= 2 ? lw[2] : lw[1]));
+                            v[e] = e <= t7 ? __uint_as_float(rr[i0 + e]) * w : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
                     }
-                    *(uint4 *)(prow + ((ck ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(prow + ((ck ^ (t & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                   pack_bf16x2(v[6], v[7]));
                 }
             }
             fence_async_smem();
             named_bar(2, 128);
-            if (pt == 0) mbar_arrive(p_ready);
+            if (pt == 0) mbar_arrive(&p_ready[i & 1]);
+            if (++s == nst) { s = 0; ph ^= 1; }
         }
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------------------ close Fenwick blocks
@@ -394,6 +403,12 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ps_read);
                 const int x = i + 1;  // position after this chunk
+                // the level MMAs of chunk i - 1 (issued after this chunk's state update) may
+                // still read the tile about to be overwritten: wait until they are done.  (Waiting on every chunk also keeps t_formed
+                // at most one phase ahead of the MMA issuer.)
+                if (i >= 1 &&
+                    !group_wait(ct == 0, 4, &c_done[(i - 1) & 1], ((i - 1) >> 1) & 1, nullptr, 0, false, ctl))
+                    break;
                 if (x < nloc && row_lane) {
                     const int d = __popc(x), r = __ffs(x) - 1;
                     // T_r = PS(x) - PS(x - 2^r); PS(x - 2^r) is the snapshot at depth d - 1.
@@ -425,39 +440,67 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 }
                 fence_async_smem();
                 named_bar(4, 128);
-                if (ct == 0) mbar_arrive(t_formed);
+                if (ct == 0) mbar_arrive(&t_formed[i & 1]);
             }
         }
     } else if (warp >= 12 && !totals) {
-        // ------------------------------------------------------------ output rows -> global
+        // ------------------------------------------------------------ combine + store rows
         const int q4 = warp & 3, ot = tid - 384;
         const int t = 16 * q4 + (lane & 15);
         const bool row_lane = lane < 16;
+        const uint32_t lq = (uint32_t)(32 * q4) << 16;
+        int slot = 0, rph = 0, s = 0, ph = 0;
         for (int i = 0; i < nloc; ++i) {
-            const int b = i & 1;
-            const int row = (tile0 + i) * LL_C + t;
-            if (!group_wait(ot == 0, 3, &o_done[b], (i >> 1) & 1, nullptr, 0, false, ctl)) break;
-            tc_fence_after();
-            const uint32_t tO = tmem + LT_O + 64 * b + ((uint32_t)(32 * q4) << 16);
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tO, r0);
-            tmem_ld32(tO + 32, r1);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[b]);
-            if (row_lane && row < a.L) {
+            const int c = tile0 + i;
+            const int row = c * LL_C + t;
+            const bool valid = row_lane && row < a.L;
+            // the stage holds this chunk's lambda rows
+            if (!group_wait(ot == 0, 3, &full[s], ph, nullptr, 0, false, ctl)) break;
+            const float *lrow = stage_l(s) + t * NL + 1 + LL_LOG2C;  // lambda_t^(7 + j) at [j]
+            float acc[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+            bool ok = true;
+            // products in issue order: P V (weight 1), then R_j for the set bits j of c
+            uint32_t bits = (uint32_t)c & ((1u << a.nlev) - 1u);
+            for (int j = -1;;) {  // j = -1: P V
+                if (!group_wait(ot == 0, 3, &r_full[slot], rph, nullptr, 0, false, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float w = j < 0 ? 1.f : (valid ? lrow[j] : 0.f);
+                const uint32_t tR = tmem + LT_R + 64 * slot + lq;
+                uint32_t r[32];
+                tmem_ld32(tR, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = fmaf(w, __uint_as_float(r[e]), acc[e]);
+                tmem_ld32(tR + 32, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_free[slot]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[32 + e] = fmaf(w, __uint_as_float(r[e]), acc[32 + e]);
+                if (++slot == LL_RING) { slot = 0; rph ^= 1; }
+                if (!bits) break;
+                j = __ffs(bits) - 1;
+                bits &= bits - 1u;
+            }
+            if (!ok) break;
+            // every output thread is past its lambda reads: the stage may be refilled
+            named_bar(3, 128);
+            if (ot == 0) mbar_arrive(&stage_free[s]);
+            if (valid) {
                 uint4 *dst = (uint4 *)(a.out + ((size_t)head * a.L + row) * LL_D);
 #pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    const uint32_t *rr = ck < 4 ? r0 : r1;
-                    const int i0 = (8 * ck) & 31;
-                    dst[ck] = make_uint4(pack_bf16x2(__uint_as_float(rr[i0]), __uint_as_float(rr[i0 + 1])),
-                                         pack_bf16x2(__uint_as_float(rr[i0 + 2]), __uint_as_float(rr[i0 + 3])),
-                                         pack_bf16x2(__uint_as_float(rr[i0 + 4]), __uint_as_float(rr[i0 + 5])),
-                                         pack_bf16x2(__uint_as_float(rr[i0 + 6]), __uint_as_float(rr[i0 + 7])));
-                }
+                for (int ck = 0; ck < 8; ++ck)
+                    dst[ck] = make_uint4(pack_bf16x2(acc[8 * ck], acc[8 * ck + 1]), pack_bf16x2(acc[8 * ck + 2], acc[8 * ck + 3]),
+                                         pack_bf16x2(acc[8 * ck + 4], acc[8 * ck + 5]),
+                                         pack_bf16x2(acc[8 * ck + 6], acc[8 * ck + 7]));
             }
+            if (++s == nst) { s = 0; ph ^= 1; }
         }
     }
 
@@ -465,7 +508,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
