@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
+    ap.add_argument("--L", type=int, default=None,
+                    help="override the workload's sequence length (profiling captures)")
     return ap.parse_args()
 
 
@@ -98,12 +100,17 @@ def flops_per_token(w, C):
     return f
 
 
-def kernel_sha1(feature_map="elu1"):
-    """Hash of the tensor-core kernel source that serves `feature_map` (plus the shared
+def kernel_sha1(w):
+    """Hash of the tensor-core kernel source that serves workload `w` (plus the shared
     headers): a committed DRAM-traffic figure is only used while this is unchanged."""
     import hashlib
     d = os.path.join(ROOT, "chunkwise_causal_linear_gb300", "csrc")
-    main = "tc_favor.cu" if feature_map == "favor" else "tc.cu"
+    if w.get("loglinear"):
+        main = "tc_loglinear.cu"
+    elif w["fm"] == "favor":
+        main = "tc_favor.cu"
+    else:
+        main = "tc.cu"
     h = hashlib.sha1()
     for name in (main, "tc_ptx.cuh", "tc_common.cuh"):
         with open(os.path.join(d, name), "rb") as f:
@@ -111,7 +118,7 @@ def kernel_sha1(feature_map="elu1"):
     return h.hexdigest()
 
 
-def ncu_traffic(workload, C, path, B, H):
+def ncu_traffic(workload, C, path, B, H, L=None):
     """DRAM bytes per launch from the committed ncu capture (profiles/traffic.json), or None
     when there is none for this workload or the kernel changed since it was taken."""
     try:
@@ -120,7 +127,9 @@ def ncu_traffic(workload, C, path, B, H):
     except Exception:
         return None
     w = synth.WORKLOADS[workload]
-    if not rec or rec.get("kernel_sha1") != kernel_sha1(w["fm"]) or (B, H) != (w["B"], w["H"]):
+    if not rec or rec.get("kernel_sha1") != kernel_sha1(w) or (B, H) != (w["B"], w["H"]):
+        return None
+    if L is not None and L != w["L"]:
         return None
     return rec["bytes_per_launch"]
 
@@ -246,6 +255,8 @@ def run_reference(args):
         w["B"] = args.B
     if args.H:
         w["H"] = args.H
+    if args.L:
+        w["L"] = args.L
     C = args.C if args.C is not None else w["C"]
     cores = host_cores()
     heads = sample_heads(w, cores)
@@ -297,6 +308,8 @@ def run_ours(args):
         w["B"] = args.B
     if args.H:
         w["H"] = args.H
+    if args.L:
+        w["L"] = args.L
     C = args.C if args.C is not None else w["C"]
     B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
     path = {"auto": la.LA_PATH_AUTO, "simt": la.LA_PATH_SIMT, "tc": la.LA_PATH_TC}[args.path]
@@ -421,7 +434,7 @@ def run_ours(args):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     kernel_s = (t_ms / args.steps) / 1e3
     achieved = io_bytes / kernel_s / 1e9
-    traffic = ncu_traffic(args.workload, C, plan["path"], B, H)
+    traffic = ncu_traffic(args.workload, C, plan["path"], B, H, L)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "traffic": traffic,
             "peak_kind": f"{peak_kind} hbm_gbs (copy)",
