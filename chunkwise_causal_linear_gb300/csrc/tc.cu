@@ -746,12 +746,16 @@ int tcf_launch(const Problem &p, int num_sms);
 bool tcl_supported(const Problem &p);
 int tcl_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tcl_launch(const Problem &p, int num_sms);
+bool tcw_supported(const Problem &p);
+int tcw_plan(const Problem &p, int num_sms, la_plan_info *info);
+int tcw_launch(const Problem &p, int num_sms);
 
 bool tc_supported(const Problem &p, int num_sms)
 {
     (void)num_sms;
     if (p.lam) return tcl_supported(p);
     if (p.fm == LA_FM_FAVOR) return tcf_supported(p);
+    if (p.C == 128 || p.C == 256) return tcw_supported(p);
     if (p.dtype != LA_BF16) return false;
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     if (p.dk != p.D) return false;
@@ -766,6 +770,7 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
 {
     if (p.lam) return tcl_plan(p, num_sms, info);
     if (p.fm == LA_FM_FAVOR) return tcf_plan(p, num_sms, info);
+    if (p.C == 128 || p.C == 256) return tcw_plan(p, num_sms, info);
     int seg_tiles = 0;
     const int nseg = tc_segments(p, num_sms, &seg_tiles);
     info->grid_x = p.B * p.H * nseg;
@@ -788,6 +793,7 @@ int tc_launch(const Problem &p, int num_sms)
     if (!tc_supported(p, num_sms)) return LA_ERR_UNSUPPORTED;
     if (p.lam) return tcl_launch(p, num_sms);
     if (p.fm == LA_FM_FAVOR) return tcf_launch(p, num_sms);
+    if (p.C == 128 || p.C == 256) return tcw_launch(p, num_sms);
     if (p.D == 128) return launch_d<128, 128>(p, num_sms);
     return p.dv == 128 ? launch_d<64, 128>(p, num_sms) : launch_d<64, 64>(p, num_sms);
 }
