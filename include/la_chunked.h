@@ -114,7 +114,7 @@ int la_chunked_fwd(const void *q, const void *k, const void *v, void *out,
  * LA_ERR_UNSUPPORTED for shapes the tensor-core path does not cover.  It covers bf16
  * storage, L >= 128, and:
  *   - identity / elu+1 features, with or without the normaliser, dk = D, (dk, dv) in
- *     {(64, 64), (64, 128), (128, 128)}, C in {16, 32, 64};
+ *     {(64, 64), (64, 128), (128, 128)}, C in {16, 32, 64, 128, 256};
  *   - FAVOR+ features, dk = 64, m = 256, dv = 64, C = 64, with or without the normaliser;
  *   - the log-linear mask: identity features, no normaliser, dk = dv = 64, C = 64, at most
  *     4096 chunks, num_levels <= 32, L * num_levels a multiple of 4 and level_weights
