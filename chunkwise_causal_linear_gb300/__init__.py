@@ -36,7 +36,8 @@ FEATURE_MAPS = {"identity": LA_FM_IDENTITY, "elu1": LA_FM_ELU1, "favor": LA_FM_F
 # every function the header declares (checked by the tests against include/la_chunked.h)
 EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_chunked_fwd_noalloc", "la_chunked_workspace_bytes", "la_chunked_plan",
-           "la_last_device_status", "la_status_string", "la_cost_model", "la_version")
+           "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
+           "la_decode_state_elems", "la_version")
 
 
 class la_feature_map(ctypes.Structure):
@@ -97,6 +98,10 @@ def lib() -> ctypes.CDLL:
             L.la_status_string.restype = ctypes.c_char_p
             L.la_cost_model.argtypes = [ll, ll, ll, ctypes.POINTER(ll), ctypes.POINTER(ll)]
             L.la_cost_model.restype = i
+            L.la_decode_step.argtypes = [p, p, p, p, p, p, i, i, i, i, fmp, i, p, i, ll, i, p]
+            L.la_decode_step.restype = i
+            L.la_decode_state_elems.argtypes = [i, i, i, i, fmp, i, ctypes.POINTER(ll)]
+            L.la_decode_state_elems.restype = ll
             L.la_version.argtypes = []
             L.la_version.restype = ctypes.c_char_p
             _lib = L
@@ -177,11 +182,63 @@ def la_cost_model(L, D, C):
     return st.value, sc.value
 
 
+def la_decode_step(q, k, v, out, state, zstate, B, H, dk, dv, feature_map, normalize,
+                   level_weights, num_levels, t, dtype, stream) -> int:
+    return lib().la_decode_step(q, k, v, out, state, zstate, B, H, dk, dv, _fm(feature_map),
+                                normalize, level_weights, num_levels, t, dtype, stream)
+
+
+def la_decode_state_elems(B, H, dk, dv, feature_map, num_levels):
+    ze = ctypes.c_longlong()
+    n = lib().la_decode_state_elems(B, H, dk, dv, _fm(feature_map), num_levels, ctypes.byref(ze))
+    return n, ze.value
+
+
 def la_version() -> str:
     return lib().la_version().decode()
 
 
 # ---- torch-tensor convenience ----------------------------------------------------------
+def decode_state(B, H, dk, dv, feature_map="identity", m=0, num_levels=0, normalize=False,
+                 device="cuda"):
+    """Zero decoding state (and normaliser state when normalize) for la_decode_step."""
+    import torch
+    fm = make_feature_map(feature_map, m, 1 if feature_map == "favor" else 0)
+    n, nz = la_decode_state_elems(B, H, dk, dv, fm, num_levels)
+    if n == 0:
+        raise LAError(LA_ERR_SHAPE, "la_decode_state_elems")
+    S = torch.zeros(n, dtype=torch.float32, device=device)
+    z = torch.zeros(nz, dtype=torch.float32, device=device) if normalize else None
+    return S, z
+
+
+def decode_step(q, k, v, state, zstate=None, t=0, feature_map="identity", omega=None,
+                normalize=False, level_weights=None, out=None, stream=None):
+    """One decoding step: q, k [B,H,dk], v [B,H,dv] CUDA tensors (one token per head);
+    state / zstate from decode_state(); level_weights [B,H,NL] fp32 for the log-linear
+    mask, with t the token position.  Returns out [B,H,dv]."""
+    import torch
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    nl = level_weights.shape[-1] if level_weights is not None else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        state.data_ptr(), zstate.data_ptr() if zstate is not None else None,
+                        B, H, dk, dv, fm, int(normalize),
+                        level_weights.data_ptr() if level_weights is not None else None,
+                        nl, int(t), dtype, stream)
+    if rc != LA_OK:
+        raise LAError(rc, "la_decode_step")
+    return out
+
+
+
 def _dtype_code(t):
     import torch
     if t.dtype == torch.bfloat16:

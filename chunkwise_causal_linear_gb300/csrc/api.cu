@@ -18,6 +18,11 @@ int simt_launch(const Problem &p, int n_inter, int log2C);
 bool tc_supported(const Problem &p, int num_sms);
 int tc_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tc_launch(const Problem &p, int num_sms);
+int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int normalize,
+                 int num_levels, long long t, bool loglinear, int *D_out, int *r_out);
+int decode_launch(const void *q, const void *k, const void *v, void *out, float *S, float *z, int B,
+                  int H, int dk, int dv, const la_feature_map *fm, int normalize, const float *lam,
+                  int num_levels, long long t, int dtype, cudaStream_t stream);
 
 int required_levels(int L)
 {
@@ -311,6 +316,33 @@ int la_cost_model(long long L, long long D, long long C, long long *state_macs,
     if (state_macs) *state_macs = 2 * L * D * D;
     if (score_macs) *score_macs = 2 * L * C * D;
     return LA_OK;
+}
+
+int la_decode_step(const void *q, const void *k, const void *v, void *out, float *state,
+                   float *zstate, int B, int H, int dk, int dv,
+                   const la_feature_map *feature_map, int normalize,
+                   const float *level_weights, int num_levels, long long t, int dtype,
+                   void *stream)
+{
+    if (!q || !k || !v || !out || !state) return LA_ERR_NULL;
+    if (normalize && !zstate) return LA_ERR_NULL;
+    if ((long long)B * H > INT_MAX / 2) return LA_ERR_SHAPE;
+    return decode_launch(q, k, v, out, state, zstate, B, H, dk, dv, feature_map, normalize,
+                         level_weights, num_levels, t, dtype, (cudaStream_t)stream);
+}
+
+long long la_decode_state_elems(int B, int H, int dk, int dv, const la_feature_map *feature_map,
+                                int num_levels, long long *z_elems)
+{
+    int D = 0, r = 0;
+    const bool ll = num_levels > 0;
+    if (decode_check(B, H, dk, dv, feature_map, 0, ll ? num_levels : 0, 0, ll, &D, &r) != LA_OK) {
+        if (z_elems) *z_elems = 0;
+        return 0;
+    }
+    const long long lv = ll ? num_levels - 1 : 1;
+    if (z_elems) *z_elems = (long long)B * H * lv * D;
+    return (long long)B * H * lv * D * dv;
 }
 
 const char *la_version(void) { return "0.1.0"; }

@@ -213,6 +213,42 @@ const char *la_status_string(int status);
 int la_cost_model(long long L, long long D, long long C, long long *state_macs,
                   long long *score_macs);
 
+/*
+ * la_decode_step -- one step of the recurrent (decoding) form for every (b, h) head, the
+ * inference counterpart of the chunked state ("Linear Attention / Performerの理論と実装",
+ * "再帰的な状態更新"; "論文紹介：Log Linear Attention", slides 17-22 for the level weights).
+ *
+ *   q, k          device [B, H, dk] (this token), dtype `dtype`
+ *   v, out        device [B, H, dv], dtype `dtype`; out is overwritten
+ *   state         device fp32, read and updated in place.  Without level weights:
+ *                 [B, H, D, dv] = S, the sum of phi(k_s) v_s^T over the tokens so far.
+ *                 With level weights: [B, H, num_levels - 1, D, dv], the Fenwick level
+ *                 states S^(1), S^(2), ... (zeros before the first token).
+ *   zstate        device fp32 normaliser, [B, H, D] or [B, H, num_levels - 1, D]; may be
+ *                 NULL when normalize is 0.  Updated in place like `state`.
+ *   level_weights NULL, or device [B, H, num_levels] fp32 lambda_t^(l) of this token.
+ *   t             this token's position (0-based); used by the level update only.
+ * D is dk, or m for FAVOR+.  Plain: state += phi(k) v^T, z += phi(k), then
+ * out = phi(q)^T state (/ phi(q)^T z).  Level weights: out = lambda^(0) (phi(q).phi(k)) v +
+ * sum_{l>=1} lambda^(l) phi(q)^T S^(l) from the states before the update; then, with r =
+ * trailing zeros of t+1, S^(r+1) = phi(k) v^T + sum_{l<=r} S^(l) and S^(1..r) = 0.  Stepping
+ * t = 0..L-1 reproduces la_chunked_fwd's rows (the same function of the sequence).
+ * Returns LA_OK, LA_ERR_NULL, LA_ERR_SHAPE (sizes, or num_levels too small for position
+ * t+1: the update needs num_levels >= 2 + trailing zeros of t+1, one more level than the
+ * forward pass over positions 0..t uses), LA_ERR_UNSUPPORTED, LA_ERR_CUDA.  Asynchronous on `stream`; the caller owns every
+ * buffer and must not run two steps of the same state concurrently.
+ */
+int la_decode_step(const void *q, const void *k, const void *v, void *out, float *state,
+                   float *zstate, int B, int H, int dk, int dv,
+                   const la_feature_map *feature_map, int normalize,
+                   const float *level_weights, int num_levels, long long t, int dtype,
+                   void *stream);
+
+/* Number of fp32 elements of la_decode_step's state and zstate for these sizes (0 on an
+ * invalid combination).  num_levels = 0 means no level weights. */
+long long la_decode_state_elems(int B, int H, int dk, int dv, const la_feature_map *feature_map,
+                                int num_levels, long long *z_elems);
+
 /* Library version string, e.g. "0.1.0". */
 const char *la_version(void);
 

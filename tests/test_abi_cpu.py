@@ -119,3 +119,36 @@ def test_workspace_too_small_rejected_before_launch(lib):
     # call reports the CUDA failure instead -- either way nothing runs
     rc = call(lam=FAKE, nl=7, C=16, L=64)
     assert rc in (la.LA_ERR_WORKSPACE, la.LA_ERR_CUDA)
+
+
+# ---------------------------------------------------------------------------
+# decoding step: host-side checks (nothing launched)
+# ---------------------------------------------------------------------------
+def test_decode_state_elems(lib):
+    fm = la.make_feature_map("identity")
+    assert la.la_decode_state_elems(2, 3, 64, 32, fm, 0) == (2 * 3 * 64 * 32, 2 * 3 * 64)
+    # log-linear: num_levels - 1 level states
+    assert la.la_decode_state_elems(2, 3, 64, 32, fm, 17) == (2 * 3 * 16 * 64 * 32, 2 * 3 * 16 * 64)
+    fav = la.make_feature_map("favor", 256, 1)
+    assert la.la_decode_state_elems(1, 2, 64, 64, fav, 0) == (2 * 256 * 64, 2 * 256)
+    assert la.la_decode_state_elems(0, 2, 64, 64, fm, 0) == (0, 0)
+
+
+def test_decode_rejects_bad_arguments_before_launch(lib):
+    fm = la.make_feature_map("identity")
+    ok = ctypes.c_void_p(16)  # never dereferenced: every call below fails on the host
+    args = dict(B=1, H=1, dk=8, dv=8, feature_map=fm, normalize=0, level_weights=None,
+                num_levels=0, t=0, dtype=la.LA_F32, stream=None)
+    assert la.la_decode_step(None, ok, ok, ok, ok, None, **args) == la.LA_ERR_NULL
+    assert la.la_decode_step(ok, ok, ok, ok, None, None, **args) == la.LA_ERR_NULL
+    # the normaliser needs its state
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, normalize=1)) == la.LA_ERR_NULL
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, dk=0)) == la.LA_ERR_SHAPE
+    # level weights: position t+1 = 8 needs level 4 (trailing zeros 3), i.e. num_levels >= 5
+    ll = dict(args, level_weights=ok, num_levels=4, t=7)
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **ll) == la.LA_ERR_SHAPE
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(ll, t=-1)) == la.LA_ERR_SHAPE
+    # FAVOR+ needs omega
+    fav = la.make_feature_map("favor", 16, 0)
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, feature_map=fav)) == la.LA_ERR_NULL
+    assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, dtype=7)) == la.LA_ERR_UNSUPPORTED
