@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     ap.add_argument("--L", type=int, default=None,
                     help="override the workload's sequence length (profiling captures)")
+    ap.add_argument("--op", default="forward", choices=["forward", "decode"],
+                    help="forward: the chunked forward (the headline metric); decode: one "
+                         "la_decode_step per step for every head of the workload")
     return ap.parse_args()
 
 
@@ -471,10 +474,125 @@ def run_ours(args):
     return 0
 
 
+def run_decode(args):
+    """Decoding steps: each timed step is one la_decode_step over every (b, h) head of the
+    workload (one token per head).  A step streams the fp32 state through the SMs once, so
+    the roofline is HBM: bytes = state (and normaliser) read + written + q, k, v, out (+ the
+    token's level weights).  L2 is flushed between steps when the state fits in it."""
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    from chunkwise_causal_linear_gb300 import build as la_build
+    if not la_build.up_to_date():
+        la_build.build()
+    torch.cuda.set_device(0)
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.B:
+        w["B"] = args.B
+    if args.H:
+        w["H"] = args.H
+    B, H, dk, dv = w["B"], w["H"], w["dk"], w["dv"]
+    T = args.warmup + args.steps
+    wt = dict(w, L=T)
+    inp = synth.make_inputs(wt, args.seed)
+    es = 2 if w["dtype"] == "bf16" else 4
+
+    def dev(x, d):
+        if w["dtype"] == "bf16":
+            t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(x)
+        return t.reshape(B, H, T, d).cuda()
+
+    q, k, v = dev(inp["q"], dk), dev(inp["k"], dk), dev(inp["v"], dv)
+    toks = [(q[:, :, t].contiguous(), k[:, :, t].contiguous(), v[:, :, t].contiguous()) for t in range(T)]
+    omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
+    lams = None
+    nl = 0
+    if inp["lam"] is not None:
+        # levels for positions up to T (one more than a forward over T rows uses)
+        nl = synth.num_levels(T + 1) + 1
+        lam = np.zeros((B, H, T, nl), dtype=np.float32)
+        src = inp["lam"].reshape(B, H, T, -1)
+        lam[..., :src.shape[-1]] = src
+        lam_d = torch.from_numpy(lam).cuda()
+        lams = [lam_d[:, :, t].contiguous() for t in range(T)]
+    D = w["m"] if w["fm"] == "favor" else dk
+    S, z = la.decode_state(B, H, dk, dv, w["fm"], w["m"], nl, w["normalize"])
+    out = torch.empty((B, H, dv), dtype=q.dtype, device="cuda")
+    state_bytes = S.numel() * 4 + (z.numel() * 4 if z is not None else 0)
+    flush = None
+    if state_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        la.decode_step(*toks[t], S, z, t=t, feature_map=w["fm"], omega=omega,
+                       normalize=w["normalize"], level_weights=lams[t] if lams else None, out=out,
+                       stream=stream.cuda_stream)
+
+    def algo_bytes(t):
+        per_level = B * H * D * (dv + (1 if w["normalize"] else 0)) * 4
+        lv = (nl - 1) if nl else 1
+        if nl:
+            x, r = t + 1, 0
+            while not (x >> r) & 1:
+                r += 1
+            written = r + 1
+        else:
+            written = 1
+        return (lv + written) * per_level + B * H * ((2 * dk + 2 * dv) * es + nl * 4)
+
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    st = la.la_last_device_status(stream.cuda_stream)
+    if st != la.LA_OK:
+        raise la.LAError(st, "device status after warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        evs[i][0].record(stream)
+        step(args.warmup + i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in evs]
+    t_ms = sum(times)
+    ms = t_ms / args.steps
+    byts = sum(algo_bytes(args.warmup + i) for i in range(args.steps)) / args.steps
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = byts / (ms / 1e3) / 1e9
+    line = {"metric": "decode tokens/sec (B·H tokens per la_decode_step)", "op": "decode",
+            "value": B * H * args.steps / (t_ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w["dtype"] == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "dk": dk, "dv": dv,
+                       "feature_map": w["fm"], "m": w["m"], "normalize": bool(w["normalize"]),
+                       "num_levels": nl, "state_bytes": state_bytes,
+                       "l2": "L2 flushed between steps (2x L2 buffer written)" if flush is not None
+                       else "state larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                         "algorithmic_bytes_per_launch": byts},
+            "cpu_baseline": None, "e2e": None, "clocks": clk, "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "decode":
+        return run_decode(args)
     return run_ours(args)
 
 

@@ -203,6 +203,87 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecArgs a)
     }
 }
 
+// Plain (no level weights) step with float4 columns: dv % 4 == 0, dv <= 512.  512 threads =
+// RG row groups x dv/4 column quads; each thread issues its rows' 16-byte loads together
+// (RGI rows at a time), so a CTA keeps ~64 KB of state reads in flight.
+constexpr int DV_THREADS = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(DV_THREADS) decode_vec_kernel(const DecArgs a)
+{
+    extern __shared__ float dsm[];
+    const int D = a.D, dv = a.dv;
+    const int nq = dv / 4;                   // column quads per row
+    const int RG = DV_THREADS / nq;          // row groups
+    float *fq = dsm;                         // [D]
+    float *fk = fq + D;                      // [D]
+    float *part = fk + D;                    // [RG][dv] column partial sums
+    float *dpart = part + RG * dv;           // [DV_THREADS]
+    const int head = blockIdx.x, tid = threadIdx.x;
+    const int cq = tid % nq, rg = tid / nq;  // column quad, row group
+    const T *q = (const T *)a.q + (size_t)head * a.dk;
+    const T *k = (const T *)a.k + (size_t)head * a.dk;
+    for (int i = tid; i < D; i += DV_THREADS) {
+        const float xq = to_f32(q[i]), xk = to_f32(k[i]);
+        fq[i] = a.fm == LA_FM_ELU1 ? phi_elu1(xq) : xq;
+        fk[i] = a.fm == LA_FM_ELU1 ? phi_elu1(xk) : xk;
+    }
+    __syncthreads();
+    float den = 0.f;
+    if (a.normalize) {
+        float *z = a.z + (size_t)head * D;
+        for (int i = tid; i < D; i += DV_THREADS) {
+            const float zi = z[i] + fk[i];
+            z[i] = zi;
+            den = fmaf(fq[i], zi, den);
+        }
+    }
+    dpart[tid] = den;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (rg < RG) {
+        const T *v = (const T *)a.v + (size_t)head * dv + 4 * cq;
+        const float v0 = to_f32(v[0]), v1 = to_f32(v[1]), v2 = to_f32(v[2]), v3 = to_f32(v[3]);
+        float4 *S = (float4 *)(a.S + (size_t)head * D * dv) + cq;
+        constexpr int RGI = 8;  // rows in flight per thread
+        for (int i0 = rg; i0 < D; i0 += RG * RGI) {
+            float4 sv[RGI];
+#pragma unroll
+            for (int u = 0; u < RGI; ++u) {
+                const int i = i0 + u * RG;
+                if (i < D) sv[u] = S[(size_t)i * nq];
+            }
+#pragma unroll
+            for (int u = 0; u < RGI; ++u) {
+                const int i = i0 + u * RG;
+                if (i < D) {
+                    const float f = fk[i], g = fq[i];
+                    sv[u].x = fmaf(f, v0, sv[u].x);
+                    sv[u].y = fmaf(f, v1, sv[u].y);
+                    sv[u].z = fmaf(f, v2, sv[u].z);
+                    sv[u].w = fmaf(f, v3, sv[u].w);
+                    S[(size_t)i * nq] = sv[u];
+                    num.x = fmaf(g, sv[u].x, num.x);
+                    num.y = fmaf(g, sv[u].y, num.y);
+                    num.z = fmaf(g, sv[u].z, num.z);
+                    num.w = fmaf(g, sv[u].w, num.w);
+                }
+            }
+        }
+        *(float4 *)(part + rg * dv + 4 * cq) = num;
+    }
+    __syncthreads();
+    for (int st = DV_THREADS / 2; st > 0; st >>= 1) {
+        if (tid < st) dpart[tid] += dpart[tid + st];
+        __syncthreads();
+    }
+    for (int c = tid; c < dv; c += DV_THREADS) {
+        float acc = 0.f;
+        for (int g = 0; g < RG; ++g) acc += part[g * dv + c];
+        const float o = a.normalize ? acc / dpart[0] : acc;
+        ((T *)a.out)[(size_t)head * dv + c] = from_f32<T>(o);
+    }
+}
+
 }  // namespace
 
 int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int normalize,
@@ -249,6 +330,27 @@ int decode_launch(const void *q, const void *k, const void *v, void *out, float 
     a.lam = lam;
     a.nl = lam ? num_levels : 0;
     a.r = r;
+    if (!lam && a.fm != LA_FM_FAVOR && dv % 4 == 0 && dv <= 512) {
+        const int RG = DV_THREADS / (dv / 4);
+        const size_t vsm = sizeof(float) * ((size_t)2 * D + (size_t)RG * dv + DV_THREADS);
+        if (vsm <= 200 * 1024) {
+            dim3 vgrid((unsigned)(B * H));
+            if (dtype == LA_BF16) {
+                auto kern = decode_vec_kernel<__nv_bfloat16>;
+                if (vsm > 48 * 1024 &&
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vsm) != cudaSuccess)
+                    return LA_ERR_CUDA;
+                kern<<<vgrid, DV_THREADS, vsm, stream>>>(a);
+            } else {
+                auto kern = decode_vec_kernel<float>;
+                if (vsm > 48 * 1024 &&
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vsm) != cudaSuccess)
+                    return LA_ERR_CUDA;
+                kern<<<vgrid, DV_THREADS, vsm, stream>>>(a);
+            }
+            return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+        }
+    }
     const size_t smem = sizeof(float) * ((size_t)2 * D + 2 * dk + DEC_RG * (DEC_COLS + 1) + DEC_THREADS);
     if (smem > 200 * 1024) return LA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)(B * H));
