@@ -206,13 +206,22 @@ def state_vs_kv(L: int, d: int) -> tuple[int, int]:
 # whole-problem helpers over heads (raw q, k, v as float64 [n_heads, L, d])
 # ---------------------------------------------------------------------------
 def head_forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
-                 method="recurrence", rows=None):
+                 method="recurrence", rows=None, causal=True):
     """One head from raw q,k,v [L, d] (float64): feature map, then the chosen order.
 
     method: "recurrence" (chunk size 1; log-linear uses the Fenwick recurrence) or
-    "scores_first" (the definition; rows= selects output rows).
+    "scores_first" (the definition; rows= selects output rows).  causal=False: every query
+    sees every key ("attention と線形の間" section 1; the bidirectional normalised form of
+    "Linear Attention / Performerの理論と実装"), computed state first.
     """
     fq, fk = phi(q, fm, omega), phi(k, fm, omega)
+    if not causal:
+        if lam is not None:
+            raise ValueError("the log-linear mask is causal")
+        if method == "scores_first":
+            return scores_first(fq, fk, v, causal=False, normalize=normalize, rows=rows)
+        out = state_first(fq, fk, v, normalize=normalize)
+        return out if rows is None else out[np.asarray(rows)]
     if method == "scores_first":
         return scores_first(fq, fk, v, causal=True, normalize=normalize, lam=lam, rows=rows)
     if method == "recurrence":
@@ -225,14 +234,14 @@ def head_forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
 
 
 def forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
-            method="recurrence", rows=None, threads=None):
+            method="recurrence", rows=None, threads=None, causal=True):
     """All heads: q,k [n, L, dk], v [n, L, dv] float64 -> [n, L or len(rows), dv]."""
     n = q.shape[0]
     results = [None] * n
 
     def one(h):
         results[h] = head_forward(q[h], k[h], v[h], fm, omega, normalize,
-                                  None if lam is None else lam[h], method, rows)
+                                  None if lam is None else lam[h], method, rows, causal)
 
     threads = threads or min(n, os.cpu_count() or 1)
     if threads <= 1 or n == 1:

@@ -380,3 +380,23 @@ def test_loglinear_low_levels_only_is_block_diagonal():
     for c0 in range(0, L, C):
         sl = slice(c0, c0 + C)
         assert np.array_equal(out[sl], np.tril(q[sl] @ k[sl].T) @ v[sl])
+
+
+def test_noncausal_normalised_equals_matrix_products():
+    """Bidirectional normalised form ("Linear Attention / Performerの理論と実装", the
+    non-causal normalised output): out = (phi(Q) phi(K)^T V) / (phi(Q) phi(K)^T 1), a plain
+    matrix-product expression computed here with numpy; both oracle orders must match it."""
+    rng = np.random.default_rng(3)
+    q, k = rng.normal(size=(2, 37, 6)), rng.normal(size=(2, 37, 6))
+    v = rng.normal(size=(2, 37, 5))
+    for fm in ("elu1", "identity"):
+        fq = np.where(q >= 0, q + 1, np.exp(q)) if fm == "elu1" else q
+        fk = np.where(k >= 0, k + 1, np.exp(k)) if fm == "elu1" else k
+        A = fq @ np.swapaxes(fk, 1, 2)
+        for norm in (False, True):
+            want = A @ v
+            if norm:
+                want = want / A.sum(-1, keepdims=True)
+            for method in ("recurrence", "scores_first"):
+                got = oracle.forward(q, k, v, fm=fm, normalize=norm, method=method, causal=False)
+                assert np.allclose(got, want, rtol=1e-12, atol=1e-12), (fm, norm, method)
