@@ -37,7 +37,8 @@ FEATURE_MAPS = {"identity": LA_FM_IDENTITY, "elu1": LA_FM_ELU1, "favor": LA_FM_F
 EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_chunked_fwd_noalloc", "la_chunked_workspace_bytes", "la_chunked_plan",
            "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
-           "la_decode_state_elems", "la_version")
+           "la_decode_state_elems", "la_noncausal_fwd", "la_noncausal_workspace_bytes",
+           "la_version")
 
 
 class la_feature_map(ctypes.Structure):
@@ -102,6 +103,10 @@ def lib() -> ctypes.CDLL:
             L.la_decode_step.restype = i
             L.la_decode_state_elems.argtypes = [i, i, i, i, fmp, i, ctypes.POINTER(ll)]
             L.la_decode_state_elems.restype = ll
+            L.la_noncausal_fwd.argtypes = [p, p, p, p, i, i, i, i, i, fmp, i, i, p, sz, p]
+            L.la_noncausal_fwd.restype = i
+            L.la_noncausal_workspace_bytes.argtypes = [i, i, i, i, i, fmp, i, i]
+            L.la_noncausal_workspace_bytes.restype = sz
             L.la_version.argtypes = []
             L.la_version.restype = ctypes.c_char_p
             _lib = L
@@ -194,11 +199,46 @@ def la_decode_state_elems(B, H, dk, dv, feature_map, num_levels):
     return n, ze.value
 
 
+def la_noncausal_fwd(q, k, v, out, B, H, L, dk, dv, feature_map, normalize, dtype, workspace,
+                     workspace_bytes, stream) -> int:
+    return lib().la_noncausal_fwd(q, k, v, out, B, H, L, dk, dv, _fm(feature_map), normalize,
+                                  dtype, workspace, workspace_bytes, stream)
+
+
+def la_noncausal_workspace_bytes(B, H, L, dk, dv, feature_map, normalize, dtype) -> int:
+    return lib().la_noncausal_workspace_bytes(B, H, L, dk, dv, _fm(feature_map), normalize, dtype)
+
+
 def la_version() -> str:
     return lib().la_version().decode()
 
 
 # ---- torch-tensor convenience ----------------------------------------------------------
+def noncausal_fwd(q, k, v, feature_map="identity", omega=None, normalize=False, out=None,
+                  workspace=None, stream=None):
+    """Bidirectional linear attention of CUDA tensors q,k [B,H,L,dk], v [B,H,L,dv]."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, L, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    need = la_noncausal_workspace_bytes(B, H, L, dk, dv, fm, int(normalize), dtype)
+    if need == 0:
+        raise LAError(LA_ERR_UNSUPPORTED, "la_noncausal_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_noncausal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, dk,
+                          dv, fm, int(normalize), dtype, workspace.data_ptr(), need, stream)
+    if rc != LA_OK:
+        raise LAError(rc, "la_noncausal_fwd")
+    return out
+
+
 def decode_state(B, H, dk, dv, feature_map="identity", m=0, num_levels=0, normalize=False,
                  device="cuda"):
     """Zero decoding state (and normaliser state when normalize) for la_decode_step."""

@@ -18,6 +18,12 @@ int simt_launch(const Problem &p, int n_inter, int log2C);
 bool tc_supported(const Problem &p, int num_sms);
 int tc_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tc_launch(const Problem &p, int num_sms);
+size_t nc_simt_workspace_bytes(int BH, int D, int dv);
+bool nc_simt_supported(int D, int dk);
+int nc_simt_launch(const Problem &p);
+bool tc_nc_supported(const Problem &p);
+size_t tc_nc_workspace(const Problem &p, int num_sms);
+int tc_nc_launch(const Problem &p, int num_sms);
 int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int normalize,
                  int num_levels, long long t, bool loglinear, int *D_out, int *r_out);
 int decode_launch(const void *q, const void *k, const void *v, void *out, float *S, float *z, int B,
@@ -343,6 +349,50 @@ long long la_decode_state_elems(int B, int H, int dk, int dv, const la_feature_m
     const long long lv = ll ? num_levels - 1 : 1;
     if (z_elems) *z_elems = (long long)B * H * lv * D;
     return (long long)B * H * lv * D * dv;
+}
+
+// non-causal: one global state per head; the tensor-core path when it covers the shape
+static int nc_problem(int B, int H, int L, int dk, int dv, const la_feature_map *fm, int normalize,
+                      int dtype, Problem *p)
+{
+    int rc = check_problem(B, H, L, dk, dv, 64, fm, normalize, false, 0, dtype, p);
+    if (rc != LA_OK) return rc;
+    if (!nc_simt_supported(p->D, p->dk)) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+size_t la_noncausal_workspace_bytes(int B, int H, int L, int dk, int dv,
+                                    const la_feature_map *feature_map, int normalize, int dtype)
+{
+    Problem p;
+    if (nc_problem(B, H, L, dk, dv, feature_map, normalize, dtype, &p) != LA_OK) return 0;
+    const int sms = device_sms();
+    size_t a = nc_simt_workspace_bytes(B * H, p.D, dv);
+    size_t b = tc_nc_supported(p) ? tc_nc_workspace(p, sms > 0 ? sms : 152) : 0;
+    return a > b ? a : b;
+}
+
+int la_noncausal_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                     int dk, int dv, const la_feature_map *feature_map, int normalize, int dtype,
+                     void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!q || !k || !v || !out) return LA_ERR_NULL;
+    Problem p;
+    int rc = nc_problem(B, H, L, dk, dv, feature_map, normalize, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
+    const int sms = device_sms();
+    if (sms <= 0) return LA_ERR_CUDA;
+    const bool tc = tc_nc_supported(p);
+    const size_t need = tc ? tc_nc_workspace(p, sms) : nc_simt_workspace_bytes(B * H, p.D, dv);
+    if (!workspace || workspace_bytes < need) return LA_ERR_WORKSPACE;
+    p.q = q; p.k = k; p.v = v; p.out = out;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes;
+    p.stream = (cudaStream_t)stream;
+    p.err = err_ptr();
+    if (!p.err) return LA_ERR_CUDA;
+    return tc ? tc_nc_launch(p, sms) : nc_simt_launch(p);
 }
 
 const char *la_version(void) { return "0.1.0"; }

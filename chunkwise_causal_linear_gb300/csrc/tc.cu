@@ -78,6 +78,10 @@ struct TcArgs {
     int *err;
     unsigned long long timeout_ns;
     int debug_stall;  // test knob: the feature-map group never signals (forces a timeout)
+    // Non-causal (bidirectional) main pass: every segment starts from the sum of all nseg_all
+    // segments' totals, the state is never updated, and P is zero, so each row gets exactly
+    // phi(q) S_total (/ phi(q) z_total).
+    int noncausal, nseg_all;
 };
 
 template <int D, int DV, int C, bool NORM>
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         for (int i = tid; i < D; i += TC_THREADS) {
             float z0 = 0.f;
             if (!totals)
-                for (int g = 0; g < seg; ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
+                for (int g = 0; g < (a.noncausal ? a.nseg_all : seg); ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
             zs[i] = z0;
         }
     }
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
         const int jr = (DV == 128) ? 32 * (warp & 3) + lane : 16 * (warp & 3) + (lane & 15);
         const bool live = (DV == 128) || lane < 16;
-        const int nprev = totals ? 0 : seg;
+        const int nprev = totals ? 0 : (a.noncausal ? a.nseg_all : seg);
 #pragma unroll 1
         for (int col = 0; col < D; col += 16) {
             float acc[16];
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
                     const int lg = c * NSUB + j;           // chunk index in this CTA
                     if (g >= nsub) break;
-                    if (lg >= 1 && !wait_phase(s_ready, (lg - 1) & 1, ctl)) {
+                    if (!a.noncausal && lg >= 1 && !wait_phase(s_ready, (lg - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         mma_ts(tO + j * CH, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
                     }
                     // state: S^T += V_g^T phi(K_g), both MN-major, K = CH in steps of 16 rows
-                    if (g + 1 < nsub) {
+                    if (g + 1 < nsub && !a.noncausal) {
 #pragma unroll
                         for (int ks = 0; ks < CH / 16; ++ks) {
                             const uint32_t ro = (j * CH + 16 * ks) * 128;
@@ -424,10 +428,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     uint32_t *wv = (uint32_t *)&wk[n];
+                    // rows past L are TMA zero fill: phi(0) may be nonzero (elu+1), keep them out of z
+                    const bool in_seq = (tile0 + c) * C + rg + n * RG < a.L;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
-                        if (NORM) {
+                        if (NORM && in_seq) {
                             colsum[2 * e] += x0;
                             colsum[2 * e + 1] += x1;
                         }
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     }
                 }
                 fence_async_smem();
-                const bool zupd = NORM && (c + 1 < nch || totals);
+                const bool zupd = NORM && (totals || (c + 1 < nch && !a.noncausal));
                 if (zupd) {
                     // column sums over the row groups: lanes g, g+G, ... of a warp, then the
                     // group's warps through shared memory
@@ -532,8 +538,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         // P keeps s in t's chunk with s <= t (block-diagonal causal mask at
                         // CH); the normaliser's row sum keeps every s <= t of the tile
                         const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
-                        const float v0 = s0 <= t ? __uint_as_float(r[2 * e]) : 0.f;
-                        const float v1 = s1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
+                        const float v0 = (s0 <= t && !a.noncausal) ? __uint_as_float(r[2 * e]) : 0.f;
+                        const float v1 = (s1 <= t && !a.noncausal) ? __uint_as_float(r[2 * e + 1]) : 0.f;
                         rs += v0 + v1;
                         if (CH == C) {
                             pk[e] = pack_bf16x2(v0, v1);
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             for (int j = 0; j < NSUB; ++j) {
                 const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
                 const int lg = c * NSUB + j;           // chunk index in this CTA
-                if (g + 1 >= a.nsub) break;  // no state update after the last chunk
+                if (a.noncausal || g + 1 >= a.nsub) break;  // no state update after the last chunk
                 if (!group_wait(pt == 0, 2, state_done, lg & 1, nullptr, 0, false, ctl)) {
                     rb_ok = false;
                     break;
@@ -677,7 +683,7 @@ size_t tc_workspace(const Problem &p, int nseg)
 }
 
 template <int D, int DV, int CH, int FM, bool NORM>
-int launch_t(const Problem &p, int num_sms)
+int launch_t(const Problem &p, int num_sms, bool noncausal = false)
 {
     constexpr int C = 64;  // rows per tile
     using Lay = TcLayout<D, DV, C, NORM>;
@@ -692,11 +698,16 @@ int launch_t(const Problem &p, int num_sms)
     a.nsub = (p.L + CH - 1) / CH;
     const int nseg = tc_segments(p, num_sms, &a.seg_tiles);
     a.BH = BH;
-    if (nseg > 1) {
-        if (!p.workspace || p.workspace_bytes < tc_workspace(p, nseg)) return LA_ERR_WORKSPACE;
+    // segments with a total: all but the last (causal); all of them (non-causal)
+    const int ntot = noncausal ? nseg : nseg - 1;
+    if (ntot > 0) {
+        const size_t need = (size_t)ntot * BH * ((size_t)DV * D + D) * sizeof(float);
+        if (!p.workspace || p.workspace_bytes < need) return LA_ERR_WORKSPACE;
         a.ws_T = (float *)p.workspace;
-        a.ws_z = a.ws_T + (size_t)(nseg - 1) * BH * DV * D;
+        a.ws_z = a.ws_T + (size_t)ntot * BH * DV * D;
     }
+    a.noncausal = noncausal ? 1 : 0;
+    a.nseg_all = nseg;
     a.err = p.err;
     a.timeout_ns = 2000000000ull;
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");
@@ -707,11 +718,11 @@ int launch_t(const Problem &p, int num_sms)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
         cudaSuccess)
         return LA_ERR_CUDA;
-    if (nseg > 1) {
-        // totals of segments 0..nseg-2, then the main pass over all segments
+    if (ntot > 0) {
+        // totals of segments 0..ntot-1, then the main pass over all segments
         a.totals = 1;
-        a.grid_seg = nseg - 1;
-        kern<<<BH * (nseg - 1), TC_THREADS, Lay::ALLOC, p.stream>>>(a);
+        a.grid_seg = ntot;
+        kern<<<BH * ntot, TC_THREADS, Lay::ALLOC, p.stream>>>(a);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }
     a.totals = 0;
@@ -796,6 +807,41 @@ int tc_launch(const Problem &p, int num_sms)
     if (p.C == 128 || p.C == 256) return tcw_launch(p, num_sms);
     if (p.D == 128) return launch_d<128, 128>(p, num_sms);
     return p.dv == 128 ? launch_d<64, 128>(p, num_sms) : launch_d<64, 64>(p, num_sms);
+}
+
+// ---- non-causal (bidirectional) on the tensor cores: totals of every segment, then a main
+// pass that only reads the summed state (64-row tiles; C plays no part)
+bool tc_nc_supported(const Problem &p)
+{
+    if (p.dtype != LA_BF16 || p.lam) return false;
+    if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
+    if (p.dk != p.D) return false;
+    if (!((p.D == 64 && (p.dv == 64 || p.dv == 128)) || (p.D == 128 && p.dv == 128))) return false;
+    return p.L >= 2 * 64;
+}
+
+size_t tc_nc_workspace(const Problem &p, int num_sms)
+{
+    const int nseg = tc_segments(p, num_sms, nullptr);
+    return (size_t)nseg * p.B * p.H * ((size_t)p.dv * p.D + p.D) * sizeof(float);
+}
+
+int tc_nc_launch(const Problem &p, int num_sms)
+{
+    if (!tc_nc_supported(p)) return LA_ERR_UNSUPPORTED;
+    auto go = [&](auto d, auto dv) -> int {
+        constexpr int D = decltype(d)::value, DV = decltype(dv)::value;
+        const bool n = p.normalize != 0;
+        if (p.fm == LA_FM_IDENTITY)
+            return n ? launch_t<D, DV, 64, LA_FM_IDENTITY, true>(p, num_sms, true)
+                     : launch_t<D, DV, 64, LA_FM_IDENTITY, false>(p, num_sms, true);
+        return n ? launch_t<D, DV, 64, LA_FM_ELU1, true>(p, num_sms, true)
+                 : launch_t<D, DV, 64, LA_FM_ELU1, false>(p, num_sms, true);
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    if (p.D == 128) return go(I128{}, I128{});
+    return p.dv == 128 ? go(I64{}, I128{}) : go(I64{}, I64{});
 }
 
 }  // namespace la

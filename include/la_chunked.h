@@ -249,6 +249,24 @@ int la_decode_step(const void *q, const void *k, const void *v, void *out, float
 long long la_decode_state_elems(int B, int H, int dk, int dv, const la_feature_map *feature_map,
                                 int num_levels, long long *z_elems);
 
+/*
+ * la_noncausal_fwd -- bidirectional (non-causal) linear attention: every query sees every
+ * key ("Linear Attention / Performerの理論と実装", the non-causal normalised form, and the
+ * Performer's bidirectional FAVOR+ attention; "attention と線形の間" section 1, StateFirst):
+ *     S = sum_s phi(k_s) v_s^T,  z = sum_s phi(k_s),  out_t = phi(q_t)^T S (/ phi(q_t)^T z).
+ * Arguments as la_chunked_fwd (no chunk size, no level weights: the mask is all ones).
+ * D (dk, or m for FAVOR+) must be at most 256.  The workspace holds the per-head state:
+ * at least la_noncausal_workspace_bytes(...) bytes.  Returns LA_OK or a negative status
+ * before any launch.
+ */
+int la_noncausal_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                     int dk, int dv, const la_feature_map *feature_map, int normalize, int dtype,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes la_noncausal_fwd needs (0 on an invalid or unsupported combination). */
+size_t la_noncausal_workspace_bytes(int B, int H, int L, int dk, int dv,
+                                    const la_feature_map *feature_map, int normalize, int dtype);
+
 /* Library version string, e.g. "0.1.0". */
 const char *la_version(void);
 

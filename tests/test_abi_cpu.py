@@ -152,3 +152,15 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     fav = la.make_feature_map("favor", 16, 0)
     assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, feature_map=fav)) == la.LA_ERR_NULL
     assert la.la_decode_step(ok, ok, ok, ok, ok, None, **dict(args, dtype=7)) == la.LA_ERR_UNSUPPORTED
+
+
+def test_noncausal_workspace_and_errors(lib):
+    fm = la.make_feature_map("identity")
+    assert la.la_noncausal_workspace_bytes(2, 3, 100, 64, 32, fm, 1, la.LA_BF16) >= 2 * 3 * (64 * 32 + 64) * 4
+    # D above 256 is not covered
+    assert la.la_noncausal_workspace_bytes(1, 1, 100, 300, 32, fm, 1, la.LA_F32) == 0
+    ok = ctypes.c_void_p(16)
+    assert la.la_noncausal_fwd(None, ok, ok, ok, 1, 1, 8, 8, 8, fm, 0, la.LA_F32, ok, 1 << 20,
+                               None) == la.LA_ERR_NULL
+    assert la.la_noncausal_fwd(ok, ok, ok, ok, 1, 1, 8, 8, 8, fm, 0, la.LA_F32, None, 0,
+                               None) in (la.LA_ERR_WORKSPACE, la.LA_ERR_CUDA)
