@@ -55,9 +55,10 @@ def parse():
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     ap.add_argument("--L", type=int, default=None,
                     help="override the workload's sequence length (profiling captures)")
-    ap.add_argument("--op", default="forward", choices=["forward", "decode"],
+    ap.add_argument("--op", default="forward", choices=["forward", "decode", "noncausal"],
                     help="forward: the chunked forward (the headline metric); decode: one "
-                         "la_decode_step per step for every head of the workload")
+                         "la_decode_step per step for every head of the workload; noncausal: "
+                         "la_noncausal_fwd over the workload (bidirectional)")
     return ap.parse_args()
 
 
@@ -347,13 +348,28 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
     lam_ptr = lam.data_ptr() if lam is not None else None
+    noncausal = args.op == "noncausal"
+    if noncausal:
+        if lam is not None:
+            raise SystemExit("--op noncausal: the log-linear mask is causal")
+        wsb = la.la_noncausal_workspace_bytes(B, H, L, dk, dv, fm, int(w["normalize"]), dtype)
+        if wsb == 0:
+            raise SystemExit("--op noncausal: unsupported sizes")
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        # two launches on either path: the per-head state, then the outputs
+        plan = dict(plan, n_launches=2, path="noncausal")
 
     def step():
-        r = la.la_chunked_fwd_path(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
-                                   H, L, dk, dv, C, fm, int(w["normalize"]), lam_ptr, nl, dtype,
-                                   ws.data_ptr(), wsb, sptr, path)
+        if noncausal:
+            r = la.la_noncausal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                    L, dk, dv, fm, int(w["normalize"]), dtype, ws.data_ptr(), wsb,
+                                    sptr)
+        else:
+            r = la.la_chunked_fwd_path(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
+                                       H, L, dk, dv, C, fm, int(w["normalize"]), lam_ptr, nl, dtype,
+                                       ws.data_ptr(), wsb, sptr, path)
         if r != la.LA_OK:
-            raise la.LAError(r, "la_chunked_fwd")
+            raise la.LAError(r, "la_noncausal_fwd" if noncausal else "la_chunked_fwd")
 
     io_bytes = B * H * L * bytes_per_token(w)
     flush = None
@@ -398,7 +414,7 @@ def run_ours(args):
 
     # ---- end to end through the host-buffer entry point (copies inside the region)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not noncausal:
         h2d = int(qh.numel() * qh.element_size() * 2 + vh.numel() * vh.element_size())
         d2h = int(outh.numel() * outh.element_size())
         qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -446,7 +462,7 @@ def run_ours(args):
             "tensor_peak_tflops": float(peaks.get("bf16_tflops", 1900.0))}
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and not noncausal:
         cores = host_cores()
         heads = sample_heads(w, cores)
         sub = {kk: (vv[heads] if kk in ("q", "k", "v", "lam") and vv is not None else vv)
@@ -465,6 +481,7 @@ def run_ours(args):
                            l2="inputs larger than L2" if flush is None else
                            "L2 flushed between steps (2x L2 buffer written)",
                            path={1: "simt", 2: "tc"}.get(plan["path"], plan["path"]),
+                           op=args.op,
                            parallelism=f"heads independent; weak scaling over {world} GPU(s)"),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": plan["n_launches"] * args.steps}

@@ -129,7 +129,7 @@ __device__ __forceinline__ float phi1(float x)
     return x;
 }
 
-template <int D, int DV, int CH, int FM, bool NORM>
+template <int D, int DV, int CH, int FM, bool NORM, bool NC>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_constant__ TcArgs a)
 {
     constexpr int C = 64;           // rows per tile
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         for (int i = tid; i < D; i += TC_THREADS) {
             float z0 = 0.f;
             if (!totals)
-                for (int g = 0; g < (a.noncausal ? a.nseg_all : seg); ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
+                for (int g = 0; g < (NC ? a.nseg_all : seg); ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
             zs[i] = z0;
         }
     }
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
         const int jr = (DV == 128) ? 32 * (warp & 3) + lane : 16 * (warp & 3) + (lane & 15);
         const bool live = (DV == 128) || lane < 16;
-        const int nprev = totals ? 0 : (a.noncausal ? a.nseg_all : seg);
+        const int nprev = totals ? 0 : (NC ? a.nseg_all : seg);
 #pragma unroll 1
         for (int col = 0; col < D; col += 16) {
             float acc[16];
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
                     const int lg = c * NSUB + j;           // chunk index in this CTA
                     if (g >= nsub) break;
-                    if (!a.noncausal && lg >= 1 && !wait_phase(s_ready, (lg - 1) & 1, ctl)) {
+                    if (!NC && lg >= 1 && !wait_phase(s_ready, (lg - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         mma_ts(tO + j * CH, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
                     }
                     // state: S^T += V_g^T phi(K_g), both MN-major, K = CH in steps of 16 rows
-                    if (g + 1 < nsub && !a.noncausal) {
+                    if (g + 1 < nsub && !NC) {
 #pragma unroll
                         for (int ks = 0; ks < CH / 16; ++ks) {
                             const uint32_t ro = (j * CH + 16 * ks) * 128;
@@ -428,8 +428,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     uint32_t *wv = (uint32_t *)&wk[n];
-                    // rows past L are TMA zero fill: phi(0) may be nonzero (elu+1), keep them out of z
-                    const bool in_seq = (tile0 + c) * C + rg + n * RG < a.L;
+                    // rows past L are TMA zero fill and phi(0) may be nonzero (elu+1): keep them out
+                    // of z where z is used after the last tile (the non-causal totals)
+                    const bool in_seq = !NC || (tile0 + c) * C + rg + n * RG < a.L;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     }
                 }
                 fence_async_smem();
-                const bool zupd = NORM && (totals || (c + 1 < nch && !a.noncausal));
+                const bool zupd = NORM && (totals || (c + 1 < nch && !NC));
                 if (zupd) {
                     // column sums over the row groups: lanes g, g+G, ... of a warp, then the
                     // group's warps through shared memory
@@ -538,8 +539,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         // P keeps s in t's chunk with s <= t (block-diagonal causal mask at
                         // CH); the normaliser's row sum keeps every s <= t of the tile
                         const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
-                        const float v0 = (s0 <= t && !a.noncausal) ? __uint_as_float(r[2 * e]) : 0.f;
-                        const float v1 = (s1 <= t && !a.noncausal) ? __uint_as_float(r[2 * e + 1]) : 0.f;
+                        const float v0 = (s0 <= t && !NC) ? __uint_as_float(r[2 * e]) : 0.f;
+                        const float v1 = (s1 <= t && !NC) ? __uint_as_float(r[2 * e + 1]) : 0.f;
                         rs += v0 + v1;
                         if (CH == C) {
                             pk[e] = pack_bf16x2(v0, v1);
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             for (int j = 0; j < NSUB; ++j) {
                 const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
                 const int lg = c * NSUB + j;           // chunk index in this CTA
-                if (a.noncausal || g + 1 >= a.nsub) break;  // no state update after the last chunk
+                if (NC || g + 1 >= a.nsub) break;  // no state update after the last chunk
                 if (!group_wait(pt == 0, 2, state_done, lg & 1, nullptr, 0, false, ctl)) {
                     rb_ok = false;
                     break;
@@ -714,7 +715,7 @@ int launch_t(const Problem &p, int num_sms, bool noncausal = false)
     if (e && *e) a.timeout_ns = strtoull(e, nullptr, 10);
     const char *st = getenv("LA_DEBUG_STALL");
     a.debug_stall = (st && *st && *st != '0') ? 1 : 0;
-    auto kern = tc_chunked_kernel<D, DV, CH, FM, NORM>;
+    auto kern = noncausal ? tc_chunked_kernel<D, DV, CH, FM, NORM, true> : tc_chunked_kernel<D, DV, CH, FM, NORM, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
         cudaSuccess)
         return LA_ERR_CUDA;
