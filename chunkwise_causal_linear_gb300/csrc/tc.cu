@@ -759,6 +759,9 @@ bool tcl_supported(const Problem &p);
 int tcl_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tcl_launch(const Problem &p, int num_sms);
 bool tcw_supported(const Problem &p);
+bool tcf_nc_supported(const Problem &p);
+size_t tcf_nc_workspace(const Problem &p, int num_sms);
+int tcf_nc_launch(const Problem &p, int num_sms);
 int tcw_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tcw_launch(const Problem &p, int num_sms);
 
@@ -814,6 +817,7 @@ int tc_launch(const Problem &p, int num_sms)
 // pass that only reads the summed state (64-row tiles; C plays no part)
 bool tc_nc_supported(const Problem &p)
 {
+    if (p.fm == LA_FM_FAVOR) return tcf_nc_supported(p);
     if (p.dtype != LA_BF16 || p.lam) return false;
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     if (p.dk != p.D) return false;
@@ -823,6 +827,7 @@ bool tc_nc_supported(const Problem &p)
 
 size_t tc_nc_workspace(const Problem &p, int num_sms)
 {
+    if (p.fm == LA_FM_FAVOR) return tcf_nc_workspace(p, num_sms);
     const int nseg = tc_segments(p, num_sms, nullptr);
     return (size_t)nseg * p.B * p.H * ((size_t)p.dv * p.D + p.D) * sizeof(float);
 }
@@ -830,6 +835,7 @@ size_t tc_nc_workspace(const Problem &p, int num_sms)
 int tc_nc_launch(const Problem &p, int num_sms)
 {
     if (!tc_nc_supported(p)) return LA_ERR_UNSUPPORTED;
+    if (p.fm == LA_FM_FAVOR) return tcf_nc_launch(p, num_sms);
     auto go = [&](auto d, auto dv) -> int {
         constexpr int D = decltype(d)::value, DV = decltype(dv)::value;
         const bool n = p.normalize != 0;

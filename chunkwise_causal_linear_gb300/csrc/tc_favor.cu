@@ -90,9 +90,13 @@ struct FvArgs {
     float *ws_z;             // [segments-1][BH][256]
     int *err;
     unsigned long long timeout_ns;
+    int nseg_all;            // non-causal: segments whose totals make the state
 };
 
-template <bool NORM>
+// NC: the bidirectional (non-causal) form.  The totals pass then covers every segment; the
+// main pass starts from the sum of all of them, never updates the state, and zeroes P, so
+// each row gets phi(q) S_total (/ phi(q) z_total).
+template <bool NORM, bool NC>
 __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_constant__ FvArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         const int l = tid - 128;                       // feature of this thread
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + FT_S + 64 * (l >> 7) + lo;
-        const int nprev = totals ? 0 : seg;
+        const int nprev = totals ? 0 : (NC ? a.nseg_all : seg);
         for (int g = 0; g < nprev; ++g) zreg += a.ws_z[((size_t)g * a.BH + head) * FV_M + l];
 #pragma unroll 1
         for (int col = 0; col < FV_DV; col += 16) {
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     mma_ss(tmem + FT_A, smem_desc(phq + ks * 2048, FV_M * 128, 1024),
                            smem_desc(phk + ks * 2048, FV_M * 128, 1024), ID_SC, ks > 0);
                 mma_commit(scores_done);
-                if (c >= 1 && !wait_phase(sbar_ready, (c - 1) & 1, ctl)) break;
+                if (!NC && c >= 1 && !wait_phase(sbar_ready, (c - 1) & 1, ctl)) break;
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t tO = tmem + FT_O + 80 * b;
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     mma_ss(tO, smem_desc(phq + ks * 2048, FV_M * 128, 1024),
                            smem_desc(sb + (ks >> 2) * FV_SBLK + (ks & 3) * 32, 16, 1024), ID_INTER, ks > 0);
                 // state: S += phi(K)^T (K-major A, features on M) x V (MN-major B), K = 64
-                if (g + 1 < a.nch) {
+                if (g + 1 < a.nch && !NC) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -349,7 +353,9 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         uint8_t *sblk = sm + FV_SBAR + (l >> 6) * FV_SBLK + ((l & 7) << 1);
         const int lch = (l & 63) >> 3;
         // phi of this thread's feature for the 64 tokens of a projected tile
-        auto phi_row = [&](const float *nr, uint8_t *dst, bool sum_z) {
+        // sum_z: the z sum over the tile's tokens; in the non-causal totals the zero-filled
+        // rows past L (whose phi is not zero) are left out, since z is used after them
+        auto phi_row = [&](const float *nr, uint8_t *dst, bool sum_z, int valid) {
             uint32_t r0[32], r1[32];
             tmem_ld32(tP, r0);
             tmem_ld32(tP + 32, r1);
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"((__uint_as_float(rr[i0 + 1]) - 0.5f * nr[t0 + 1]) * log2e));
                     e0 *= inv_sqrt_m;
                     e1 *= inv_sqrt_m;
-                    if (sum_z) zs += e0 + e1;
+                    if (sum_z) zs += (!NC || t0 < valid ? e0 : 0.f) + (!NC || t0 + 1 < valid ? e1 : 0.f);
                     w[e] = pack_bf16x2(e0, e1);
                 }
                 *(uint4 *)(dst + ((ck ^ (l & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             if (!totals) {
                 if (!group_wait(l == 0, 1, pq_done, c & 1, nullptr, 0, false, ctl, 256)) break;
                 tc_fence_after();
-                phi_row(nrm, rowq, false);
+                phi_row(nrm, rowq, false, 0);
                 // z_c (before this chunk) as bf16 hi / lo in S~ rows 64, 65 at column l
                 const __nv_bfloat16 zh = __float2bfloat16_rn(zreg);
                 const __nv_bfloat16 zl = __float2bfloat16_rn(zreg - __bfloat162float(zh));
@@ -417,12 +423,15 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             }
             if (!group_wait(l == 0, 1, pk_done, c & 1, nullptr, 0, false, ctl, 256)) break;
             tc_fence_after();
-            zreg += phi_row(nrm + 64, rowk, true);
+            {
+                const float zk = phi_row(nrm + 64, rowk, totals || !NC, a.L - g * FV_C);
+                if (totals || !NC) zreg += zk;
+            }
             fence_async_smem();
             named_bar(1, 256);
             if (l == 0) mbar_arrive(phi_ready);
             // bf16 copy of the state (S~ rows 0..63, column l) for the next chunk
-            if (!totals && g + 1 < a.nch) {
+            if (!totals && !NC && g + 1 < a.nch) {
                 if (!group_wait(l == 0, 1, state_done, c & 1, nullptr, 0, false, ctl, 256)) break;
                 tc_fence_after();
                 const uint32_t tS = tmem + FT_S + 64 * half + lo;
@@ -492,8 +501,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     for (int e = 0; e < 4; ++e) {
                         const int s0 = 8 * ck + 2 * e, s1 = s0 + 1;
                         const uint32_t *rr = s0 < 32 ? r0 : r1;
-                        const float v0 = s0 <= t ? __uint_as_float(rr[s0 & 31]) : 0.f;
-                        const float v1 = s1 <= t ? __uint_as_float(rr[s1 & 31]) : 0.f;
+                        const float v0 = (!NC && s0 <= t) ? __uint_as_float(rr[s0 & 31]) : 0.f;
+                        const float v1 = (!NC && s1 <= t) ? __uint_as_float(rr[s1 & 31]) : 0.f;
                         rs += v0 + v1;
                         w[e] = pack_bf16x2(v0, v1);
                     }
@@ -559,7 +568,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
 }
 
 template <bool NORM>
-int launch_fv(const Problem &p, int num_sms)
+int launch_fv(const Problem &p, int num_sms, bool noncausal = false)
 {
     FvArgs a;
     memset(&a, 0, sizeof(a));
@@ -577,19 +586,21 @@ int launch_fv(const Problem &p, int num_sms)
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");
     if (e && *e) a.timeout_ns = strtoull(e, nullptr, 10);
     const int nseg = split_segments(BH, a.nch, num_sms, 4, &a.seg_tiles);
-    if (nseg > 1) {
-        const size_t need = (size_t)(nseg - 1) * BH * ((size_t)FV_M * FV_DV + FV_M) * sizeof(float);
+    const int ntot = noncausal ? nseg : nseg - 1;  // segments with a totals pass
+    if (ntot > 0) {
+        const size_t need = (size_t)ntot * BH * ((size_t)FV_M * FV_DV + FV_M) * sizeof(float);
         if (!p.workspace || p.workspace_bytes < need) return LA_ERR_WORKSPACE;
         a.ws_S = (float *)p.workspace;
-        a.ws_z = a.ws_S + (size_t)(nseg - 1) * BH * FV_M * FV_DV;
+        a.ws_z = a.ws_S + (size_t)ntot * BH * FV_M * FV_DV;
     }
-    auto kern = tc_favor_kernel<NORM>;
+    a.nseg_all = nseg;
+    auto kern = noncausal ? tc_favor_kernel<NORM, true> : tc_favor_kernel<NORM, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FV_ALLOC) != cudaSuccess)
         return LA_ERR_CUDA;
-    if (nseg > 1) {
+    if (ntot > 0) {
         a.totals = 1;
-        a.grid_seg = nseg - 1;
-        kern<<<BH * (nseg - 1), FV_THREADS, FV_ALLOC, p.stream>>>(a);
+        a.grid_seg = ntot;
+        kern<<<BH * ntot, FV_THREADS, FV_ALLOC, p.stream>>>(a);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }
     a.totals = 0;
@@ -625,6 +636,26 @@ int tcf_launch(const Problem &p, int num_sms)
 {
     if (!tcf_supported(p)) return LA_ERR_UNSUPPORTED;
     return p.normalize ? launch_fv<true>(p, num_sms) : launch_fv<false>(p, num_sms);
+}
+
+// non-causal FAVOR+ (the Performer's bidirectional form), C plays no part
+bool tcf_nc_supported(const Problem &p)
+{
+    return p.dtype == LA_BF16 && !p.lam && p.fm == LA_FM_FAVOR && p.dk == FV_DK && p.m == FV_M &&
+           p.dv == FV_DV && p.L >= 2 * FV_C;
+}
+
+size_t tcf_nc_workspace(const Problem &p, int num_sms)
+{
+    const int nch = (p.L + FV_C - 1) / FV_C;
+    const int nseg = split_segments(p.B * p.H, nch, num_sms, 4, nullptr);
+    return (size_t)nseg * p.B * p.H * ((size_t)FV_M * FV_DV + FV_M) * sizeof(float);
+}
+
+int tcf_nc_launch(const Problem &p, int num_sms)
+{
+    if (!tcf_nc_supported(p)) return LA_ERR_UNSUPPORTED;
+    return p.normalize ? launch_fv<true>(p, num_sms, true) : launch_fv<false>(p, num_sms, true);
 }
 
 }  // namespace la

@@ -51,7 +51,10 @@ CASES = [
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=777)),            # tensor cores, ragged
     ("identity-d64-L2048", dict(B=1, H=2, L=2048)),             # tensor cores, split sequence
     ("identity-d64-L2048", dict(B=1, H=3, L=1000, normalize=True, fm="elu1", scale=1.0)),
-    ("favor-m256-d64-L16384", dict(B=1, H=2, L=600)),           # Performer, generic path
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=600)),           # Performer, tensor cores
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=4096)),          # Performer, split sequence
+    ("favor-m256-d64-L16384", dict(B=1, H=1, L=777, normalize=False)),
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=100, dtype="f32")),  # Performer, generic path
     ("elu1-norm-d128-L8192", dict(B=2, H=1, L=100, dk=32, dv=48)),  # generic path
 ]
 
