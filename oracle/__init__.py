@@ -66,6 +66,10 @@ def lib():
             L.orc_loglinear_recurrence.argtypes = [_dp, _dp, _dp, c_long, c_int, c_int, _dp,
                                                    c_int, c_int, _dp]
             L.orc_loglinear_recurrence.restype = c_int
+            L.orc_decay_recurrence.argtypes = [_dp, _dp, _dp, c_long, c_int, c_int,
+                                               ctypes.c_double, c_int, _dp]
+            L.orc_decay_scores_first.argtypes = [_dp, _dp, _dp, c_long, c_int, c_int,
+                                                 ctypes.c_double, c_int, _lp, c_long, _dp]
             for name in ("orc_state_flops", "orc_score_flops", "orc_total_flops"):
                 getattr(L, name).argtypes = [c_ll, c_ll, c_ll]
                 getattr(L, name).restype = c_ll
@@ -187,6 +191,31 @@ def loglinear_recurrence(fq, fk, v, lam, normalize=False):
     return out
 
 
+def decay_recurrence(fq, fk, v, gamma, normalize=False):
+    """Retention update S_t = gamma S_{t-1} + phi(k_t) v_t^T (z decays alike)."""
+    fq, fk, v = _c(fq), _c(fk), _c(v)
+    L, D = fq.shape
+    dv = v.shape[1]
+    out = np.empty((L, dv))
+    lib().orc_decay_recurrence(_p(fq), _p(fk), _p(v), L, D, dv, float(gamma), int(normalize),
+                               _p(out))
+    return out
+
+
+def decay_scores_first(fq, fk, v, gamma, normalize=False, rows=None):
+    """The decayed output as a sum over the past with weights gamma^(t-s)."""
+    fq, fk, v = _c(fq), _c(fk), _c(v)
+    L, D = fq.shape
+    dv = v.shape[1]
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = L if rows is None else len(rows_a)
+    out = np.empty((n, dv))
+    lib().orc_decay_scores_first(_p(fq), _p(fk), _p(v), L, D, dv, float(gamma), int(normalize),
+                                 None if rows_a is None else rows_a.ctypes.data_as(_lp), n,
+                                 _p(out))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # cost model
 # ---------------------------------------------------------------------------
@@ -206,15 +235,25 @@ def state_vs_kv(L: int, d: int) -> tuple[int, int]:
 # whole-problem helpers over heads (raw q, k, v as float64 [n_heads, L, d])
 # ---------------------------------------------------------------------------
 def head_forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
-                 method="recurrence", rows=None, causal=True):
+                 method="recurrence", rows=None, causal=True, gamma=None):
     """One head from raw q,k,v [L, d] (float64): feature map, then the chosen order.
 
     method: "recurrence" (chunk size 1; log-linear uses the Fenwick recurrence) or
     "scores_first" (the definition; rows= selects output rows).  causal=False: every query
     sees every key ("attention と線形の間" section 1; the bidirectional normalised form of
-    "Linear Attention / Performerの理論と実装"), computed state first.
+    "Linear Attention / Performerの理論と実装"), computed state first.  gamma: the
+    Retention decay of that page (S_t = gamma S_{t-1} + phi(k_t) v_t^T), causal only.
     """
     fq, fk = phi(q, fm, omega), phi(k, fm, omega)
+    if gamma is not None:
+        if lam is not None or not causal:
+            raise ValueError("the decay is defined for the plain causal mask only")
+        if method == "scores_first":
+            return decay_scores_first(fq, fk, v, gamma, normalize=normalize, rows=rows)
+        if method == "recurrence":
+            out = decay_recurrence(fq, fk, v, gamma, normalize=normalize)
+            return out if rows is None else out[np.asarray(rows)]
+        raise ValueError(method)
     if not causal:
         if lam is not None:
             raise ValueError("the log-linear mask is causal")
@@ -234,14 +273,14 @@ def head_forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
 
 
 def forward(q, k, v, fm="identity", omega=None, normalize=False, lam=None,
-            method="recurrence", rows=None, threads=None, causal=True):
+            method="recurrence", rows=None, threads=None, causal=True, gamma=None):
     """All heads: q,k [n, L, dk], v [n, L, dv] float64 -> [n, L or len(rows), dv]."""
     n = q.shape[0]
     results = [None] * n
 
     def one(h):
         results[h] = head_forward(q[h], k[h], v[h], fm, omega, normalize,
-                                  None if lam is None else lam[h], method, rows, causal)
+                                  None if lam is None else lam[h], method, rows, causal, gamma)
 
     threads = threads or min(n, os.cpu_count() or 1)
     if threads <= 1 or n == 1:

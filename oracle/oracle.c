@@ -22,6 +22,8 @@
  *   [loglinear] "論文紹介：Log Linear Attention" (docswell slides): Fenwick tree
  *               partition (slides 15-16, 20-21), level weights (slide 17), decoding
  *               update rule (slide 22).
+ *   [perf] also gives the Retention form of the update, S_t = gamma S_{t-1} + phi(k_t)
+ *               v_t^T with 0 < gamma < 1 (the section on the RNN without forgetting).
  *
  * Parity status: every routine here is pinned by CPU tests against printed values,
  * closed forms, library routines or brute force (tests/test_oracle_*.py).
@@ -311,6 +313,63 @@ int orc_loglinear_recurrence(const double *fq, const double *fk, const double *v
     free(z);
     free(num);
     return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decay (Retention)                                                           */
+/* ------------------------------------------------------------------------- */
+
+/* [perf], the section on the RNN without forgetting: the Retention update
+ *   S_t = gamma S_{t-1} + phi(k_t) v_t^T,   S_{-1} = 0,
+ * read by y_t = phi(q_t)^T S_t.  The page gives the update of S only; the normaliser is
+ * read the plainest way that keeps y_t a weighted mean of the values: z decays with the
+ * same gamma, z_t = gamma z_{t-1} + phi(k_t), and y_t = phi(q_t)^T S_t / phi(q_t)^T z_t.
+ * gamma = 1 is the plain recurrence. */
+void orc_decay_recurrence(const double *fq, const double *fk, const double *v, long L, int D,
+                          int dv, double gamma, int normalize, double *out)
+{
+    double *S = (double *)calloc((size_t)D * dv, sizeof(double));
+    double *z = (double *)calloc((size_t)D, sizeof(double));
+    for (long t = 0; t < L; ++t) {
+        const double *kt = fk + t * D, *vt = v + t * dv, *qt = fq + t * D;
+        for (int i = 0; i < D; ++i) {
+            z[i] = gamma * z[i] + kt[i];
+            for (int j = 0; j < dv; ++j) S[i * dv + j] = gamma * S[i * dv + j] + kt[i] * vt[j];
+        }
+        double den = dot(qt, z, D);
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < D; ++i) acc += qt[i] * S[i * dv + j];
+            out[t * dv + j] = normalize ? acc / den : acc;
+        }
+    }
+    free(S);
+    free(z);
+}
+
+/* The same output written out as a weighted sum over the past (unrolling the update):
+ *   num_t = sum_{s<=t} gamma^(t-s) (phi(q_t) . phi(k_s)) v_s,
+ *   den_t = sum_{s<=t} gamma^(t-s) (phi(q_t) . phi(k_s)),
+ * i.e. the causal mask of [chunked] section 2 with entries gamma^(t-s) instead of 1.
+ * rows: the output rows to compute (NULL = all L, in order); out: [nrows, dv]. */
+void orc_decay_scores_first(const double *fq, const double *fk, const double *v, long L, int D,
+                            int dv, double gamma, int normalize, const long *rows, long nrows,
+                            double *out)
+{
+    double *num = (double *)malloc(sizeof(double) * (size_t)dv);
+    long n = rows ? nrows : L;
+    for (long r = 0; r < n; ++r) {
+        long t = rows ? rows[r] : r;
+        double den = 0.0;
+        for (int j = 0; j < dv; ++j) num[j] = 0.0;
+        for (long s = 0; s <= t; ++s) {
+            double a = pow(gamma, (double)(t - s)) * dot(fq + t * D, fk + s * D, D);
+            for (int j = 0; j < dv; ++j) num[j] += a * v[s * dv + j];
+            den += a;
+        }
+        for (int j = 0; j < dv; ++j) out[r * dv + j] = normalize ? num[j] / den : num[j];
+    }
+    free(num);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -400,3 +400,102 @@ def test_noncausal_normalised_equals_matrix_products():
             for method in ("recurrence", "scores_first"):
                 got = oracle.forward(q, k, v, fm=fm, normalize=norm, method=method, causal=False)
                 assert np.allclose(got, want, rtol=1e-12, atol=1e-12), (fm, norm, method)
+
+
+# ---------------------------------------------------------------------------
+# Retention decay: "Linear Attention / Performerの理論と実装", the section on the RNN
+# without forgetting (S_t = gamma S_{t-1} + phi(k_t) v_t^T, 0 < gamma < 1)
+# ---------------------------------------------------------------------------
+def _decay_both(q, k, v, gamma, normalize=False):
+    a = oracle.forward(q, k, v, normalize=normalize, gamma=gamma, method="recurrence")
+    b = oracle.forward(q, k, v, normalize=normalize, gamma=gamma, method="scores_first")
+    return a, b
+
+
+@pytest.mark.parametrize("gamma", [0.5, 0.9, 0.98])
+def test_decay_geometric_series_closed_form(gamma):
+    """One feature, q = k = v = 1: y_t = sum_{s<=t} gamma^(t-s) = (1 - gamma^(t+1)) / (1 -
+    gamma).  A wrong exponent (gamma^(t-s+1), gamma^(s-t)) or decaying after the write
+    breaks it at t = 0 already."""
+    L = 40
+    one = np.ones((1, L, 1))
+    t = np.arange(L)
+    want = (1 - gamma ** (t + 1)) / (1 - gamma)
+    for got in _decay_both(one, one, one, gamma):
+        assert np.allclose(got[0, :, 0], want, rtol=1e-13, atol=0)
+
+
+def test_decay_single_value_spike():
+    """Only v_{s0} is non-zero: y_t = gamma^(t-s0) (q_t . k_{s0}) v_{s0} for t >= s0 and 0
+    before, with random q, k (fixes the direction of the exponent and the index s)."""
+    rng = np.random.default_rng(11)
+    L, d, dv, s0, gamma = 30, 5, 3, 7, 0.83
+    q, k = rng.normal(size=(1, L, d)), rng.normal(size=(1, L, d))
+    v = np.zeros((1, L, dv))
+    v[0, s0] = rng.normal(size=dv)
+    want = np.zeros((L, dv))
+    for t in range(s0, L):
+        want[t] = gamma ** (t - s0) * (q[0, t] @ k[0, s0]) * v[0, s0]
+    for got in _decay_both(q, k, v, gamma):
+        assert np.allclose(got[0], want, rtol=1e-12, atol=1e-14)
+
+
+def test_decay_gamma_one_is_plain_linear_attention():
+    """gamma = 1 leaves the additive update S_t = S_{t-1} + phi(k_t) v_t^T: on small
+    integers both decay routines equal numpy's tril(q k^T) v exactly."""
+    rng = np.random.default_rng(12)
+    q, k, v = ints(rng, (2, 23, 4)), ints(rng, (2, 23, 4)), ints(rng, (2, 23, 3))
+    want = np.stack([np.tril(q[h] @ k[h].T) @ v[h] for h in range(2)])
+    for got in _decay_both(q, k, v, 1.0):
+        assert np.array_equal(got, want)
+
+
+def test_decay_normalised_constant_values():
+    """Normalised with z decaying alike, y_t is a weighted mean of the values: constant
+    values come back unchanged for any gamma (positive elu+1 features keep den > 0)."""
+    rng = np.random.default_rng(13)
+    q, k = rng.normal(size=(1, 50, 6)), rng.normal(size=(1, 50, 6))
+    v = np.full((1, 50, 4), 2.5)
+    for gamma in (0.6, 0.95):
+        for method in ("recurrence", "scores_first"):
+            got = oracle.forward(q, k, v, fm="elu1", normalize=True, gamma=gamma, method=method)
+            assert np.allclose(got, 2.5, rtol=1e-13)
+
+
+def test_decay_matrix_form_with_numpy():
+    """The decayed causal output as one matrix expression, numpy only: (Q K^T * G) V with
+    G[t, s] = gamma^(t-s) for s <= t, 0 above the diagonal; normalised rows divide by
+    the row sums of Q K^T * G."""
+    rng = np.random.default_rng(14)
+    L, gamma = 45, 0.9
+    q, k = rng.normal(size=(2, L, 5)), rng.normal(size=(2, L, 5))
+    v = rng.normal(size=(2, L, 3))
+    t = np.arange(L)
+    G = np.tril(gamma ** (t[:, None] - t[None, :]).clip(min=0))
+    for norm in (False, True):
+        fq = np.where(q >= 0, q + 1, np.exp(q))
+        fk = np.where(k >= 0, k + 1, np.exp(k))
+        A = (fq @ np.swapaxes(fk, 1, 2)) * G
+        want = A @ v
+        if norm:
+            want = want / A.sum(-1, keepdims=True)
+        for m in ("recurrence", "scores_first"):
+            got = oracle.forward(q, k, v, fm="elu1", normalize=norm, gamma=gamma, method=m)
+            assert np.allclose(got, want, rtol=1e-11, atol=1e-12), norm
+
+
+def test_decay_printed_retention_after_ten_steps(golden):
+    """"Kimi K3 と Qwen 3.8 の Attention 機構比較分析", section 3.3.7: a memory written at
+    step 0 whose later keys are all orthogonal to it keeps gamma^t of itself; the page
+    prints about 0.82 for gamma = 0.98 after 10 steps.  Here: key e_1 with value 1 at
+    t = 0, keys e_2 (value 0) after, and the query e_1 reads the memory at t = 10."""
+    (gamma, steps, printed), = golden("decay_retention_gamma098_t10.txt")
+    gamma, steps, printed = float(gamma), int(steps), float(printed)
+    L, D = steps + 1, 2
+    k = np.zeros((1, L, D)); k[0, 0, 0] = 1; k[0, 1:, 1] = 1
+    q = np.zeros((1, L, D)); q[0, :, 0] = 1
+    v = np.zeros((1, L, 1)); v[0, 0, 0] = 1
+    for got in _decay_both(q, k, v, gamma):
+        kept = got[0, steps, 0]
+        assert abs(kept - printed) < 0.005
+        assert kept == pytest.approx(gamma ** steps, rel=1e-14)
