@@ -82,7 +82,7 @@ def workload_config(name, w, C):
     return {"workload": name, "B": w["B"], "H": w["H"], "L": w["L"], "dk": w["dk"],
             "dv": w["dv"], "C": C, "feature_map": w["fm"], "m": w["m"],
             "normalize": bool(w["normalize"]), "loglinear": bool(w.get("loglinear")),
-            "storage": w["dtype"]}
+            "storage": w["dtype"], **({"gamma": w["gamma"]} if w.get("gamma") else {})}
 
 
 def bytes_per_token(w):
@@ -216,7 +216,7 @@ def cpu_baseline(w, inp_heads, heads_used, threads):
     oracle.lib()
     t0 = time.perf_counter()
     oracle.forward(q, k, v, fm=w["fm"], omega=om, normalize=w["normalize"], lam=lam,
-                   method="recurrence", threads=threads)
+                   method="recurrence", threads=threads, gamma=w.get("gamma"))
     dt = time.perf_counter() - t0
     toks = heads_used * w["L"]
     return toks / dt, dt
@@ -339,12 +339,19 @@ def run_ours(args):
         B, H, L, -1).cuda()
     nl = 0 if lam is None else lam.shape[-1]
     fm = la.make_feature_map(w["fm"], w["m"], omega.data_ptr() if omega is not None else 0)
-    wsb = la.la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), nl, dtype)
+    gamma = w.get("gamma")  # Retention decay: la_decay_fwd
+    if gamma is not None and args.op != "forward":
+        raise SystemExit("decay workloads: --op forward only")
+    if gamma is None:
+        wsb = la.la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), nl, dtype)
+        rc, plan = la.la_chunked_plan(B, H, L, dk, dv, C, fm, int(w["normalize"]),
+                                      int(lam is not None), nl, dtype, path, 0)
+    else:
+        wsb = la.la_decay_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), gamma, dtype)
+        rc, plan = la.la_decay_plan(B, H, L, dk, dv, C, fm, int(w["normalize"]), gamma, dtype, path)
     ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
-    rc, plan = la.la_chunked_plan(B, H, L, dk, dv, C, fm, int(w["normalize"]), int(lam is not None),
-                                  nl, dtype, path, 0)
     if rc != la.LA_OK:
-        raise la.LAError(rc, "la_chunked_plan")
+        raise la.LAError(rc, "plan")
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
     lam_ptr = lam.data_ptr() if lam is not None else None
@@ -364,6 +371,10 @@ def run_ours(args):
             r = la.la_noncausal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
                                     L, dk, dv, fm, int(w["normalize"]), dtype, ws.data_ptr(), wsb,
                                     sptr)
+        elif gamma is not None:
+            r = la.la_decay_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L,
+                                dk, dv, C, fm, int(w["normalize"]), gamma, dtype, ws.data_ptr(),
+                                wsb, sptr, path)
         else:
             r = la.la_chunked_fwd_path(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
                                        H, L, dk, dv, C, fm, int(w["normalize"]), lam_ptr, nl, dtype,
@@ -420,6 +431,18 @@ def run_ours(args):
         qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
         def e2e_step():
+            if gamma is not None:
+                # no host-buffer entry point for the decay: the same copies, queued around it
+                qd.copy_(qh, non_blocking=True)
+                kd.copy_(kh, non_blocking=True)
+                vd.copy_(vh, non_blocking=True)
+                r = la.la_decay_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(), B,
+                                    H, L, dk, dv, C, fm, int(w["normalize"]), gamma, dtype,
+                                    ws.data_ptr(), wsb, sptr, path)
+                if r != la.LA_OK:
+                    raise la.LAError(r, "la_decay_fwd")
+                outh.copy_(out, non_blocking=True)
+                return
             r = la.la_chunked_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(),
                                        outh.data_ptr(), qd.data_ptr(), kd.data_ptr(),
                                        vd.data_ptr(), out.data_ptr(), B, H, L, dk, dv, C, fm,

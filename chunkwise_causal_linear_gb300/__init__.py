@@ -26,6 +26,7 @@ LA_ERR_CUDA = -5
 LA_ERR_TIMEOUT = -6
 LA_ERR_DEVICE = -7
 LA_ERR_SCRATCH_LIMIT = -8
+LA_ERR_ARG = -9
 
 LA_FM_IDENTITY, LA_FM_ELU1, LA_FM_FAVOR = 0, 1, 2
 LA_BF16, LA_F32 = 0, 1
@@ -38,6 +39,7 @@ EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_chunked_fwd_noalloc", "la_chunked_workspace_bytes", "la_chunked_plan",
            "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
            "la_decode_state_elems", "la_noncausal_fwd", "la_noncausal_workspace_bytes",
+           "la_decay_fwd", "la_decay_decode_step", "la_decay_workspace_bytes", "la_decay_plan",
            "la_version")
 
 
@@ -107,6 +109,16 @@ def lib() -> ctypes.CDLL:
             L.la_noncausal_fwd.restype = i
             L.la_noncausal_workspace_bytes.argtypes = [i, i, i, i, i, fmp, i, i]
             L.la_noncausal_workspace_bytes.restype = sz
+            f = ctypes.c_float
+            L.la_decay_fwd.argtypes = [p, p, p, p, i, i, i, i, i, i, fmp, i, f, i, p, sz, p, i]
+            L.la_decay_fwd.restype = i
+            L.la_decay_decode_step.argtypes = [p, p, p, p, p, p, i, i, i, i, fmp, i, f, i, p]
+            L.la_decay_decode_step.restype = i
+            L.la_decay_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, f, i]
+            L.la_decay_workspace_bytes.restype = sz
+            L.la_decay_plan.argtypes = [i, i, i, i, i, i, fmp, i, f, i, i, i,
+                                        ctypes.POINTER(la_plan_info)]
+            L.la_decay_plan.restype = i
             L.la_version.argtypes = []
             L.la_version.restype = ctypes.c_char_p
             _lib = L
@@ -209,6 +221,30 @@ def la_noncausal_workspace_bytes(B, H, L, dk, dv, feature_map, normalize, dtype)
     return lib().la_noncausal_workspace_bytes(B, H, L, dk, dv, _fm(feature_map), normalize, dtype)
 
 
+def la_decay_fwd(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype,
+                 workspace, workspace_bytes, stream, path) -> int:
+    return lib().la_decay_fwd(q, k, v, out, B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                              gamma, dtype, workspace, workspace_bytes, stream, path)
+
+
+def la_decay_decode_step(q, k, v, out, state, zstate, B, H, dk, dv, feature_map, normalize,
+                         gamma, dtype, stream) -> int:
+    return lib().la_decay_decode_step(q, k, v, out, state, zstate, B, H, dk, dv,
+                                      _fm(feature_map), normalize, gamma, dtype, stream)
+
+
+def la_decay_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype) -> int:
+    return lib().la_decay_workspace_bytes(B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                          gamma, dtype)
+
+
+def la_decay_plan(B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype, path, num_sms=0):
+    info = la_plan_info()
+    rc = lib().la_decay_plan(B, H, L, dk, dv, C, _fm(feature_map), normalize, gamma, dtype, path,
+                             num_sms, ctypes.byref(info))
+    return rc, info.as_dict()
+
+
 def la_version() -> str:
     return lib().la_version().decode()
 
@@ -277,6 +313,56 @@ def decode_step(q, k, v, state, zstate=None, t=0, feature_map="identity", omega=
         raise LAError(rc, "la_decode_step")
     return out
 
+
+
+def decay_fwd(q, k, v, gamma, C=64, feature_map="identity", omega=None, normalize=False,
+              out=None, workspace=None, stream=None, path=LA_PATH_AUTO):
+    """Causal linear attention with the Retention decay gamma (la_decay_fwd) of CUDA
+    tensors q,k [B,H,L,dk], v [B,H,L,dv]."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, L, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    need = la_decay_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), float(gamma), dtype)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_decay_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, dk, dv,
+                      C, fm, int(normalize), float(gamma), dtype,
+                      workspace.data_ptr() if need else None, need, stream, path)
+    if rc != LA_OK:
+        raise LAError(rc, "la_decay_fwd")
+    return out
+
+
+def decay_decode_step(q, k, v, state, gamma, zstate=None, feature_map="identity", omega=None,
+                      normalize=False, out=None, stream=None):
+    """One decoding step with the Retention decay (la_decay_decode_step); state / zstate
+    from decode_state().  Returns out [B,H,dv]."""
+    import torch
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_decay_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              state.data_ptr(), zstate.data_ptr() if zstate is not None else None,
+                              B, H, dk, dv, fm, int(normalize), float(gamma), dtype, stream)
+    if rc != LA_OK:
+        raise LAError(rc, "la_decay_decode_step")
+    return out
 
 
 def _dtype_code(t):

@@ -2,6 +2,7 @@
 //
 // Declarations and the meaning of every argument: include/la_chunked.h.
 #include <limits.h>
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -28,7 +29,8 @@ int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int nor
                  int num_levels, long long t, bool loglinear, int *D_out, int *r_out);
 int decode_launch(const void *q, const void *k, const void *v, void *out, float *S, float *z, int B,
                   int H, int dk, int dv, const la_feature_map *fm, int normalize, const float *lam,
-                  int num_levels, long long t, int dtype, cudaStream_t stream);
+                  int num_levels, long long t, int dtype, cudaStream_t stream,
+                  float gamma);
 
 int required_levels(int L)
 {
@@ -119,6 +121,16 @@ static int check_problem(int B, int H, int L, int dk, int dv, int C, const la_fe
     return LA_OK;
 }
 
+// Decay factor: 0 < gamma <= 1 (NaN fails the test); gamma = 1 is the plain recurrence.
+static int set_decay(Problem *p, float gamma)
+{
+    if (!(gamma > 0.f && gamma <= 1.f)) return LA_ERR_ARG;
+    p->decay = 1;
+    p->gamma = gamma;
+    p->l2g = (float)log2((double)gamma);
+    return LA_OK;
+}
+
 static size_t simt_ws(const Problem &p, bool loglinear)
 {
     return simt_workspace_bytes(p.B, p.H, p.L, p.D, p.dv, p.C, loglinear);
@@ -154,13 +166,14 @@ static int plan_problem(const Problem &p, bool loglinear, int path, int num_sms,
 static int run(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
                int dk, int dv, int C, const la_feature_map *fm, int normalize,
                const float *lam, int num_levels, int dtype, void *ws, size_t ws_bytes,
-               void *stream, int path)
+               void *stream, int path, bool decay = false, float gamma = 1.f)
 {
     if (!q || !k || !v || !out) return LA_ERR_NULL;
     const bool ll = lam != nullptr;
     Problem p;
     int rc = check_problem(B, H, L, dk, dv, C, fm, normalize, ll, num_levels, dtype, &p);
     if (rc != LA_OK) return rc;
+    if (decay && (rc = set_decay(&p, gamma)) != LA_OK) return rc;
     if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
     const int sms = device_sms();
     if (sms <= 0) return LA_ERR_CUDA;
@@ -184,9 +197,9 @@ static int run(const void *q, const void *k, const void *v, void *out, int B, in
     if (!p.err) return LA_ERR_CUDA;
     if (trace_enabled())
         fprintf(stderr,
-                "[la] B=%d H=%d L=%d dk=%d dv=%d C=%d D=%d fm=%d norm=%d ll=%d dtype=%d -> "
+                "[la] B=%d H=%d L=%d dk=%d dv=%d C=%d D=%d fm=%d norm=%d ll=%d gamma=%g dtype=%d -> "
                 "path=%d grid=(%d,%d) block=%d smem=%d ws=%zu launches=%d\n",
-                B, H, L, dk, dv, p.C, p.D, p.fm, p.normalize, (int)ll, dtype, info.path,
+                B, H, L, dk, dv, p.C, p.D, p.fm, p.normalize, (int)ll, decay ? gamma : 1.0, dtype, info.path,
                 info.grid_x, info.grid_y, info.block, info.smem_bytes, info.workspace_bytes,
                 info.n_launches);
     if (info.path == LA_PATH_TC) return tc_launch(p, sms);
@@ -308,6 +321,7 @@ const char *la_status_string(int status)
     case LA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
     case LA_ERR_DEVICE: return "a device-side check failed";
     case LA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed no-alloc buffer (8 MiB) holds";
+    case LA_ERR_ARG: return "an argument value is out of range";
     default: return "unknown status";
     }
 }
@@ -334,7 +348,20 @@ int la_decode_step(const void *q, const void *k, const void *v, void *out, float
     if (normalize && !zstate) return LA_ERR_NULL;
     if ((long long)B * H > INT_MAX / 2) return LA_ERR_SHAPE;
     return decode_launch(q, k, v, out, state, zstate, B, H, dk, dv, feature_map, normalize,
-                         level_weights, num_levels, t, dtype, (cudaStream_t)stream);
+                         level_weights, num_levels, t, dtype, (cudaStream_t)stream, 1.f);
+}
+
+int la_decay_decode_step(const void *q, const void *k, const void *v, void *out, float *state,
+                         float *zstate, int B, int H, int dk, int dv,
+                         const la_feature_map *feature_map, int normalize, float gamma,
+                         int dtype, void *stream)
+{
+    if (!q || !k || !v || !out || !state) return LA_ERR_NULL;
+    if (normalize && !zstate) return LA_ERR_NULL;
+    if ((long long)B * H > INT_MAX / 2) return LA_ERR_SHAPE;
+    if (!(gamma > 0.f && gamma <= 1.f)) return LA_ERR_ARG;
+    return decode_launch(q, k, v, out, state, zstate, B, H, dk, dv, feature_map, normalize,
+                         nullptr, 0, 0, dtype, (cudaStream_t)stream, gamma);
 }
 
 long long la_decode_state_elems(int B, int H, int dk, int dv, const la_feature_map *feature_map,
@@ -393,6 +420,43 @@ int la_noncausal_fwd(const void *q, const void *k, const void *v, void *out, int
     p.err = err_ptr();
     if (!p.err) return LA_ERR_CUDA;
     return tc ? tc_nc_launch(p, sms) : nc_simt_launch(p);
+}
+
+// ---- decay (Retention)
+int la_decay_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                 int dk, int dv, int C, const la_feature_map *feature_map, int normalize,
+                 float gamma, int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                 int path)
+{
+    return run(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, nullptr, 0, dtype,
+               workspace, workspace_bytes, stream, path, true, gamma);
+}
+
+size_t la_decay_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                const la_feature_map *feature_map, int normalize, float gamma,
+                                int dtype)
+{
+    Problem p;
+    if (check_problem(B, H, L, dk, dv, C, feature_map, normalize, false, 0, dtype, &p) != LA_OK ||
+        set_decay(&p, gamma) != LA_OK)
+        return 0;
+    const int sms = device_sms();
+    la_plan_info info;
+    if (plan_problem(p, false, LA_PATH_AUTO, sms > 0 ? sms : 152, &info) != LA_OK) return 0;
+    return info.workspace_bytes;  // the generic path needs none
+}
+
+int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_map *feature_map,
+                  int normalize, float gamma, int dtype, int path, int num_sms, la_plan_info *info)
+{
+    if (!info) return LA_ERR_NULL;
+    Problem p;
+    int rc = check_problem(B, H, L, dk, dv, C, feature_map, normalize, false, 0, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if ((rc = set_decay(&p, gamma)) != LA_OK) return rc;
+    if (num_sms <= 0) num_sms = device_sms();
+    if (num_sms <= 0) return LA_ERR_CUDA;
+    return plan_problem(p, false, path, num_sms, info);
 }
 
 const char *la_version(void) { return "0.1.0"; }

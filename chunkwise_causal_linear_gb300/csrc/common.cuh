@@ -55,6 +55,9 @@ struct Problem {
     size_t workspace_bytes;
     cudaStream_t stream;
     int *err;                // device error word
+    int decay;               // 1: Retention decay S_t = gamma S_{t-1} + phi(k_t) v_t^T
+    float gamma;             // decay factor, 0 < gamma <= 1
+    float l2g;               // log2(gamma), rounded from the double value
 };
 
 // Host-side queries used by the planner.

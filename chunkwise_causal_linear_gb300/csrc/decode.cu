@@ -9,7 +9,8 @@
 //     out_t = lambda^(0) (q_t.k_t) v_t + sum_{l>=1} lambda^(l) q_t^T S^(l)
 // from the states before the update, and then, with r = trailing zeros of t+1, level r+1
 // becomes k_t v_t^T + sum_{l<=r} S^(l) and levels 1..r are emptied (the normaliser levels
-// z^(l) alike).
+// z^(l) alike).  With the Retention decay of the first page (S_t = gamma S_{t-1} + phi(k_t)
+// v_t^T) the old state and normaliser are scaled by gamma before the token joins them.
 //
 // A decoding step moves the whole state through the SM once (read and write), so it is
 // bandwidth-bound; it runs on the CUDA cores.  Grid: one CTA per head (so z is read and
@@ -37,6 +38,7 @@ struct DecArgs {
     const float *omega;  // FAVOR+: [m][dk]
     const float *lam;    // log-linear: [BH][NL] for this token, else NULL
     int nl, r;           // log-linear: levels, trailing zeros of t+1
+    float gamma;         // decay of the plain state (1: none)
 };
 
 template <typename T>
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecArgs a)
         if (!lam) {
             float *z = a.z + (size_t)head * D;
             for (int i = tid; i < D; i += DEC_THREADS) {
-                const float zi = z[i] + fk[i];
+                const float zi = a.gamma * z[i] + fk[i];
                 z[i] = zi;
                 den = fmaf(fq[i], zi, den);
             }
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecArgs a)
                 // S += phi(k) v^T, then phi(q) S
                 float *S = a.S + (size_t)head * sz;
                 for (int i = rg; i < D; i += DEC_RG) {
-                    const float sv = S[(size_t)i * a.dv + jj] + fk[i] * vj;
+                    const float sv = a.gamma * S[(size_t)i * a.dv + jj] + fk[i] * vj;
                     S[(size_t)i * a.dv + jj] = sv;
                     num = fmaf(fq[i], sv, num);
                 }
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(DV_THREADS) decode_vec_kernel(const DecArgs a)
     if (a.normalize) {
         float *z = a.z + (size_t)head * D;
         for (int i = tid; i < D; i += DV_THREADS) {
-            const float zi = z[i] + fk[i];
+            const float zi = a.gamma * z[i] + fk[i];
             z[i] = zi;
             den = fmaf(fq[i], zi, den);
         }
@@ -256,11 +258,11 @@ __global__ void __launch_bounds__(DV_THREADS) decode_vec_kernel(const DecArgs a)
             for (int u = 0; u < RGI; ++u) {
                 const int i = i0 + u * RG;
                 if (i < D) {
-                    const float f = fk[i], g = fq[i];
-                    sv[u].x = fmaf(f, v0, sv[u].x);
-                    sv[u].y = fmaf(f, v1, sv[u].y);
-                    sv[u].z = fmaf(f, v2, sv[u].z);
-                    sv[u].w = fmaf(f, v3, sv[u].w);
+                    const float f = fk[i], g = fq[i], gm = a.gamma;
+                    sv[u].x = fmaf(f, v0, gm * sv[u].x);
+                    sv[u].y = fmaf(f, v1, gm * sv[u].y);
+                    sv[u].z = fmaf(f, v2, gm * sv[u].z);
+                    sv[u].w = fmaf(f, v3, gm * sv[u].w);
                     S[(size_t)i * nq] = sv[u];
                     num.x = fmaf(g, sv[u].x, num.x);
                     num.y = fmaf(g, sv[u].y, num.y);
@@ -313,7 +315,7 @@ int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int nor
 
 int decode_launch(const void *q, const void *k, const void *v, void *out, float *S, float *z, int B,
                   int H, int dk, int dv, const la_feature_map *fm, int normalize, const float *lam,
-                  int num_levels, long long t, int dtype, cudaStream_t stream)
+                  int num_levels, long long t, int dtype, cudaStream_t stream, float gamma)
 {
     int D = 0, r = 0;
     int rc = decode_check(B, H, dk, dv, fm, normalize, num_levels, t, lam != nullptr, &D, &r);
@@ -330,6 +332,7 @@ int decode_launch(const void *q, const void *k, const void *v, void *out, float 
     a.lam = lam;
     a.nl = lam ? num_levels : 0;
     a.r = r;
+    a.gamma = gamma;
     if (!lam && a.fm != LA_FM_FAVOR && dv % 4 == 0 && dv <= 512) {
         const int RG = DV_THREADS / (dv / 4);
         const size_t vsm = sizeof(float) * ((size_t)2 * D + (size_t)RG * dv + DV_THREADS);

@@ -17,6 +17,12 @@
 // the chunk plus every lower level, and the lower levels are emptied.  These level
 // states live in the caller's workspace (global memory).
 //
+// Decay (the Retention update S_t = gamma S_{t-1} + phi(k_t) v_t^T of "Linear Attention /
+// Performerの理論と実装", z decaying alike): with i, j rows of the chunk, the inter part is
+// weighted by gamma^(i+1), the in-chunk scores by gamma^(i-j), and the chunk joins the
+// state as S <- gamma^len S + sum_j gamma^(len-1-j) phi(k_j) v_j^T.  Powers are exp2 of
+// log2(gamma) times the integer exponent.
+//
 // Every product accumulates in fp32 in a fixed order; on small-integer inputs whose
 // partial sums stay below 2^24 the result is exact.  Rows are handled in tiles of R, so
 // any chunk size C >= 1 works (tiles never straddle a chunk boundary).
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                         }
                     }
                 }
+                if (p.decay) acc *= exp2f(p.l2g * (float)(qt + r + 1));
                 sAcc[e] = acc;
             }
             for (int r = tid; r < R; r += NT) {
@@ -187,6 +194,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                             den += lam[(long)t * p.nl + 1 + a.log2C + jl] * part;
                         }
                     }
+                    if (p.decay) den *= exp2f(p.l2g * (float)(qt + r + 1));
                 }
                 sDen[r] = den;
             }
@@ -206,6 +214,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                     if (r < nq && s < nk && u <= t) {
                         for (int i = 0; i < D; ++i) sc += sQ[r * D + i] * sK[s * D + i];
                         if (ll) sc *= lam[(long)(c0 + t) * p.nl + fenwick_level(c0 + t, c0 + u)];
+                        if (p.decay) sc *= exp2f(p.l2g * (float)(t - u));
                     }
                     sP[e] = sc;
                 }
@@ -253,6 +262,9 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
             }
             __syncthreads();
         }
+        // decay: the state so far fades by gamma^cl over the chunk (each thread scales the
+        // elements it updates below, before their first update)
+        const float gl = p.decay ? exp2f(p.l2g * (float)cl) : 1.f;
         for (int kt = 0; kt < cl; kt += R) {
             const int nk = min(R, cl - kt);
             load_phi_rows<T>(k, c0 + kt, nk, a, sK, sX, sNrm);
@@ -260,18 +272,22 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                 const int s = e / WV, j = e - s * WV;
                 sV[e] = (s < nk && j < wv) ? to_f32(v[(long)(c0 + kt + s) * dv + j0 + j]) : 0.f;
             }
+            if (p.decay) {
+                // key row kt + s of the chunk weighted by gamma^(cl - 1 - kt - s)
+                for (int e = tid; e < nk * D; e += NT) sK[e] *= exp2f(p.l2g * (float)(cl - 1 - kt - e / D));
+            }
             __syncthreads();
             for (int e = tid; e < D * WV; e += NT) {
                 const int i = e / WV, j = e - i * WV;
                 float acc = 0.f;
                 for (int s = 0; s < nk; ++s) acc += sK[s * D + i] * sV[s * WV + j];
-                tS[e] += acc;
+                tS[e] = (kt == 0 ? gl * tS[e] : tS[e]) + acc;
             }
             if (p.normalize)
                 for (int i = tid; i < D; i += NT) {
                     float acc = 0.f;
                     for (int s = 0; s < nk; ++s) acc += sK[s * D + i];
-                    tz[i] += acc;
+                    tz[i] = (kt == 0 ? gl * tz[i] : tz[i]) + acc;
                 }
             __syncthreads();
         }

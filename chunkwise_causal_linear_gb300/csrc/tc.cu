@@ -38,6 +38,19 @@
 //   state   S^T  += V_j^T phi(K_j)               M=dv  N=D      K=CH  per chunk j
 //   intra   O^T  += V_T^T P_T^T                  M=dv  N=T      K=T   once per tile
 //
+// Decay (the Retention update S_t = gamma S_{t-1} + phi(k_t) v_t^T of "Linear Attention /
+// Performerの理論と実装", one chunk per tile): with i, j the rows of the chunk,
+//     y_i = gamma^(i+1) phi(q_i) S + sum_{j<=i} gamma^(i-j) (phi(q_i).phi(k_j)) v_j.
+// The feature-map group writes K~_j = gamma^(C-1-j) phi(k_j), so the unmasked scores carry
+// gamma^(C-1-j); the state copy that the inter product reads is gamma^C S, so the sum that
+// lands in O^T is gamma^(C-1-i) y_i and the epilogue multiplies by gamma^(i+1-C) (with the
+// normaliser the factor cancels: z rides along as gamma^C z, and den gets the same
+// factor).  The chunk's state update S^T += V^T K~ then adds sum_j gamma^(C-1-j) phi(k_j)
+// v_j^T onto the fp32 accumulator, which the readback warps have scaled to gamma^C S in
+// place (load, scale, store back) when they made the bf16 copy.  The totals pass scales
+// each key by gamma^(segment end - s) instead and needs no rescaling of the accumulator;
+// a segment starts from sum_g gamma^(rows after segment g) T_g.
+//
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA records
 // LA_ERR_TIMEOUT in the device error word, raises a shared abort flag that the other roles
 // poll, drains its own async copies / MMAs, frees TMEM and exits.
@@ -82,7 +95,11 @@ struct TcArgs {
     // segments' totals, the state is never updated, and P is zero, so each row gets exactly
     // phi(q) S_total (/ phi(q) z_total).
     int noncausal, nseg_all;
+    float l2g;  // decay: log2(gamma)
 };
+
+// kernel modes
+constexpr int TC_CAUSAL = 0, TC_NONCAUSAL = 1, TC_DECAY = 2;
 
 template <int D, int DV, int C, bool NORM>
 struct TcLayout {
@@ -129,11 +146,14 @@ __device__ __forceinline__ float phi1(float x)
     return x;
 }
 
-template <int D, int DV, int CH, int FM, bool NORM, bool NC>
+template <int D, int DV, int CH, int FM, bool NORM, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_constant__ TcArgs a)
 {
     constexpr int C = 64;           // rows per tile
     constexpr int NSUB = C / CH;    // chunks per tile
+    constexpr bool NC = MODE == TC_NONCAUSAL;
+    constexpr bool DK = MODE == TC_DECAY;
+    static_assert(!DK || CH == C, "decay: one chunk per tile");
     using Lay = TcLayout<D, DV, C, NORM>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles (offset taken in the shared window)
@@ -165,6 +185,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     const int nch = min(a.seg_tiles, a.nch - tile0);     // tiles of this CTA
     const bool totals = a.totals != 0;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
+    const float gC = DK ? exp2f(a.l2g * (float)C) : 1.f;  // gamma^C
+    // decay: weight of earlier segment g's total at this segment's start
+    auto seg_w = [&](int g) { return DK ? exp2f(a.l2g * (float)((seg - 1 - g) * a.seg_tiles * C)) : 1.f; };
 
     auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
     auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
@@ -205,10 +228,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         for (int i = tid; i < D; i += TC_THREADS) {
             float z0 = 0.f;
             if (!totals)
-                for (int g = 0; g < (NC ? a.nseg_all : seg); ++g) z0 += a.ws_z[((size_t)g * a.BH + head) * D + i];
+                for (int g = 0; g < (NC ? a.nseg_all : seg); ++g)
+                    z0 += seg_w(g) * a.ws_z[((size_t)g * a.BH + head) * D + i];
             zs[i] = z0;
         }
     }
+    if (DK && !NORM)
+        for (int i = tid; i < C; i += TC_THREADS) rden[i] = exp2f(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_async_smem();
     tc_fence_before();
@@ -231,12 +257,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             if (live)
                 for (int g = 0; g < nprev; ++g) {
                     const float4 *src = (const float4 *)(a.ws_T + (((size_t)g * a.BH + head) * DV + jr) * D + col);
+                    const float w = seg_w(g);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float4 v4 = src[q];
-                        acc[4 * q] += v4.x; acc[4 * q + 1] += v4.y; acc[4 * q + 2] += v4.z; acc[4 * q + 3] += v4.w;
+                        acc[4 * q] += w * v4.x; acc[4 * q + 1] += w * v4.y;
+                        acc[4 * q + 2] += w * v4.z; acc[4 * q + 3] += w * v4.w;
                     }
                 }
+            if (DK)  // the first chunk reads gamma^C S and accumulates onto it
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] *= gC;
             uint32_t w32[16], w16[8];
 #pragma unroll
             for (int e = 0; e < 16; ++e) w32[e] = __float_as_uint(acc[e]);
@@ -291,7 +322,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 // totals pass: only the state, over whole tiles
                 for (int c = 0; c < nch; ++c) {
                     const int s = c % TC_STAGES;
-                    uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM) ? &full[s] : &phi_ready[s];
+                    uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM && !DK) ? &full[s] : &phi_ready[s];
                     if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) {
                         ok = false;
                         break;
@@ -309,7 +340,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             }
             for (int c = 0; ok && c < nch; ++c) {
                 const int s = c % TC_STAGES, b = c & 1;
-                uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM) ? &full[s] : &phi_ready[s];
+                uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM && !DK) ? &full[s] : &phi_ready[s];
                 if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
                 if (c >= 2 && !wait_phase(&a_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 tc_fence_after();
@@ -382,7 +413,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const int kb = g >> 3, ch = g & 7;
         const int q_swz = kb * C * 128 + ((ch ^ (rg & 7)) << 4) + rg * 128;
         const int k_swz = kb * Lay::K_BLK + ((ch ^ (rg & 7)) << 4) + rg * 128;
-        if (FM != LA_FM_IDENTITY || NORM) {
+        if (FM != LA_FM_IDENTITY || NORM || DK) {
             for (int c = 0; c < nch; ++c) {
                 const int s = c % TC_STAGES;
                 if (!group_wait(ft == 0, 1, &full[s], (c / TC_STAGES) & 1, nullptr, 0, false, ctl,
@@ -401,7 +432,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const int zkb = ft / 16, zr = (ft / 8) & 1, zch = ft & 7;
                     const float4 z0 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4];
                     const float4 z1 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4 + 1];
-                    const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+                    // decay: gamma^C z, matching the state copy the inter product reads
+                    const float zz[8] = {gC * z0.x, gC * z0.y, gC * z0.z, gC * z0.w,
+                                         gC * z1.x, gC * z1.y, gC * z1.z, gC * z1.w};
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -431,20 +464,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     // rows past L are TMA zero fill and phi(0) may be nonzero (elu+1): keep them out
                     // of z where z is used after the last tile (the non-causal totals)
                     const bool in_seq = !NC || (tile0 + c) * C + rg + n * RG < a.L;
+                    // decay: key row r weighted by gamma^(C-1-r), or by gamma^(segment end - row)
+                    // in the totals pass
+                    float rf = 1.f;
+                    if (DK) {
+                        const int r = rg + n * RG;
+                        rf = exp2f(a.l2g * (float)(C - 1 - r + (totals ? (nch - 1 - c) * C : 0)));
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
+                        float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
+                        if (DK) {
+                            x0 *= rf;
+                            x1 *= rf;
+                        }
                         if (NORM && in_seq) {
                             colsum[2 * e] += x0;
                             colsum[2 * e + 1] += x1;
                         }
-                        if (FM != LA_FM_IDENTITY) wv[e] = pack_bf16x2(x0, x1);
+                        if (FM != LA_FM_IDENTITY || DK) wv[e] = pack_bf16x2(x0, x1);
                     }
                 }
-                if (FM != LA_FM_IDENTITY) {
+                if (FM != LA_FM_IDENTITY || DK) {
 #pragma unroll
                     for (int n = 0; n < NR; ++n) {
-                        if (!totals) qp[n * RG * 8] = wq[n];
+                        if (FM != LA_FM_IDENTITY && !totals) qp[n * RG * 8] = wq[n];
                         kp[n * RG * 8] = wk[n];
                     }
                 }
@@ -470,7 +514,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         float acc = 0.f;
 #pragma unroll
                         for (int w = 0; w < TC_FWARPS; ++w) acc += zpart[w * D + i];
-                        zs[i] += acc;
+                        zs[i] = (DK && !totals) ? gC * zs[i] + acc : zs[i] + acc;
                     }
                     named_bar(1, NF);
                 }
@@ -582,6 +626,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     uint32_t sv[32], pk[16];
                     tmem_ld32(tS + lane_off + cb * 32, sv);
                     tmem_wait_ld();
+                    if (DK) {
+                        // gamma^C S: the next chunk's inter product reads it and its state
+                        // update accumulates onto it
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(gC * __uint_as_float(sv[e]));
+                        tmem_st16(tS + lane_off + cb * 32, *reinterpret_cast<const uint32_t(*)[16]>(sv));
+                        tmem_st16(tS + lane_off + cb * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(sv + 16));
+                    }
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack_bf16x2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]));
@@ -626,8 +678,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     if (lane == 0) mbar_arrive(&o_free[b]);
                 }
                 float rd[32];
-                if (NORM) {
-                    const float4 *rp = (const float4 *)(rden + slot * C + 32 * h);
+                if (NORM || DK) {
+                    // 1 / den per row, or (decay, no normaliser) gamma^(i+1-C)
+                    const float4 *rp = (const float4 *)(rden + (NORM ? slot * C : 0) + 32 * h);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 v = rp[q];
@@ -639,7 +692,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
-                    if (NORM) {
+                    if (NORM || DK) {
                         a0 *= rd[2 * u];
                         a1 *= rd[2 * u + 1];
                     }
@@ -684,8 +737,9 @@ size_t tc_workspace(const Problem &p, int nseg)
 }
 
 template <int D, int DV, int CH, int FM, bool NORM>
-int launch_t(const Problem &p, int num_sms, bool noncausal = false)
+int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
 {
+    const bool noncausal = mode == TC_NONCAUSAL;
     constexpr int C = 64;  // rows per tile
     using Lay = TcLayout<D, DV, C, NORM>;
     TcArgs a;
@@ -709,13 +763,20 @@ int launch_t(const Problem &p, int num_sms, bool noncausal = false)
     }
     a.noncausal = noncausal ? 1 : 0;
     a.nseg_all = nseg;
+    a.l2g = mode == TC_DECAY ? p.l2g : 0.f;
     a.err = p.err;
     a.timeout_ns = 2000000000ull;
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");
     if (e && *e) a.timeout_ns = strtoull(e, nullptr, 10);
     const char *st = getenv("LA_DEBUG_STALL");
     a.debug_stall = (st && *st && *st != '0') ? 1 : 0;
-    auto kern = noncausal ? tc_chunked_kernel<D, DV, CH, FM, NORM, true> : tc_chunked_kernel<D, DV, CH, FM, NORM, false>;
+    auto kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_CAUSAL>;
+    if constexpr (CH == C) {
+        if (mode == TC_NONCAUSAL) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_NONCAUSAL>;
+        if (mode == TC_DECAY) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_DECAY>;
+    } else if (mode != TC_CAUSAL) {
+        return LA_ERR_UNSUPPORTED;
+    }
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
         cudaSuccess)
         return LA_ERR_CUDA;
@@ -733,18 +794,20 @@ int launch_t(const Problem &p, int num_sms, bool noncausal = false)
 }
 
 template <int D, int DV, int CH>
-int launch_dc(const Problem &p, int sms)
+int launch_dc(const Problem &p, int sms, int mode = TC_CAUSAL)
 {
     const bool n = p.normalize != 0;
     if (p.fm == LA_FM_IDENTITY)
-        return n ? launch_t<D, DV, CH, LA_FM_IDENTITY, true>(p, sms)
-                 : launch_t<D, DV, CH, LA_FM_IDENTITY, false>(p, sms);
-    return n ? launch_t<D, DV, CH, LA_FM_ELU1, true>(p, sms) : launch_t<D, DV, CH, LA_FM_ELU1, false>(p, sms);
+        return n ? launch_t<D, DV, CH, LA_FM_IDENTITY, true>(p, sms, mode)
+                 : launch_t<D, DV, CH, LA_FM_IDENTITY, false>(p, sms, mode);
+    return n ? launch_t<D, DV, CH, LA_FM_ELU1, true>(p, sms, mode)
+             : launch_t<D, DV, CH, LA_FM_ELU1, false>(p, sms, mode);
 }
 
 template <int D, int DV>
 int launch_d(const Problem &p, int sms)
 {
+    if (p.decay) return launch_dc<D, DV, 64>(p, sms, TC_DECAY);
     if (p.C == 16) return launch_dc<D, DV, 16>(p, sms);
     if (p.C == 32) return launch_dc<D, DV, 32>(p, sms);
     return launch_dc<D, DV, 64>(p, sms);
@@ -768,6 +831,12 @@ int tcw_launch(const Problem &p, int num_sms);
 bool tc_supported(const Problem &p, int num_sms)
 {
     (void)num_sms;
+    if (p.decay) {
+        // one 64-row chunk per tile; gamma^64 >= 2^-64 keeps the scaled keys and the
+        // output factor gamma^(i+1-64) well inside the fp32 / bf16 range
+        if (p.lam || p.C != 64 || p.l2g < -1.f) return false;
+        if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
+    }
     if (p.lam) return tcl_supported(p);
     if (p.fm == LA_FM_FAVOR) return tcf_supported(p);
     if (p.C == 128 || p.C == 256) return tcw_supported(p);
@@ -840,10 +909,10 @@ int tc_nc_launch(const Problem &p, int num_sms)
         constexpr int D = decltype(d)::value, DV = decltype(dv)::value;
         const bool n = p.normalize != 0;
         if (p.fm == LA_FM_IDENTITY)
-            return n ? launch_t<D, DV, 64, LA_FM_IDENTITY, true>(p, num_sms, true)
-                     : launch_t<D, DV, 64, LA_FM_IDENTITY, false>(p, num_sms, true);
-        return n ? launch_t<D, DV, 64, LA_FM_ELU1, true>(p, num_sms, true)
-                 : launch_t<D, DV, 64, LA_FM_ELU1, false>(p, num_sms, true);
+            return n ? launch_t<D, DV, 64, LA_FM_IDENTITY, true>(p, num_sms, TC_NONCAUSAL)
+                     : launch_t<D, DV, 64, LA_FM_IDENTITY, false>(p, num_sms, TC_NONCAUSAL);
+        return n ? launch_t<D, DV, 64, LA_FM_ELU1, true>(p, num_sms, TC_NONCAUSAL)
+                 : launch_t<D, DV, 64, LA_FM_ELU1, false>(p, num_sms, TC_NONCAUSAL);
     };
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;

@@ -54,8 +54,9 @@ enum la_status {
     LA_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, copy, attribute)      */
     LA_ERR_TIMEOUT = -6,     /* device: a bounded wait gave up (read via la_last_device_status) */
     LA_ERR_DEVICE = -7,      /* device: an index or shape check failed inside a kernel    */
-    LA_ERR_SCRATCH_LIMIT = -8 /* la_chunked_fwd_noalloc: the problem needs more scratch than
-                                 its fixed buffer holds (8 MiB)                           */
+    LA_ERR_SCRATCH_LIMIT = -8, /* la_chunked_fwd_noalloc: the problem needs more scratch than
+                                  its fixed buffer holds (8 MiB)                          */
+    LA_ERR_ARG = -9            /* an argument value is out of range (la_decay_*: gamma)    */
 };
 
 /* ---- feature maps phi -------------------------------------------------------------- */
@@ -266,6 +267,46 @@ int la_noncausal_fwd(const void *q, const void *k, const void *v, void *out, int
 /* Workspace bytes la_noncausal_fwd needs (0 on an invalid or unsupported combination). */
 size_t la_noncausal_workspace_bytes(int B, int H, int L, int dk, int dv,
                                     const la_feature_map *feature_map, int normalize, int dtype);
+
+/*
+ * la_decay_fwd -- causal linear attention with the Retention decay ("Linear Attention /
+ * Performerの理論と実装", the section on the RNN without forgetting):
+ *     S_t = gamma S_{t-1} + phi(k_t) v_t^T,        out_t = phi(q_t)^T S_t,
+ * i.e. out_t = sum_{s<=t} gamma^(t-s) (phi(q_t).phi(k_s)) v_s.  With normalize the
+ * normaliser decays alike, z_t = gamma z_{t-1} + phi(k_t), and out_t = phi(q_t)^T S_t /
+ * phi(q_t)^T z_t (a weighted mean of the values; the page gives the update of S only).
+ *   gamma   0 < gamma <= 1, one value for every head; gamma = 1 is la_chunked_fwd's result.
+ *           Outside that range (or NaN): LA_ERR_ARG.
+ *   path    enum la_path.  LA_PATH_TC covers bf16, identity / elu+1 features, dk = D,
+ *           (dk, dv) in {(64, 64), (64, 128), (128, 128)}, C = 64, L >= 128 and
+ *           gamma >= 0.5 (gamma^64 >= 2^-64); LA_PATH_AUTO takes it there and the generic
+ *           fp32 path elsewhere (any C, dtype, feature map).
+ * Other arguments, layouts and errors as la_chunked_fwd (no level weights).  The workspace
+ * must hold la_decay_workspace_bytes(...) bytes (the few-head sequence split's totals).
+ */
+int la_decay_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                 int dk, int dv, int C, const la_feature_map *feature_map, int normalize,
+                 float gamma, int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                 int path);
+
+/* la_decode_step with the Retention decay: state = gamma state + phi(k) v^T, zstate =
+ * gamma zstate + phi(k), then out = phi(q)^T state (/ phi(q)^T zstate).  Stepping t =
+ * 0..L-1 from zero state reproduces la_decay_fwd's rows.  Buffers as la_decode_step without
+ * level weights ([B, H, D, dv] and [B, H, D] fp32).  gamma as la_decay_fwd (LA_ERR_ARG
+ * outside 0 < gamma <= 1). */
+int la_decay_decode_step(const void *q, const void *k, const void *v, void *out, float *state,
+                         float *zstate, int B, int H, int dk, int dv,
+                         const la_feature_map *feature_map, int normalize, float gamma,
+                         int dtype, void *stream);
+
+/* Workspace bytes la_decay_fwd needs (0 when none, or on invalid arguments). */
+size_t la_decay_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                const la_feature_map *feature_map, int normalize, float gamma,
+                                int dtype);
+
+/* la_chunked_plan for la_decay_fwd: the plan la_decay_fwd(path) would run. */
+int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_map *feature_map,
+                  int normalize, float gamma, int dtype, int path, int num_sms, la_plan_info *info);
 
 /* Library version string, e.g. "0.1.0". */
 const char *la_version(void);

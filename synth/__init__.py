@@ -120,7 +120,7 @@ def iid_gaussian(seed: int, m: int, d: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# the five measured workloads
+# the measured workloads
 # ---------------------------------------------------------------------------
 WORKLOADS = {
     # exactness case: integers in {-3..3} stored as fp32, identity features, no normaliser
@@ -139,6 +139,12 @@ WORKLOADS = {
     "favor-m256-d64-L16384": dict(B=2, H=12, L=16384, dk=64, dv=64, dtype="bf16",
                                   dist="normal", scale=1.0, fm="favor", m=256, normalize=True,
                                   C=64, Cs=(64,), loglinear=False),
+    # the elu+1 normalised workload with the Retention decay, gamma = 0.98 (the scalar gate
+    # value printed in the Kimi/Qwen comparison page, section 3.3.7)
+    "decay-elu1-norm-d128-L8192": dict(B=8, H=16, L=8192, dk=128, dv=128, dtype="bf16",
+                                       dist="normal", scale=1.0, fm="elu1", m=0,
+                                       normalize=True, C=64, Cs=(64,), loglinear=False,
+                                       gamma=0.98),
     # Fenwick-level-weighted log-linear mask, 17 level weights per token ~ U(0,1)
     "loglinear-d64-L65536": dict(B=1, H=16, L=65536, dk=64, dv=64, dtype="bf16",
                                  dist="normal", scale=1.0 / 8.0, fm="identity", m=0,

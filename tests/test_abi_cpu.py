@@ -164,3 +164,34 @@ def test_noncausal_workspace_and_errors(lib):
                                None) == la.LA_ERR_NULL
     assert la.la_noncausal_fwd(ok, ok, ok, ok, 1, 1, 8, 8, 8, fm, 0, la.LA_F32, None, 0,
                                None) in (la.LA_ERR_WORKSPACE, la.LA_ERR_CUDA)
+
+
+def test_decay_arguments_and_plan(lib):
+    fm = la.make_feature_map("elu1")
+    ok = ctypes.c_void_p(16)
+    for g in (0.0, -1.0, 1.0001, float("nan"), float("inf")):
+        assert la.la_decay_fwd(ok, ok, ok, ok, 1, 1, 256, 64, 64, 64, fm, 1, g, la.LA_BF16, None,
+                               0, None, la.LA_PATH_AUTO) == la.LA_ERR_ARG, g
+        assert la.la_decay_workspace_bytes(1, 1, 256, 64, 64, 64, fm, 1, g, la.LA_BF16) == 0
+        assert la.la_decay_decode_step(ok, ok, ok, ok, ok, ok, 1, 1, 64, 64, fm, 1, g,
+                                       la.LA_BF16, None) == la.LA_ERR_ARG, g
+    assert la.la_decay_fwd(None, ok, ok, ok, 1, 1, 256, 64, 64, 64, fm, 1, 0.9, la.LA_BF16,
+                           None, 0, None, 0) == la.LA_ERR_NULL
+    assert la.la_decay_decode_step(ok, ok, ok, ok, ok, None, 1, 1, 64, 64, fm, 1, 0.9,
+                                   la.LA_BF16, None) == la.LA_ERR_NULL
+    # tensor cores: C = 64 and gamma >= 0.5 only; the generic path takes the rest
+    rc, info = la.la_decay_plan(8, 16, 8192, 128, 128, 64, fm, 1, 0.98, la.LA_BF16,
+                                la.LA_PATH_AUTO, 152)
+    assert rc == la.LA_OK and info["path"] == la.LA_PATH_TC
+    for C, g in ((64, 0.49), (32, 0.98), (128, 0.98)):
+        rc, info = la.la_decay_plan(8, 16, 8192, 128, 128, C, fm, 1, g, la.LA_BF16,
+                                    la.LA_PATH_AUTO, 152)
+        assert rc == la.LA_OK and info["path"] == la.LA_PATH_SIMT, (C, g)
+        rc, _ = la.la_decay_plan(8, 16, 8192, 128, 128, C, fm, 1, g, la.LA_BF16, la.LA_PATH_TC,
+                                 152)
+        assert rc == la.LA_ERR_UNSUPPORTED
+    # few heads: the sequence split's totals need a workspace, as for the plain mask
+    rc, info = la.la_decay_plan(1, 1, 8192, 128, 128, 64, fm, 1, 0.98, la.LA_BF16,
+                                la.LA_PATH_AUTO, 152)
+    assert rc == la.LA_OK and info["n_launches"] == 2 and info["workspace_bytes"] > 0
+    assert la.la_status_string(la.LA_ERR_ARG) != "unknown status"
