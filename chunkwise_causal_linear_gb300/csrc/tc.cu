@@ -45,11 +45,19 @@
 // gamma^(C-1-j); the state copy that the inter product reads is gamma^C S, so the sum that
 // lands in O^T is gamma^(C-1-i) y_i and the epilogue multiplies by gamma^(i+1-C) (with the
 // normaliser the factor cancels: z rides along as gamma^C z, and den gets the same
-// factor).  The chunk's state update S^T += V^T K~ then adds sum_j gamma^(C-1-j) phi(k_j)
-// v_j^T onto the fp32 accumulator, which the readback warps have scaled to gamma^C S in
-// place (load, scale, store back) when they made the bf16 copy.  The totals pass scales
-// each key by gamma^(segment end - s) instead and needs no rescaling of the accumulator;
-// a segment starts from sum_g gamma^(rows after segment g) T_g.
+// factor).  The fp32 accumulator A is rescaled in TMEM (load, scale, store back) only
+// once every P chunks.  Inside a period, chunk m = 0..P-1 scales its keys by a further
+// gamma^(-C m); so that its scores, its inter product and its normaliser share that
+// factor, it reads the state copy gamma^(C (1-m)) S and the z rows gamma^(C (1-m)) z, and
+// the unnormalised epilogue multiplies by gamma^(i+1-C+C m).  After the update of chunk m,
+// A = gamma^(-C m) S_m, which is exactly the copy chunk m+1 needs; at the period's end the
+// readback scales A by gamma^(C P) (= gamma^C S), stores it back and copies it.  P is the
+// largest period with gamma^(C P) >= 2^-64 (at least 1, as gamma^C >= 2^-64), so every
+// factor used here, gamma^(C P) included, is a normal fp32 number (the factors come from
+// the flush-to-zero hardware ex2), and every scaled key, A and the copy stay well inside
+// the fp32 / bf16 range.  The totals pass scales each
+// key by gamma^(segment end - s) instead and needs no rescaling of the accumulator; a
+// segment starts from sum_g gamma^(rows after segment g) T_g.
 //
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA records
 // LA_ERR_TIMEOUT in the device error word, raises a shared abort flag that the other roles
@@ -96,6 +104,7 @@ struct TcArgs {
     // phi(q) S_total (/ phi(q) z_total).
     int noncausal, nseg_all;
     float l2g;  // decay: log2(gamma)
+    int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
 
 // kernel modes
@@ -133,6 +142,14 @@ struct TcLayout {
     static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
     static_assert(ALLOC <= 232448, "shared memory budget");
 };
+
+// 2^x on the SFU (hardware ex2, relative error ~2^-22, flush-to-zero): the decay factors
+__device__ __forceinline__ float ex2(float x)
+{
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x));
+    return e;
+}
 
 template <int FM>
 __device__ __forceinline__ float phi1(float x)
@@ -185,9 +202,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     const int nch = min(a.seg_tiles, a.nch - tile0);     // tiles of this CTA
     const bool totals = a.totals != 0;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
-    const float gC = DK ? exp2f(a.l2g * (float)C) : 1.f;  // gamma^C
+    const float gC = DK ? ex2(a.l2g * (float)C) : 1.f;  // gamma^C
     // decay: weight of earlier segment g's total at this segment's start
-    auto seg_w = [&](int g) { return DK ? exp2f(a.l2g * (float)((seg - 1 - g) * a.seg_tiles * C)) : 1.f; };
+    auto seg_w = [&](int g) { return DK ? ex2(a.l2g * (float)((seg - 1 - g) * a.seg_tiles * C)) : 1.f; };
 
     auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
     auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
@@ -234,7 +251,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         }
     }
     if (DK && !NORM)
-        for (int i = tid; i < C; i += TC_THREADS) rden[i] = exp2f(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
+        for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_async_smem();
     tc_fence_before();
@@ -414,8 +431,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const int q_swz = kb * C * 128 + ((ch ^ (rg & 7)) << 4) + rg * 128;
         const int k_swz = kb * Lay::K_BLK + ((ch ^ (rg & 7)) << 4) + rg * 128;
         if (FM != LA_FM_IDENTITY || NORM || DK) {
-            for (int c = 0; c < nch; ++c) {
+            // decay: key row r of chunk c is weighted by gamma^(C-1-r) (rowf, fixed) times
+            // gamma^(-C m) with m = c's place in the rescale period (main pass), or times
+            // gamma^(C (nch-1-c)) (totals pass)
+            float rowf[NR];
+#pragma unroll
+            for (int n = 0; n < NR; ++n) rowf[n] = DK ? ex2(a.l2g * (float)(C - 1 - rg - n * RG)) : 1.f;
+            int pm = 0;  // c mod period
+            for (int c = 0; c < nch; ++c, pm = (pm + 1 == a.period) ? 0 : pm + 1) {
                 const int s = c % TC_STAGES;
+                const float chf = DK ? ex2(a.l2g * (float)(totals ? (nch - 1 - c) * C : -C * pm)) : 1.f;
                 if (!group_wait(ft == 0, 1, &full[s], (c / TC_STAGES) & 1, nullptr, 0, false, ctl,
                                 NF))
                     break;
@@ -432,9 +457,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const int zkb = ft / 16, zr = (ft / 8) & 1, zch = ft & 7;
                     const float4 z0 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4];
                     const float4 z1 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4 + 1];
-                    // decay: gamma^C z, matching the state copy the inter product reads
-                    const float zz[8] = {gC * z0.x, gC * z0.y, gC * z0.z, gC * z0.w,
-                                         gC * z1.x, gC * z1.y, gC * z1.z, gC * z1.w};
+                    // decay: gamma^(C (1-m)) z, matching the state copy the inter product reads
+                    const float zf = DK ? ex2(a.l2g * (float)(C * (1 - pm))) : 1.f;
+                    const float zz[8] = {zf * z0.x, zf * z0.y, zf * z0.z, zf * z0.w,
+                                         zf * z1.x, zf * z1.y, zf * z1.z, zf * z1.w};
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -466,11 +492,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const bool in_seq = !NC || (tile0 + c) * C + rg + n * RG < a.L;
                     // decay: key row r weighted by gamma^(C-1-r), or by gamma^(segment end - row)
                     // in the totals pass
-                    float rf = 1.f;
-                    if (DK) {
-                        const int r = rg + n * RG;
-                        rf = exp2f(a.l2g * (float)(C - 1 - r + (totals ? (nch - 1 - c) * C : 0)));
-                    }
+                    const float rf = rowf[n] * chf;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
@@ -514,7 +536,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         float acc = 0.f;
 #pragma unroll
                         for (int w = 0; w < TC_FWARPS; ++w) acc += zpart[w * D + i];
-                        zs[i] = (DK && !totals) ? gC * zs[i] + acc : zs[i] + acc;
+                        // decay: the keys carried gamma^(-C m) of the state's period
+                        zs[i] = (DK && !totals) ? gC * zs[i] + ex2(a.l2g * (float)(C * pm)) * acc
+                                                : zs[i] + acc;
                     }
                     named_bar(1, NF);
                 }
@@ -612,6 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             }
             // bf16 copy of the state for each next chunk's inter product
             bool rb_ok = true;
+            const int pm = DK ? c % a.period : 0;  // once per tile (NSUB = 1 under decay)
             for (int j = 0; j < NSUB; ++j) {
                 const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
                 const int lg = c * NSUB + j;           // chunk index in this CTA
@@ -621,16 +646,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     break;
                 }
                 tc_fence_after();
+                // decay: chunk m of the period leaves A = gamma^(-C m) S, the copy chunk m+1
+                // reads; at the period's end A becomes gamma^(C P) A = gamma^C S
+                const bool restore = DK && pm == a.period - 1;
+                const float cf = restore ? ex2(a.l2g * (float)(C * a.period)) : 1.f;
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t sv[32], pk[16];
                     tmem_ld32(tS + lane_off + cb * 32, sv);
                     tmem_wait_ld();
-                    if (DK) {
-                        // gamma^C S: the next chunk's inter product reads it and its state
-                        // update accumulates onto it
+                    if (restore) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(gC * __uint_as_float(sv[e]));
+                        for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(cf * __uint_as_float(sv[e]));
                         tmem_st16(tS + lane_off + cb * 32, *reinterpret_cast<const uint32_t(*)[16]>(sv));
                         tmem_st16(tS + lane_off + cb * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(sv + 16));
                     }
@@ -679,12 +706,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
                 float rd[32];
                 if (NORM || DK) {
-                    // 1 / den per row, or (decay, no normaliser) gamma^(i+1-C)
+                    // 1 / den per row, or (decay, no normaliser) gamma^(i+1-C) gamma^(C m)
                     const float4 *rp = (const float4 *)(rden + (NORM ? slot * C : 0) + 32 * h);
+                    const float mf = (DK && !NORM) ? ex2(a.l2g * (float)(C * (c % a.period))) : 1.f;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 v = rp[q];
-                        rd[4 * q] = v.x; rd[4 * q + 1] = v.y; rd[4 * q + 2] = v.z; rd[4 * q + 3] = v.w;
+                        rd[4 * q] = mf * v.x; rd[4 * q + 1] = mf * v.y;
+                        rd[4 * q + 2] = mf * v.z; rd[4 * q + 3] = mf * v.w;
                     }
                 }
                 // Lanes j, j^1 swap one value per pair of rows so that each writes two
@@ -764,6 +793,10 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     a.noncausal = noncausal ? 1 : 0;
     a.nseg_all = nseg;
     a.l2g = mode == TC_DECAY ? p.l2g : 0.f;
+    // largest period P with C P |log2 gamma| <= 64 (gamma^(C P) >= 2^-64); tc_supported keeps
+    // gamma^C >= 2^-64, so P >= 1
+    a.period = 1 << 20;
+    if (a.l2g < 0.f) a.period = (int)fmax(1.0, fmin((double)(1 << 20), floor(64.0 / (C * -(double)a.l2g))));
     a.err = p.err;
     a.timeout_ns = 2000000000ull;
     const char *e = getenv("LA_DEBUG_TIMEOUT_NS");

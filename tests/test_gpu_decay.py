@@ -71,6 +71,9 @@ CASES = [
     ("identity-d64-L2048", dict(B=1, H=3, L=1000), 0.95, 2),
     ("identity-d64-L2048", dict(B=1, H=2, L=640, dv=128), 0.7, 2),
     ("identity-d64-L2048", dict(B=1, H=2, L=640, normalize=True, fm="elu1", scale=1.0), 0.5, 2),
+    # gamma = 0.75: the fp32 state is rescaled every second chunk
+    ("identity-d64-L2048", dict(B=1, H=2, L=640, normalize=True, fm="elu1", scale=1.0), 0.75, 2),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=700, normalize=False, scale=0.3), 0.75, 2),
     ("identity-d64-L2048", dict(B=1, H=2, L=2048), 0.99, 2),             # split sequence
     ("elu1-norm-d128-L8192", dict(B=1, H=1, L=4096), 0.999, 2),          # split sequence
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=300), 0.3, 0),             # gamma < 0.5: generic
