@@ -151,18 +151,6 @@ __device__ __forceinline__ float ex2(float x)
     return e;
 }
 
-template <int FM>
-__device__ __forceinline__ float phi1(float x)
-{
-    if (FM == LA_FM_ELU1) {
-        // e^x = 2^(x log2 e) on the SFU (hardware ex2, flush-to-zero); x >= 0 takes x + 1
-        float e;
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-        return x >= 0.f ? x + 1.f : e;
-    }
-    return x;
-}
-
 template <int D, int DV, int CH, int FM, bool NORM, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_constant__ TcArgs a)
 {
@@ -477,8 +465,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     for (int n = 0; n < NR; ++n) {
                         uint32_t *wv = (uint32_t *)&wq[n];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16x2(phi1<FM>(bf_lo(wv[e])), phi1<FM>(bf_hi(wv[e])));
+                        for (int e = 0; e < 4; ++e) wv[e] = elu1_bf16x2(wv[e]);
                     }
                 }
                 float colsum[8];
@@ -495,7 +482,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const float rf = rowf[n] * chf;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float x0 = phi1<FM>(bf_lo(wv[e])), x1 = phi1<FM>(bf_hi(wv[e]));
+                        // elu+1 in bf16x2; the decay scales the bf16 features in fp32
+                        if (FM == LA_FM_ELU1) wv[e] = elu1_bf16x2(wv[e]);
+                        float x0 = bf_lo(wv[e]), x1 = bf_hi(wv[e]);
                         if (DK) {
                             x0 *= rf;
                             x1 *= rf;
@@ -504,7 +493,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                             colsum[2 * e] += x0;
                             colsum[2 * e + 1] += x1;
                         }
-                        if (FM != LA_FM_IDENTITY || DK) wv[e] = pack_bf16x2(x0, x1);
+                        if (DK) wv[e] = pack_bf16x2(x0, x1);
                     }
                 }
                 if (FM != LA_FM_IDENTITY || DK) {

@@ -93,17 +93,6 @@ struct TwLayout {
     static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-template <int FM>
-__device__ __forceinline__ float phiw(float x)
-{
-    if (FM == LA_FM_ELU1) {
-        float e;
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-        return x >= 0.f ? x + 1.f : e;
-    }
-    return x;
-}
-
 template <int D, int DV, int R, int FM, bool NORM>
 __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_constant__ TwArgs a)
 {
@@ -454,8 +443,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     for (int n = 0; n < NR; ++n) {
                         uint32_t *wv = (uint32_t *)&wq[n];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16x2(phiw<FM>(bf_lo(wv[e])), phiw<FM>(bf_hi(wv[e])));
+                        for (int e = 0; e < 4; ++e) wv[e] = elu1_bf16x2(wv[e]);
                     }
                 }
                 float colsum[8];
@@ -466,12 +454,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     uint32_t *wv = (uint32_t *)&wk[n];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x0 = phiw<FM>(bf_lo(wv[e])), x1 = phiw<FM>(bf_hi(wv[e]));
+                        if (PHI) wv[e] = elu1_bf16x2(wv[e]);
                         if (NORM) {
-                            colsum[2 * e] += x0;
-                            colsum[2 * e + 1] += x1;
+                            colsum[2 * e] += bf_lo(wv[e]);
+                            colsum[2 * e + 1] += bf_hi(wv[e]);
                         }
-                        if (PHI) wv[e] = pack_bf16x2(x0, x1);
                     }
                 }
                 if (PHI) {
@@ -521,8 +508,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                             uint4 w = rp[n * RG * 8];
                             uint32_t *wv = (uint32_t *)&w;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                wv[e] = pack_bf16x2(phiw<FM>(bf_lo(wv[e])), phiw<FM>(bf_hi(wv[e])));
+                            for (int e = 0; e < 4; ++e) wv[e] = elu1_bf16x2(wv[e]);
                             rp[n * RG * 8] = w;
                         }
                         fence_async_smem();
