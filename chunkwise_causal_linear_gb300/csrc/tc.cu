@@ -10,7 +10,8 @@
 // GB300 mapping (everything stays on chip except q, k, v in and out):
 //   * warp 0       TMA producer: Q_c, K_c, V_c tiles (128-byte swizzled) into a 3-stage ring.
 //   * warp 1       one thread issues every tcgen05.mma; the warp owns the TMEM allocation.
-//   * warps 4-11   feature map phi applied in place in shared memory; with the normaliser,
+//   * warps 2-4, 6-8, 10-11 (not on the MMA issuer's sub-partition)
+//                  feature map phi applied in place in shared memory; with the normaliser,
 //                  the fp32 column sums of phi(K_c) update z, and z_c is written (as a bf16
 //                  hi/lo pair) into two extra rows after the chunk's 64 key rows, so the
 //                  scores MMA also returns phi(q_t).z_c in fp32.
@@ -80,6 +81,16 @@ namespace {
 
 constexpr int TC_THREADS = 640;
 constexpr int TC_FWARPS = 8;  // warps in the feature-map group
+
+// The feature-map group is warps 2, 3, 4, 6, 7, 8, 10, 11: none shares a sub-partition
+// (warp % 4) with the MMA issuer (warp 1), whose single issuing thread would otherwise
+// compete with two busy feature-map warps for issue slots.  Returns the warp's rank in
+// the group, or -1.
+__device__ __forceinline__ int phi_rank(int warp)
+{
+    if (warp < 2 || warp >= 12 || (warp & 3) == 1) return -1;
+    return warp - 2 - (warp > 5) - (warp > 9);
+}
 constexpr int TC_STAGES = 3;
 constexpr int TC_DEN = 4;  // ring of per-chunk 1/den vectors
 
@@ -404,12 +415,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             while (!mbar_try_sleep(drain, 0, 200000u))
                 if (globaltimer() - t0 > ctl.timeout_ns) break;
         }
-    } else if (warp >= 4 && warp < 4 + TC_FWARPS) {
+    } else if (phi_rank(warp) >= 0) {
         // ------------------------------------------------------------ feature map / z
         // Thread (rg, g) owns 16-byte chunk g (8 features) of rows rg, rg + RG, ...: it
         // loads all its Q and K chunks at once, transforms them in registers and stores
         // them back in place (same swizzled slot).
-        const int ft = tid - 128;
+        const int ft = 32 * phi_rank(warp) + lane;
         constexpr int NF = 32 * TC_FWARPS;  // threads in the group
         constexpr int G = D / 8;            // 16-byte chunks per row
         constexpr int RG = NF / G;          // row groups
