@@ -251,6 +251,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     }
     if (DK && !NORM)
         for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
+    if (CH == C)
+        // P rows 0-31, columns 32-63: always zero (causal mask), written once
+        for (int e = tid; e < 32 * 4; e += TC_THREADS) {
+            const int t = e >> 2, chn = 4 + (e & 3);
+            *(uint4 *)(p_tile + t * 128 + ((chn ^ (t & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_async_smem();
     tc_fence_before();
@@ -581,21 +587,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                             ((c / TC_DEN) - 1) & 1, NORM && c >= TC_DEN, ctl))
                 break;
             tc_fence_after();
-            // one 32-column half of the scores row at a time (register budget)
+            // one 32-column half of the scores row at a time (register budget).  With one chunk
+            // per tile, rows 0-31 (warps 0, 1 of the group) keep nothing from columns 32-63: their
+            // P there is the zero block written at the start, and they load only the first half.
             const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off;
+            const int nh = (CH == C && q4 < 2) ? 1 : 2;
             float rs = 0.f, dz = 0.f;
-            if (NORM) {
-                uint32_t rz[8];
-                tmem_ld8(tA + C, rz);
-                tmem_wait_ld();
-                dz = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);  // phi(q_t).z_c (hi + lo)
-            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                if (h >= nh) break;
                 uint32_t r[32];
                 tmem_ld32(tA + 32 * h, r);
-                tmem_wait_ld();
-                if (h == 1) {
+                if (NORM && h == 0) {
+                    // phi(q_t).z_c (hi + lo), loaded with the first half
+                    uint32_t rz[8];
+                    tmem_ld8(tA + C, rz);
+                    tmem_wait_ld();
+                    dz = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);
+                } else {
+                    tmem_wait_ld();
+                }
+                if (h == nh - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&a_free[b]);
