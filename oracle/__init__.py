@@ -70,6 +70,9 @@ def lib():
                                                ctypes.c_double, c_int, _dp]
             L.orc_decay_scores_first.argtypes = [_dp, _dp, _dp, c_long, c_int, c_int,
                                                  ctypes.c_double, c_int, _lp, c_long, _dp]
+            L.orc_backward_features.argtypes = [_dp, _dp, _dp, _dp, c_long, c_int, c_int, c_int,
+                                                ctypes.c_double, _dp, _dp, _dp]
+            L.orc_phi_grad.argtypes = [_dp, c_long, c_int, c_int, _dp, c_int, _dp, _dp]
             for name in ("orc_state_flops", "orc_score_flops", "orc_total_flops"):
                 getattr(L, name).argtypes = [c_ll, c_ll, c_ll]
                 getattr(L, name).restype = c_ll
@@ -214,6 +217,62 @@ def decay_scores_first(fq, fk, v, gamma, normalize=False, rows=None):
                                  None if rows_a is None else rows_a.ctypes.data_as(_lp), n,
                                  _p(out))
     return out
+
+
+# ---------------------------------------------------------------------------
+# backward pass
+# ---------------------------------------------------------------------------
+_FM_CODE = {"identity": 0, "elu1": 1, "favor": 2}
+
+
+def backward_features(fq, fk, v, dout, normalize=False, gamma=None):
+    """Gradients (dphi(q), dphi(k), dv) of the causal output, by the chain rule on the plain
+    definition (gamma: Retention decay, None for none)."""
+    fq, fk, v, dout = _c(fq), _c(fk), _c(v), _c(dout)
+    L, D = fq.shape
+    dv = v.shape[1]
+    dfq, dfk, dvo = np.empty((L, D)), np.empty((L, D)), np.empty((L, dv))
+    lib().orc_backward_features(_p(fq), _p(fk), _p(v), _p(dout), L, D, dv, int(normalize),
+                                -1.0 if gamma is None else float(gamma), _p(dfq), _p(dfk),
+                                _p(dvo))
+    return dfq, dfk, dvo
+
+
+def phi_grad(x, dphi, kind, omega=None):
+    """dx from dphi through the feature map (identity / elu1 / favor)."""
+    x, dphi = _c(x), _c(dphi)
+    rows, d = x.shape
+    om = None if omega is None else _c(omega)
+    m = 0 if om is None else om.shape[0]
+    dx = np.empty_like(x)
+    lib().orc_phi_grad(_p(x), rows, d, _FM_CODE[kind], _p(om), m, _p(dphi), _p(dx))
+    return dx
+
+
+def head_backward(q, k, v, dout, fm="identity", omega=None, normalize=False, gamma=None):
+    """(dq, dk, dv) of one head from raw q, k [L, dk], v, dout [L, dv] (float64)."""
+    fq, fk = phi(q, fm, omega), phi(k, fm, omega)
+    dfq, dfk, dvo = backward_features(fq, fk, v, dout, normalize, gamma)
+    return phi_grad(q, dfq, fm, omega), phi_grad(k, dfk, fm, omega), dvo
+
+
+def backward(q, k, v, dout, fm="identity", omega=None, normalize=False, gamma=None,
+             threads=None):
+    """All heads: q, k [n, L, dk], v, dout [n, L, dv] -> (dq, dk, dv) stacked over heads."""
+    n = q.shape[0]
+    res = [None] * n
+
+    def one(h):
+        res[h] = head_backward(q[h], k[h], v[h], dout[h], fm, omega, normalize, gamma)
+
+    threads = threads or min(n, os.cpu_count() or 1)
+    if threads <= 1 or n == 1:
+        for h in range(n):
+            one(h)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(n)))
+    return tuple(np.stack([r[i] for r in res]) for i in range(3))
 
 
 # ---------------------------------------------------------------------------

@@ -373,6 +373,104 @@ void orc_decay_scores_first(const double *fq, const double *fk, const double *v,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Backward pass (gradients of the causal output)                             */
+/* ------------------------------------------------------------------------- */
+
+/* The pages give no formulas for the backward pass; this is the chain rule applied to the
+ * plain definition used by orc_scores_first / orc_decay_scores_first, with M[t,s] = 1 or
+ * gamma^(t-s) for s <= t and a_ts = phi(q_t) . phi(k_s):
+ *   num_t = sum_{s<=t} M a_ts v_s,  den_t = sum_{s<=t} M a_ts,
+ *   out_t = num_t (unnormalised) or num_t / den_t.
+ * Given dout (the gradient of a scalar loss with respect to out), the loss depends on a_ts
+ * through num_t (and den_t), so
+ *   unnormalised: g_ts = M (dout_t . v_s)
+ *   normalised:   g_ts = M (dout_t . v_s - dout_t . out_t) / den_t
+ *   dv_s     = sum_{t>=s} M a_ts dout_t   (divided by den_t when normalised)
+ *   dphiq_t  = sum_{s<=t} g_ts phi(k_s),   dphik_s = sum_{t>=s} g_ts phi(q_t).
+ * gamma <= 0 means no decay (M = 1).  Inputs are feature-mapped rows; out: [L, D], [L, D],
+ * [L, dv]. */
+void orc_backward_features(const double *fq, const double *fk, const double *v, const double *dout,
+                           long L, int D, int dv, int normalize, double gamma, double *dfq,
+                           double *dfk, double *dvo)
+{
+    double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+    memset(dfq, 0, sizeof(double) * (size_t)L * D);
+    memset(dfk, 0, sizeof(double) * (size_t)L * D);
+    memset(dvo, 0, sizeof(double) * (size_t)L * dv);
+    for (long t = 0; t < L; ++t) {
+        const double *qt = fq + t * D, *dt = dout + t * dv;
+        /* the forward row: num_t, den_t, out_t */
+        double den = 0.0;
+        for (int j = 0; j < dv; ++j) o[j] = 0.0;
+        for (long s = 0; s <= t; ++s) {
+            double m = gamma > 0.0 ? pow(gamma, (double)(t - s)) : 1.0;
+            double a = m * dot(qt, fk + s * D, D);
+            for (int j = 0; j < dv; ++j) o[j] += a * v[s * dv + j];
+            den += a;
+        }
+        double scale = 1.0, dto = 0.0;
+        if (normalize) {
+            for (int j = 0; j < dv; ++j) o[j] /= den;
+            scale = 1.0 / den;
+            dto = dot(dt, o, dv);
+        }
+        for (long s = 0; s <= t; ++s) {
+            double m = gamma > 0.0 ? pow(gamma, (double)(t - s)) : 1.0;
+            double a = m * dot(qt, fk + s * D, D);
+            double g = m * (dot(dt, v + s * dv, dv) - dto) * scale;
+            for (int i = 0; i < D; ++i) {
+                dfq[t * D + i] += g * fk[s * D + i];
+                dfk[s * D + i] += g * qt[i];
+            }
+            for (int j = 0; j < dv; ++j) dvo[s * dv + j] += a * scale * dt[j];
+        }
+    }
+    free(o);
+}
+
+/* Chain rule through the feature map: dx from dphi for rows x [rows, d].
+ *   identity: dx = dphi;
+ *   elu+1:    dx = dphi * (x >= 0 ? 1 : e^x)   ([perf] ELU feature map);
+ *   FAVOR+:   with s = d^{-1/4}, xs = s x and phi_l = exp(omega_l . xs - |xs|^2 / 2) / sqrt(m),
+ *             d phi_l / d x_i = s phi_l (omega_li - xs_i), so
+ *             dx_i = s sum_l dphi_l phi_l (omega_li - xs_i).
+ * kind: 0 identity, 1 elu+1, 2 FAVOR+ (omega [m, d], dphi [rows, m]). */
+void orc_phi_grad(const double *x, long rows, int d, int kind, const double *omega, int m,
+                  const double *dphi, double *dx)
+{
+    if (kind == 0) {
+        for (long e = 0; e < rows * d; ++e) dx[e] = dphi[e];
+        return;
+    }
+    if (kind == 1) {
+        for (long e = 0; e < rows * d; ++e) dx[e] = dphi[e] * (x[e] >= 0.0 ? 1.0 : exp(x[e]));
+        return;
+    }
+    const double s = pow((double)d, -0.25);
+    double *xs = (double *)malloc(sizeof(double) * (size_t)d);
+    double *ph = (double *)malloc(sizeof(double) * (size_t)m);
+    for (long r = 0; r < rows; ++r) {
+        double nrm2 = 0.0;
+        for (int j = 0; j < d; ++j) {
+            xs[j] = x[r * d + j] * s;
+            nrm2 += xs[j] * xs[j];
+        }
+        for (int l = 0; l < m; ++l) {
+            double p = 0.0;
+            for (int j = 0; j < d; ++j) p += omega[(long)l * d + j] * xs[j];
+            ph[l] = exp(p - 0.5 * nrm2) / sqrt((double)m);
+        }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int l = 0; l < m; ++l) acc += dphi[r * m + l] * ph[l] * (omega[(long)l * d + i] - xs[i]);
+            dx[r * d + i] = s * acc;
+        }
+    }
+    free(xs);
+    free(ph);
+}
+
+/* ------------------------------------------------------------------------- */
 /* Cost model                                                                  */
 /* ------------------------------------------------------------------------- */
 

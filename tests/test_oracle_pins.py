@@ -499,3 +499,59 @@ def test_decay_printed_retention_after_ten_steps(golden):
         kept = got[0, steps, 0]
         assert abs(kept - printed) < 0.005
         assert kept == pytest.approx(gamma ** steps, rel=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# backward pass: the chain rule on the definition, pinned by finite differences of the
+# oracle's forward recurrence (another code path) and by numpy matrix products
+# ---------------------------------------------------------------------------
+def _fd_grads(q, k, v, dout, fm, omega, normalize, gamma, eps=1e-6):
+    """Central differences of loss = sum(out * dout) through oracle.forward (recurrence)."""
+    def loss(qq, kk, vv):
+        out = oracle.forward(qq[None], kk[None], vv[None], fm=fm, omega=omega,
+                             normalize=normalize, gamma=gamma, method="recurrence")[0]
+        return float((out * dout).sum())
+    grads = []
+    for which in range(3):
+        base = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(base[which])
+        for idx in np.ndindex(*g.shape):
+            plus = [b.copy() for b in base]
+            minus = [b.copy() for b in base]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            g[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("fm", ["identity", "elu1", "favor"])
+@pytest.mark.parametrize("normalize", [False, True])
+@pytest.mark.parametrize("gamma", [None, 0.8])
+def test_backward_matches_finite_differences(fm, normalize, gamma):
+    rng = np.random.default_rng(31)
+    L, d, dv = 7, 3, 2
+    q, k = rng.normal(size=(L, d)) * 0.7, rng.normal(size=(L, d)) * 0.7
+    if fm == "identity" and normalize:
+        q, k = np.abs(q) + 0.2, np.abs(k) + 0.2  # keep the denominators away from zero
+    v, dout = rng.normal(size=(L, dv)), rng.normal(size=(L, dv))
+    omega = synth.block_orthogonal_gaussian(5, 8, d) if fm == "favor" else None
+    dq, dk, dvv = oracle.backward(q[None], k[None], v[None], dout[None], fm=fm, omega=omega,
+                                  normalize=normalize, gamma=gamma)
+    fq, fk, fv = _fd_grads(q, k, v, dout, fm, omega, normalize, gamma)
+    for got, want in ((dq[0], fq), (dk[0], fk), (dvv[0], fv)):
+        assert np.allclose(got, want, rtol=1e-6, atol=1e-7), np.abs(got - want).max()
+
+
+def test_backward_identity_unnormalised_is_masked_matmuls():
+    """out = tril(Q K^T) V gives dV = tril(Q K^T)^T dO, dQ = tril(dO V^T) K and
+    dK = tril(dO V^T)^T Q; on small integers every partial sum is exact."""
+    rng = np.random.default_rng(32)
+    q, k = ints(rng, (1, 11, 4)), ints(rng, (1, 11, 4))
+    v, dout = ints(rng, (1, 11, 3)), ints(rng, (1, 11, 3))
+    dq, dk, dvv = oracle.backward(q, k, v, dout)
+    A = np.tril(q[0] @ k[0].T)
+    G = np.tril(dout[0] @ v[0].T)
+    assert np.array_equal(dvv[0], A.T @ dout[0])
+    assert np.array_equal(dq[0], G @ k[0])
+    assert np.array_equal(dk[0], G.T @ q[0])
