@@ -40,7 +40,7 @@ EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
            "la_decode_state_elems", "la_noncausal_fwd", "la_noncausal_workspace_bytes",
            "la_decay_fwd", "la_decay_decode_step", "la_decay_workspace_bytes", "la_decay_plan",
-           "la_version")
+           "la_chunked_bwd", "la_chunked_bwd_workspace_bytes", "la_version")
 
 
 class la_feature_map(ctypes.Structure):
@@ -119,6 +119,11 @@ def lib() -> ctypes.CDLL:
             L.la_decay_plan.argtypes = [i, i, i, i, i, i, fmp, i, f, i, i, i,
                                         ctypes.POINTER(la_plan_info)]
             L.la_decay_plan.restype = i
+            L.la_chunked_bwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, fmp, i, f, i, p,
+                                         sz, p]
+            L.la_chunked_bwd.restype = i
+            L.la_chunked_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i]
+            L.la_chunked_bwd_workspace_bytes.restype = sz
             L.la_version.argtypes = []
             L.la_version.restype = ctypes.c_char_p
             _lib = L
@@ -245,6 +250,18 @@ def la_decay_plan(B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype, path
     return rc, info.as_dict()
 
 
+def la_chunked_bwd(q, k, v, out, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map, normalize,
+                   gamma, dtype, workspace, workspace_bytes, stream) -> int:
+    return lib().la_chunked_bwd(q, k, v, out, dout, dq, dk, dv, B, H, L, dk_, dv_, C,
+                                _fm(feature_map), normalize, gamma, dtype, workspace,
+                                workspace_bytes, stream)
+
+
+def la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, dtype) -> int:
+    return lib().la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                                dtype)
+
+
 def la_version() -> str:
     return lib().la_version().decode()
 
@@ -363,6 +380,33 @@ def decay_decode_step(q, k, v, state, gamma, zstate=None, feature_map="identity"
     if rc != LA_OK:
         raise LAError(rc, "la_decay_decode_step")
     return out
+
+
+def chunked_bwd(q, k, v, dout, out=None, C=64, feature_map="identity", omega=None,
+                normalize=False, gamma=1.0, workspace=None, stream=None):
+    """(dq, dk, dv) of the causal forward for CUDA tensors q,k [B,H,L,dk], v, dout [B,H,L,dv];
+    out (the forward output) is needed with normalize."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    need = la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), dtype)
+    if need == 0:
+        raise LAError(LA_ERR_UNSUPPORTED, "la_chunked_bwd_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                        out.data_ptr() if out is not None else None, dout.data_ptr(),
+                        dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H, L, dk, dv, C, fm,
+                        int(normalize), float(gamma), dtype, workspace.data_ptr(), need, stream)
+    if rc != LA_OK:
+        raise LAError(rc, "la_chunked_bwd")
+    return dq, dk_t, dv_t
 
 
 def _dtype_code(t):

@@ -58,6 +58,8 @@ struct Problem {
     int decay;               // 1: Retention decay S_t = gamma S_{t-1} + phi(k_t) v_t^T
     float gamma;             // decay factor, 0 < gamma <= 1
     float l2g;               // log2(gamma), rounded from the double value
+    int rev;                 // 1: anti-causal (generic path only): row t reads the rows s >= t,
+                             // computed as the causal pass over the reversed sequence
 };
 
 // Host-side queries used by the planner.

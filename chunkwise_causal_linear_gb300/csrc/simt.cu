@@ -23,6 +23,9 @@
 // state as S <- gamma^len S + sum_j gamma^(len-1-j) phi(k_j) v_j^T.  Powers are exp2 of
 // log2(gamma) times the integer exponent.
 //
+// Anti-causal (used by the backward pass): every row index t of q, k, v and out is read as
+// L-1-t, so the causal sweep over the reversed sequence gives row t the rows s >= t.
+//
 // Every product accumulates in fp32 in a fixed order; on small-integer inputs whose
 // partial sums stay below 2^24 the result is exact.  Rows are handled in tiles of R, so
 // any chunk size C >= 1 works (tiles never straddle a chunk boundary).
@@ -66,6 +69,9 @@ size_t simt_workspace_bytes(int B, int H, int L, int D, int dv, int C, bool logl
     return (size_t)B * H * ns * ni * ((size_t)D * SIMT_WV + D) * sizeof(float);
 }
 
+// storage row of sweep position t (reversed for the anti-causal pass)
+__device__ __forceinline__ int srow(const Problem &p, int t) { return p.rev ? p.L - 1 - t : t; }
+
 // phi of rows [row0, row0 + n) of x ([L, dk], storage T) into dst [R][D] (fp32);
 // rows >= n are zero.  Ends with __syncthreads().
 template <typename T>
@@ -79,7 +85,7 @@ __device__ void load_phi_rows(const T *x, int row0, int n, const SimtArgs &a, fl
             int r = e / D, i = e - r * D;
             float val = 0.f;
             if (r < n) {
-                val = to_f32(x[(long)(row0 + r) * dk + i]);
+                val = to_f32(x[(long)srow(p, row0 + r) * dk + i]);
                 if (p.fm == LA_FM_ELU1) val = phi_elu1(val);
             }
             dst[e] = val;
@@ -91,7 +97,7 @@ __device__ void load_phi_rows(const T *x, int row0, int n, const SimtArgs &a, fl
     const float s = rsqrtf(sqrtf((float)dk));
     for (int e = tid; e < SIMT_R * dk; e += SIMT_NT) {
         int r = e / dk, j = e - r * dk;
-        sX[e] = (r < n) ? to_f32(x[(long)(row0 + r) * dk + j]) * s : 0.f;
+        sX[e] = (r < n) ? to_f32(x[(long)srow(p, row0 + r) * dk + j]) * s : 0.f;
     }
     __syncthreads();
     for (int r = tid; r < SIMT_R; r += SIMT_NT) {
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                 load_phi_rows<T>(k, c0 + kt, nk, a, sK, sX, sNrm);
                 for (int e = tid; e < R * WV; e += NT) {
                     const int s = e / WV, j = e - s * WV;
-                    sV[e] = (s < nk && j < wv) ? to_f32(v[(long)(c0 + kt + s) * dv + j0 + j]) : 0.f;
+                    sV[e] = (s < nk && j < wv) ? to_f32(v[(long)srow(p, c0 + kt + s) * dv + j0 + j]) : 0.f;
                 }
                 for (int e = tid; e < R * R; e += NT) {
                     const int r = e / R, s = e - r * R;
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                 if (r < nq && j < wv) {
                     float val = sAcc[e];
                     if (p.normalize) val = val / sDen[r];
-                    out[(long)(c0 + qt + r) * dv + j0 + j] = from_f32<T>(val);
+                    out[(long)srow(p, c0 + qt + r) * dv + j0 + j] = from_f32<T>(val);
                 }
             }
             __syncthreads();
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
             load_phi_rows<T>(k, c0 + kt, nk, a, sK, sX, sNrm);
             for (int e = tid; e < R * WV; e += NT) {
                 const int s = e / WV, j = e - s * WV;
-                sV[e] = (s < nk && j < wv) ? to_f32(v[(long)(c0 + kt + s) * dv + j0 + j]) : 0.f;
+                sV[e] = (s < nk && j < wv) ? to_f32(v[(long)srow(p, c0 + kt + s) * dv + j0 + j]) : 0.f;
             }
             if (p.decay) {
                 // key row kt + s of the chunk weighted by gamma^(cl - 1 - kt - s)

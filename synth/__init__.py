@@ -21,7 +21,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 # tensor ids used in the Philox key
-T_Q, T_K, T_V, T_LAMBDA, T_OMEGA_G, T_OMEGA_CHI = 1, 2, 3, 4, 5, 6
+T_Q, T_K, T_V, T_LAMBDA, T_OMEGA_G, T_OMEGA_CHI, T_DOUT = 1, 2, 3, 4, 5, 6, 7
 
 
 def _gen(seed: int, tensor: int, head: int) -> np.random.Generator:

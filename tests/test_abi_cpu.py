@@ -195,3 +195,22 @@ def test_decay_arguments_and_plan(lib):
                                 la.LA_PATH_AUTO, 152)
     assert rc == la.LA_OK and info["n_launches"] == 2 and info["workspace_bytes"] > 0
     assert la.la_status_string(la.LA_ERR_ARG) != "unknown status"
+
+
+def test_backward_workspace_and_errors(lib):
+    fm = la.make_feature_map("elu1")
+    rows = 2 * 3 * 100
+    need = la.la_chunked_bwd_workspace_bytes(2, 3, 100, 64, 32, 64, fm, 1, la.LA_BF16)
+    # phi(q), phi(k), dphi(q), dphi(k) [D], D', v' [dv + 1], D, dv [dv], den, ones
+    assert need >= rows * 4 * (4 * 64 + 2 * 33 + 2 * 32 + 2)
+    assert la.la_chunked_bwd_workspace_bytes(1, 1, 100, 600, 32, 64, fm, 1, la.LA_F32) == 0
+    ok = ctypes.c_void_p(16)
+    args = (1, 1, 64, 16, 16, 64, fm)
+    assert la.la_chunked_bwd(None, ok, ok, ok, ok, ok, ok, ok, *args, 0, 1.0, la.LA_F32, ok,
+                             1 << 20, None) == la.LA_ERR_NULL
+    assert la.la_chunked_bwd(ok, ok, ok, None, ok, ok, ok, ok, *args, 1, 1.0, la.LA_F32, ok,
+                             1 << 20, None) == la.LA_ERR_NULL
+    assert la.la_chunked_bwd(ok, ok, ok, ok, ok, ok, ok, ok, *args, 0, 0.0, la.LA_F32, ok,
+                             1 << 20, None) == la.LA_ERR_ARG
+    assert la.la_chunked_bwd(ok, ok, ok, ok, ok, ok, ok, ok, *args, 0, 1.0, la.LA_F32, ok,
+                             16, None) == la.LA_ERR_WORKSPACE

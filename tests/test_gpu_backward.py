@@ -1,0 +1,123 @@
+"""Backward pass (la_chunked_bwd) against the oracle's gradients.
+
+The oracle applies the chain rule to the plain causal definition (pinned by finite
+differences of its forward recurrence); the library composes causal and anti-causal
+linear-attention passes on the generic fp32 path.  With the normaliser the library is
+given its own forward output, as a caller would; the oracle recomputes its own.
+"""
+import numpy as np
+import pytest
+
+import synth
+from parity_util import assert_close, from_device, to_device, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunkwise_causal_linear_gb300 import build
+    build.build()
+
+
+def run_bwd(w, inp, dout_bits, C, gamma=1.0):
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
+    q = to_device(inp["q"], w["dtype"], (B, H, L, dk))
+    k = to_device(inp["k"], w["dtype"], (B, H, L, dk))
+    v = to_device(inp["v"], w["dtype"], (B, H, L, dv))
+    do = to_device(dout_bits, w["dtype"], (B, H, L, dv))
+    omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
+    out = None
+    if w["normalize"]:
+        if gamma == 1.0:
+            out = la.chunked_fwd(q, k, v, C=64, feature_map=w["fm"], omega=omega, normalize=True)
+        else:
+            out = la.decay_fwd(q, k, v, gamma, C=64, feature_map=w["fm"], omega=omega,
+                               normalize=True)
+    dq, dk_, dv_ = la.chunked_bwd(q, k, v, do, out=out, C=C, feature_map=w["fm"], omega=omega,
+                                  normalize=w["normalize"], gamma=gamma)
+    torch.cuda.synchronize()
+    st = la.la_last_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == la.LA_OK, la.la_status_string(st)
+    n = B * H
+    return (from_device(dq).reshape(n, L, dk), from_device(dk_).reshape(n, L, dk),
+            from_device(dv_).reshape(n, L, dv))
+
+
+def oracle_bwd(w, inp, dout_bits, gamma=1.0):
+    import oracle
+    f = lambda x: synth.as_f64(x, w["dtype"])  # noqa: E731
+    om = None if inp["omega"] is None else inp["omega"].astype(np.float64)
+    return oracle.backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(dout_bits), fm=w["fm"],
+                           omega=om, normalize=w["normalize"],
+                           gamma=None if gamma == 1.0 else gamma)
+
+
+def dout_for(w, seed):
+    """The upstream gradient: seeded N(0,1) values in the storage dtype, [B*H, L, dv]."""
+    return synth.tensor_values(seed, synth.T_DOUT, w["B"], w["H"], w["L"], w["dv"], "normal", 1.0,
+                               w["dtype"])
+
+
+CASES = [
+    # (base workload, overrides, C, gamma)
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=333, dk=64, dv=64), 64, 1.0),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=300, dk=32, dv=48, normalize=False), 16, 1.0),
+    ("identity-d64-L2048", dict(B=2, H=1, L=257), 64, 1.0),
+    ("identity-d64-L2048", dict(B=1, H=2, L=200), 100, 0.9),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=190, dk=64, dv=64), 32, 0.95),
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=150), 64, 1.0),
+    ("favor-m256-d64-L16384", dict(B=1, H=1, L=130, normalize=False), 64, 1.0),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=2048), 64, 1.0),  # d128, 32 tiles per head
+]
+
+
+@pytest.mark.parametrize("base,over,C,gamma", CASES)
+def test_backward_matches_oracle(base, over, C, gamma):
+    w = workload(base, **over)
+    inp = synth.make_inputs(w, seed=41)
+    do = dout_for(w, 41)
+    got = run_bwd(w, inp, do, C, gamma)
+    ref = oracle_bwd(w, inp, do, gamma)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g, r, f"{name} {base} {over} C={C} gamma={gamma}")
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_backward_fp32_tight(normalize):
+    """fp32 storage: gradients at fp32 rounding level, and independent of the chunk size."""
+    w = workload("tiny-int-exact", B=1, H=2, L=150, dk=12, dv=10, dist="normal", scale=0.5,
+                 fm="elu1", normalize=normalize)
+    inp = synth.make_inputs(w, seed=42)
+    do = dout_for(w, 42)
+    ref = oracle_bwd(w, inp, do)
+    runs = [run_bwd(w, inp, do, C) for C in (1, 16, 150)]
+    for got in runs:
+        for g, r in zip(got, ref):
+            err = np.abs(g - r).max() / np.abs(r).max()
+            assert err < 2e-5, err
+
+
+def test_backward_rejects_bad_arguments():
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    fm = la.make_feature_map("elu1")
+    t = torch.zeros(1, 1, 64, 16, device="cuda", dtype=torch.bfloat16)
+    p = t.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    args = (1, 1, 64, 16, 16, 64, fm)
+    # the normaliser needs the forward output
+    assert la.la_chunked_bwd(p, p, p, None, p, p, p, p, *args, 1, 1.0, la.LA_BF16, ws.data_ptr(),
+                             ws.numel(), s) == la.LA_ERR_NULL
+    assert la.la_chunked_bwd(p, p, p, p, p, p, p, p, *args, 0, 1.5, la.LA_BF16, ws.data_ptr(),
+                             ws.numel(), s) == la.LA_ERR_ARG
+    assert la.la_chunked_bwd(p, p, p, p, p, p, p, p, *args, 0, 1.0, la.LA_BF16, ws.data_ptr(), 16,
+                             s) == la.LA_ERR_WORKSPACE
