@@ -55,10 +55,12 @@ def parse():
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     ap.add_argument("--L", type=int, default=None,
                     help="override the workload's sequence length (profiling captures)")
-    ap.add_argument("--op", default="forward", choices=["forward", "decode", "noncausal"],
+    ap.add_argument("--op", default="forward",
+                    choices=["forward", "decode", "noncausal", "backward"],
                     help="forward: the chunked forward (the headline metric); decode: one "
                          "la_decode_step per step for every head of the workload; noncausal: "
-                         "la_noncausal_fwd over the workload (bidirectional)")
+                         "la_noncausal_fwd over the workload (bidirectional); backward: "
+                         "la_chunked_bwd over the workload")
     return ap.parse_args()
 
 
@@ -627,12 +629,108 @@ def run_decode(args):
     return 0
 
 
+def run_backward(args):
+    """Backward passes: each timed step is one la_chunked_bwd over the whole workload.
+    Algorithmic bytes per step: q, k, v, dout read and dq, dk, dv written once each."""
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    from chunkwise_causal_linear_gb300 import build as la_build
+    if not la_build.up_to_date():
+        la_build.build()
+    torch.cuda.set_device(0)
+    w = dict(synth.WORKLOADS[args.workload])
+    for key in ("B", "H", "L"):
+        if getattr(args, key):
+            w[key] = getattr(args, key)
+    if w.get("loglinear"):
+        raise SystemExit("--op backward: the log-linear mask has no backward pass")
+    B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
+    C = args.C if args.C is not None else w["C"]
+    gamma = w.get("gamma") or 1.0
+    inp = synth.make_inputs(w, args.seed)
+    do_bits = synth.tensor_values(args.seed, synth.T_DOUT, B, H, L, dv, "normal", 1.0, w["dtype"])
+    es = 2 if w["dtype"] == "bf16" else 4
+
+    def dev(x, d):
+        if w["dtype"] == "bf16":
+            t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(x)
+        return t.reshape(B, H, L, d).cuda()
+
+    q, k, v, do = dev(inp["q"], dk), dev(inp["k"], dk), dev(inp["v"], dv), dev(do_bits, dv)
+    omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
+    fm = la.make_feature_map(w["fm"], w["m"], omega.data_ptr() if omega is not None else 0)
+    dtype = la.LA_BF16 if w["dtype"] == "bf16" else la.LA_F32
+    need = la.la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), dtype)
+    if need == 0:
+        raise SystemExit("--op backward: unsupported sizes")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dq, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        r = la.la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                              dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H,
+                              L, dk, dv, C, fm, int(w["normalize"]), float(gamma), dtype,
+                              ws.data_ptr(), need, stream.cuda_stream)
+        if r != la.LA_OK:
+            raise la.LAError(r, "la_chunked_bwd")
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    st = la.la_last_device_status(stream.cuda_stream)
+    if st != la.LA_OK:
+        raise la.LAError(st, "device status after warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t_ms = sum(a.elapsed_time(b) for a, b in evs)
+    ms = t_ms / args.steps
+    byts = B * H * L * es * (4 * dk + 3 * dv)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = byts / (ms / 1e3) / 1e9
+    # the tensor-core route (bf16, identity / elu+1, no decay, dk = dv in {64, 128}): features,
+    # prep, chain, and 3 passes (+ 3 for the normaliser, one launch each without a sequence
+    # split); the generic route: 2 features, v', prep, 3 passes, 2 chain, 1 cast (+ 1 pass)
+    tc_route = (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1") and gamma == 1.0
+                and L >= 128 and dk == dv and dk in (64, 128))
+    launches = (6 + (3 if w["normalize"] else 0)) if tc_route else (10 + (1 if w["normalize"] else 0))
+    line = {"metric": "backward tokens/sec (B·H·L/s, la_chunked_bwd)", "op": "backward",
+            "value": B * H * L * args.steps / (t_ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w["dtype"] == "bf16" else "f32", "data": "synthetic",
+            "config": dict(workload_config(args.workload, w, C), path="tc" if tc_route else "simt",
+                           l2="inputs larger than L2"),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                         "algorithmic_bytes_per_launch": byts},
+            "cpu_baseline": None, "e2e": None, "clocks": clk,
+            "gpu_launches": launches * args.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "decode":
         return run_decode(args)
+    if args.op == "backward":
+        return run_backward(args)
     return run_ours(args)
 
 

@@ -119,8 +119,8 @@ def lib() -> ctypes.CDLL:
             L.la_decay_plan.argtypes = [i, i, i, i, i, i, fmp, i, f, i, i, i,
                                         ctypes.POINTER(la_plan_info)]
             L.la_decay_plan.restype = i
-            L.la_chunked_bwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, fmp, i, f, i, p,
-                                         sz, p]
+            L.la_chunked_bwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, fmp, i, f, i, p, sz,
+                                         p, i]
             L.la_chunked_bwd.restype = i
             L.la_chunked_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i]
             L.la_chunked_bwd_workspace_bytes.restype = sz
@@ -250,11 +250,11 @@ def la_decay_plan(B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype, path
     return rc, info.as_dict()
 
 
-def la_chunked_bwd(q, k, v, out, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map, normalize,
-                   gamma, dtype, workspace, workspace_bytes, stream) -> int:
-    return lib().la_chunked_bwd(q, k, v, out, dout, dq, dk, dv, B, H, L, dk_, dv_, C,
+def la_chunked_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map, normalize, gamma,
+                   dtype, workspace, workspace_bytes, stream, path=LA_PATH_AUTO) -> int:
+    return lib().la_chunked_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C,
                                 _fm(feature_map), normalize, gamma, dtype, workspace,
-                                workspace_bytes, stream)
+                                workspace_bytes, stream, path)
 
 
 def la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, dtype) -> int:
@@ -382,10 +382,9 @@ def decay_decode_step(q, k, v, state, gamma, zstate=None, feature_map="identity"
     return out
 
 
-def chunked_bwd(q, k, v, dout, out=None, C=64, feature_map="identity", omega=None,
-                normalize=False, gamma=1.0, workspace=None, stream=None):
-    """(dq, dk, dv) of the causal forward for CUDA tensors q,k [B,H,L,dk], v, dout [B,H,L,dv];
-    out (the forward output) is needed with normalize."""
+def chunked_bwd(q, k, v, dout, C=64, feature_map="identity", omega=None, normalize=False,
+                gamma=1.0, workspace=None, stream=None, path=LA_PATH_AUTO):
+    """(dq, dk, dv) of the causal forward for CUDA tensors q,k [B,H,L,dk], v, dout [B,H,L,dv]."""
     import torch
     B, H, L, dk = q.shape
     dv = v.shape[-1]
@@ -400,10 +399,10 @@ def chunked_bwd(q, k, v, dout, out=None, C=64, feature_map="identity", omega=Non
     dq, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    rc = la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                        out.data_ptr() if out is not None else None, dout.data_ptr(),
+    rc = la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
                         dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H, L, dk, dv, C, fm,
-                        int(normalize), float(gamma), dtype, workspace.data_ptr(), need, stream)
+                        int(normalize), float(gamma), dtype, workspace.data_ptr(), need, stream,
+                        path)
     if rc != LA_OK:
         raise LAError(rc, "la_chunked_bwd")
     return dq, dk_t, dv_t

@@ -27,9 +27,11 @@ size_t tc_nc_workspace(const Problem &p, int num_sms);
 int tc_nc_launch(const Problem &p, int num_sms);
 int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int normalize,
                  int num_levels, long long t, bool loglinear, int *D_out, int *r_out);
-size_t bwd_workspace_bytes(const Problem &p);
+size_t bwd_workspace_bytes(const Problem &p, int sms);
 bool bwd_supported(const Problem &p);
-int bwd_launch(const Problem &p, const void *out, const void *dout, void *dq, void *dk, void *dv);
+bool bwd_tc_supported(const Problem &p, int sms);
+int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, void *dk,
+               void *dv);
 int decode_launch(const void *q, const void *k, const void *v, void *out, float *S, float *z, int B,
                   int H, int dk, int dv, const la_feature_map *fm, int normalize, const float *lam,
                   int num_levels, long long t, int dtype, cudaStream_t stream,
@@ -479,28 +481,31 @@ size_t la_chunked_bwd_workspace_bytes(int B, int H, int L, int dk, int dv, int C
 {
     Problem p;
     if (bwd_problem(B, H, L, dk, dv, C, feature_map, normalize, 1.f, dtype, &p) != LA_OK) return 0;
-    return bwd_workspace_bytes(p);
+    const int sms = device_sms();
+    return bwd_workspace_bytes(p, sms > 0 ? sms : 152);
 }
 
-int la_chunked_bwd(const void *q, const void *k, const void *v, const void *out,
-                   const void *dout, void *dq, void *dk_, void *dv_, int B, int H, int L, int dk,
+int la_chunked_bwd(const void *q, const void *k, const void *v, const void *dout, void *dq,
+                   void *dk_, void *dv_, int B, int H, int L, int dk,
                    int dv, int C, const la_feature_map *feature_map, int normalize, float gamma,
-                   int dtype, void *workspace, size_t workspace_bytes, void *stream)
+                   int dtype, void *workspace, size_t workspace_bytes, void *stream, int path)
 {
     if (!q || !k || !v || !dout || !dq || !dk_ || !dv_) return LA_ERR_NULL;
-    if (normalize && !out) return LA_ERR_NULL;
     Problem p;
     int rc = bwd_problem(B, H, L, dk, dv, C, feature_map, normalize, gamma, dtype, &p);
     if (rc != LA_OK) return rc;
     if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
-    if (!workspace || workspace_bytes < bwd_workspace_bytes(p)) return LA_ERR_WORKSPACE;
+    if (path != LA_PATH_AUTO && path != LA_PATH_SIMT && path != LA_PATH_TC) return LA_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return LA_ERR_CUDA;
+    if (!workspace || workspace_bytes < bwd_workspace_bytes(p, sms)) return LA_ERR_WORKSPACE;
     p.q = q; p.k = k; p.v = v;
     p.workspace = workspace;
     p.workspace_bytes = workspace_bytes;
     p.stream = (cudaStream_t)stream;
     p.err = err_ptr();
     if (!p.err) return LA_ERR_CUDA;
-    return bwd_launch(p, out, dout, dq, dk_, dv_);
+    return bwd_launch(p, sms, path, dout, dq, dk_, dv_);
 }
 
 const char *la_version(void) { return "0.1.0"; }

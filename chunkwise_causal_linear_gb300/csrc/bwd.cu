@@ -14,28 +14,47 @@
 //   dphi(q) = causal(q = D', k = v', v = phi(k)),   dphi(k) = anticausal(q = v', k = D', v = phi(q)),
 //   dv = anticausal(q = phi(k), k = phi(q), v = D)
 // with identity features and no normaliser, on the generic chunked kernel in fp32 (the
-// anti-causal pass is its sweep over the reversed sequence).  den_t itself is one more
-// causal pass, causal(q = phi(q), k = phi(k), v = 1).  Finally dq = dphi(q) through the
+// anti-causal pass is its sweep over the reversed sequence).  With the normaliser the
+// forward output is recomputed in fp32 by one more causal pass, causal(q = phi(q), k =
+// phi(k), v = v') = [num, den]: dphi(q) is a small difference of two large sums (g_t Z_t
+// against sum_s (D_t . v_s) phi(k_s)), and a bf16-stored output's rounding would come back
+// amplified about thirtyfold.  Finally dq = dphi(q) through the
 // feature map's derivative (elu+1: 1 or e^x; FAVOR+: s sum_l dphi_l phi_l (omega_l - s x)),
 // likewise dk, and the gradients are stored in the input dtype.
 //
-// Workspace (fp32, per (b, h) head, rows of L): phi(q), phi(k) [D]; den [1]; ones [1];
+// Workspace (fp32, per (b, h) head, rows of L): phi(q), phi(k) [D]; [num, den] [w];
 // D' [w = dv + normalise]; v' [w]; D [dv]; dphi(q), dphi(k) [D]; dv [dv].
+//
+// Tensor-core route (bf16, identity / elu+1, no decay): the same passes run on the causal
+// tensor-core forward with identity features.  An anti-causal pass is the causal pass over
+// reversed rows R(x)_t = x_{L-1-t}: the elementwise kernels write the reversed operands and
+// the last one reads the reversed results back.  The normaliser's extra column becomes two
+// more passes against constant rows e = (1, 0, ..., 0): Z_t = sum_{s<=t} phi(k_s) (so den_t =
+// phi(q_t).Z_t and dphi(q)_t -= g_t Z_t) and the suffix sums sum_{t>=s} g_t phi(q_t)
+// (subtracted from dphi(k)_s); the forward output is recomputed by one more pass, num =
+// causal(phi(q), phi(k), v), over the same bf16 features, so that out = num / den and the
+// other sums cancel exactly for those features.  The feature-gradient passes run in the
+// kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows out).
 #include <math.h>
 #include <stdio.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 
 namespace la {
 
 int simt_launch(const Problem &p, int n_inter, int log2C);
+bool tc_supported(const Problem &p, int num_sms);
+int tc_plan(const Problem &p, int num_sms, la_plan_info *info);
+int tc_launch(const Problem &p, int num_sms);
 
 namespace {
 
 constexpr int BW_THREADS = 256;
 
 struct BwdBufs {
-    float *fq, *fk, *den, *ones, *dw, *vw, *dn, *dfq, *dfk, *dvf;
+    float *fq, *fk, *nd, *dw, *vw, *dn, *dfq, *dfk, *dvf;
 };
 
 size_t bwd_floats(long rows, int D, int dv, int normalize, float *base, BwdBufs *b)
@@ -50,8 +69,7 @@ size_t bwd_floats(long rows, int D, int dv, int normalize, float *base, BwdBufs 
     BwdBufs *t = b ? b : &dummy;
     take(&t->fq, (size_t)rows * D);
     take(&t->fk, (size_t)rows * D);
-    take(&t->den, normalize ? (size_t)rows : 0);
-    take(&t->ones, normalize ? (size_t)rows : 0);
+    take(&t->nd, normalize ? (size_t)rows * w : 0);
     take(&t->dw, (size_t)rows * w);
     take(&t->vw, (size_t)rows * w);
     take(&t->dn, (size_t)rows * dv);
@@ -100,24 +118,35 @@ __global__ void __launch_bounds__(BW_THREADS) bw_phi_kernel(const T *x, float *f
     }
 }
 
-// per row: D = dout (/ den), D' = [D, -D . out], v' = [v, 1] (normalised) or D' = D, v' = v
+// v' = [v, 1] (normalised) or v, fp32
 template <typename T>
-__global__ void __launch_bounds__(BW_THREADS) bw_prep_kernel(const T *dout, const T *out, const T *v,
-                                                           const float *den, float *dn, float *dw,
-                                                           float *vw, long rows, int dv, int normalize)
+__global__ void bw_vw_kernel(const T *v, float *vw, long rows, int dv, int normalize)
+{
+    const int w = dv + (normalize ? 1 : 0);
+    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < rows * w; e += (long)gridDim.x * blockDim.x) {
+        const long r = e / w;
+        const int j = (int)(e - r * w);
+        vw[e] = j < dv ? to_f32(v[r * dv + j]) : 1.f;
+    }
+}
+
+// per row: D = dout (/ den), D' = [D, -D . out] with out = num / den from nd = [num, den]
+// (normalised), or D' = D
+template <typename T>
+__global__ void __launch_bounds__(BW_THREADS) bw_prep_kernel(const T *dout, const float *nd, float *dn,
+                                                           float *dw, long rows, int dv, int normalize)
 {
     const long r = blockIdx.x;
     if (r >= rows) return;
     const int w = dv + (normalize ? 1 : 0);
-    const float inv = normalize ? 1.f / den[r] : 1.f;
+    const float inv = normalize ? 1.f / nd[r * w + dv] : 1.f;
     __shared__ float red[BW_THREADS / 32];
     float g = 0.f;
     for (int j = threadIdx.x; j < dv; j += BW_THREADS) {
         const float d = to_f32(dout[r * dv + j]) * inv;
         dn[r * dv + j] = d;
         dw[r * w + j] = d;
-        vw[r * w + j] = to_f32(v[r * dv + j]);
-        if (normalize) g = fmaf(d, to_f32(out[r * dv + j]), g);
+        if (normalize) g = fmaf(d, nd[r * w + j] * inv, g);
     }
     if (!normalize) return;
     for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
@@ -127,13 +156,7 @@ __global__ void __launch_bounds__(BW_THREADS) bw_prep_kernel(const T *dout, cons
         float t = 0.f;
         for (int wi = 0; wi < BW_THREADS / 32; ++wi) t += red[wi];
         dw[r * w + dv] = -t;
-        vw[r * w + dv] = 1.f;
     }
-}
-
-__global__ void bw_fill_kernel(float *x, long n, float v)
-{
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) x[i] = v;
 }
 
 // dx = dphi through the feature map, stored as T.  x [rows, dk] raw input, df [rows, D].
@@ -217,7 +240,7 @@ int pass(const Problem &base, const float *q, const float *k, const float *v, fl
 }
 
 template <typename T>
-int bwd_t(const Problem &p, const void *out, const void *dout, void *dq, void *dk_, void *dv_)
+int bwd_t(const Problem &p, const void *dout, void *dq, void *dk_, void *dv_)
 {
     const long rows = (long)p.B * p.H * p.L;
     const int D = p.D, w = p.dv + (p.normalize ? 1 : 0);
@@ -229,12 +252,10 @@ int bwd_t(const Problem &p, const void *out, const void *dout, void *dq, void *d
     bw_phi_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)p.k, b.fk, rows, p.dk, D, p.fm, p.omega, p.m);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     int rc;
-    if (p.normalize) {
-        bw_fill_kernel<<<1024, 256, 0, st>>>(b.ones, rows, 1.f);
-        if ((rc = pass(p, b.fq, b.fk, b.ones, b.den, D, 1, 0)) != LA_OK) return rc;
-    }
-    bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, (const T *)out, (const T *)p.v, b.den,
-                                                 b.dn, b.dw, b.vw, rows, p.dv, p.normalize);
+    bw_vw_kernel<T><<<1024, 256, 0, st>>>((const T *)p.v, b.vw, rows, p.dv, p.normalize);
+    if (p.normalize && (rc = pass(p, b.fq, b.fk, b.vw, b.nd, D, w, 0)) != LA_OK) return rc;  // [num, den]
+    bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
+                                                 p.normalize);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     if ((rc = pass(p, b.dw, b.vw, b.fk, b.dfq, w, D, 0)) != LA_OK) return rc;   // dphi(q)
     if ((rc = pass(p, b.vw, b.dw, b.fq, b.dfk, w, D, 1)) != LA_OK) return rc;   // dphi(k)
@@ -247,22 +268,256 @@ int bwd_t(const Problem &p, const void *out, const void *dout, void *dq, void *d
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- tensor-core route
+typedef __nv_bfloat16 bf16;
+
+struct TcBufs {
+    bf16 *fq, *fk, *rfq, *rfk, *rv, *dn, *rd, *rgq, *e;  // operands
+    float *zc, *num, *dqm, *dkr, *zsr;                   // pass outputs (fp32 rows)
+    bf16 *dvr;
+    float *g;
+    void *ws;                                            // tensor-core pass workspace
+    size_t ws_bytes;
+};
+
+// one identity-feature, unnormalised causal pass on the tensor cores (bf16 rows)
+Problem tc_pass(const Problem &base, const void *q, const void *k, const void *v, void *out, int dk,
+                int dv)
+{
+    Problem p = base;
+    p.q = q; p.k = k; p.v = v; p.out = out;
+    p.dk = dk; p.dv = dv; p.D = dk;
+    p.C = 64;
+    p.fm = LA_FM_IDENTITY; p.m = 0; p.omega = nullptr;
+    p.normalize = 0;
+    p.lam = nullptr; p.nl = 0;
+    p.dtype = LA_BF16;
+    p.decay = 0; p.rev = 0;
+    p.out_f32 = 0;
+    return p;
+}
+
+// the passes of the route, in order (unused ones have out == nullptr when !normalize)
+int tc_passes(const Problem &p, const TcBufs &b, const void *dout, Problem *ps)
+{
+    const int D = p.D, dv = p.dv;
+    int n = 0;
+    // the feature-gradient passes store fp32: dphi(q) = pass - g Z and dphi(k) = pass - suffix
+    // can cancel, so those terms are not rounded to bf16 before the subtraction
+    if (p.normalize) ps[n++] = tc_pass(p, b.e, b.e, b.fk, b.zc, 64, D);                  // Z
+    if (p.normalize) ps[n++] = tc_pass(p, b.fq, b.fk, p.v, b.num, D, dv);                 // num
+    ps[n++] = tc_pass(p, p.normalize ? (const void *)b.dn : dout, p.v, b.fk, b.dqm, dv, D);  // dphi(q)
+    ps[n++] = tc_pass(p, b.rv, b.rd, b.rfq, b.dkr, dv, D);                                // R dphi(k)
+    if (p.normalize) ps[n++] = tc_pass(p, b.e, b.e, b.rgq, b.zsr, 64, D);                 // R suffix
+    for (int i = 0; i < n; ++i) ps[i].out_f32 = 1;
+    ps[n++] = tc_pass(p, b.rfk, b.rfq, b.rd, b.dvr, D, dv);                               // R dv
+    return n;
+}
+
+size_t tc_bufs(const Problem &p, int sms, char *base, TcBufs *b)
+{
+    const size_t rows = (size_t)p.B * p.H * p.L;
+    const int D = p.D, dv = p.dv;
+    size_t off = 0;
+    TcBufs dummy;
+    TcBufs *t = b ? b : &dummy;
+    auto take = [&](auto **ptr, size_t bytes) {
+        if (b) *ptr = (std::remove_reference_t<decltype(**ptr)> *)(base + off);
+        off += (bytes + 1023) / 1024 * 1024;
+    };
+    const size_t N = p.normalize ? 1 : 0;
+    take(&t->fq, rows * D * 2);
+    take(&t->fk, rows * D * 2);
+    take(&t->rfq, rows * D * 2);
+    take(&t->rfk, rows * D * 2);
+    take(&t->rv, rows * dv * 2);
+    take(&t->dn, N * rows * dv * 2);
+    take(&t->rd, rows * dv * 2);
+    take(&t->rgq, N * rows * D * 2);
+    take(&t->e, N * rows * 64 * 2);
+    take(&t->zc, N * rows * D * 4);
+    take(&t->num, N * rows * dv * 4);
+    take(&t->dqm, rows * D * 4);
+    take(&t->dkr, rows * D * 4);
+    take(&t->zsr, N * rows * D * 4);
+    take(&t->dvr, rows * dv * 2);
+    take(&t->g, N * rows * 4);
+    // the passes run one after another on the stream and share one workspace
+    Problem ps[6];
+    TcBufs nb{};
+    const int n = tc_passes(p, nb, nullptr, ps);
+    size_t wmax = 0;
+    for (int i = 0; i < n; ++i) {
+        la_plan_info info;
+        if (tc_plan(ps[i], sms, &info) == LA_OK && info.workspace_bytes > wmax) wmax = info.workspace_bytes;
+    }
+    if (b) {
+        t->ws = base + off;
+        t->ws_bytes = wmax;
+    }
+    off += (wmax + 1023) / 1024 * 1024;
+    return off;
+}
+
+// phi(q), phi(k) as bf16 rows and reversed rows; reversed v; constant rows e (normaliser)
+__global__ void __launch_bounds__(BW_THREADS) tb_feat_kernel(const bf16 *q, const bf16 *k, const bf16 *v,
+                                                           TcBufs b, int L, int dk, int dv, int fm,
+                                                           int normalize)
+{
+    const long r = blockIdx.x;
+    const long head = r / L, t = r % L;
+    const long rr = head * L + (L - 1 - t);
+    for (int i = threadIdx.x; i < dk; i += BW_THREADS) {
+        float xq = to_f32(q[r * dk + i]), xk = to_f32(k[r * dk + i]);
+        if (fm == LA_FM_ELU1) {
+            xq = phi_elu1(xq);
+            xk = phi_elu1(xk);
+        }
+        const bf16 fq = __float2bfloat16_rn(xq), fk = __float2bfloat16_rn(xk);
+        b.fq[r * dk + i] = fq;
+        b.fk[r * dk + i] = fk;
+        b.rfq[rr * dk + i] = fq;
+        b.rfk[rr * dk + i] = fk;
+    }
+    for (int j = threadIdx.x; j < dv; j += BW_THREADS) b.rv[rr * dv + j] = v[r * dv + j];
+    if (normalize)
+        for (int j = threadIdx.x; j < 64; j += BW_THREADS)
+            b.e[r * 64 + j] = __float2bfloat16_rn(j == 0 ? 1.f : 0.f);
+}
+
+// D = dout (/ den, den = phi(q).Z), reversed D; normaliser: g = D . num / den and R(g phi(q))
+__global__ void __launch_bounds__(BW_THREADS) tb_prep_kernel(const bf16 *dout, TcBufs b, int L, int D,
+                                                           int dv, int normalize)
+{
+    const long r = blockIdx.x;
+    const long head = r / L, t = r % L;
+    const long rr = head * L + (L - 1 - t);
+    __shared__ float red[BW_THREADS / 32];
+    auto block_sum = [&](float x) {
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+        __syncthreads();
+        float tot = 0.f;
+        for (int wi = 0; wi < BW_THREADS / 32; ++wi) tot += red[wi];
+        return tot;
+    };
+    if (!normalize) {
+        for (int j = threadIdx.x; j < dv; j += BW_THREADS) b.rd[rr * dv + j] = dout[r * dv + j];
+        return;
+    }
+    float part = 0.f;
+    for (int i = threadIdx.x; i < D; i += BW_THREADS) part += to_f32(b.fq[r * D + i]) * b.zc[r * D + i];
+    const float den = block_sum(part);
+    const float inv = 1.f / den;
+    float gp = 0.f;
+    for (int j = threadIdx.x; j < dv; j += BW_THREADS) {
+        // g from the same bf16 D the passes read, so dphi(q) = pass - g Z is the exact
+        // gradient for that D (its rounding is not amplified by the subtraction)
+        const bf16 db = __float2bfloat16_rn(to_f32(dout[r * dv + j]) * inv);
+        b.dn[r * dv + j] = db;
+        b.rd[rr * dv + j] = db;
+        gp += to_f32(db) * (b.num[r * dv + j] * inv);
+    }
+    const float g = block_sum(gp);
+    if (threadIdx.x == 0) b.g[r] = g;
+    for (int i = threadIdx.x; i < D; i += BW_THREADS)
+        b.rgq[rr * D + i] = __float2bfloat16_rn(g * to_f32(b.fq[r * D + i]));
+}
+
+// dq, dk through the feature map from the pass outputs (reversed ones read back), dv
+__global__ void __launch_bounds__(BW_THREADS) tb_chain_kernel(const bf16 *q, const bf16 *k, TcBufs b, bf16 *dq,
+                                                            bf16 *dk, bf16 *dv, int L, int D, int dvn,
+                                                            int fm, int normalize)
+{
+    const long r = blockIdx.x;
+    const long head = r / L, t = r % L;
+    const long rr = head * L + (L - 1 - t);
+    const float g = normalize ? b.g[r] : 0.f;
+    for (int i = threadIdx.x; i < D; i += BW_THREADS) {
+        float a = b.dqm[r * D + i], c = b.dkr[rr * D + i];
+        if (normalize) {
+            a -= g * b.zc[r * D + i];
+            c -= b.zsr[rr * D + i];
+        }
+        if (fm == LA_FM_ELU1) {
+            const float xq = to_f32(q[r * D + i]), xk = to_f32(k[r * D + i]);
+            if (xq < 0.f) a *= expf(xq);
+            if (xk < 0.f) c *= expf(xk);
+        }
+        dq[r * D + i] = __float2bfloat16_rn(a);
+        dk[r * D + i] = __float2bfloat16_rn(c);
+    }
+    for (int j = threadIdx.x; j < dvn; j += BW_THREADS) dv[r * dvn + j] = b.dvr[rr * dvn + j];
+}
+
+int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, void *dv)
+{
+    TcBufs b;
+    tc_bufs(p, sms, (char *)p.workspace, &b);
+    const long rows = (long)p.B * p.H * p.L;
+    cudaStream_t st = p.stream;
+    tb_feat_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k,
+                                                         (const bf16 *)p.v, b, p.L, p.dk, p.dv, p.fm,
+                                                         p.normalize);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    Problem ps[6];
+    const int n = tc_passes(p, b, dout, ps);
+    for (int i = 0; i < n; ++i) {
+        ps[i].workspace = b.ws;
+        ps[i].workspace_bytes = b.ws_bytes;
+    }
+    int i = 0, rc;
+    if (p.normalize) {  // Z, num
+        for (; i < 2; ++i)
+            if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
+    }
+    tb_prep_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)dout, b, p.L, p.D, p.dv,
+                                                         p.normalize);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    for (; i < n; ++i)
+        if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
+    tb_chain_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b,
+                                                          (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, p.L, p.D,
+                                                          p.dv, p.fm, p.normalize);
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
 }  // namespace
 
-size_t bwd_workspace_bytes(const Problem &p)
+// The tensor-core route: bf16, identity / elu+1 features, no decay, and every pass of a
+// shape the tensor-core forward covers.
+bool bwd_tc_supported(const Problem &p, int sms)
 {
-    return bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float);
+    if (p.dtype != LA_BF16 || p.decay || p.lam || p.L < 128) return false;
+    if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
+    Problem ps[6];
+    TcBufs nb{};
+    const int n = tc_passes(p, nb, nullptr, ps);
+    for (int i = 0; i < n; ++i)
+        if (!tc_supported(ps[i], sms)) return false;
+    return true;
+}
+
+size_t bwd_workspace_bytes(const Problem &p, int sms)
+{
+    const size_t simt = bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float);
+    const size_t tc = bwd_tc_supported(p, sms) ? tc_bufs(p, sms, nullptr, nullptr) : 0;
+    return simt > tc ? simt : tc;
 }
 
 // D, dk <= 512 and dv < 512 (the generic kernel's shared-memory rows); no level weights
 bool bwd_supported(const Problem &p) { return p.D <= 512 && p.dk <= 512 && p.dv < 512 && !p.lam; }
 
-int bwd_launch(const Problem &p, const void *out, const void *dout, void *dq, void *dk, void *dv)
+int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, void *dk, void *dv)
 {
     if (!bwd_supported(p)) return LA_ERR_UNSUPPORTED;
-    if (!p.workspace || p.workspace_bytes < bwd_workspace_bytes(p)) return LA_ERR_WORKSPACE;
-    if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, out, dout, dq, dk, dv);
-    return bwd_t<float>(p, out, dout, dq, dk, dv);
+    if (!p.workspace || p.workspace_bytes < bwd_workspace_bytes(p, sms)) return LA_ERR_WORKSPACE;
+    const bool tc = bwd_tc_supported(p, sms);
+    if (path == LA_PATH_TC && !tc) return LA_ERR_UNSUPPORTED;
+    if (path != LA_PATH_SIMT && tc) return tc_route(p, sms, dout, dq, dk, dv);
+    if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, dout, dq, dk, dv);
+    return bwd_t<float>(p, dout, dq, dk, dv);
 }
 
 }  // namespace la

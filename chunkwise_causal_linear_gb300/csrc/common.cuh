@@ -60,6 +60,8 @@ struct Problem {
     float l2g;               // log2(gamma), rounded from the double value
     int rev;                 // 1: anti-causal (generic path only): row t reads the rows s >= t,
                              // computed as the causal pass over the reversed sequence
+    int out_f32;             // 1: out is fp32 rows (tensor-core path, identity features, no
+                             // normaliser; the backward pass's internal passes)
 };
 
 // Host-side queries used by the planner.

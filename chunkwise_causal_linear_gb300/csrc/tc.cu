@@ -118,10 +118,10 @@ struct TcArgs {
     int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
 
-// kernel modes
-constexpr int TC_CAUSAL = 0, TC_NONCAUSAL = 1, TC_DECAY = 2;
+// kernel modes (TC_F32OUT: causal, output stored as fp32 rows)
+constexpr int TC_CAUSAL = 0, TC_NONCAUSAL = 1, TC_DECAY = 2, TC_F32OUT = 3;
 
-template <int D, int DV, int C, bool NORM>
+template <int D, int DV, int C, bool NORM, bool F32O = false>
 struct TcLayout {
     static constexpr int KROWS = NORM ? C + 8 : C;    // key rows (+ z hi/lo + zero rows)
     static constexpr int NSC = KROWS;                 // N of the scores MMA
@@ -132,12 +132,13 @@ struct TcLayout {
     static constexpr int STAGE_BYTES = Q_BYTES + K_BYTES + V_BYTES;
     static constexpr int STAGE_TX = Q_BYTES + C * D * 2 + V_BYTES;  // bytes TMA delivers
     static constexpr int P_BYTES = C * C * 2;
-    static constexpr int O_BYTES = C * DV * 2;
+    static constexpr int O_BYTES = C * DV * (F32O ? 4 : 2);
     // P and the output tile are single-buffered: MMAs complete in issue order, so the
     // scores of chunk c+1 finishing implies the intra product of chunk c has read P.
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_P = TC_STAGES * STAGE_BYTES;
-    static constexpr int OFF_O = OFF_P + P_BYTES;
+    // fp32-output mode: P as a bf16 hi tile and a lo tile (P - hi)
+    static constexpr int OFF_O = OFF_P + (F32O ? 2 : 1) * P_BYTES;
     static constexpr int OFF_F32 = OFF_O + O_BYTES;
     // floats: rden[TC_DEN][C], z[D], zpart[TC_FWARPS][D]
     static constexpr int N_F32 = TC_DEN * C + D + TC_FWARPS * D;
@@ -147,7 +148,10 @@ struct TcLayout {
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
     // TMEM columns
-    static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 192, T_A = 320, A_STRIDE = 80;
+    // fp32-output mode (no normaliser: scores are C = 64 columns): the state copy is a bf16
+    // hi / lo pair, S^T fp32 | hi | lo | O^T x2 | scores x2 fills the 512 columns
+    static constexpr uint32_t T_S = 0, T_SB = 128, T_SL = 192, T_O = F32O ? 256 : 192,
+                              T_A = F32O ? 384 : 320, A_STRIDE = F32O ? 64 : 80;
     static_assert(D <= 128 && (DV == 64 || DV == 128), "tensor-core path: D <= 128, dv 64 or 128");
     static_assert(C == 64, "tensor-core path: 64-row tiles");
     static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
@@ -169,8 +173,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     constexpr int NSUB = C / CH;    // chunks per tile
     constexpr bool NC = MODE == TC_NONCAUSAL;
     constexpr bool DK = MODE == TC_DECAY;
+    constexpr bool FO = MODE == TC_F32OUT;
     static_assert(!DK || CH == C, "decay: one chunk per tile");
-    using Lay = TcLayout<D, DV, C, NORM>;
+    static_assert(!FO || (FM == LA_FM_IDENTITY && !NORM), "fp32 output: identity features, no normaliser");
+    using Lay = TcLayout<D, DV, C, NORM, FO>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles (offset taken in the shared window)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -252,10 +258,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     if (DK && !NORM)
         for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
     if (CH == C)
-        // P rows 0-31, columns 32-63: always zero (causal mask), written once
-        for (int e = tid; e < 32 * 4; e += TC_THREADS) {
-            const int t = e >> 2, chn = 4 + (e & 3);
-            *(uint4 *)(p_tile + t * 128 + ((chn ^ (t & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        // P rows 0-31, columns 32-63: always zero (causal mask), written once (both tiles
+        // in the fp32-output mode)
+        for (int e = tid; e < (FO ? 2 : 1) * 32 * 4; e += TC_THREADS) {
+            const int t = (e >> 2) & 31, chn = 4 + (e & 3);
+            *(uint4 *)(p_tile + (e >> 7) * Lay::P_BYTES + t * 128 + ((chn ^ (t & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
         }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_async_smem();
@@ -263,7 +271,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB;
+    const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB, tSL = tmem + Lay::T_SL;
+    // fp32-output mode: bf16 hi / lo split of fp32 values (x = hi + lo to ~2^-16 relative)
+    auto lo_of = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
     if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
         // the state and its bf16 copy start at the sum of the earlier segments' totals (zero
         // for the first segment and for the totals pass)
@@ -297,6 +307,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             for (int e = 0; e < 8; ++e) w16[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
             tmem_st16(tS + lo + col, w32);
             tmem_st8(tSB + lo + col / 2, w16);
+            if (FO) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w16[e] = pack_bf16x2(lo_of(acc[2 * e]), lo_of(acc[2 * e + 1]));
+                tmem_st8(tSL + lo + col / 2, w16);
+            }
         }
         tmem_wait_st();
     }
@@ -393,6 +408,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32 + j * CH * 128;
                         mma_ts(tO + j * CH, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
                     }
+                    if (FO)  // the state copy's lo part
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32 + j * CH * 128;
+                            mma_ts(tO + j * CH, tSL + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, 1);
+                        }
                     // state: S^T += V_g^T phi(K_g), both MN-major, K = CH in steps of 16 rows
                     if (g + 1 < nsub && !NC) {
 #pragma unroll
@@ -412,6 +433,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ss(tO, smem_desc(va + ks * 2048, C * 128, 1024),
                            smem_desc(pa + ks * 32, 16, 1024), ID_INTRA, 1);
+                if (FO)  // P's lo tile
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_ss(tO, smem_desc(va + ks * 2048, C * 128, 1024),
+                               smem_desc(pa + Lay::P_BYTES + ks * 32, 16, 1024), ID_INTRA, 1);
                 mma_commit(&o_done[b]);
                 mma_commit(&stage_free[s]);
             }
@@ -636,6 +662,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         *(uint4 *)(prow + ((chn ^ (t & 7)) << 4)) =
                             make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
+                    if (FO) {
+                        // P's lo tile: the rounding residue of each kept score (CH == C here)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
+                            const float v0 = s0 <= t ? __uint_as_float(r[2 * e]) : 0.f;
+                            const float v1 = s1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
+                            pk[e] = pack_bf16x2(lo_of(v0), lo_of(v1));
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int chn = 4 * h + q;
+                            *(uint4 *)(prow + Lay::P_BYTES + ((chn ^ (t & 7)) << 4)) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        }
+                    }
                 }
             }
             // den = phi(q_t).z_c + masked row sum
@@ -677,6 +719,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack_bf16x2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]));
                     tmem_st16(tSB + lane_off + cb * 16, pk);
+                    if (FO) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16x2(lo_of(__uint_as_float(sv[2 * e])), lo_of(__uint_as_float(sv[2 * e + 1])));
+                        tmem_st16(tSL + lane_off + cb * 16, pk);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -728,6 +776,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         rd[4 * q + 2] = mf * v.z; rd[4 * q + 3] = mf * v.w;
                     }
                 }
+                if (FO) {
+                    // fp32 rows: column j of token tt in 32-column box j / 32, 128-byte swizzle
+                    uint8_t *const fb = o_tile + (j >> 5) * C * 128 + ((j & 3) << 2);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int tt = 32 * h + u;
+                        if (live) *(uint32_t *)(fb + tt * 128 + ((((j & 31) >> 2) ^ (tt & 7)) << 4)) = r[u];
+                    }
+                    continue;
+                }
                 // Lanes j, j^1 swap one value per pair of rows so that each writes two
                 // neighbouring columns of one row as a single 32-bit word.
 #pragma unroll
@@ -746,8 +804,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             fence_async_smem();
             named_bar(3, 128);
             if (ot == 0) {
-                for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, (tile0 + c) * C, head);
+                if (FO)
+                    for (int jb = 0; jb < DV / 32; ++jb)
+                        tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 32, (tile0 + c) * C, head);
+                else
+                    for (int jb = 0; jb < DV / 64; ++jb)
+                        tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, (tile0 + c) * C, head);
                 tma_commit_group();
                 if (NORM) mbar_arrive(&den_empty[slot]);
             }
@@ -786,8 +848,10 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     TcArgs a;
     memset(&a, 0, sizeof(a));
     const int BH = p.B * p.H;
+    const bool fo = mode == TC_F32OUT;
     if (!make_map(&a.tm_q, p.q, BH, p.L, p.dk, C) || !make_map(&a.tm_k, p.k, BH, p.L, p.dk, C) ||
-        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, C) || !make_map(&a.tm_o, p.out, BH, p.L, p.dv, C))
+        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, C) ||
+        !(fo ? make_map_f32(&a.tm_o, p.out, BH, p.L, p.dv, C) : make_map(&a.tm_o, p.out, BH, p.L, p.dv, C)))
         return LA_ERR_CUDA;
     a.L = p.L;
     a.nch = (p.L + C - 1) / C;
@@ -816,25 +880,33 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     const char *st = getenv("LA_DEBUG_STALL");
     a.debug_stall = (st && *st && *st != '0') ? 1 : 0;
     auto kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_CAUSAL>;
+    int alloc = Lay::ALLOC;
     if constexpr (CH == C) {
         if (mode == TC_NONCAUSAL) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_NONCAUSAL>;
         if (mode == TC_DECAY) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_DECAY>;
+        if (mode == TC_F32OUT) {
+            if constexpr (FM == LA_FM_IDENTITY && !NORM) {
+                kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_F32OUT>;
+                alloc = TcLayout<D, DV, C, NORM, true>::ALLOC;
+            } else {
+                return LA_ERR_UNSUPPORTED;
+            }
+        }
     } else if (mode != TC_CAUSAL) {
         return LA_ERR_UNSUPPORTED;
     }
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc) != cudaSuccess)
         return LA_ERR_CUDA;
     if (ntot > 0) {
         // totals of segments 0..ntot-1, then the main pass over all segments
         a.totals = 1;
         a.grid_seg = ntot;
-        kern<<<BH * ntot, TC_THREADS, Lay::ALLOC, p.stream>>>(a);
+        kern<<<BH * ntot, TC_THREADS, alloc, p.stream>>>(a);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }
     a.totals = 0;
     a.grid_seg = nseg;
-    kern<<<BH * nseg, TC_THREADS, Lay::ALLOC, p.stream>>>(a);
+    kern<<<BH * nseg, TC_THREADS, alloc, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
@@ -853,6 +925,7 @@ template <int D, int DV>
 int launch_d(const Problem &p, int sms)
 {
     if (p.decay) return launch_dc<D, DV, 64>(p, sms, TC_DECAY);
+    if (p.out_f32) return launch_dc<D, DV, 64>(p, sms, TC_F32OUT);
     if (p.C == 16) return launch_dc<D, DV, 16>(p, sms);
     if (p.C == 32) return launch_dc<D, DV, 32>(p, sms);
     return launch_dc<D, DV, 64>(p, sms);
@@ -882,6 +955,8 @@ bool tc_supported(const Problem &p, int num_sms)
         if (p.lam || p.C != 64 || p.l2g < -1.f) return false;
         if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     }
+    if (p.out_f32 && (p.decay || p.lam || p.C != 64 || p.fm != LA_FM_IDENTITY || p.normalize))
+        return false;
     if (p.lam) return tcl_supported(p);
     if (p.fm == LA_FM_FAVOR) return tcf_supported(p);
     if (p.C == 128 || p.C == 256) return tcw_supported(p);

@@ -93,6 +93,21 @@ inline bool make_map(CUtensorMap *m, const void *ptr, int BH, int L, int d, int 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 rows [BH][L][d]: boxes of 32 columns (128 bytes) x C rows, 128-byte swizzle
+inline bool make_map_f32(CUtensorMap *m, const void *ptr, int BH, int L, int d, int C)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)L * d * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Segments per head for a sequence of `tiles` 64-row tiles: split when the heads alone leave
 // most SMs idle, keeping at least `min_tiles` tiles per segment.
 inline int split_segments(int BH, int tiles, int num_sms, int min_tiles, int *seg_tiles)

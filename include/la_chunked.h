@@ -312,26 +312,33 @@ int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_m
  * la_chunked_bwd -- backward pass of the causal forward (la_chunked_fwd without level
  * weights, or la_decay_fwd): given dout = dL/dout, writes dq, dk, dv.  The pages give no
  * backward formulas; these follow from the chain rule on the causal definition (mask 1 or
- * gamma^(t-s), with or without the normaliser), then through the feature map.  Computed on
- * the generic path in fp32 as three linear-attention passes with the roles swapped (two of
- * them anti-causal) plus, with the normaliser, one for the denominators.
- *   q, k, v, dout   device, as la_chunked_fwd's q, k, v and out ([B, H, L, d], dtype)
- *   out             the forward output (needed with normalize; may be NULL without)
+ * gamma^(t-s), with or without the normaliser), then through the feature map.  They are
+ * linear-attention passes with the roles swapped, two of them anti-causal:
+ *   - LA_PATH_TC: bf16, identity / elu+1 features, no decay, L >= 128 and pass shapes the
+ *     tensor-core forward covers ((dk, dv) in {(64, 64), (128, 128)}); the anti-causal
+ *     passes run over reversed rows and the normaliser adds two passes; pass outputs are
+ *     bf16 like the forward's;
+ *   - LA_PATH_SIMT: every supported case, in fp32 on the generic kernel;
+ *   - LA_PATH_AUTO picks the first that applies.
+ *   q, k, v, dout   device, as la_chunked_fwd's q, k, v and out ([B, H, L, d], dtype).
+ *                   The forward output is not an input: with the normaliser, dq is a small
+ *                   difference of two large sums, so the pass recomputes the output in fp32
+ *                   (a bf16-stored one would carry its rounding into dq about thirtyfold).
  *   grad_q, grad_k, grad_v  device outputs dq, dk, dv: same shapes and dtype as q, k, v;
  *                   fully overwritten
  *   gamma           1 for the plain mask, else the decay (0 < gamma < 1; LA_ERR_ARG outside)
- *   C               chunk size of the internal passes (any value; the result does not
- *                   depend on it beyond rounding)
+ *   C               chunk size of the generic path's passes (any value; the result does
+ *                   not depend on it beyond rounding); the tensor-core passes use 64
  *   workspace       at least la_chunked_bwd_workspace_bytes(...) bytes (fp32 intermediates,
  *                   about 4 (D + dv) floats per row)
  * D (dk, or m for FAVOR+) and dk must be at most 512 and dv below 512.  Returns LA_OK or a
  * negative status before any launch.
  */
-int la_chunked_bwd(const void *q, const void *k, const void *v, const void *out,
-                   const void *dout, void *grad_q, void *grad_k, void *grad_v, int B, int H,
+int la_chunked_bwd(const void *q, const void *k, const void *v, const void *dout,
+                   void *grad_q, void *grad_k, void *grad_v, int B, int H,
                    int L, int dk, int dv, int C, const la_feature_map *feature_map,
                    int normalize, float gamma, int dtype, void *workspace,
-                   size_t workspace_bytes, void *stream);
+                   size_t workspace_bytes, void *stream, int path);
 
 /* Workspace bytes la_chunked_bwd needs (0 on an invalid or unsupported combination). */
 size_t la_chunked_bwd_workspace_bytes(int B, int H, int L, int dk, int dv, int C,

@@ -2,8 +2,7 @@
 
 The oracle applies the chain rule to the plain causal definition (pinned by finite
 differences of its forward recurrence); the library composes causal and anti-causal
-linear-attention passes on the generic fp32 path.  With the normaliser the library is
-given its own forward output, as a caller would; the oracle recomputes its own.
+linear-attention passes, on the generic fp32 path or on the tensor cores.
 """
 import numpy as np
 import pytest
@@ -23,7 +22,7 @@ def _built():
     build.build()
 
 
-def run_bwd(w, inp, dout_bits, C, gamma=1.0):
+def run_bwd(w, inp, dout_bits, C, gamma=1.0, path=0):
     import torch
 
     import chunkwise_causal_linear_gb300 as la
@@ -33,15 +32,8 @@ def run_bwd(w, inp, dout_bits, C, gamma=1.0):
     v = to_device(inp["v"], w["dtype"], (B, H, L, dv))
     do = to_device(dout_bits, w["dtype"], (B, H, L, dv))
     omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
-    out = None
-    if w["normalize"]:
-        if gamma == 1.0:
-            out = la.chunked_fwd(q, k, v, C=64, feature_map=w["fm"], omega=omega, normalize=True)
-        else:
-            out = la.decay_fwd(q, k, v, gamma, C=64, feature_map=w["fm"], omega=omega,
-                               normalize=True)
-    dq, dk_, dv_ = la.chunked_bwd(q, k, v, do, out=out, C=C, feature_map=w["fm"], omega=omega,
-                                  normalize=w["normalize"], gamma=gamma)
+    dq, dk_, dv_ = la.chunked_bwd(q, k, v, do, C=C, feature_map=w["fm"], omega=omega,
+                                  normalize=w["normalize"], gamma=gamma, path=path)
     torch.cuda.synchronize()
     st = la.la_last_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == la.LA_OK, la.la_status_string(st)
@@ -75,7 +67,15 @@ CASES = [
     ("favor-m256-d64-L16384", dict(B=1, H=2, L=150), 64, 1.0),
     ("favor-m256-d64-L16384", dict(B=1, H=1, L=130, normalize=False), 64, 1.0),
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=2048), 64, 1.0),  # d128, 32 tiles per head
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=700, normalize=False), 64, 1.0),
+    ("identity-d64-L2048", dict(B=1, H=3, L=1000, normalize=True, fm="elu1", scale=1.0), 64, 1.0),
 ]
+
+
+def bwd_path(w, gamma):
+    """1 (generic) or 2 (tensor cores): the path la_chunked_bwd takes on AUTO."""
+    return 2 if (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1") and gamma == 1.0
+                 and w["L"] >= 128 and w["dk"] == w["dv"] and w["dk"] in (64, 128)) else 1
 
 
 @pytest.mark.parametrize("base,over,C,gamma", CASES)
@@ -83,10 +83,30 @@ def test_backward_matches_oracle(base, over, C, gamma):
     w = workload(base, **over)
     inp = synth.make_inputs(w, seed=41)
     do = dout_for(w, 41)
-    got = run_bwd(w, inp, do, C, gamma)
     ref = oracle_bwd(w, inp, do, gamma)
-    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        assert_close(g, r, f"{name} {base} {over} C={C} gamma={gamma}")
+    paths = [1] + ([2] if bwd_path(w, gamma) == 2 else [])
+    for path in paths:
+        got = run_bwd(w, inp, do, C, gamma, path)
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            assert_close(g, r, f"{name} {base} {over} C={C} gamma={gamma} path={path}")
+
+
+def test_backward_tensor_core_route_is_taken():
+    """LA_PATH_TC succeeds where the route applies and is refused where it does not."""
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    w = workload("elu1-norm-d128-L8192", B=1, H=2, L=256)
+    inp = synth.make_inputs(w, seed=43)
+    do = dout_for(w, 43)
+    run_bwd(w, inp, do, 64, 1.0, path=2)
+    with pytest.raises(la.LAError):
+        run_bwd(w, inp, do, 64, 0.9, path=2)  # decay: generic path only
+    wf = workload("elu1-norm-d128-L8192", B=1, H=1, L=256, dtype="f32")
+    inpf = synth.make_inputs(wf, seed=43)
+    with pytest.raises(la.LAError):
+        run_bwd(wf, inpf, dout_for(wf, 43), 64, 1.0, path=2)  # fp32 storage
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("normalize", [False, True])
@@ -114,10 +134,9 @@ def test_backward_rejects_bad_arguments():
     s = torch.cuda.current_stream().cuda_stream
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     args = (1, 1, 64, 16, 16, 64, fm)
-    # the normaliser needs the forward output
-    assert la.la_chunked_bwd(p, p, p, None, p, p, p, p, *args, 1, 1.0, la.LA_BF16, ws.data_ptr(),
+    assert la.la_chunked_bwd(p, p, p, None, p, p, p, *args, 1, 1.0, la.LA_BF16, ws.data_ptr(),
                              ws.numel(), s) == la.LA_ERR_NULL
-    assert la.la_chunked_bwd(p, p, p, p, p, p, p, p, *args, 0, 1.5, la.LA_BF16, ws.data_ptr(),
+    assert la.la_chunked_bwd(p, p, p, p, p, p, p, *args, 0, 1.5, la.LA_BF16, ws.data_ptr(),
                              ws.numel(), s) == la.LA_ERR_ARG
-    assert la.la_chunked_bwd(p, p, p, p, p, p, p, p, *args, 0, 1.0, la.LA_BF16, ws.data_ptr(), 16,
+    assert la.la_chunked_bwd(p, p, p, p, p, p, p, *args, 0, 1.0, la.LA_BF16, ws.data_ptr(), 16,
                              s) == la.LA_ERR_WORKSPACE
