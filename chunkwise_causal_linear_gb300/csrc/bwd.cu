@@ -36,6 +36,7 @@
 // other sums cancel exactly for those features.  The feature-gradient passes run in the
 // kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows out).
 #include <math.h>
+#include <stdint.h>
 #include <stdio.h>
 
 #include <type_traits>
@@ -359,96 +360,153 @@ size_t tc_bufs(const Problem &p, int sms, char *base, TcBufs *b)
     return off;
 }
 
-// phi(q), phi(k) as bf16 rows and reversed rows; reversed v; constant rows e (normaliser)
-__global__ void __launch_bounds__(BW_THREADS) tb_feat_kernel(const bf16 *q, const bf16 *k, const bf16 *v,
-                                                           TcBufs b, int L, int dk, int dv, int fm,
-                                                           int normalize)
+// The elementwise kernels of the route: one warp per row, four consecutive elements per
+// lane (8-byte bf16 / 16-byte fp32 accesses), reductions by warp shuffles.  D and dv are
+// 64 or 128 here.
+constexpr int TB_ROWS = 8;  // rows (warps) per block
+
+__device__ __forceinline__ void ld4(const bf16 *p, float (&x)[4])
 {
-    const long r = blockIdx.x;
+    const uint2 u = *(const uint2 *)p;
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ void st4(bf16 *p, const float (&x)[4])
+{
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *(const uint32_t *)&a;
+    u.y = *(const uint32_t *)&b;
+    *(uint2 *)p = u;
+}
+__device__ __forceinline__ void ld4(const float *p, float (&x)[4])
+{
+    const float4 f = *(const float4 *)p;
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+}
+__device__ __forceinline__ float warp_sum(float x)
+{
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// phi(q), phi(k) as bf16 rows and reversed rows; reversed v; constant rows e (normaliser)
+__global__ void __launch_bounds__(32 * TB_ROWS) tb_feat_kernel(const bf16 *q, const bf16 *k, const bf16 *v,
+                                                             TcBufs b, long rows, int L, int dk, int dv,
+                                                             int fm, int normalize)
+{
+    const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
     const long head = r / L, t = r % L;
     const long rr = head * L + (L - 1 - t);
-    for (int i = threadIdx.x; i < dk; i += BW_THREADS) {
-        float xq = to_f32(q[r * dk + i]), xk = to_f32(k[r * dk + i]);
-        if (fm == LA_FM_ELU1) {
-            xq = phi_elu1(xq);
-            xk = phi_elu1(xk);
-        }
-        const bf16 fq = __float2bfloat16_rn(xq), fk = __float2bfloat16_rn(xk);
-        b.fq[r * dk + i] = fq;
-        b.fk[r * dk + i] = fk;
-        b.rfq[rr * dk + i] = fq;
-        b.rfk[rr * dk + i] = fk;
+    for (int i = 4 * lane; i < dk; i += 128) {
+        float xq[4], xk[4];
+        ld4(q + r * dk + i, xq);
+        ld4(k + r * dk + i, xk);
+        if (fm == LA_FM_ELU1)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                xq[e] = phi_elu1(xq[e]);
+                xk[e] = phi_elu1(xk[e]);
+            }
+        st4(b.fq + r * dk + i, xq);
+        st4(b.fk + r * dk + i, xk);
+        st4(b.rfq + rr * dk + i, xq);
+        st4(b.rfk + rr * dk + i, xk);
     }
-    for (int j = threadIdx.x; j < dv; j += BW_THREADS) b.rv[rr * dv + j] = v[r * dv + j];
-    if (normalize)
-        for (int j = threadIdx.x; j < 64; j += BW_THREADS)
-            b.e[r * 64 + j] = __float2bfloat16_rn(j == 0 ? 1.f : 0.f);
+    for (int j = 4 * lane; j < dv; j += 128) *(uint2 *)(b.rv + rr * dv + j) = *(const uint2 *)(v + r * dv + j);
+    if (normalize && lane < 16) {
+        const float ev[4] = {lane == 0 ? 1.f : 0.f, 0.f, 0.f, 0.f};
+        st4(b.e + r * 64 + 4 * lane, ev);
+    }
 }
 
 // D = dout (/ den, den = phi(q).Z), reversed D; normaliser: g = D . num / den and R(g phi(q))
-__global__ void __launch_bounds__(BW_THREADS) tb_prep_kernel(const bf16 *dout, TcBufs b, int L, int D,
-                                                           int dv, int normalize)
+__global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout, TcBufs b, long rows, int L,
+                                                             int D, int dv, int normalize)
 {
-    const long r = blockIdx.x;
+    const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
     const long head = r / L, t = r % L;
     const long rr = head * L + (L - 1 - t);
-    __shared__ float red[BW_THREADS / 32];
-    auto block_sum = [&](float x) {
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        __syncthreads();
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-        __syncthreads();
-        float tot = 0.f;
-        for (int wi = 0; wi < BW_THREADS / 32; ++wi) tot += red[wi];
-        return tot;
-    };
     if (!normalize) {
-        for (int j = threadIdx.x; j < dv; j += BW_THREADS) b.rd[rr * dv + j] = dout[r * dv + j];
+        for (int j = 4 * lane; j < dv; j += 128) *(uint2 *)(b.rd + rr * dv + j) = *(const uint2 *)(dout + r * dv + j);
         return;
     }
     float part = 0.f;
-    for (int i = threadIdx.x; i < D; i += BW_THREADS) part += to_f32(b.fq[r * D + i]) * b.zc[r * D + i];
-    const float den = block_sum(part);
-    const float inv = 1.f / den;
+    for (int i = 4 * lane; i < D; i += 128) {
+        float f[4], z[4];
+        ld4(b.fq + r * D + i, f);
+        ld4(b.zc + r * D + i, z);
+        part += f[0] * z[0] + f[1] * z[1] + f[2] * z[2] + f[3] * z[3];
+    }
+    const float inv = 1.f / warp_sum(part);
     float gp = 0.f;
-    for (int j = threadIdx.x; j < dv; j += BW_THREADS) {
+    for (int j = 4 * lane; j < dv; j += 128) {
         // g from the same bf16 D the passes read, so dphi(q) = pass - g Z is the exact
         // gradient for that D (its rounding is not amplified by the subtraction)
-        const bf16 db = __float2bfloat16_rn(to_f32(dout[r * dv + j]) * inv);
-        b.dn[r * dv + j] = db;
-        b.rd[rr * dv + j] = db;
-        gp += to_f32(db) * (b.num[r * dv + j] * inv);
+        float d[4], n[4];
+        ld4(dout + r * dv + j, d);
+        ld4(b.num + r * dv + j, n);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[e] = __bfloat162float(__float2bfloat16_rn(d[e] * inv));
+        st4(b.dn + r * dv + j, d);
+        st4(b.rd + rr * dv + j, d);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gp += d[e] * (n[e] * inv);
     }
-    const float g = block_sum(gp);
-    if (threadIdx.x == 0) b.g[r] = g;
-    for (int i = threadIdx.x; i < D; i += BW_THREADS)
-        b.rgq[rr * D + i] = __float2bfloat16_rn(g * to_f32(b.fq[r * D + i]));
+    const float g = warp_sum(gp);
+    if (lane == 0) b.g[r] = g;
+    for (int i = 4 * lane; i < D; i += 128) {
+        float f[4];
+        ld4(b.fq + r * D + i, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] *= g;
+        st4(b.rgq + rr * D + i, f);
+    }
 }
 
 // dq, dk through the feature map from the pass outputs (reversed ones read back), dv
-__global__ void __launch_bounds__(BW_THREADS) tb_chain_kernel(const bf16 *q, const bf16 *k, TcBufs b, bf16 *dq,
-                                                            bf16 *dk, bf16 *dv, int L, int D, int dvn,
-                                                            int fm, int normalize)
+__global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, const bf16 *k, TcBufs b,
+                                                              bf16 *dq, bf16 *dk, bf16 *dv, long rows,
+                                                              int L, int D, int dvn, int fm, int normalize)
 {
-    const long r = blockIdx.x;
+    const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
     const long head = r / L, t = r % L;
     const long rr = head * L + (L - 1 - t);
     const float g = normalize ? b.g[r] : 0.f;
-    for (int i = threadIdx.x; i < D; i += BW_THREADS) {
-        float a = b.dqm[r * D + i], c = b.dkr[rr * D + i];
+    for (int i = 4 * lane; i < D; i += 128) {
+        float a[4], c[4];
+        ld4(b.dqm + r * D + i, a);
+        ld4(b.dkr + rr * D + i, c);
         if (normalize) {
-            a -= g * b.zc[r * D + i];
-            c -= b.zsr[rr * D + i];
+            float z[4], zs[4];
+            ld4(b.zc + r * D + i, z);
+            ld4(b.zsr + rr * D + i, zs);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a[e] -= g * z[e];
+                c[e] -= zs[e];
+            }
         }
         if (fm == LA_FM_ELU1) {
-            const float xq = to_f32(q[r * D + i]), xk = to_f32(k[r * D + i]);
-            if (xq < 0.f) a *= expf(xq);
-            if (xk < 0.f) c *= expf(xk);
+            float xq[4], xk[4];
+            ld4(q + r * D + i, xq);
+            ld4(k + r * D + i, xk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (xq[e] < 0.f) a[e] *= expf(xq[e]);
+                if (xk[e] < 0.f) c[e] *= expf(xk[e]);
+            }
         }
-        dq[r * D + i] = __float2bfloat16_rn(a);
-        dk[r * D + i] = __float2bfloat16_rn(c);
+        st4(dq + r * D + i, a);
+        st4(dk + r * D + i, c);
     }
-    for (int j = threadIdx.x; j < dvn; j += BW_THREADS) dv[r * dvn + j] = b.dvr[rr * dvn + j];
+    for (int j = 4 * lane; j < dvn; j += 128) *(uint2 *)(dv + r * dvn + j) = *(const uint2 *)(b.dvr + rr * dvn + j);
 }
 
 int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, void *dv)
@@ -457,9 +515,9 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     tc_bufs(p, sms, (char *)p.workspace, &b);
     const long rows = (long)p.B * p.H * p.L;
     cudaStream_t st = p.stream;
-    tb_feat_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k,
-                                                         (const bf16 *)p.v, b, p.L, p.dk, p.dv, p.fm,
-                                                         p.normalize);
+    const unsigned tgrid = (unsigned)((rows + TB_ROWS - 1) / TB_ROWS);
+    tb_feat_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, (const bf16 *)p.v, b,
+                                                  rows, p.L, p.dk, p.dv, p.fm, p.normalize);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     Problem ps[6];
     const int n = tc_passes(p, b, dout, ps);
@@ -472,14 +530,14 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
         for (; i < 2; ++i)
             if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
     }
-    tb_prep_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)dout, b, p.L, p.D, p.dv,
-                                                         p.normalize);
+    tb_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, p.L, p.D, p.dv,
+                                                  p.normalize);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     for (; i < n; ++i)
         if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
-    tb_chain_kernel<<<(unsigned)rows, BW_THREADS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b,
-                                                          (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, p.L, p.D,
-                                                          p.dv, p.fm, p.normalize);
+    tb_chain_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b, (bf16 *)dq,
+                                                   (bf16 *)dk, (bf16 *)dv, rows, p.L, p.D, p.dv, p.fm,
+                                                   p.normalize);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
@@ -513,7 +571,10 @@ int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, 
 {
     if (!bwd_supported(p)) return LA_ERR_UNSUPPORTED;
     if (!p.workspace || p.workspace_bytes < bwd_workspace_bytes(p, sms)) return LA_ERR_WORKSPACE;
-    const bool tc = bwd_tc_supported(p, sms);
+    // the route's elementwise kernels use 8- and 16-byte accesses on the caller's rows
+    const uintptr_t al = (uintptr_t)p.q | (uintptr_t)p.k | (uintptr_t)p.v | (uintptr_t)dout |
+                         (uintptr_t)dq | (uintptr_t)dk | (uintptr_t)dv;
+    const bool tc = bwd_tc_supported(p, sms) && (al & 15) == 0;
     if (path == LA_PATH_TC && !tc) return LA_ERR_UNSUPPORTED;
     if (path != LA_PATH_SIMT && tc) return tc_route(p, sms, dout, dq, dk, dv);
     if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, dout, dq, dk, dv);
