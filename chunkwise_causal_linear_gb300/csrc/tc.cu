@@ -384,12 +384,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
                                va = smem_u32(stage_v(s)), pa = smem_u32(p_tile);
                 const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
+                // Descriptors: one per operand and tile; a constant byte offset goes into the
+                // address field (addr >> 4), which never carries since shared addresses stay
+                // below 256 KB.  This keeps the issuing thread's work per MMA to one add.
+                const uint64_t dQ = smem_desc(qa, 16, 1024), dK = smem_desc(ka, 16, 1024);
+                const uint64_t dVmn = smem_desc(va, C * 128, 1024), dKmn = smem_desc(ka, Lay::K_BLK, 1024);
+                const uint64_t dP = smem_desc(pa, 16, 1024);
+                auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
                 // scores of the tile: phi(Q) [phi(K); z]^T, both K-major, K = D in steps of 16
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32;
                     const uint32_t ko = (ks >> 2) * Lay::K_BLK + (ks & 3) * 32;
-                    mma_ss(tA, smem_desc(qa + qo, 16, 1024), smem_desc(ka + ko, 16, 1024), ID_SC, ks > 0);
+                    mma_ss(tA, dadd(dQ, qo), dadd(dK, ko), ID_SC, ks > 0);
                 }
                 mma_commit(&scores_done[b]);
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
@@ -406,21 +413,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32 + j * CH * 128;
-                        mma_ts(tO + j * CH, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
+                        mma_ts(tO + j * CH, tSB + ks * 8, dadd(dQ, qo), ID_INTER, ks > 0);
                     }
                     if (FO)  // the state copy's lo part
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint32_t qo = (ks >> 2) * C * 128 + (ks & 3) * 32 + j * CH * 128;
-                            mma_ts(tO + j * CH, tSL + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, 1);
+                            mma_ts(tO + j * CH, tSL + ks * 8, dadd(dQ, qo), ID_INTER, 1);
                         }
                     // state: S^T += V_g^T phi(K_g), both MN-major, K = CH in steps of 16 rows
                     if (g + 1 < nsub && !NC) {
 #pragma unroll
                         for (int ks = 0; ks < CH / 16; ++ks) {
                             const uint32_t ro = (j * CH + 16 * ks) * 128;
-                            mma_ss(tS, smem_desc(va + ro, C * 128, 1024),
-                                   smem_desc(ka + ro, Lay::K_BLK, 1024), ID_STATE, 1);
+                            mma_ss(tS, dadd(dVmn, ro), dadd(dKmn, ro), ID_STATE, 1);
                         }
                         mma_commit(state_done);
                     }
@@ -431,13 +437,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 // intra: V^T (MN-major A) x P^T (K-major B) over the tile, K = 64
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
-                    mma_ss(tO, smem_desc(va + ks * 2048, C * 128, 1024),
-                           smem_desc(pa + ks * 32, 16, 1024), ID_INTRA, 1);
+                    mma_ss(tO, dadd(dVmn, ks * 2048), dadd(dP, ks * 32), ID_INTRA, 1);
                 if (FO)  // P's lo tile
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks)
-                        mma_ss(tO, smem_desc(va + ks * 2048, C * 128, 1024),
-                               smem_desc(pa + Lay::P_BYTES + ks * 32, 16, 1024), ID_INTRA, 1);
+                        mma_ss(tO, dadd(dVmn, ks * 2048), dadd(dP, Lay::P_BYTES + ks * 32), ID_INTRA, 1);
                 mma_commit(&o_done[b]);
                 mma_commit(&stage_free[s]);
             }
