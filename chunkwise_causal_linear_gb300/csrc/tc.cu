@@ -143,7 +143,7 @@ struct TcLayout {
     // floats: rden[TC_DEN][C], z[D], zpart[TC_FWARPS][D]
     static constexpr int N_F32 = TC_DEN * C + D + TC_FWARPS * D;
     static constexpr int OFF_BAR = OFF_F32 + ((N_F32 * 4 + 15) / 16) * 16;
-    static constexpr int N_BAR = 3 * TC_STAGES + 2 * 5 + 2 * TC_DEN + 3;
+    static constexpr int N_BAR = 3 * TC_STAGES + 2 * 4 + 2 * TC_DEN + 3;
     static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -189,8 +189,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     uint64_t *phi_ready = full + TC_STAGES;          // [S] feature map -> MMA
     uint64_t *stage_free = phi_ready + TC_STAGES;    // [S] MMA -> TMA
     uint64_t *scores_done = stage_free + TC_STAGES;  // [2]
-    uint64_t *a_free = scores_done + 2;              // [2]
-    uint64_t *p_ready = a_free + 2;                  // [2]
+    uint64_t *p_ready = scores_done + 2;             // [2]
     uint64_t *o_done = p_ready + 2;                  // [2]
     uint64_t *o_free = o_done + 2;                   // [2]
     uint64_t *den_full = o_free + 2;                 // [TC_DEN]
@@ -225,7 +224,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&scores_done[i], 1);
-            mbar_init(&a_free[i], 4);
             mbar_init(&p_ready[i], 1);
             mbar_init(&o_done[i], 1);
             mbar_init(&o_free[i], 4);
@@ -379,7 +377,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const int s = c % TC_STAGES, b = c & 1;
                 uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM && !DK) ? &full[s] : &phi_ready[s];
                 if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
-                if (c >= 2 && !wait_phase(&a_free[b], ((c >> 1) - 1) & 1, ctl)) break;
+                // Scores buffer b was last read by the P warps for tile c-2.  No wait is
+                // needed: this thread already waited for p_ready of tile c-1, which the P
+                // warps raise only after finishing tile c-2 (in order), and each P warp fences
+                // its TMEM loads (fence::before_thread_sync) before the barrier that precedes
+                // that arrive.
                 tc_fence_after();
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
                                va = smem_u32(stage_v(s)), pa = smem_u32(p_tile);
@@ -637,11 +639,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 } else {
                     tmem_wait_ld();
                 }
-                if (h == nh - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_free[b]);
-                }
+                if (h == nh - 1) tc_fence_before();  // scores buffer b read (see the MMA issuer)
                 if (row_lane) {
                     uint32_t pk[16];
 #pragma unroll
