@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         rd[4 * q + 2] = mf * v.z; rd[4 * q + 3] = mf * v.w;
                     }
                 }
-                if (FO) {
+                if constexpr (FO) {
                     // fp32 rows: column j of token tt in 32-column box j / 32, 128-byte swizzle
                     uint8_t *const fb = o_tile + (j >> 5) * C * 128 + ((j & 3) << 2);
 #pragma unroll
@@ -786,21 +786,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         const int tt = 32 * h + u;
                         if (live) *(uint32_t *)(fb + tt * 128 + ((((j & 31) >> 2) ^ (tt & 7)) << 4)) = r[u];
                     }
-                    continue;
-                }
-                // Lanes j, j^1 swap one value per pair of rows so that each writes two
-                // neighbouring columns of one row as a single 32-bit word.
+                } else {
+                    // Lanes j, j^1 swap one value per pair of rows so that each writes two
+                    // neighbouring columns of one row as a single 32-bit word.
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
-                    if (NORM || DK) {
-                        a0 *= rd[2 * u];
-                        a1 *= rd[2 * u + 1];
+                    for (int u = 0; u < 16; ++u) {
+                        float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
+                        if (NORM || DK) {
+                            a0 *= rd[2 * u];
+                            a1 *= rd[2 * u + 1];
+                        }
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+                        const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
+                        const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
+                        if (live) *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
                     }
-                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
-                    const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
-                    const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-                    if (live) *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
                 }
             }
             fence_async_smem();

@@ -253,8 +253,13 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             const uint32_t om = smem_u32(sm + FV_OMEGA), phq = smem_u32(sm + FV_PHIQ),
                            phk = smem_u32(sm + FV_PHIK), sb = smem_u32(sm + FV_SBAR),
                            pa = smem_u32(sm + FV_P);
+            // one descriptor per operand, constant offsets added (desc_add)
+            const uint64_t dOm = smem_desc(om, 16, 1024), dPhqMN = smem_desc(phq, FV_M * 128, 1024),
+                           dPhkMN = smem_desc(phk, FV_M * 128, 1024), dPhk = smem_desc(phk, 16, 1024),
+                           dSb = smem_desc(sb, 16, 1024), dPa = smem_desc(pa, 16, 1024);
             // projection of a raw 64x64 tile into TMEM (features on lanes), omega hi + lo
             auto project = [&](uint32_t xa) {
+                const uint64_t dX = smem_desc(xa, 16, 1024);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -262,8 +267,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
                             mma_ss(tmem + FT_P + 64 * h,
-                                   smem_desc(om + part * FV_M * 128 + h * 128 * 128 + ks * 32, 16, 1024),
-                                   smem_desc(xa + ks * 32, 16, 1024), ID_PROJ, (part | ks) != 0);
+                                   desc_add(dOm, part * FV_M * 128 + h * 128 * 128 + ks * 32),
+                                   desc_add(dX, ks * 32), ID_PROJ, (part | ks) != 0);
             };
             int pfree_n = 0;  // completions of p_free waited for
             for (int c = 0; c < nch; ++c) {
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 const int g = tile0 + c;  // chunk index in the sequence
                 if (!wait_phase(&full[s], (c / FV_STAGES) & 1, ctl)) break;
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
+                const uint64_t dVmn = smem_desc(va, FV_C * 128, 1024);
                 if (!totals) {
                     if (c >= 1 && !wait_phase(p_free, (pfree_n++) & 1, ctl)) break;
                     tc_fence_after();
@@ -291,8 +297,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tmem + FT_S + 64 * h, smem_desc(phk + h * 128 * 128 + ks * 32, 16, 1024),
-                                   smem_desc(va + ks * 2048, FV_C * 128, 1024), ID_STATE, (c > 0) || (ks > 0));
+                            mma_ss(tmem + FT_S + 64 * h, desc_add(dPhk, h * 128 * 128 + ks * 32),
+                                   desc_add(dVmn, ks * 2048), ID_STATE, (c > 0) || (ks > 0));
                     mma_commit(&stage_free[s]);
                     continue;
                 }
@@ -301,8 +307,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 // scores: phi(Q) (MN-major A) x phi(K)^T (MN-major B), K = 256 features
 #pragma unroll
                 for (int ks = 0; ks < FV_M / 16; ++ks)
-                    mma_ss(tmem + FT_A, smem_desc(phq + ks * 2048, FV_M * 128, 1024),
-                           smem_desc(phk + ks * 2048, FV_M * 128, 1024), ID_SC, ks > 0);
+                    mma_ss(tmem + FT_A, desc_add(dPhqMN, ks * 2048), desc_add(dPhkMN, ks * 2048), ID_SC, ks > 0);
                 mma_commit(scores_done);
                 if (!NC && c >= 1 && !wait_phase(sbar_ready, (c - 1) & 1, ctl)) break;
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
@@ -311,16 +316,16 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 // inter: phi(Q) (MN-major A) x [S~ | z] (K-major B, 72 rows), K = 256
 #pragma unroll
                 for (int ks = 0; ks < FV_M / 16; ++ks)
-                    mma_ss(tO, smem_desc(phq + ks * 2048, FV_M * 128, 1024),
-                           smem_desc(sb + (ks >> 2) * FV_SBLK + (ks & 3) * 32, 16, 1024), ID_INTER, ks > 0);
+                    mma_ss(tO, desc_add(dPhqMN, ks * 2048), desc_add(dSb, (ks >> 2) * FV_SBLK + (ks & 3) * 32),
+                           ID_INTER, ks > 0);
                 // state: S += phi(K)^T (K-major A, features on M) x V (MN-major B), K = 64
                 if (g + 1 < a.nch && !NC) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tmem + FT_S + 64 * h, smem_desc(phk + h * 128 * 128 + ks * 32, 16, 1024),
-                                   smem_desc(va + ks * 2048, FV_C * 128, 1024), ID_STATE, 1);
+                            mma_ss(tmem + FT_S + 64 * h, desc_add(dPhk, h * 128 * 128 + ks * 32),
+                                   desc_add(dVmn, ks * 2048), ID_STATE, 1);
                     mma_commit(state_done);
                 }
                 if (!wait_phase(p_ready, c & 1, ctl)) break;
@@ -328,8 +333,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 // intra: P (K-major A) x V (MN-major B), K = 64
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tO, smem_desc(pa + ks * 32, 16, 1024), smem_desc(va + ks * 2048, FV_C * 128, 1024),
-                           ID_INTRA, 1);
+                    mma_ss(tO, desc_add(dPa, ks * 32), desc_add(dVmn, ks * 2048), ID_INTRA, 1);
                 mma_commit(&o_done[b]);
                 mma_commit(&stage_free[s]);
             }

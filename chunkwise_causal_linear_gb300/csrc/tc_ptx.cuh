@@ -247,6 +247,11 @@ LA_DEV uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
     return d;
 }
 
+// desc_add(smem_desc(a, lbo, sbo), off) == smem_desc(a + off, lbo, sbo) for 16-byte aligned a
+// and off with a + off below 256 KB (the address field, bits 0-13 of (addr >> 4), never
+// carries there): an MMA issuer builds one descriptor per operand and adds constants.
+LA_DEV uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A/B major-ness,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn)

@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     const uint32_t ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
 #pragma unroll
                     for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tS, smem_desc(va + ks * 2048, T * 128, 1024),
-                               smem_desc(ka + ks * 2048, Lay::K_BLK, 1024), ID_STATE, 1);
+                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), ks * 2048),
+                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), ks * 2048), ID_STATE, 1);
                     mma_commit(&stage_free[s]);
                     if (++s == TW_STAGES) { s = 0; sph ^= 1; }
                 }
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
                             const uint32_t ko = (ks >> 2) * Lay::K_BLK + (ks & 3) * 32;
-                            mma_ss(tA, smem_desc(qa + qo, 16, 1024), smem_desc(ka + ko, 16, 1024), ID_SCD, ks > 0);
+                            mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(ka, 16, 1024), ko),
+                                   ID_SCD, ks > 0);
                         }
                     } else {
                         const int slot = (kuse + n - 1) % TW_KR, u = (kuse + n - 1) / TW_KR;
@@ -334,7 +335,8 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
-                            mma_ss(tA, smem_desc(qa + qo, 16, 1024), smem_desc(rk + qo, 16, 1024), ID_SCO, ks > 0);
+                            mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(rk, 16, 1024), qo),
+                                   ID_SCO, ks > 0);
                         }
                     }
                     mma_commit(&scores_done[bb]);
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     const uint32_t vv = n == 0 ? va : smem_u32(ring_v((kuse + n - 1) % TW_KR));
 #pragma unroll
                     for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tO, smem_desc(vv + ks * 2048, T * 128, 1024), smem_desc(pa + ks * 32, 16, 1024),
+                        mma_ss(tO, desc_add(smem_desc(vv, T * 128, 1024), ks * 2048), desc_add(smem_desc(pa, 16, 1024), ks * 32),
                                ID_INTRA, 1);
                     if (n > 0) mma_commit(&kfree[(kuse + n - 1) % TW_KR]);
                     return true;
@@ -365,14 +367,14 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
-                    mma_ts(tO, tSB + ks * 8, smem_desc(qa + qo, 16, 1024), ID_INTER, ks > 0);
+                    mma_ts(tO, tSB + ks * 8, desc_add(smem_desc(qa, 16, 1024), qo), ID_INTER, ks > 0);
                 }
                 // state: every tile joins the fp32 state; the copy is refreshed at chunk ends
                 if (gt + 1 < a.nch) {
 #pragma unroll
                     for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tS, smem_desc(va + ks * 2048, T * 128, 1024),
-                               smem_desc(ka + ks * 2048, Lay::K_BLK, 1024), ID_STATE, 1);
+                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), ks * 2048),
+                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), ks * 2048), ID_STATE, 1);
                     if (r == R - 1) mma_commit(state_done);
                 }
                 // scores run one block ahead of the intra products (P is double-buffered)
