@@ -578,7 +578,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         zs[i] = (DK && !totals) ? gC * zs[i] + ex2(a.l2g * (float)(C * pm)) * acc
                                                 : zs[i] + acc;
                     }
-                    named_bar(1, NF);
+                    // no barrier here: the next tile's group wait (a barrier of the whole
+                    // group) orders these zs writes before its z rows are formed, and the
+                    // zpart reads before zpart is written again
                 }
             }
             if (totals && NORM)
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // P there is the zero block written at the start, and they load only the first half.
             const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off;
             const int nh = (CH == C && q4 < 2) ? 1 : 2;
-            float rs = 0.f, dz = 0.f;
+            float rsa[4] = {0.f, 0.f, 0.f, 0.f}, dz = 0.f;  // row sum: four short chains
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (h >= nh) break;
@@ -649,7 +651,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
                         const float v0 = (s0 <= t && !NC) ? __uint_as_float(r[2 * e]) : 0.f;
                         const float v1 = (s1 <= t && !NC) ? __uint_as_float(r[2 * e + 1]) : 0.f;
-                        rs += v0 + v1;
+                        rsa[e & 3] += v0 + v1;
                         if (CH == C) {
                             pk[e] = pack_bf16x2(v0, v1);
                         } else {
@@ -683,7 +685,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
             }
             // den = phi(q_t).z_c + masked row sum
-            if (NORM && row_lane) rden[slot * C + t] = __frcp_rn(dz + rs);
+            // (fast division: 1/den only scales the fp32 row before its bf16 rounding)
+            if (NORM && row_lane) rden[slot * C + t] = __fdividef(1.f, dz + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])));
             fence_async_smem();
             named_bar(2, 128);
             if (pt == 0) {
