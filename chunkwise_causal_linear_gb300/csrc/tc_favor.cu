@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(a_free);
             if (row_lane) {
-                float rs = 0.f;
+                float rsa[4] = {0.f, 0.f, 0.f, 0.f};  // row sum: four short chains
                 uint8_t *prow = sm + FV_P + t * 128;
 #pragma unroll
                 for (int ck = 0; ck < 8; ++ck) {
@@ -507,12 +507,12 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                         const uint32_t *rr = s0 < 32 ? r0 : r1;
                         const float v0 = (!NC && s0 <= t) ? __uint_as_float(rr[s0 & 31]) : 0.f;
                         const float v1 = (!NC && s1 <= t) ? __uint_as_float(rr[s1 & 31]) : 0.f;
-                        rs += v0 + v1;
+                        rsa[e] += v0 + v1;
                         w[e] = pack_bf16x2(v0, v1);
                     }
                     *(uint4 *)(prow + ((ck ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                if (NORM) den_intra[slot * FV_C + t] = rs;
+                if (NORM) den_intra[slot * FV_C + t] = (rsa[0] + rsa[1]) + (rsa[2] + rsa[3]);
             }
             fence_async_smem();
             named_bar(2, 128);
@@ -543,7 +543,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             if (lane == 0) mbar_arrive(&o_free[b]);
             float inv = 1.f;
             if (NORM && row_lane)
-                inv = __frcp_rn(__uint_as_float(rz[0]) + __uint_as_float(rz[1]) + den_intra[slot * FV_C + t]);
+                // fast division: 1/den only scales the fp32 row before its bf16 rounding
+                inv = __fdividef(1.f, __uint_as_float(rz[0]) + __uint_as_float(rz[1]) + den_intra[slot * FV_C + t]);
             named_bar(3, 128);
             if (NORM && ot == 0) mbar_arrive(&den_empty[slot]);
             if (row_lane && row < a.L) {

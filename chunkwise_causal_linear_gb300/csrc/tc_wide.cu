@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
         int kb = 0, nref = 0;
         for (int c = 0; c < nt && !totals; ++c) {
             const int slot = c % TW_DEN, r = c % R, gt = tile0 + c;
-            float rs = 0.f, dz = 0.f;
+            float rsa[4] = {0.f, 0.f, 0.f, 0.f}, dz = 0.f;  // row sum: four short chains
             bool ok = true;
             for (int n = 0; n <= r && ok; ++n, ++kb) {
                 const int bb = kb & 1;
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                             const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
                             const float v0 = (n > 0 || s0 <= t) ? __uint_as_float(rr[2 * e]) : 0.f;
                             const float v1 = (n > 0 || s1 <= t) ? __uint_as_float(rr[2 * e + 1]) : 0.f;
-                            rs += v0 + v1;
+                            rsa[e & 3] += v0 + v1;
                             pk[e] = pack_bf16x2(v0, v1);
                         }
                         uint8_t *prow = p_tile(bb) + t * 128;
@@ -602,7 +602,9 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                         }
                     }
                 }
-                if (NORM && n == r && row_lane) rden[slot * T + t] = __frcp_rn(dz + rs);
+                // fast division: 1/den only scales the fp32 row before its bf16 rounding
+                if (NORM && n == r && row_lane)
+                    rden[slot * T + t] = __fdividef(1.f, dz + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])));
                 fence_async_smem();
                 named_bar(2, 128);
                 if (pt == 0) {
