@@ -40,7 +40,8 @@ EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
            "la_decode_state_elems", "la_noncausal_fwd", "la_noncausal_workspace_bytes",
            "la_decay_fwd", "la_decay_decode_step", "la_decay_workspace_bytes", "la_decay_plan",
-           "la_chunked_bwd", "la_chunked_bwd_workspace_bytes", "la_version")
+           "la_chunked_bwd", "la_chunked_bwd_workspace_bytes", "la_chunked_state",
+           "la_state_combine", "la_chunked_fwd_init", "la_version")
 
 
 class la_feature_map(ctypes.Structure):
@@ -124,6 +125,13 @@ def lib() -> ctypes.CDLL:
             L.la_chunked_bwd.restype = i
             L.la_chunked_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i]
             L.la_chunked_bwd_workspace_bytes.restype = sz
+            L.la_chunked_state.argtypes = [p, p, p, p, i, i, i, i, i, fmp, f, i, p]
+            L.la_chunked_state.restype = i
+            L.la_state_combine.argtypes = [p, p, p, p, i, i, i, i, f, p]
+            L.la_state_combine.restype = i
+            L.la_chunked_fwd_init.argtypes = [p, p, p, p, i, i, i, i, i, i, fmp, i, f, p, p, i, p, sz,
+                                              p, i]
+            L.la_chunked_fwd_init.restype = i
             L.la_version.argtypes = []
             L.la_version.restype = ctypes.c_char_p
             _lib = L
@@ -260,6 +268,22 @@ def la_chunked_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map,
 def la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, dtype) -> int:
     return lib().la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, _fm(feature_map), normalize,
                                                 dtype)
+
+
+def la_chunked_state(k, v, state, zstate, B, H, L, dk, dv, feature_map, gamma, dtype, stream) -> int:
+    return lib().la_chunked_state(k, v, state, zstate, B, H, L, dk, dv, _fm(feature_map), gamma,
+                                  dtype, stream)
+
+
+def la_state_combine(state, zstate, seg_state, seg_zstate, B, H, D, dv, factor, stream) -> int:
+    return lib().la_state_combine(state, zstate, seg_state, seg_zstate, B, H, D, dv, factor, stream)
+
+
+def la_chunked_fwd_init(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, gamma, state0,
+                        zstate0, dtype, workspace, workspace_bytes, stream, path=LA_PATH_AUTO) -> int:
+    return lib().la_chunked_fwd_init(q, k, v, out, B, H, L, dk, dv, C, _fm(feature_map), normalize,
+                                     gamma, state0, zstate0, dtype, workspace, workspace_bytes,
+                                     stream, path)
 
 
 def la_version() -> str:
@@ -406,6 +430,57 @@ def chunked_bwd(q, k, v, dout, C=64, feature_map="identity", omega=None, normali
     if rc != LA_OK:
         raise LAError(rc, "la_chunked_bwd")
     return dq, dk_t, dv_t
+
+
+def chunked_state(k, v, feature_map="identity", omega=None, gamma=1.0, normalize=True,
+                  stream=None):
+    """(state [B,H,D,dv], zstate [B,H,D] or None) a causal pass over k, v ends with."""
+    import torch
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    D = omega.shape[0] if omega is not None else dk
+    S = torch.empty((B, H, D, dv), dtype=torch.float32, device=k.device)
+    z = torch.empty((B, H, D), dtype=torch.float32, device=k.device) if normalize else None
+    fm = make_feature_map(feature_map, D if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(k.device).cuda_stream
+    rc = la_chunked_state(k.data_ptr(), v.data_ptr(), S.data_ptr(),
+                          z.data_ptr() if z is not None else None, B, H, L, dk, dv, fm,
+                          float(gamma), _dtype_code(k), stream)
+    if rc != LA_OK:
+        raise LAError(rc, "la_chunked_state")
+    return S, z
+
+
+def chunked_fwd_init(q, k, v, state0, zstate0=None, C=64, feature_map="identity", omega=None,
+                     normalize=False, gamma=1.0, out=None, workspace=None, stream=None,
+                     path=LA_PATH_AUTO):
+    """The causal forward of q, k, v started from state0 [B,H,D,dv] (zstate0 [B,H,D])."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, L, dv), dtype=q.dtype, device=q.device)
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    if gamma == 1.0:
+        need = la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), 0, dtype)
+    else:
+        need = la_decay_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), float(gamma), dtype)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_chunked_fwd_init(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, dk,
+                             dv, C, fm, int(normalize), float(gamma),
+                             state0.data_ptr() if state0 is not None else None,
+                             zstate0.data_ptr() if zstate0 is not None else None, dtype,
+                             workspace.data_ptr() if need else None, need, stream, path)
+    if rc != LA_OK:
+        raise LAError(rc, "la_chunked_fwd_init")
+    return out
 
 
 def _dtype_code(t):

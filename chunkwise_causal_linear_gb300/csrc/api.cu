@@ -27,6 +27,9 @@ size_t tc_nc_workspace(const Problem &p, int num_sms);
 int tc_nc_launch(const Problem &p, int num_sms);
 int decode_check(int B, int H, int dk, int dv, const la_feature_map *fm, int normalize,
                  int num_levels, long long t, bool loglinear, int *D_out, int *r_out);
+int nc_state_launch(const Problem &p, float *S, float *z);
+int state_combine_launch(float *S, float *z, const float *Sg, const float *zg, long nS, long nz, float factor,
+                         cudaStream_t st);
 size_t bwd_workspace_bytes(const Problem &p, int sms);
 bool bwd_supported(const Problem &p);
 bool bwd_tc_supported(const Problem &p, int sms);
@@ -171,7 +174,8 @@ static int plan_problem(const Problem &p, bool loglinear, int path, int num_sms,
 static int run(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
                int dk, int dv, int C, const la_feature_map *fm, int normalize,
                const float *lam, int num_levels, int dtype, void *ws, size_t ws_bytes,
-               void *stream, int path, bool decay = false, float gamma = 1.f)
+               void *stream, int path, bool decay = false, float gamma = 1.f,
+               const float *S0 = nullptr, const float *z0 = nullptr)
 {
     if (!q || !k || !v || !out) return LA_ERR_NULL;
     const bool ll = lam != nullptr;
@@ -179,6 +183,8 @@ static int run(const void *q, const void *k, const void *v, void *out, int B, in
     int rc = check_problem(B, H, L, dk, dv, C, fm, normalize, ll, num_levels, dtype, &p);
     if (rc != LA_OK) return rc;
     if (decay && (rc = set_decay(&p, gamma)) != LA_OK) return rc;
+    p.S0 = S0;
+    p.z0 = z0;
     if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
     const int sms = device_sms();
     if (sms <= 0) return LA_ERR_CUDA;
@@ -506,6 +512,44 @@ int la_chunked_bwd(const void *q, const void *k, const void *v, const void *dout
     p.err = err_ptr();
     if (!p.err) return LA_ERR_CUDA;
     return bwd_launch(p, sms, path, dout, dq, dk_, dv_);
+}
+
+// ---- carried state: final state of a pass, combining segment states, a pass from a state
+int la_chunked_state(const void *k, const void *v, float *state, float *zstate, int B, int H, int L,
+                     int dk, int dv, const la_feature_map *feature_map, float gamma, int dtype,
+                     void *stream)
+{
+    if (!k || !v || !state) return LA_ERR_NULL;
+    Problem p;
+    int rc = check_problem(B, H, L, dk, dv, 1, feature_map, zstate != nullptr, false, 0, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if (gamma != 1.f && (rc = set_decay(&p, gamma)) != LA_OK) return rc;
+    if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
+    p.k = k;
+    p.v = v;
+    p.stream = (cudaStream_t)stream;
+    return nc_state_launch(p, state, zstate);
+}
+
+int la_state_combine(float *state, float *zstate, const float *seg_state, const float *seg_zstate,
+                     int B, int H, int D, int dv, float factor, void *stream)
+{
+    if (!state || !seg_state) return LA_ERR_NULL;
+    if ((zstate == nullptr) != (seg_zstate == nullptr)) return LA_ERR_NULL;
+    if (B <= 0 || H <= 0 || D <= 0 || dv <= 0) return LA_ERR_SHAPE;
+    if (!(factor >= 0.f && factor <= 1.f)) return LA_ERR_ARG;
+    const long nS = (long)B * H * D * dv, nz = zstate ? (long)B * H * D : 0;
+    return state_combine_launch(state, zstate, seg_state, seg_zstate, nS, nz, factor,
+                                (cudaStream_t)stream);
+}
+
+int la_chunked_fwd_init(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                        int dk, int dv, int C, const la_feature_map *feature_map, int normalize,
+                        float gamma, const float *state0, const float *zstate0, int dtype,
+                        void *workspace, size_t workspace_bytes, void *stream, int path)
+{
+    return run(q, k, v, out, B, H, L, dk, dv, C, feature_map, normalize, nullptr, 0, dtype,
+               workspace, workspace_bytes, stream, path, gamma != 1.f, gamma, state0, zstate0);
 }
 
 const char *la_version(void) { return "0.1.0"; }

@@ -62,6 +62,8 @@ struct Problem {
                              // computed as the causal pass over the reversed sequence
     int out_f32;             // 1: out is fp32 rows (tensor-core path, identity features, no
                              // normaliser; the backward pass's internal passes)
+    const float *S0, *z0;    // NULL, or the state (and normaliser) before row 0: fp32
+                             // [B*H][D][dv] and [B*H][D] (the decoding state's layout)
 };
 
 // Host-side queries used by the planner.

@@ -31,6 +31,8 @@ struct NcArgs {
     const float *omega;
     float *S;  // [BH][D][dv]
     float *z;  // [BH][D]
+    int decay;   // final state of a decayed causal pass: token t weighted by gamma^(L-1-t)
+    float l2g;   // log2(gamma)
 };
 
 // phi of `rows` raw rows x[rows][dk] (shared) into f[rows][D] (shared); FAVOR+ uses omega
@@ -87,6 +89,10 @@ __global__ void __launch_bounds__(NC_THREADS) nc_state_kernel(const NcArgs a)
         __syncthreads();
         nc_phi(a, x, f, rows);
         __syncthreads();
+        if (a.decay) {
+            for (int e = tid; e < rows * a.D; e += NC_THREADS) f[e] *= exp2f(a.l2g * (float)(a.L - 1 - t0 - e / a.D));
+            __syncthreads();
+        }
         for (int r = 0; r < rows; ++r) {
             const float vv = vt[r * NC_COLS + j];
 #pragma unroll
@@ -160,6 +166,55 @@ size_t nc_simt_workspace_bytes(int BH, int D, int dv) { return (size_t)BH * ((si
 
 bool nc_simt_supported(int D, int dk) { return D <= 256 && dk <= 512; }
 
+// S = sum_t w_t phi(k_t) v_t^T and z = sum_t w_t phi(k_t) (w_t = 1, or gamma^(L-1-t)) of
+// every head straight into S [BH][D][dv] and z [BH][D] (z may be NULL): the state a causal
+// pass ends with.  One launch of the state kernel above.
+int nc_state_launch(const Problem &p, float *S, float *z)
+{
+    if (!nc_simt_supported(p.D, p.dk)) return LA_ERR_UNSUPPORTED;
+    NcArgs a;
+    a.q = nullptr; a.k = p.k; a.v = p.v; a.out = nullptr;
+    a.L = p.L; a.dk = p.dk; a.dv = p.dv; a.D = p.D;
+    a.fm = p.fm; a.m = p.m; a.normalize = z ? 1 : 0;
+    a.omega = p.omega;
+    a.S = S;
+    a.z = z;
+    a.decay = p.decay;
+    a.l2g = p.l2g;
+    const size_t sm1 = sizeof(float) * ((size_t)NC_TT * p.dk + NC_TT * p.D + NC_TT * NC_COLS);
+    dim3 g1((unsigned)(p.B * p.H), (unsigned)((p.dv + NC_COLS - 1) / NC_COLS));
+    auto go = [&](auto k1) -> int {
+        if (sm1 > 48 * 1024 &&
+            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1) != cudaSuccess)
+            return LA_ERR_CUDA;
+        k1<<<g1, NC_THREADS, sm1, p.stream>>>(a);
+        return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    };
+    if (p.dtype == LA_BF16) return go(nc_state_kernel<__nv_bfloat16>);
+    return go(nc_state_kernel<float>);
+}
+
+// state = factor * state + seg (and z alike): one step of an exclusive prefix over segments
+__global__ void state_combine_kernel(float *S, float *z, const float *Sg, const float *zg, long nS, long nz,
+                                     float factor)
+{
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nS + nz; i += (long)gridDim.x * blockDim.x) {
+        if (i < nS)
+            S[i] = factor * S[i] + Sg[i];
+        else
+            z[i - nS] = factor * z[i - nS] + zg[i - nS];
+    }
+}
+
+int state_combine_launch(float *S, float *z, const float *Sg, const float *zg, long nS, long nz, float factor,
+                         cudaStream_t st)
+{
+    const long n = nS + nz;
+    const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    state_combine_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(S, z, Sg, zg, nS, nz, factor);
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
 int nc_simt_launch(const Problem &p)
 {
     const int BH = p.B * p.H;
@@ -170,6 +225,8 @@ int nc_simt_launch(const Problem &p)
     a.L = p.L; a.dk = p.dk; a.dv = p.dv; a.D = p.D;
     a.fm = p.fm; a.m = p.m; a.normalize = p.normalize;
     a.omega = p.omega;
+    a.decay = 0;
+    a.l2g = 0.f;
     a.S = (float *)p.workspace;
     a.z = a.S + (size_t)BH * p.D * p.dv;
     const size_t sm1 = sizeof(float) * ((size_t)NC_TT * p.dk + NC_TT * p.D + NC_TT * NC_COLS);

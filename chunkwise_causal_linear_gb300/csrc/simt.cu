@@ -154,8 +154,12 @@ __global__ void __launch_bounds__(SIMT_NT) simt_chunked_kernel(SimtArgs a)
                     ? a.levels + ((size_t)head * a.n_slices + blockIdx.y) * a.n_inter * lvl_stride
                     : nullptr;
 
-    for (int e = tid; e < D * WV; e += NT) sS[e] = 0.f;
-    for (int i = tid; i < D; i += NT) sz[i] = 0.f;
+    // the state before row 0: zero, or the given one (columns j0 .. j0 + WV of S0)
+    for (int e = tid; e < D * WV; e += NT) {
+        const int i = e / WV, j = e - i * WV;
+        sS[e] = (p.S0 && j < wv) ? p.S0[((size_t)head * D + i) * dv + j0 + j] : 0.f;
+    }
+    for (int i = tid; i < D; i += NT) sz[i] = p.z0 ? p.z0[(size_t)head * D + i] : 0.f;
     if (Lv)
         for (size_t e = tid; e < (size_t)a.n_inter * lvl_stride; e += NT) Lv[e] = 0.f;
     __syncthreads();

@@ -115,6 +115,7 @@ struct TcArgs {
     // phi(q) S_total (/ phi(q) z_total).
     int noncausal, nseg_all;
     float l2g;  // decay: log2(gamma)
+    const float *S0, *z0;  // NULL, or the state before row 0 ([BH][D][DV], [BH][D])
     int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
 
@@ -247,9 +248,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         }
         for (int i = tid; i < D; i += TC_THREADS) {
             float z0 = 0.f;
-            if (!totals)
+            if (!totals) {
                 for (int g = 0; g < (NC ? a.nseg_all : seg); ++g)
                     z0 += seg_w(g) * a.ws_z[((size_t)g * a.BH + head) * D + i];
+                if (a.z0) z0 += seg_w(-1) * a.z0[(size_t)head * D + i];  // the given state
+            }
             zs[i] = z0;
         }
     }
@@ -295,6 +298,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         acc[4 * q + 2] += w * v4.z; acc[4 * q + 3] += w * v4.w;
                     }
                 }
+            if (live && a.S0 && !totals) {
+                // the given state before row 0 (S[i][j] at S0 + (head D + i) DV + j), decayed
+                // over the rows of the earlier segments
+                const float w = seg_w(-1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] += w * a.S0[((size_t)head * D + col + e) * DV + jr];
+            }
             if (DK)  // the first chunk reads gamma^C S and accumulates onto it
 #pragma unroll
                 for (int e = 0; e < 16; ++e) acc[e] *= gC;
@@ -874,6 +884,8 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     a.noncausal = noncausal ? 1 : 0;
     a.nseg_all = nseg;
     a.l2g = mode == TC_DECAY ? p.l2g : 0.f;
+    a.S0 = p.S0;
+    a.z0 = p.z0;
     // largest period P with C P |log2 gamma| <= 64 (gamma^(C P) >= 2^-64); tc_supported keeps
     // gamma^C >= 2^-64, so P >= 1
     a.period = 1 << 20;
@@ -962,6 +974,8 @@ bool tc_supported(const Problem &p, int num_sms)
     }
     if (p.out_f32 && (p.decay || p.lam || p.C != 64 || p.fm != LA_FM_IDENTITY || p.normalize))
         return false;
+    // a given initial state: the identity / elu+1 kernel with C <= 64 (or the decay mode)
+    if ((p.S0 || p.z0) && (p.lam || p.fm == LA_FM_FAVOR || p.C > 64)) return false;
     if (p.lam) return tcl_supported(p);
     if (p.fm == LA_FM_FAVOR) return tcf_supported(p);
     if (p.C == 128 || p.C == 256) return tcw_supported(p);

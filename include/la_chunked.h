@@ -346,6 +346,46 @@ size_t la_chunked_bwd_workspace_bytes(int B, int H, int L, int dk, int dv, int C
                                       const la_feature_map *feature_map, int normalize,
                                       int dtype);
 
+/*
+ * Carried state.  The state a causal pass ends with seeds a decoding loop (prefill, then
+ * la_decode_step / la_decay_decode_step) or the next segment of a sequence cut into
+ * segments (one per stream, thread or rank): each segment's own final state T_r, an
+ * exclusive prefix P_r = gamma^len_{r-1} P_{r-1} + T_{r-1} over the earlier segments (the
+ * "attention と線形の間" section 2 chunk scan at segment granularity), and the segment's pass
+ * started from P_r give the same rows as one pass over the whole sequence.
+ *
+ * la_chunked_state -- the final state of a causal pass over k, v ([B, H, L, dk], [B, H, L,
+ * dv], dtype): state[b,h,i,j] = sum_t w_t phi(k_t)_i v_t,j and zstate[b,h,i] = sum_t w_t
+ * phi(k_t)_i, with w_t = 1, or gamma^(L-1-t) for the Retention decay (gamma as
+ * la_decay_fwd; 1 = none).  state: device fp32 [B, H, D, dv], zstate: device fp32 [B, H, D]
+ * or NULL (not computed); both fully overwritten, the la_decode_step layout.  D (dk, or m
+ * for FAVOR+) at most 256; no level weights.  Generic path (fp32 accumulation).
+ */
+int la_chunked_state(const void *k, const void *v, float *state, float *zstate, int B, int H, int L,
+                     int dk, int dv, const la_feature_map *feature_map, float gamma, int dtype,
+                     void *stream);
+
+/* state = factor * state + seg_state, zstate likewise (both NULL or both given): one step of
+ * the prefix above.  [B, H, D, dv] and [B, H, D] fp32 device arrays; factor in [0, 1] (the
+ * decay over seg_state's segment, gamma^len, or 1), else LA_ERR_ARG. */
+int la_state_combine(float *state, float *zstate, const float *seg_state, const float *seg_zstate,
+                     int B, int H, int D, int dv, float factor, void *stream);
+
+/*
+ * la_chunked_fwd_init -- the causal forward (plain mask, or the decay when gamma != 1)
+ * starting from a given state: row t also reads gamma^(t+1) phi(q_t)^T state0 (and
+ * zstate0 in the normaliser), as if the rows that produced state0 preceded row 0.
+ * state0, zstate0: device fp32 [B, H, D, dv] and [B, H, D] (la_chunked_state's layout), or
+ * NULL for zero.  Other arguments as la_decay_fwd; no level weights.  The tensor-core path
+ * covers it for identity / elu+1 with C <= 64 (decay: C = 64); FAVOR+ and C > 64 run on the
+ * generic path.  The workspace is la_chunked_workspace_bytes (gamma = 1) or
+ * la_decay_workspace_bytes.
+ */
+int la_chunked_fwd_init(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                        int dk, int dv, int C, const la_feature_map *feature_map, int normalize,
+                        float gamma, const float *state0, const float *zstate0, int dtype,
+                        void *workspace, size_t workspace_bytes, void *stream, int path);
+
 /* Library version string, e.g. "0.1.0". */
 const char *la_version(void);
 
