@@ -271,6 +271,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (NC && NORM && !totals) {
+        // non-causal main pass: z of the whole sequence as a bf16 hi / lo pair in key rows C and
+        // C+1 of every stage (no keys are loaded in this pass, so they stay)
+        for (int e = tid; e < TC_STAGES * (D / 8) * 2; e += TC_THREADS) {
+            const int st = e / ((D / 8) * 2), zr = e & 1, cg = (e >> 1) % (D / 8);
+            const int zkb = cg >> 3, zch = cg & 7, row = C + zr;
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float z0 = zs[8 * cg + 2 * u], z1 = zs[8 * cg + 2 * u + 1];
+                const float h0 = __bfloat162float(__float2bfloat16_rn(z0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(z1));
+                pk[u] = zr ? pack_bf16x2(z0 - h0, z1 - h1) : pack_bf16x2(h0, h1);
+            }
+            *(uint4 *)(stage_k(st) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_async_smem();
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB, tSL = tmem + Lay::T_SL;
     // fp32-output mode: bf16 hi / lo split of fp32 values (x = hi + lo to ~2^-16 relative)
@@ -331,18 +350,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int issued = 0;
+            // the non-causal main pass reads the whole sequence's state: only Q is loaded
+            const bool qonly = NC && !totals;
             for (int c = 0; c < nch; ++c) {
                 const int s = c % TC_STAGES;
                 if (c >= TC_STAGES && !wait_phase(&stage_free[s], ((c / TC_STAGES) - 1) & 1, ctl))
                     break;
                 const int row = (tile0 + c) * C;
-                mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES : Lay::STAGE_TX);
+                mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES
+                                                : (qonly ? Lay::Q_BYTES : Lay::STAGE_TX));
                 for (int kb = 0; kb < D / 64; ++kb) {
                     if (!totals)
                         tma_load_3d(stage_q(s) + kb * C * 128, &a.tm_q, kb * 64, row, head, &full[s]);
-                    tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &full[s]);
+                    if (!qonly)
+                        tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &full[s]);
                 }
-                for (int jb = 0; jb < DV / 64; ++jb)
+                for (int jb = 0; jb < DV / 64 && !qonly; ++jb)
                     tma_load_3d(stage_v(s) + jb * C * 128, &a.tm_v, jb * 64, row, head, &full[s]);
                 issued = c + 1;
             }
@@ -382,6 +405,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
                 if (ok) mma_commit(state_done);
                 ok = false;  // skip the main loop
+            }
+            if constexpr (NC) {
+                // non-causal main pass: every row reads the whole sequence's state, so a tile
+                // needs only the inter product and (normaliser) phi(Q) z, from the z rows of
+                // the K tile alone; no scores over keys, no intra product
+                constexpr uint32_t ID_Z = idesc_bf16_f32(C, 16, 0, 0);
+                auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+                for (int c = 0; ok && c < nch; ++c) {
+                    const int s = c % TC_STAGES, b = c & 1;
+                    uint64_t *ph = (FM == LA_FM_IDENTITY) ? &full[s] : &phi_ready[s];
+                    if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
+                    // scores buffer b: the P warps are done with tile c-2
+                    if (NORM && c >= 2 && !wait_phase(&p_ready[b], ((c >> 1) - 1) & 1, ctl)) break;
+                    if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
+                    tc_fence_after();
+                    const uint64_t dQ = smem_desc(smem_u32(stage_q(s)), 16, 1024);
+                    const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
+                    if (NORM) {
+                        // z hi / lo in rows C, C+1 of each 64-feature block: TMEM columns C, C+1
+                        const uint64_t dZ = smem_desc(smem_u32(stage_k(s)) + C * 128, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            mma_ss(tA + C, dadd(dQ, (ks >> 2) * C * 128 + (ks & 3) * 32),
+                                   dadd(dZ, (ks >> 2) * Lay::K_BLK + (ks & 3) * 32), ID_Z, ks > 0);
+                        mma_commit(&scores_done[b]);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_ts(tO, tSB + ks * 8, dadd(dQ, (ks >> 2) * C * 128 + (ks & 3) * 32), ID_INTER, ks > 0);
+                    mma_commit(&o_done[b]);
+                    mma_commit(&stage_free[s]);
+                }
+                ok = false;
             }
             for (int c = 0; ok && c < nch; ++c) {
                 const int s = c % TC_STAGES, b = c & 1;
@@ -477,7 +533,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const int kb = g >> 3, ch = g & 7;
         const int q_swz = kb * C * 128 + ((ch ^ (rg & 7)) << 4) + rg * 128;
         const int k_swz = kb * Lay::K_BLK + ((ch ^ (rg & 7)) << 4) + rg * 128;
-        if (FM != LA_FM_IDENTITY || NORM || DK) {
+        // non-causal main pass: no keys; the z rows were written once at the start, so only
+        // phi(Q) is formed (nothing at all for identity features)
+        const bool qonly = NC && !totals;
+        if ((FM != LA_FM_IDENTITY || NORM || DK) && !(qonly && FM == LA_FM_IDENTITY)) {
             // decay: key row r of chunk c is weighted by gamma^(C-1-r) (rowf, fixed) times
             // gamma^(-C m) with m = c's place in the rescale period (main pass), or times
             // gamma^(C (nch-1-c)) (totals pass)
@@ -497,9 +556,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     if (FM != LA_FM_IDENTITY && !totals) wq[n] = qp[n * RG * 8];
-                    wk[n] = kp[n * RG * 8];
+                    if (!qonly) wk[n] = kp[n * RG * 8];
                 }
-                if (NORM && !totals && ft < 8 * (D / 64) * 2) {
+                if (NORM && !totals && !NC && ft < 8 * (D / 64) * 2) {
                     // z_c (before this chunk) as a bf16 hi/lo pair in key rows C and C+1
                     const int zkb = ft / 16, zr = (ft / 8) & 1, zch = ft & 7;
                     const float4 z0 = ((const float4 *)zs)[(64 * zkb + 8 * zch) / 4];
@@ -531,7 +590,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) colsum[e] = 0.f;
 #pragma unroll
-                for (int n = 0; n < NR; ++n) {
+                for (int n = 0; n < NR && !qonly; ++n) {
                     uint32_t *wv = (uint32_t *)&wk[n];
                     // rows past L are TMA zero fill and phi(0) may be nonzero (elu+1): keep them out
                     // of z where z is used after the last tile (the non-causal totals)
@@ -559,7 +618,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
 #pragma unroll
                     for (int n = 0; n < NR; ++n) {
                         if (FM != LA_FM_IDENTITY && !totals) qp[n * RG * 8] = wq[n];
-                        kp[n * RG * 8] = wk[n];
+                        if (!qonly) kp[n * RG * 8] = wk[n];
                     }
                 }
                 fence_async_smem();
@@ -625,7 +684,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
             }
         }
-        for (int c = 0; c < nch && !totals; ++c) {
+        // non-causal main pass (normaliser): den = phi(q_t).z (hi + lo) of the whole sequence
+        for (int c = 0; NC && NORM && c < nch && !totals; ++c) {
+            const int b = c & 1, slot = c % TC_DEN;
+            if (!group_wait(pt == 0, 2, &scores_done[b], (c >> 1) & 1, &den_empty[slot],
+                            ((c / TC_DEN) - 1) & 1, c >= TC_DEN, ctl))
+                break;
+            tc_fence_after();
+            uint32_t rz[8];
+            tmem_ld8(tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off + C, rz);
+            tmem_wait_ld();
+            tc_fence_before();  // scores buffer b read
+            if (row_lane) rden[slot * C + t] = __fdividef(1.f, __uint_as_float(rz[0]) + __uint_as_float(rz[1]));
+            named_bar(2, 128);
+            if (pt == 0) {
+                mbar_arrive(&p_ready[b]);
+                mbar_arrive(&den_full[slot]);
+            }
+        }
+        for (int c = 0; c < nch && !totals && !NC; ++c) {
             const int b = c & 1, slot = c % TC_DEN;
             if (!group_wait(pt == 0, 2, &scores_done[b], (c >> 1) & 1, &den_empty[slot],
                             ((c / TC_DEN) - 1) & 1, NORM && c >= TC_DEN, ctl))

@@ -56,6 +56,11 @@ CASES = [
     ("favor-m256-d64-L16384", dict(B=1, H=1, L=777, normalize=False)),
     ("favor-m256-d64-L16384", dict(B=1, H=2, L=100, dtype="f32")),  # Performer, generic path
     ("elu1-norm-d128-L8192", dict(B=2, H=1, L=100, dk=32, dv=48)),  # generic path
+    # tensor cores: each branch of the main pass (Q-only tiles, z rows written once)
+    ("identity-d64-L2048", dict(B=1, H=2, L=1500, normalize=True, dist="uniform01")),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=1100, normalize=False)),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=1000, dk=64, dv=128)),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=4000)),            # split sequence, ragged
 ]
 
 
@@ -81,3 +86,20 @@ def test_noncausal_last_row_equals_causal_last_row():
     nc = run_nc(w, inp)
     ca, _ = run_gpu(w, inp, 64, 0)
     assert_close(nc[:, -1:], ca[:, -1:], "last rows")
+
+
+def test_noncausal_full_size_sampled_rows():
+    """The benchmark's workload (B8 H16 L8192 d128, elu+1 + normaliser): sampled rows of the
+    first and last head against the oracle's definition, every output finite."""
+    from parity_util import sample_rows
+    w = workload("elu1-norm-d128-L8192")
+    inp = synth.make_inputs(w, seed=12)
+    out = run_nc(w, inp)
+    heads = [0, w["B"] * w["H"] - 1]
+    rows = sample_rows(w["L"], 64, 48, seed=12)
+    import oracle
+    f = lambda x: synth.as_f64(x[heads], w["dtype"])  # noqa: E731
+    ref = oracle.forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), fm=w["fm"], normalize=True,
+                         causal=False, method="scores_first", rows=rows)
+    assert_close(out[heads][:, rows], ref, "non-causal full size")
+    assert np.isfinite(out).all()
