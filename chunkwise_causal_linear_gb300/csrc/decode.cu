@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecArgs a)
 }
 
 // Plain (no level weights) step with float4 columns: dv % 4 == 0, dv <= 512.  512 threads =
-// RG row groups x dv/4 column quads; each thread issues its rows' 16-byte loads together
-// (RGI rows at a time), so a CTA keeps ~64 KB of state reads in flight.
+// RG row groups x dv/4 column quads.  The step is a chain of memory latencies, so every
+// global read that depends on nothing (the thread's first RGI state rows, q, k, z) is issued
+// at the start, and the denominator is reduced with warp shuffles.
 constexpr int DV_THREADS = 512;
 
 template <typename T>
@@ -220,68 +221,82 @@ __global__ void __launch_bounds__(DV_THREADS) decode_vec_kernel(const DecArgs a)
     float *fq = dsm;                         // [D]
     float *fk = fq + D;                      // [D]
     float *part = fk + D;                    // [RG][dv] column partial sums
-    float *dpart = part + RG * dv;           // [DV_THREADS]
+    float *wden = part + RG * dv;            // [DV_THREADS / 32] per-warp denominator sums
     const int head = blockIdx.x, tid = threadIdx.x;
     const int cq = tid % nq, rg = tid / nq;  // column quad, row group
+    const bool active = rg < RG;
+    constexpr int RGI = 8;                   // rows in flight per thread
+    float4 *S = (float4 *)(a.S + (size_t)head * D * dv) + cq;
+    float4 sv[RGI];
+    if (active)
+#pragma unroll
+        for (int u = 0; u < RGI; ++u) {
+            const int i = rg + u * RG;
+            if (i < D) sv[u] = S[(size_t)i * nq];
+        }
     const T *q = (const T *)a.q + (size_t)head * a.dk;
     const T *k = (const T *)a.k + (size_t)head * a.dk;
+    float *z = a.normalize ? a.z + (size_t)head * D : nullptr;
+    // this thread's normaliser entries (i = tid, tid + 512, ...): z and phi(q) kept for den
+    float den = 0.f;
     for (int i = tid; i < D; i += DV_THREADS) {
         const float xq = to_f32(q[i]), xk = to_f32(k[i]);
-        fq[i] = a.fm == LA_FM_ELU1 ? phi_elu1(xq) : xq;
-        fk[i] = a.fm == LA_FM_ELU1 ? phi_elu1(xk) : xk;
-    }
-    __syncthreads();
-    float den = 0.f;
-    if (a.normalize) {
-        float *z = a.z + (size_t)head * D;
-        for (int i = tid; i < D; i += DV_THREADS) {
-            const float zi = a.gamma * z[i] + fk[i];
+        const float zo = a.normalize ? z[i] : 0.f;
+        const float gq = a.fm == LA_FM_ELU1 ? phi_elu1(xq) : xq;
+        const float gk = a.fm == LA_FM_ELU1 ? phi_elu1(xk) : xk;
+        fq[i] = gq;
+        fk[i] = gk;
+        if (a.normalize) {
+            const float zi = a.gamma * zo + gk;
             z[i] = zi;
-            den = fmaf(fq[i], zi, den);
+            den = fmaf(gq, zi, den);
         }
     }
-    dpart[tid] = den;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if ((tid & 31) == 0) wden[tid >> 5] = den;
+    __syncthreads();
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (rg < RG) {
+    if (active) {
         const T *v = (const T *)a.v + (size_t)head * dv + 4 * cq;
         const float v0 = to_f32(v[0]), v1 = to_f32(v[1]), v2 = to_f32(v[2]), v3 = to_f32(v[3]);
-        float4 *S = (float4 *)(a.S + (size_t)head * D * dv) + cq;
-        constexpr int RGI = 8;  // rows in flight per thread
+        const float gm = a.gamma;
         for (int i0 = rg; i0 < D; i0 += RG * RGI) {
-            float4 sv[RGI];
+            if (i0 != rg)  // later rounds (D > RG * RGI): load here
 #pragma unroll
-            for (int u = 0; u < RGI; ++u) {
-                const int i = i0 + u * RG;
-                if (i < D) sv[u] = S[(size_t)i * nq];
-            }
+                for (int u = 0; u < RGI; ++u) {
+                    const int i = i0 + u * RG;
+                    if (i < D) sv[u] = S[(size_t)i * nq];
+                }
 #pragma unroll
             for (int u = 0; u < RGI; ++u) {
                 const int i = i0 + u * RG;
                 if (i < D) {
-                    const float f = fk[i], g = fq[i], gm = a.gamma;
-                    sv[u].x = fmaf(f, v0, gm * sv[u].x);
-                    sv[u].y = fmaf(f, v1, gm * sv[u].y);
-                    sv[u].z = fmaf(f, v2, gm * sv[u].z);
-                    sv[u].w = fmaf(f, v3, gm * sv[u].w);
-                    S[(size_t)i * nq] = sv[u];
-                    num.x = fmaf(g, sv[u].x, num.x);
-                    num.y = fmaf(g, sv[u].y, num.y);
-                    num.z = fmaf(g, sv[u].z, num.z);
-                    num.w = fmaf(g, sv[u].w, num.w);
+                    const float f = fk[i], g = fq[i];
+                    float4 x = sv[u];
+                    x.x = fmaf(f, v0, gm * x.x);
+                    x.y = fmaf(f, v1, gm * x.y);
+                    x.z = fmaf(f, v2, gm * x.z);
+                    x.w = fmaf(f, v3, gm * x.w);
+                    S[(size_t)i * nq] = x;
+                    num.x = fmaf(g, x.x, num.x);
+                    num.y = fmaf(g, x.y, num.y);
+                    num.z = fmaf(g, x.z, num.z);
+                    num.w = fmaf(g, x.w, num.w);
                 }
             }
         }
         *(float4 *)(part + rg * dv + 4 * cq) = num;
     }
     __syncthreads();
-    for (int st = DV_THREADS / 2; st > 0; st >>= 1) {
-        if (tid < st) dpart[tid] += dpart[tid + st];
-        __syncthreads();
-    }
+    float den_all = 0.f;
+    if (a.normalize)
+#pragma unroll
+        for (int w = 0; w < DV_THREADS / 32; ++w) den_all += wden[w];
     for (int c = tid; c < dv; c += DV_THREADS) {
         float acc = 0.f;
         for (int g = 0; g < RG; ++g) acc += part[g * dv + c];
-        const float o = a.normalize ? acc / dpart[0] : acc;
+        const float o = a.normalize ? acc / den_all : acc;
         ((T *)a.out)[(size_t)head * dv + c] = from_f32<T>(o);
     }
 }
@@ -335,7 +350,7 @@ int decode_launch(const void *q, const void *k, const void *v, void *out, float 
     a.gamma = gamma;
     if (!lam && a.fm != LA_FM_FAVOR && dv % 4 == 0 && dv <= 512) {
         const int RG = DV_THREADS / (dv / 4);
-        const size_t vsm = sizeof(float) * ((size_t)2 * D + (size_t)RG * dv + DV_THREADS);
+        const size_t vsm = sizeof(float) * ((size_t)2 * D + (size_t)RG * dv + DV_THREADS / 32);
         if (vsm <= 200 * 1024) {
             dim3 vgrid((unsigned)(B * H));
             if (dtype == LA_BF16) {
