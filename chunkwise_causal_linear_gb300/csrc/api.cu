@@ -175,7 +175,7 @@ static int run(const void *q, const void *k, const void *v, void *out, int B, in
                int dk, int dv, int C, const la_feature_map *fm, int normalize,
                const float *lam, int num_levels, int dtype, void *ws, size_t ws_bytes,
                void *stream, int path, bool decay = false, float gamma = 1.f,
-               const float *S0 = nullptr, const float *z0 = nullptr)
+               const float *S0 = nullptr, const float *z0 = nullptr, int sms_fixed = 0)
 {
     if (!q || !k || !v || !out) return LA_ERR_NULL;
     const bool ll = lam != nullptr;
@@ -186,7 +186,8 @@ static int run(const void *q, const void *k, const void *v, void *out, int B, in
     p.S0 = S0;
     p.z0 = z0;
     if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
-    const int sms = device_sms();
+    // sms_fixed = 1 keeps every head in one segment (no sequence split, no totals pass)
+    const int sms = sms_fixed > 0 ? sms_fixed : device_sms();
     if (sms <= 0) return LA_ERR_CUDA;
     la_plan_info info;
     rc = plan_problem(p, ll, path, sms, &info);
@@ -253,23 +254,96 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
     if (!q_host || !k_host || !v_host || !out_host) return LA_ERR_NULL;
     if (!q_dev || !k_dev || !v_dev || !out_dev) return LA_ERR_NULL;
     Problem p;
-    int rc = check_problem(B, H, L, dk, dv, C, feature_map, normalize, level_weights != nullptr,
-                           num_levels, dtype, &p);
+    const bool ll = level_weights != nullptr;
+    int rc = check_problem(B, H, L, dk, dv, C, feature_map, normalize, ll, num_levels, dtype, &p);
     if (rc != LA_OK) return rc;
+    if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
+    const int sms = device_sms();
+    if (sms <= 0) return LA_ERR_CUDA;
+    la_plan_info info;
+    if ((rc = plan_problem(p, ll, LA_PATH_AUTO, sms, &info)) != LA_OK) return rc;
+    if (info.workspace_bytes > 0 && (!workspace || workspace_bytes < info.workspace_bytes))
+        return LA_ERR_WORKSPACE;
     const size_t es = dtype == LA_F32 ? 4 : 2;
-    const size_t nqk = (size_t)B * H * L * dk * es, nv = (size_t)B * H * L * dv * es;
+    const int BH = B * H;
+    const size_t hqk = (size_t)L * dk * es, hv = (size_t)L * dv * es;  // bytes per head
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(q_dev, q_host, nqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(k_dev, k_host, nqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(v_dev, v_host, nv, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return LA_ERR_CUDA;
-    rc = la_chunked_fwd(q_dev, k_dev, v_dev, out_dev, B, H, L, dk, dv, C, feature_map,
-                        normalize, level_weights, num_levels, dtype, workspace, workspace_bytes,
-                        stream);
-    if (rc != LA_OK) return rc;
-    if (cudaMemcpyAsync(out_host, out_dev, nv, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return LA_ERR_CUDA;
-    return LA_OK;
+    // Pipelined over groups of heads when the plan is one unsplit launch and the step moves
+    // enough bytes: the copies in of group i+1 and out of group i-1 run on their own streams
+    // (the two copy directions at once) while group i computes.  Every group runs unsplit,
+    // so each head gets exactly the arithmetic of the whole launch.
+    int ng = 1;
+    if (info.n_launches == 1 && (size_t)BH * 2 * (hqk + hv) >= ((size_t)64 << 20)) ng = BH < 8 ? BH : 8;
+    const int hg = (BH + ng - 1) / ng;
+    ng = (BH + hg - 1) / hg;
+    if (ng > 1) {
+        Problem pg;
+        la_plan_info gi;
+        if (check_problem(1, hg, L, dk, dv, C, feature_map, normalize, ll, num_levels, dtype, &pg) != LA_OK ||
+            plan_problem(pg, ll, LA_PATH_AUTO, 1, &gi) != LA_OK || gi.path != info.path ||
+            (gi.workspace_bytes > 0 && (!workspace || workspace_bytes < gi.workspace_bytes)))
+            ng = 1;
+    }
+    if (ng == 1) {
+        if (cudaMemcpyAsync(q_dev, q_host, BH * hqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(k_dev, k_host, BH * hqk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(v_dev, v_host, BH * hv, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return LA_ERR_CUDA;
+        rc = la_chunked_fwd(q_dev, k_dev, v_dev, out_dev, B, H, L, dk, dv, C, feature_map,
+                            normalize, level_weights, num_levels, dtype, workspace, workspace_bytes,
+                            stream);
+        if (rc != LA_OK) return rc;
+        if (cudaMemcpyAsync(out_host, out_dev, BH * hv, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return LA_ERR_CUDA;
+        return LA_OK;
+    }
+    // streams and events of this call (released once their work completes)
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t ev[2 * 8 + 3] = {};
+    const int nev = 2 * ng + 3;
+    bool ok = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < nev; ++i)
+        ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    cudaEvent_t start = ev[0], done = ev[1];
+    // both copy streams start after the work already queued on the caller's stream
+    ok = ok && cudaEventRecord(start, s) == cudaSuccess && cudaStreamWaitEvent(cin, start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(cout, start, 0) == cudaSuccess;
+    rc = ok ? LA_OK : LA_ERR_CUDA;
+    auto at = [](const void *base, size_t off) { return (void *)((const char *)base + off); };
+    for (int g = 0; rc == LA_OK && g < ng; ++g) {
+        const int h0 = g * hg, hn = BH - h0 < hg ? BH - h0 : hg;
+        cudaEvent_t in_done = ev[2 + 2 * g], run_done = ev[3 + 2 * g];
+        const size_t oqk = (size_t)h0 * hqk, ov = (size_t)h0 * hv;
+        if (cudaMemcpyAsync(at(q_dev, oqk), at(q_host, oqk), hn * hqk, cudaMemcpyHostToDevice, cin) != cudaSuccess ||
+            cudaMemcpyAsync(at(k_dev, oqk), at(k_host, oqk), hn * hqk, cudaMemcpyHostToDevice, cin) != cudaSuccess ||
+            cudaMemcpyAsync(at(v_dev, ov), at(v_host, ov), hn * hv, cudaMemcpyHostToDevice, cin) != cudaSuccess ||
+            cudaEventRecord(in_done, cin) != cudaSuccess || cudaStreamWaitEvent(s, in_done, 0) != cudaSuccess) {
+            rc = LA_ERR_CUDA;
+            break;
+        }
+        const float *lam = ll ? level_weights + (size_t)h0 * L * num_levels : nullptr;
+        rc = run(at(q_dev, oqk), at(k_dev, oqk), at(v_dev, ov), at(out_dev, ov), 1, hn, L, dk, dv, C,
+                 feature_map, normalize, lam, num_levels, dtype, workspace, workspace_bytes, stream,
+                 LA_PATH_AUTO, false, 1.f, nullptr, nullptr, 1);
+        if (rc != LA_OK) break;
+        if (cudaEventRecord(run_done, s) != cudaSuccess || cudaStreamWaitEvent(cout, run_done, 0) != cudaSuccess ||
+            cudaMemcpyAsync(at(out_host, ov), at(out_dev, ov), hn * hv, cudaMemcpyDeviceToHost, cout) != cudaSuccess)
+            rc = LA_ERR_CUDA;
+    }
+    // the caller's stream reaches the end of the call after every copy of both streams,
+    // also when a group failed to queue (nothing is left running past the call)
+    cudaEvent_t in_end = ev[nev - 1];
+    if (done && in_end && cin && cout) {
+        if (cudaEventRecord(in_end, cin) != cudaSuccess || cudaStreamWaitEvent(s, in_end, 0) != cudaSuccess ||
+            cudaEventRecord(done, cout) != cudaSuccess || cudaStreamWaitEvent(s, done, 0) != cudaSuccess)
+            if (rc == LA_OK) rc = LA_ERR_CUDA;
+    }
+    for (int i = 0; i < nev; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    if (cin) cudaStreamDestroy(cin);
+    if (cout) cudaStreamDestroy(cout);
+    return rc;
 }
 
 size_t la_chunked_workspace_bytes(int B, int H, int L, int dk, int dv, int C,

@@ -133,10 +133,15 @@ int la_chunked_fwd_path(const void *q, const void *k, const void *v, void *out,
  * la_chunked_fwd_host -- the same forward pass from HOST buffers: copies q, k, v (and
  * nothing else: omega and level_weights stay device pointers) from host memory into the
  * caller's device buffers q_dev, k_dev, v_dev, runs la_chunked_fwd on them into out_dev,
- * copies out_dev back into out_host, all queued on `stream`.  Host buffers should be
- * pinned (cudaHostAlloc / page-locked) for the copies to be asynchronous; the host
- * buffers must stay valid until the stream reaches the end of the call.  Sizes and error
- * behaviour as la_chunked_fwd.
+ * copies out_dev back into out_host.  Host buffers should be pinned (cudaHostAlloc /
+ * page-locked) for the copies to be asynchronous; the host buffers must stay valid until
+ * the stream reaches the end of the call.  Sizes and error behaviour as la_chunked_fwd.
+ * When the plan is one unsplit launch and the step moves at least 64 MB, the call runs as a
+ * pipeline over up to 8 groups of heads: copies in on one internal stream, the groups'
+ * launches on `stream`, copies out on another internal stream, so the two copy directions
+ * and the compute overlap.  Each head's arithmetic is that of la_chunked_fwd (identical
+ * outputs).  Either way the work is ordered after what `stream` already holds, and `stream`
+ * reaches the end of the call only after every copy.
  */
 int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_host,
                         void *out_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,

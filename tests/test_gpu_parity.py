@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 
 import synth
-from parity_util import (assert_close, oracle_heads, run_gpu, sample_rows, workload)
+from parity_util import (assert_close, from_device, oracle_heads, run_gpu, sample_rows, to_device,
+                         workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -142,3 +143,53 @@ def test_full_size_sampled_rows(name, C):
     assert_close(out[heads][:, rows], ref, f"{name} C={C}")
     # whole-output sanity: finite everywhere
     assert np.isfinite(out).all()
+
+
+HOST_CASES = [
+    # (workload, overrides): pipelined over head groups (>= 64 MB moved), or one sequence
+    ("elu1-norm-d128-L8192", dict(L=2048)),             # 128 heads, 268 MB: 8 groups of 16
+    ("elu1-norm-d128-L8192", dict(B=3, H=27, L=1000)),  # 81 heads: 7 groups of 11 and one of 4
+    ("identity-d64-L2048", dict()),                     # 33 MB, split plan: one sequence
+    ("loglinear-d64-L65536", dict(B=2, H=48, L=4096)),  # level weights offset per group
+]
+
+
+@pytest.mark.parametrize("name,over", HOST_CASES)
+def test_host_entry_point_equals_device_path(name, over):
+    """la_chunked_fwd_host (pinned host buffers in and out) returns exactly the device
+    entry point's output, and that output matches the oracle on sampled rows."""
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    w = workload(name, **over)
+    inp = synth.make_inputs(w, seed=31)
+    out_dev, _ = run_gpu(w, inp, w["C"], AUTO)
+    B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
+    q = to_device(inp["q"], w["dtype"], (B, H, L, dk))
+    k = to_device(inp["k"], w["dtype"], (B, H, L, dk))
+    v = to_device(inp["v"], w["dtype"], (B, H, L, dv))
+    qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+    outh = torch.empty((B, H, L, dv), dtype=q.dtype).pin_memory()
+    qd, kd, vd = (torch.empty_like(x) for x in (q, k, v))
+    od = torch.empty((B, H, L, dv), dtype=q.dtype, device="cuda")
+    lam = None if inp["lam"] is None else torch.from_numpy(inp["lam"]).reshape(B, H, L, -1).cuda()
+    nl = 0 if lam is None else lam.shape[-1]
+    fm = la.make_feature_map(w["fm"])
+    dt = la.LA_BF16 if w["dtype"] == "bf16" else la.LA_F32
+    wsb = la.la_chunked_workspace_bytes(B, H, L, dk, dv, w["C"], fm, int(w["normalize"]), nl, dt)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = la.la_chunked_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), outh.data_ptr(),
+                                qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), B, H, L,
+                                dk, dv, w["C"], fm, int(w["normalize"]),
+                                None if lam is None else lam.data_ptr(), nl, dt, ws.data_ptr(), wsb, s)
+    assert rc == la.LA_OK, la.la_status_string(rc)
+    torch.cuda.current_stream().synchronize()
+    st = la.la_last_device_status(s)
+    assert st == la.LA_OK, la.la_status_string(st)
+    got = from_device(outh).reshape(B * H, L, dv)
+    assert np.array_equal(got, out_dev), np.abs(got - out_dev).max()
+    heads = [0, B * H - 1]
+    rows = sample_rows(L, w["C"], 24, seed=31)
+    ref = oracle_heads(w, inp, heads, method="scores_first", rows=rows)
+    assert_close(got[heads][:, rows], ref, f"host entry point {name} {over}")
