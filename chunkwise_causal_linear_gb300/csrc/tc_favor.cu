@@ -8,22 +8,25 @@
 // m = 256 features, dv = 64, chunks of 64 rows.
 //
 // Layout (TMEM 512 columns, ~222 KB shared memory, 640 threads):
-//   * projection, transposed: P^T = omega' x^T (M = 128 features per half, N = 64 tokens,
-//     K = dk), omega' = omega dk^{-1/4} held as bf16 hi + lo (two accumulated MMAs: a single
-//     bf16 copy of omega' misses the tolerance).  TMEM lanes are features, so each of the 256
-//     feature-map threads owns one feature l: it exponentiates its 64 tokens, writes row l of
-//     phi^T ([l][t], t contiguous: one 128-byte row) and keeps z_l as a private fp32 sum.
+//   * projection, transposed: P^T = omega' [Q; K]^T (M = 128 features per half, N = 128: the
+//     chunk's 64 query rows and 64 key rows, contiguous in the stage, in one product; K = dk),
+//     omega' = omega dk^{-1/4} held as bf16 hi + lo (two accumulated MMAs: a single bf16 copy
+//     of omega' misses the tolerance).  TMEM lanes are features, so each of the 256
+//     feature-map threads owns one feature l: it exponentiates its 64 query and 64 key
+//     tokens, writes row l of phi(Q)^T and phi(K)^T ([l][t], t contiguous: one 128-byte row)
+//     and keeps z_l as a private fp32 sum.
 //   * the phi^T tiles are MN-major A (scores, inter: M = t, K = l), MN-major B (scores: N = s)
 //     and K-major A (state: M = l, K = s) -- the same bytes serve all three.
 //   * state S (256 x 64) not transposed: two M = 128 halves in TMEM, 128 columns, all lanes.
 //     Its bf16 copy S~ is a K-major B operand [j][l] in shared memory with two extra rows
 //     j = 64, 65 holding z_hi, z_lo, so the inter MMA (N = 72) also returns phi(q_t).z.
-//   * output O (M = 64 tokens, N = 72) double-buffered in TMEM; each output thread owns one
-//     row and stores it straight to global memory (128 contiguous bytes).
+//   * output O (M = 64 tokens, N = 72) in TMEM; each output thread owns one row and stores it
+//     straight to global memory (128 contiguous bytes).  The scores share the projection's
+//     columns: the projection is read before the scores are written, and the next chunk's
+//     projection waits for the scores to be read.
 //
 // MMAs per chunk (bf16 in, fp32 accumulate):
-//   projQ   P^T  = omega'(hi+lo) Q^T    M=128 x2  N=64  K=64  (x2 for hi, lo)
-//   projK   P^T  = omega'(hi+lo) K^T    M=128 x2  N=64  K=64
+//   proj    P^T  = omega'(hi+lo) [Q;K]^T  M=128 x2  N=128 K=64  (x2 for hi, lo)
 //   scores  A    = phi(Q) phi(K)^T      M=64      N=64  K=256
 //   inter   O'   = phi(Q) [S~ | z]      M=64      N=72  K=256
 //   state   S   += phi(K)^T V           M=128 x2  N=64  K=64
@@ -76,9 +79,9 @@ static_assert(FV_SBLK % 1024 == 0, "swizzle atoms stay aligned");
 
 // TMEM columns
 constexpr uint32_t FT_S = 0;      // S: half h at columns 64h (lanes = features 128h..)
-constexpr uint32_t FT_P = 128;    // projection: half h at 128 + 64h (lanes = features)
-constexpr uint32_t FT_O = 256;    // O' buffers at 256 + 80b (M = 64 layout, 72 columns)
-constexpr uint32_t FT_A = 416;    // scores (M = 64 layout, 64 columns)
+constexpr uint32_t FT_P = 128;    // projection: half h at 128 + 128h, Q tokens then K tokens
+constexpr uint32_t FT_A = 128;    // scores (M = 64 layout, 64 columns), inside the projection's
+constexpr uint32_t FT_O = 384;    // O' (M = 64 layout, 72 columns)
 
 struct FvArgs {
     CUtensorMap tm_q, tm_k, tm_v;
@@ -106,17 +109,16 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
     uint64_t *bars = (uint64_t *)(sm + FV_BAR);
     uint64_t *full = bars;                         // [S]
     uint64_t *stage_free = full + FV_STAGES;       // [S]
-    uint64_t *pq_done = stage_free + FV_STAGES;    // projection of Q in TMEM
-    uint64_t *pk_done = pq_done + 1;               // projection of K in TMEM
-    uint64_t *p_free = pk_done + 1;                // projection read (twice per chunk)
-    uint64_t *phi_ready = p_free + 1;              // phi(Q), phi(K), z rows written
+    uint64_t *p_done = stage_free + FV_STAGES;     // projection of the chunk in TMEM
+    uint64_t *phi_ready = p_done + 3;              // phi(Q), phi(K), z rows written (and the
+                                                   // projection read)
     uint64_t *scores_done = phi_ready + 1;
-    uint64_t *a_free = scores_done + 1;
+    uint64_t *a_free = scores_done + 1;            // scores read (their columns reusable)
     uint64_t *p_ready = a_free + 1;
     uint64_t *state_done = p_ready + 1;
     uint64_t *sbar_ready = state_done + 1;         // S~ rows for the next chunk written
-    uint64_t *o_done = sbar_ready + 1;             // [2]
-    uint64_t *o_free = o_done + 2;                 // [2]
+    uint64_t *o_done = sbar_ready + 1;             // [1] (slot 2 spare)
+    uint64_t *o_free = o_done + 2;                 // [1] (slot 2 spare)
     uint64_t *drain = o_free + 2;
     uint64_t *totals_done = drain + 1;
     uint64_t *den_full = totals_done + 2;          // [FV_DEN]
@@ -139,9 +141,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             mbar_init(&full[i], 1);
             mbar_init(&stage_free[i], 1);
         }
-        mbar_init(pq_done, 1);
-        mbar_init(pk_done, 1);
-        mbar_init(p_free, 8);
+        mbar_init(p_done, 1);
         mbar_init(phi_ready, 1);
         mbar_init(scores_done, 1);
         mbar_init(a_free, 4);
@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_PROJ = idesc_bf16_f32(128, 64, 0, 0);
+            constexpr uint32_t ID_PROJ = idesc_bf16_f32(128, 64, 0, 0);    // K rows only
+            constexpr uint32_t ID_PROJ2 = idesc_bf16_f32(128, 128, 0, 0);  // Q and K rows
             constexpr uint32_t ID_SC = idesc_bf16_f32(64, 64, 1, 1);
             constexpr uint32_t ID_INTER = idesc_bf16_f32(64, FV_SROWS, 1, 0);
             constexpr uint32_t ID_STATE = idesc_bf16_f32(128, 64, 0, 1);
@@ -257,8 +258,9 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             const uint64_t dOm = smem_desc(om, 16, 1024), dPhqMN = smem_desc(phq, FV_M * 128, 1024),
                            dPhkMN = smem_desc(phk, FV_M * 128, 1024), dPhk = smem_desc(phk, 16, 1024),
                            dSb = smem_desc(sb, 16, 1024), dPa = smem_desc(pa, 16, 1024);
-            // projection of a raw 64x64 tile into TMEM (features on lanes), omega hi + lo
-            auto project = [&](uint32_t xa) {
+            // projection of raw rows into TMEM (features on lanes), omega hi + lo: the 128 rows
+            // Q, K of the stage (main pass) or the 64 K rows (totals pass)
+            auto project = [&](uint32_t xa, uint32_t idesc) {
                 const uint64_t dX = smem_desc(xa, 16, 1024);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -266,29 +268,25 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tmem + FT_P + 64 * h,
+                            mma_ss(tmem + FT_P + 128 * h,
                                    desc_add(dOm, part * FV_M * 128 + h * 128 * 128 + ks * 32),
-                                   desc_add(dX, ks * 32), ID_PROJ, (part | ks) != 0);
+                                   desc_add(dX, ks * 32), idesc, (part | ks) != 0);
             };
-            int pfree_n = 0;  // completions of p_free waited for
             for (int c = 0; c < nch; ++c) {
-                const int s = c % FV_STAGES, b = c & 1;
+                const int s = c % FV_STAGES;
                 const int g = tile0 + c;  // chunk index in the sequence
                 if (!wait_phase(&full[s], (c / FV_STAGES) & 1, ctl)) break;
+                // the projection's columns hold the previous chunk's scores until the P warps
+                // have read them; the previous projection itself was read before phi_ready
+                if (!totals && c >= 1 && !wait_phase(a_free, (c - 1) & 1, ctl)) break;
                 const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
                 const uint64_t dVmn = smem_desc(va, FV_C * 128, 1024);
-                if (!totals) {
-                    if (c >= 1 && !wait_phase(p_free, (pfree_n++) & 1, ctl)) break;
-                    tc_fence_after();
-                    project(qa);
-                    mma_commit(pq_done);
-                }
-                if (c >= 1 || !totals) {
-                    if (!wait_phase(p_free, (pfree_n++) & 1, ctl)) break;
-                }
                 tc_fence_after();
-                project(ka);
-                mma_commit(pk_done);
+                if (totals)
+                    project(ka, ID_PROJ);
+                else
+                    project(qa, ID_PROJ2);  // K follows Q in the stage: rows 0-63 Q, 64-127 K
+                mma_commit(p_done);
                 if (!wait_phase(phi_ready, c & 1, ctl)) break;
                 tc_fence_after();
                 if (totals) {
@@ -302,17 +300,16 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     mma_commit(&stage_free[s]);
                     continue;
                 }
-                if (c >= 1 && !wait_phase(a_free, (c - 1) & 1, ctl)) break;
-                tc_fence_after();
-                // scores: phi(Q) (MN-major A) x phi(K)^T (MN-major B), K = 256 features
+                // scores: phi(Q) (MN-major A) x phi(K)^T (MN-major B), K = 256 features, into
+                // the projection's columns (read by now: phi_ready)
 #pragma unroll
                 for (int ks = 0; ks < FV_M / 16; ++ks)
                     mma_ss(tmem + FT_A, desc_add(dPhqMN, ks * 2048), desc_add(dPhkMN, ks * 2048), ID_SC, ks > 0);
                 mma_commit(scores_done);
                 if (!NC && c >= 1 && !wait_phase(sbar_ready, (c - 1) & 1, ctl)) break;
-                if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
+                if (c >= 1 && !wait_phase(o_free, (c - 1) & 1, ctl)) break;
                 tc_fence_after();
-                const uint32_t tO = tmem + FT_O + 80 * b;
+                const uint32_t tO = tmem + FT_O;
                 // inter: phi(Q) (MN-major A) x [S~ | z] (K-major B, 72 rows), K = 256
 #pragma unroll
                 for (int ks = 0; ks < FV_M / 16; ++ks)
@@ -334,7 +331,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_ss(tO, desc_add(dPa, ks * 32), desc_add(dVmn, ks * 2048), ID_INTRA, 1);
-                mma_commit(&o_done[b]);
+                mma_commit(o_done);
                 mma_commit(&stage_free[s]);
             }
             if (totals) mma_commit(totals_done);
@@ -348,7 +345,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         const int l = tid - 128;
         const int half = l >> 7;
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tP = tmem + FT_P + 64 * half + lo;
+        const uint32_t tP = tmem + FT_P + 128 * half + lo;  // Q tokens at +0, K tokens at +64
         const float inv_sqrt_m = 0.0625f;      // 1 / sqrt(256)
         const float log2e = 1.4426950408889634f;
         uint8_t *rowq = sm + FV_PHIQ + l * 128;
@@ -359,14 +356,13 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         // phi of this thread's feature for the 64 tokens of a projected tile
         // sum_z: the z sum over the tile's tokens; in the non-causal totals the zero-filled
         // rows past L (whose phi is not zero) are left out, since z is used after them
-        auto phi_row = [&](const float *nr, uint8_t *dst, bool sum_z, int valid) {
+        // (tokens at TMEM columns col .. col+63 of this thread's projection row)
+        auto phi_row = [&](uint32_t col, const float *nr, uint8_t *dst, bool sum_z, int valid) {
             uint32_t r0[32], r1[32];
-            tmem_ld32(tP, r0);
-            tmem_ld32(tP + 32, r1);
+            tmem_ld32(tP + col, r0);
+            tmem_ld32(tP + col + 32, r1);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_free);
+            tc_fence_before();  // the projection read, before the barrier ahead of phi_ready
             float zs = 0.f;
 #pragma unroll
             for (int ck = 0; ck < 8; ++ck) {
@@ -415,20 +411,18 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 }
             }
             named_bar(1, 256);
+            if (!group_wait(l == 0, 1, p_done, c & 1, nullptr, 0, false, ctl, 256)) break;
+            tc_fence_after();
             if (!totals) {
-                if (!group_wait(l == 0, 1, pq_done, c & 1, nullptr, 0, false, ctl, 256)) break;
-                tc_fence_after();
-                phi_row(nrm, rowq, false, 0);
+                phi_row(0, nrm, rowq, false, 0);
                 // z_c (before this chunk) as bf16 hi / lo in S~ rows 64, 65 at column l
                 const __nv_bfloat16 zh = __float2bfloat16_rn(zreg);
                 const __nv_bfloat16 zl = __float2bfloat16_rn(zreg - __bfloat162float(zh));
                 *(__nv_bfloat16 *)(sblk + 64 * 128 + ((lch ^ 0) << 4)) = zh;
                 *(__nv_bfloat16 *)(sblk + 65 * 128 + ((lch ^ 1) << 4)) = zl;
             }
-            if (!group_wait(l == 0, 1, pk_done, c & 1, nullptr, 0, false, ctl, 256)) break;
-            tc_fence_after();
             {
-                const float zk = phi_row(nrm + 64, rowk, totals || !NC, a.L - g * FV_C);
+                const float zk = phi_row(totals ? 0 : 64, nrm + 64, rowk, totals || !NC, a.L - g * FV_C);
                 if (totals || !NC) zreg += zk;
             }
             fence_async_smem();
@@ -527,12 +521,12 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         const int t = 16 * q4 + (lane & 15);
         const bool row_lane = lane < 16;
         for (int c = 0; c < nch; ++c) {
-            const int b = c & 1, slot = c % FV_DEN;
+            const int slot = c % FV_DEN;
             const int row = (tile0 + c) * FV_C + t;
-            if (!group_wait(ot == 0, 3, &o_done[b], (c >> 1) & 1, &den_full[slot], (c / FV_DEN) & 1, NORM, ctl))
+            if (!group_wait(ot == 0, 3, o_done, c & 1, &den_full[slot], (c / FV_DEN) & 1, NORM, ctl))
                 break;
             tc_fence_after();
-            const uint32_t tO = tmem + FT_O + 80 * b + ((uint32_t)(32 * q4) << 16);
+            const uint32_t tO = tmem + FT_O + ((uint32_t)(32 * q4) << 16);
             uint32_t r0[32], r1[32], rz[8];
             tmem_ld32(tO, r0);
             tmem_ld32(tO + 32, r1);
@@ -540,7 +534,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[b]);
+            if (lane == 0) mbar_arrive(o_free);
             float inv = 1.f;
             if (NORM && row_lane)
                 // fast division: 1/den only scales the fp32 row before its bf16 rounding
