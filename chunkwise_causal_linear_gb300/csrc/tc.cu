@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 // non-causal main pass: every row reads the whole sequence's state, so a tile
                 // needs only the inter product and (normaliser) phi(Q) z, from the z rows of
                 // the K tile alone; no scores over keys, no intra product
-                constexpr uint32_t ID_Z = idesc_bf16_f32(C, 16, 0, 0);
+                constexpr uint32_t ID_Z = idesc_bf16_f32(C, 8, 0, 0);  // rows C .. C+7 of a block
                 auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
                 for (int c = 0; ok && c < nch; ++c) {
                     const int s = c % TC_STAGES, b = c & 1;
@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     const uint64_t dQ = smem_desc(smem_u32(stage_q(s)), 16, 1024);
                     const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
                     if (NORM) {
-                        // z hi / lo in rows C, C+1 of each 64-feature block: TMEM columns C, C+1
+                        // z hi / lo in rows C, C+1 of each 64-feature block (then six zero
+                        // rows): TMEM columns C, C+1
                         const uint64_t dZ = smem_desc(smem_u32(stage_k(s)) + C * 128, 16, 1024);
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks)
