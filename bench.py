@@ -225,6 +225,15 @@ def cpu_baseline(w, inp_heads, heads_used, threads):
     return toks / dt, dt
 
 
+def cpu_baseline_one_core(w, inp_heads):
+    """The same oracle recurrence on one head, one thread: the single-core rate."""
+    one = {kk: (vv[:1] if kk in ("q", "k", "v", "lam") and vv is not None else vv)
+           for kk, vv in inp_heads.items()}
+    val, dt = cpu_baseline(w, one, 1, 1)
+    return {"value": val, "unit": "tokens/s", "cores": 1,
+            "sample": f"1 head x L={w['L']}, {dt:.2f} s wall"}
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -284,7 +293,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(args.workload, w, C),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "one_core": cpu_baseline_one_core(w, inp)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -510,7 +520,8 @@ def run_ours(args):
         cpu = {"value": val, "unit": "tokens/s", "cores": min(cores, len(heads)),
                "kind": "oracle",
                "sample": f"{len(heads)} of {B * H} heads x L={L}, chunk-size-1 recurrence in "
-                         f"fp64, {dt:.1f} s wall"}
+                         f"fp64, {dt:.1f} s wall",
+               "one_core": cpu_baseline_one_core(w, sub)}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

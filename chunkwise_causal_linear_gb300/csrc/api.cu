@@ -262,6 +262,10 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
     if (sms <= 0) return LA_ERR_CUDA;
     la_plan_info info;
     if ((rc = plan_problem(p, ll, LA_PATH_AUTO, sms, &info)) != LA_OK) return rc;
+    // as in run(): level weights that are not 16-byte aligned take the generic path
+    if (info.path == LA_PATH_TC && ll && ((uintptr_t)level_weights & 15) != 0 &&
+        (rc = plan_problem(p, ll, LA_PATH_SIMT, sms, &info)) != LA_OK)
+        return rc;
     if (info.workspace_bytes > 0 && (!workspace || workspace_bytes < info.workspace_bytes))
         return LA_ERR_WORKSPACE;
     const size_t es = dtype == LA_F32 ? 4 : 2;
@@ -277,11 +281,14 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
     const int hg = (BH + ng - 1) / ng;
     ng = (BH + hg - 1) / hg;
     if (ng > 1) {
+        // every group runs on the whole problem's path with a workspace that fits it; a
+        // group's level weights start 16-byte aligned when the whole array does
         Problem pg;
         la_plan_info gi;
         if (check_problem(1, hg, L, dk, dv, C, feature_map, normalize, ll, num_levels, dtype, &pg) != LA_OK ||
-            plan_problem(pg, ll, LA_PATH_AUTO, 1, &gi) != LA_OK || gi.path != info.path ||
-            (gi.workspace_bytes > 0 && (!workspace || workspace_bytes < gi.workspace_bytes)))
+            plan_problem(pg, ll, info.path, 1, &gi) != LA_OK || gi.path != info.path ||
+            (gi.workspace_bytes > 0 && (!workspace || workspace_bytes < gi.workspace_bytes)) ||
+            (ll && ((size_t)hg * L * num_levels) % 4 != 0))
             ng = 1;
     }
     if (ng == 1) {
@@ -325,7 +332,7 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
         const float *lam = ll ? level_weights + (size_t)h0 * L * num_levels : nullptr;
         rc = run(at(q_dev, oqk), at(k_dev, oqk), at(v_dev, ov), at(out_dev, ov), 1, hn, L, dk, dv, C,
                  feature_map, normalize, lam, num_levels, dtype, workspace, workspace_bytes, stream,
-                 LA_PATH_AUTO, false, 1.f, nullptr, nullptr, 1);
+                 info.path, false, 1.f, nullptr, nullptr, 1);
         if (rc != LA_OK) break;
         if (cudaEventRecord(run_done, s) != cudaSuccess || cudaStreamWaitEvent(cout, run_done, 0) != cudaSuccess ||
             cudaMemcpyAsync(at(out_host, ov), at(out_dev, ov), hn * hv, cudaMemcpyDeviceToHost, cout) != cudaSuccess)

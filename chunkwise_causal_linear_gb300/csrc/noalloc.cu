@@ -8,24 +8,29 @@
 // the caller; this one takes it from a fixed array that lives in the library image, so it
 // never allocates.
 //
-// The only path that needs scratch is the log-linear mask on the generic CUDA-core path
-// (one fp32 state per inter-chunk Fenwick level, per head and value slice).  The kernel
-// zeroes its part of the scratch at the start of every call, so nothing left over from an
-// earlier call is ever read.
+// Every plan with a nonzero la_chunked_workspace_bytes takes its scratch from the array:
+//   - the tensor-core paths when they cut a sequence into segments (few heads: any feature
+//     map and chunk size), for the fp32 segment totals S and z;
+//   - the log-linear mask: the per-level fp32 chunk states of the generic path, and the
+//     segment totals and running-state snapshots of the tensor-core path.
+// Each call writes every scratch word it later reads (the totals launch writes the totals
+// before the main launch reads them; the generic kernel zeroes its level states first), so
+// nothing left over from an earlier call is ever read.
 #include <mutex>
 
 #include "common.cuh"
 
 namespace {
 
-// Fixed scratch, 8 MiB: enough for the log-linear level states of, e.g., 16 heads at
-// L = 65,536, d = 64, C = 64 (2.7 MB).  Every GPU that loads the library holds it until
+// Fixed scratch, 8 MiB: enough for, e.g., the log-linear mask over 16 heads at L = 65,536,
+// d = 64, C = 64, or the fp32 totals of 127 segments of d = 128 heads (66 KB each).  Every GPU that loads the library holds it until
 // the process exits.
 constexpr size_t kScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char la_noalloc_scratch[kScratchBytes];
 
 // In host code `la_noalloc_scratch` only names the symbol; its device address is looked up
-// once per device (with that device current) and cached here.
+// once per device (with that device current) and cached here.  cudaDeviceReset destroys the
+// context that address belongs to, so calls after a reset of that device are not supported.
 std::mutex g_mu;
 void *g_scratch[64] = {nullptr};
 

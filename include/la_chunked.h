@@ -156,13 +156,16 @@ int la_chunked_fwd_host(const void *q_host, const void *k_host, const void *v_ho
  * application owns every device allocation, real-time loops that must never call
  * cudaMalloc / cudaFree).  No counterpart on the pages: it is a deployment variant.
  *
- * It allocates nothing.  Where the problem needs scratch (the log-linear mask's per-level
- * chunk states), it uses a fixed 8 MiB array compiled into the library; every GPU that
- * loads the library holds those 8 MiB until the process exits.  Problems that need more
- * return LA_ERR_SCRATCH_LIMIT before anything is launched (la_chunked_workspace_bytes tells
- * how much a problem needs).
+ * It allocates nothing.  Every problem whose la_chunked_workspace_bytes is nonzero takes
+ * that scratch from a fixed 8 MiB array compiled into the library: the segment totals of a
+ * sequence cut into segments (few heads, on the tensor-core paths), and the log-linear
+ * mask's per-level chunk states.  Every GPU that loads the library holds those 8 MiB until
+ * the process exits.  Problems that need more return LA_ERR_SCRATCH_LIMIT before anything
+ * is launched (la_chunked_workspace_bytes tells how much a problem needs).
  *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current); make that first call before any stream capture.  The address is kept for
+ *     the life of the process: calls after cudaDeviceReset of that device are not
+ *     supported.
  *   - All calls share the one array and it keeps the last call's contents; the kernel
  *     clears what it needs at the start of every call.  Calls that may overlap on the GPU
  *     (different streams, or different host threads) race on it: serialise them.

@@ -119,17 +119,19 @@ def test_decay_gamma_one_equals_plain(path):
     assert np.array_equal(a, b)
 
 
-def test_decay_full_size_sampled_rows():
+def test_decay_full_size_all_outputs():
     """The decayed workload at full size (B=8, H=16, L=8192, d=128, elu+1, normaliser,
-    gamma = 0.98) on the tensor cores, as the benchmark runs it: sampled rows of a few
-    heads against the oracle's weighted sum over the past."""
+    gamma = 0.98) on the tensor cores, as the benchmark runs it: every head and row against
+    the oracle's recurrence, and sampled rows of three heads against its weighted sum over
+    the past."""
     w = workload("decay-elu1-norm-d128-L8192")
     gamma = w["gamma"]
     rc, info = plan_path(w, gamma)
     assert rc == 0 and info["path"] == 2
-    heads = [0, 77, 127]
     inp = synth.make_inputs(w, seed=24)
     out = run_decay(w, inp, gamma)
+    assert_close(out, oracle_decay(w, inp, gamma), "full-size decay, all outputs")
+    heads = [0, 77, 127]
     rows = [0, 1, 63, 64, 65, 4095, 4096, 8190, 8191]
     ref = oracle_decay(w, {k: (v[heads] if isinstance(v, np.ndarray) else v)
                            for k, v in inp.items()}, gamma, rows=rows)

@@ -88,18 +88,21 @@ def test_noncausal_last_row_equals_causal_last_row():
     assert_close(nc[:, -1:], ca[:, -1:], "last rows")
 
 
-def test_noncausal_full_size_sampled_rows():
-    """The benchmark's workload (B8 H16 L8192 d128, elu+1 + normaliser): sampled rows of the
-    first and last head against the oracle's definition, every output finite."""
+@pytest.mark.parametrize("name", ["elu1-norm-d128-L8192", "favor-m256-d64-L16384"])
+def test_noncausal_full_size_all_outputs(name):
+    """The benchmark's workloads (B8 H16 L8192 d128 elu+1 + normaliser; B2 H12 L16384 FAVOR+
+    m=256): every head and row against the oracle's state-first form, and sampled rows of the
+    first and last head against its definition (scores first)."""
     from parity_util import sample_rows
-    w = workload("elu1-norm-d128-L8192")
+    w = workload(name)
     inp = synth.make_inputs(w, seed=12)
     out = run_nc(w, inp)
+    assert_close(out, oracle_nc(w, inp), f"non-causal full size {name}, all outputs")
     heads = [0, w["B"] * w["H"] - 1]
     rows = sample_rows(w["L"], 64, 48, seed=12)
     import oracle
     f = lambda x: synth.as_f64(x[heads], w["dtype"])  # noqa: E731
-    ref = oracle.forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), fm=w["fm"], normalize=True,
-                         causal=False, method="scores_first", rows=rows)
-    assert_close(out[heads][:, rows], ref, "non-causal full size")
-    assert np.isfinite(out).all()
+    om = None if inp["omega"] is None else inp["omega"].astype(np.float64)
+    ref = oracle.forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), fm=w["fm"], omega=om,
+                         normalize=w["normalize"], causal=False, method="scores_first", rows=rows)
+    assert_close(out[heads][:, rows], ref, f"non-causal full size {name}, sampled rows")

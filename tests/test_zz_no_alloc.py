@@ -3,7 +3,8 @@
 Some callers cannot allocate device memory (code inside an allocator or memory-pool
 callback, plugins whose host application owns every allocation, real-time loops that must
 not call cudaMalloc).  la_chunked_fwd_noalloc serves them from a fixed scratch buffer in the
-library.  This file is collected last so that, if it fails, a run that stops at the first
+library: every plan that needs scratch uses it (sequences cut into segments on the tensor-core
+paths, the log-linear mask's level states).  This file is collected last so that, if it fails, a run that stops at the first
 failure has already run every other test.
 """
 import numpy as np
@@ -26,34 +27,43 @@ def la_mod():
     return la
 
 
-def test_noalloc_matches_main_entry_point_twice(la_mod):
+# Problems whose plan needs scratch: the log-linear mask (three heads: level states and a
+# sequence cut into segments), and elu+1 with the normaliser on one d = 128 head, where the
+# tensor-core path cuts the sequence into segments and keeps their fp32 totals in scratch.
+NOALLOC_CASES = [
+    ("loglinear-d64-L65536", dict(B=1, H=3, L=1500)),
+    ("elu1-norm-d128-L8192", dict(B=1, H=1, L=8192)),
+]
+
+
+@pytest.mark.parametrize("name,over", NOALLOC_CASES)
+def test_noalloc_matches_main_entry_point_twice(la_mod, name, over):
     import torch
     la = la_mod
-    # a log-linear problem: the only one whose path needs scratch
-    w = workload("loglinear-d64-L65536", B=1, H=3, L=1500)
+    w = workload(name, **over)
     B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
     C = 64
-    fm = la.make_feature_map("identity")
+    fm = la.make_feature_map(w["fm"])
+    norm = int(w["normalize"])
     stream = torch.cuda.current_stream().cuda_stream
     for call, seed in enumerate((21, 22)):  # two calls in a row on the shared scratch
         inp = synth.make_inputs(w, seed=seed)
         q = to_device(inp["q"], "bf16", (B, H, L, dk))
         k = to_device(inp["k"], "bf16", (B, H, L, dk))
         v = to_device(inp["v"], "bf16", (B, H, L, dv))
-        lam = torch.from_numpy(inp["lam"]).reshape(B, H, L, -1).cuda()
-        nl = lam.shape[-1]
-        need = la.la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, 0, nl, la.LA_BF16)
+        lam = None if inp["lam"] is None else torch.from_numpy(inp["lam"]).reshape(B, H, L, -1).cuda()
+        nl = 0 if lam is None else lam.shape[-1]
+        lp = None if lam is None else lam.data_ptr()
+        need = la.la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, norm, nl, la.LA_BF16)
         assert need > 0
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         ref = torch.empty_like(v)
         got = torch.full_like(v, float("nan"))
         rc = la.la_chunked_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ref.data_ptr(), B, H, L,
-                               dk, dv, C, fm, 0, lam.data_ptr(), nl, la.LA_BF16, ws.data_ptr(),
-                               need, stream)
+                               dk, dv, C, fm, norm, lp, nl, la.LA_BF16, ws.data_ptr(), need, stream)
         assert rc == la.LA_OK, la.la_status_string(rc)
         rc = la.la_chunked_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), got.data_ptr(),
-                                       B, H, L, dk, dv, C, fm, 0, lam.data_ptr(), nl,
-                                       la.LA_BF16, stream)
+                                       B, H, L, dk, dv, C, fm, norm, lp, nl, la.LA_BF16, stream)
         assert rc == la.LA_OK, la.la_status_string(rc)
         torch.cuda.synchronize()
         assert la.la_last_device_status(stream) == la.LA_OK
