@@ -8,7 +8,8 @@
 // beside it: z_c = sum of phi(k) over the chunks before c, kept in fp32.
 //
 // GB300 mapping (everything stays on chip except q, k, v in and out):
-//   * warp 0       TMA producer: Q_c, K_c, V_c tiles (128-byte swizzled) into a 3-stage ring.
+//   * warp 0       TMA producer: Q_c, K_c, V_c tiles (128-byte swizzled) into a ring of four
+//                  stages (three where four do not fit in shared memory).
 //   * warp 1       one thread issues every tcgen05.mma; the warp owns the TMEM allocation.
 //   * warps 2-4, 6-8, 10-11 (not on the MMA issuer's sub-partition)
 //                  feature map phi applied in place in shared memory; with the normaliser,
@@ -17,10 +18,10 @@
 //                  scores MMA also returns phi(q_t).z_c in fp32.
 //   * warps 12-15  scores -> P: read the scores row from TMEM, causal mask (diagonal kept),
 //                  fp32 row sum, 1 / (phi(q_t).z_c + row sum) for the normaliser, bf16 P
-//                  into shared memory; after each state update, S^T (fp32 in TMEM) -> its
-//                  bf16 copy in TMEM.
-//   * warps 16-19  output epilogue: O^T from TMEM, normaliser, bf16, swizzled shared-memory
-//                  tile, TMA store.
+//                  into one of two shared-memory P tiles; after each state update, S^T (fp32
+//                  in TMEM) -> its bf16 copy in TMEM.
+//   * warps 16-19  output epilogue: O^T from TMEM, normaliser, bf16 rows stored from
+//                  registers (a warp writes 64 contiguous bytes of a row per store).
 // With dv = 64 the dv-row accumulators use the M = 64 lane layout (row m in lane
 // m%16 + 32*(m/16)), which is also where an M = 64 A operand is read from in TMEM.
 // TMEM (512 columns): S^T fp32 [dv lanes x D] | S^T bf16 [dv x D/2] | O^T x2 [dv x C] |
@@ -38,6 +39,11 @@
 //   inter   O^T_j = bf16(S_j)^T phi(Q_j)^T       M=dv  N=CH     K=D   per chunk j (A in TMEM)
 //   state   S^T  += V_j^T phi(K_j)               M=dv  N=D      K=CH  per chunk j
 //   intra   O^T  += V_T^T P_T^T                  M=dv  N=T      K=T   once per tile
+// The MMA thread issues, per tile c: inter and state of c, the scores of c+1, the intra product
+// of c (with four chunks per tile, the scores of c first).  The P warps then find the next
+// scores ready when they finish a tile, so the chain scores -> P -> intra does not wait for
+// each intra product to be issued; the fourth ring stage absorbs the longer hold of a stage
+// (its stage is released when the intra product completes, after the next tile's phi).
 //
 // Decay (the Retention update S_t = gamma S_{t-1} + phi(k_t) v_t^T of "Linear Attention /
 // Performerの理論と実装", one chunk per tile): with i, j the rows of the chunk,
@@ -91,11 +97,11 @@ __device__ __forceinline__ int phi_rank(int warp)
     if (warp < 2 || warp >= 12 || (warp & 3) == 1) return -1;
     return warp - 2 - (warp > 5) - (warp > 9);
 }
-constexpr int TC_STAGES = 3;
 constexpr int TC_DEN = 4;  // ring of per-chunk 1/den vectors
 
 struct TcArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
+    void *out;   // [BH][L][DV], bf16 (fp32 in the fp32-output mode); rows stored from registers
     int L, nch;  // nch: number of 64-row tiles of a head
     int nsub;    // number of chunks of CH rows of a head
     // Sequence split: a head's tiles are cut into segments of seg_tiles tiles, one CTA each.
@@ -133,18 +139,24 @@ struct TcLayout {
     static constexpr int STAGE_BYTES = Q_BYTES + K_BYTES + V_BYTES;
     static constexpr int STAGE_TX = Q_BYTES + C * D * 2 + V_BYTES;  // bytes TMA delivers
     static constexpr int P_BYTES = C * C * 2;
-    static constexpr int O_BYTES = C * DV * (F32O ? 4 : 2);
-    // P and the output tile are single-buffered: MMAs complete in issue order, so the
-    // scores of chunk c+1 finishing implies the intra product of chunk c has read P.
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_P = TC_STAGES * STAGE_BYTES;
-    // fp32-output mode: P as a bf16 hi tile and a lo tile (P - hi)
-    static constexpr int OFF_O = OFF_P + (F32O ? 2 : 1) * P_BYTES;
-    static constexpr int OFF_F32 = OFF_O + O_BYTES;
+    // P is double-buffered (tile c in buffer c & 1): the scores of tile c+1 are issued before
+    // the intra product of tile c, and the commit after them also covers the intra product
+    // of tile c-1, the last reader of buffer (c+1) & 1.  fp32-output mode: each buffer holds
+    // a bf16 hi tile and a lo tile (P - hi).
+    static constexpr int P_SET = (F32O ? 2 : 1) * P_BYTES;
     // floats: rden[TC_DEN][C], z[D], zpart[TC_FWARPS][D]
     static constexpr int N_F32 = TC_DEN * C + D + TC_FWARPS * D;
-    static constexpr int OFF_BAR = OFF_F32 + ((N_F32 * 4 + 15) / 16) * 16;
-    static constexpr int N_BAR = 3 * TC_STAGES + 2 * 4 + 2 * TC_DEN + 3;
+    static constexpr int F32_BYTES = ((N_F32 * 4 + 15) / 16) * 16;
+    // everything but the stage ring: P, floats, barriers (at most 4 stages), misc, slack for
+    // the 1024-byte alignment of the swizzled tiles
+    static constexpr int FIXED = 2 * P_SET + F32_BYTES + (3 * 4 + 2 * 4 + 2 * TC_DEN + 3) * 8 + 16 + 1024;
+    // the TMA ring: four stages where they fit in shared memory, else three
+    static constexpr int STAGES = (4 * STAGE_BYTES + FIXED <= 232448) ? 4 : 3;
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_P = STAGES * STAGE_BYTES;
+    static constexpr int OFF_F32 = OFF_P + 2 * P_SET;
+    static constexpr int OFF_BAR = OFF_F32 + F32_BYTES;
+    static constexpr int N_BAR = 3 * STAGES + 2 * 4 + 2 * TC_DEN + 3;
     static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -178,6 +190,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     static_assert(!DK || CH == C, "decay: one chunk per tile");
     static_assert(!FO || (FM == LA_FM_IDENTITY && !NORM), "fp32 output: identity features, no normaliser");
     using Lay = TcLayout<D, DV, C, NORM, FO>;
+    constexpr int ST = Lay::STAGES;  // TMA ring depth
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles (offset taken in the shared window)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -187,9 +200,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     float *zpart = zs + D;               // [TC_FWARPS][D]
     uint64_t *bars = (uint64_t *)(sm + Lay::OFF_BAR);
     uint64_t *full = bars;                           // [S] TMA -> feature map
-    uint64_t *phi_ready = full + TC_STAGES;          // [S] feature map -> MMA
-    uint64_t *stage_free = phi_ready + TC_STAGES;    // [S] MMA -> TMA
-    uint64_t *scores_done = stage_free + TC_STAGES;  // [2]
+    uint64_t *phi_ready = full + ST;          // [S] feature map -> MMA
+    uint64_t *stage_free = phi_ready + ST;    // [S] MMA -> TMA
+    uint64_t *scores_done = stage_free + ST;  // [2]
     uint64_t *p_ready = scores_done + 2;             // [2]
     uint64_t *o_done = p_ready + 2;                  // [2]
     uint64_t *o_free = o_done + 2;                   // [2]
@@ -214,11 +227,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
     auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
     auto stage_v = [&](int s) { return stage_k(s) + Lay::K_BYTES; };
-    uint8_t *const p_tile = sm + Lay::OFF_P;
-    uint8_t *const o_tile = sm + Lay::OFF_O;
+    uint8_t *const p_tile = sm + Lay::OFF_P;  // P buffer b at p_tile + b * Lay::P_SET
 
     if (tid == 0) {
-        for (int i = 0; i < TC_STAGES; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&phi_ready[i], 1);
             mbar_init(&stage_free[i], 1);
@@ -241,7 +253,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     }
     if (NORM) {
         // the z rows of every stage's K tile: rows C, C+1 rewritten per chunk, the rest zero
-        for (int e = tid; e < TC_STAGES * (D / 64) * 8 * 8; e += TC_THREADS) {
+        for (int e = tid; e < ST * (D / 64) * 8 * 8; e += TC_THREADS) {
             const int st = e / ((D / 64) * 64), r = e % ((D / 64) * 64);
             const int kb = r / 64, row = C + (r % 64) / 8, chn = r % 8;
             *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
@@ -259,9 +271,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     if (DK && !NORM)
         for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
     if (CH == C)
-        // P rows 0-31, columns 32-63: always zero (causal mask), written once (both tiles
-        // in the fp32-output mode)
-        for (int e = tid; e < (FO ? 2 : 1) * 32 * 4; e += TC_THREADS) {
+        // P rows 0-31, columns 32-63: always zero (causal mask), written once in every P tile
+        // (both buffers; hi and lo tiles in the fp32-output mode)
+        for (int e = tid; e < 2 * (FO ? 2 : 1) * 32 * 4; e += TC_THREADS) {
             const int t = (e >> 2) & 31, chn = 4 + (e & 3);
             *(uint4 *)(p_tile + (e >> 7) * Lay::P_BYTES + t * 128 + ((chn ^ (t & 7)) << 4)) =
                 make_uint4(0, 0, 0, 0);
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     if (NC && NORM && !totals) {
         // non-causal main pass: z of the whole sequence as a bf16 hi / lo pair in key rows C and
         // C+1 of every stage (no keys are loaded in this pass, so they stay)
-        for (int e = tid; e < TC_STAGES * (D / 8) * 2; e += TC_THREADS) {
+        for (int e = tid; e < ST * (D / 8) * 2; e += TC_THREADS) {
             const int st = e / ((D / 8) * 2), zr = e & 1, cg = (e >> 1) % (D / 8);
             const int zkb = cg >> 3, zch = cg & 7, row = C + zr;
             uint32_t pk[4];
@@ -353,8 +365,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // the non-causal main pass reads the whole sequence's state: only Q is loaded
             const bool qonly = NC && !totals;
             for (int c = 0; c < nch; ++c) {
-                const int s = c % TC_STAGES;
-                if (c >= TC_STAGES && !wait_phase(&stage_free[s], ((c / TC_STAGES) - 1) & 1, ctl))
+                const int s = c % ST;
+                if (c >= ST && !wait_phase(&stage_free[s], ((c / ST) - 1) & 1, ctl))
                     break;
                 const int row = (tile0 + c) * C;
                 mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES
@@ -370,10 +382,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 issued = c + 1;
             }
             // never leave the CTA with loads in flight: wait for every issued stage to land
-            for (int c = (issued > TC_STAGES ? issued - TC_STAGES : 0); c < issued; ++c) {
-                const int s = c % TC_STAGES;
+            for (int c = (issued > ST ? issued - ST : 0); c < issued; ++c) {
+                const int s = c % ST;
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_sleep(&full[s], (c / TC_STAGES) & 1, 200000u))
+                while (!mbar_try_sleep(&full[s], (c / ST) & 1, 200000u))
                     if (globaltimer() - t0 > ctl.timeout_ns) break;
             }
         }
@@ -389,9 +401,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             if (totals) {
                 // totals pass: only the state, over whole tiles
                 for (int c = 0; c < nch; ++c) {
-                    const int s = c % TC_STAGES;
+                    const int s = c % ST;
                     uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM && !DK) ? &full[s] : &phi_ready[s];
-                    if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) {
+                    if (!wait_phase(ph, (c / ST) & 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -413,9 +425,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 constexpr uint32_t ID_Z = idesc_bf16_f32(C, 8, 0, 0);  // rows C .. C+7 of a block
                 auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
                 for (int c = 0; ok && c < nch; ++c) {
-                    const int s = c % TC_STAGES, b = c & 1;
+                    const int s = c % ST, b = c & 1;
                     uint64_t *ph = (FM == LA_FM_IDENTITY) ? &full[s] : &phi_ready[s];
-                    if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
+                    if (!wait_phase(ph, (c / ST) & 1, ctl)) break;
                     // scores buffer b: the P warps are done with tile c-2
                     if (NORM && c >= 2 && !wait_phase(&p_ready[b], ((c >> 1) - 1) & 1, ctl)) break;
                     if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
@@ -440,26 +452,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 }
                 ok = false;
             }
-            for (int c = 0; ok && c < nch; ++c) {
-                const int s = c % TC_STAGES, b = c & 1;
+            // Software-pipelined order (one or two chunks per tile): inter and state of tile
+            // c, then the scores of tile c+1, then the intra product of tile c.  The P warps
+            // find the scores of tile c+1 complete when they finish tile c, so the loop-carried
+            // chain scores -> P -> intra no longer waits for each intra product to be issued.
+            // With four chunks per tile the chain of state updates and their bf16 copies binds
+            // instead, and the scores of tile c go first in its own iteration.
+            constexpr bool EARLY = NSUB <= 2;
+            auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+            auto issue_scores = [&](int c) -> bool {
+                const int s = c % ST, b = c & 1;
                 uint64_t *ph = (FM == LA_FM_IDENTITY && !NORM && !DK) ? &full[s] : &phi_ready[s];
-                if (!wait_phase(ph, (c / TC_STAGES) & 1, ctl)) break;
+                if (!wait_phase(ph, (c / ST) & 1, ctl)) return false;
                 // Scores buffer b was last read by the P warps for tile c-2.  No wait is
-                // needed: this thread already waited for p_ready of tile c-1, which the P
-                // warps raise only after finishing tile c-2 (in order), and each P warp fences
-                // its TMEM loads (fence::before_thread_sync) before the barrier that precedes
-                // that arrive.
+                // needed: this thread already waited for p_ready of tile c-2 (before its
+                // intra product), which the P warps raise after fencing their TMEM loads
+                // (fence::before_thread_sync before the barrier that precedes the arrive).
                 tc_fence_after();
-                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
-                               va = smem_u32(stage_v(s)), pa = smem_u32(p_tile);
-                const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE, tO = tmem + Lay::T_O + b * C;
                 // Descriptors: one per operand and tile; a constant byte offset goes into the
                 // address field (addr >> 4), which never carries since shared addresses stay
                 // below 256 KB.  This keeps the issuing thread's work per MMA to one add.
-                const uint64_t dQ = smem_desc(qa, 16, 1024), dK = smem_desc(ka, 16, 1024);
-                const uint64_t dVmn = smem_desc(va, C * 128, 1024), dKmn = smem_desc(ka, Lay::K_BLK, 1024);
-                const uint64_t dP = smem_desc(pa, 16, 1024);
-                auto dadd = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+                const uint64_t dQ = smem_desc(smem_u32(stage_q(s)), 16, 1024);
+                const uint64_t dK = smem_desc(smem_u32(stage_k(s)), 16, 1024);
+                const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE;
                 // scores of the tile: phi(Q) [phi(K); z]^T, both K-major, K = D in steps of 16
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -468,6 +483,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     mma_ss(tA, dadd(dQ, qo), dadd(dK, ko), ID_SC, ks > 0);
                 }
                 mma_commit(&scores_done[b]);
+                return true;
+            };
+            if (EARLY && ok && nch > 0) ok = issue_scores(0);
+            for (int c = 0; ok && c < nch; ++c) {
+                const int s = c % ST, b = c & 1;
+                if (!EARLY && !issue_scores(c)) break;
+                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
+                               va = smem_u32(stage_v(s)), pa = smem_u32(p_tile + b * Lay::P_SET);
+                const uint32_t tO = tmem + Lay::T_O + b * C;
+                const uint64_t dQ = smem_desc(qa, 16, 1024);
+                const uint64_t dVmn = smem_desc(va, C * 128, 1024), dKmn = smem_desc(ka, Lay::K_BLK, 1024);
+                const uint64_t dP = smem_desc(pa, 16, 1024);
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 for (int j = 0; j < NSUB; ++j) {
                     const int g = (tile0 + c) * NSUB + j;  // chunk index in the sequence
@@ -501,6 +528,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     }
                 }
                 if (!ok) break;
+                if (EARLY && c + 1 < nch && !issue_scores(c + 1)) break;
                 if (!wait_phase(&p_ready[b], (c >> 1) & 1, ctl)) break;
                 tc_fence_after();
                 // intra: V^T (MN-major A) x P^T (K-major B) over the tile, K = 64
@@ -546,9 +574,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             for (int n = 0; n < NR; ++n) rowf[n] = DK ? ex2(a.l2g * (float)(C - 1 - rg - n * RG)) : 1.f;
             int pm = 0;  // c mod period
             for (int c = 0; c < nch; ++c, pm = (pm + 1 == a.period) ? 0 : pm + 1) {
-                const int s = c % TC_STAGES;
+                const int s = c % ST;
                 const float chf = DK ? ex2(a.l2g * (float)(totals ? (nch - 1 - c) * C : -C * pm)) : 1.f;
-                if (!group_wait(ft == 0, 1, &full[s], (c / TC_STAGES) & 1, nullptr, 0, false, ctl,
+                if (!group_wait(ft == 0, 1, &full[s], (c / ST) & 1, nullptr, 0, false, ctl,
                                 NF))
                     break;
                 uint4 *qp = (uint4 *)(stage_q(s) + q_swz);
@@ -603,16 +631,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     for (int e = 0; e < 4; ++e) {
                         // elu+1 in bf16x2; the decay scales the bf16 features in fp32
                         if (FM == LA_FM_ELU1) wv[e] = elu1_bf16x2(wv[e]);
-                        float x0 = bf_lo(wv[e]), x1 = bf_hi(wv[e]);
                         if (DK) {
-                            x0 *= rf;
-                            x1 *= rf;
+                            const float x0 = bf_lo(wv[e]) * rf, x1 = bf_hi(wv[e]) * rf;
+                            if (NORM && in_seq) {
+                                colsum[2 * e] += x0;
+                                colsum[2 * e + 1] += x1;
+                            }
+                            wv[e] = pack_bf16x2(x0, x1);
+                        } else if (NORM && in_seq) {
+                            add_bf16x2_to_f32(colsum[2 * e], colsum[2 * e + 1], wv[e]);
                         }
-                        if (NORM && in_seq) {
-                            colsum[2 * e] += x0;
-                            colsum[2 * e + 1] += x1;
-                        }
-                        if (DK) wv[e] = pack_bf16x2(x0, x1);
                     }
                 }
                 if (FM != LA_FM_IDENTITY || DK) {
@@ -747,7 +775,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                             pk[e] = pack_bf16x2(s0 >= tlo ? v0 : 0.f, s1 >= tlo ? v1 : 0.f);
                         }
                     }
-                    uint8_t *prow = p_tile + t * 128;
+                    uint8_t *prow = p_tile + b * Lay::P_SET + t * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int chn = 4 * h + q;
@@ -828,6 +856,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         }
     } else if (warp >= 8 + TC_FWARPS) {
         // ------------------------------------------------------------ output epilogue
+        // Rows go from registers straight to global memory: for each token a warp writes 32
+        // neighbouring output columns (64 contiguous bytes in bf16, 128 in fp32), so no
+        // shared-memory staging tile is needed; rows past L are skipped.
         const int q4 = warp & 3;
         const int ot = tid - 32 * (8 + TC_FWARPS);
         // row j of O^T: lane j (dv = 128), or lane j%16 of quadrant j/16 (dv = 64)
@@ -835,17 +866,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const bool live = (DV == 128) || lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const bool odd = lane & 1;
-        uint8_t *const ob = o_tile + (j >> 6) * C * 128 + (((j & 7) & ~1) << 1);
-        const int jc = (j & 63) >> 3;
         for (int c = 0; c < nch && !totals; ++c) {
             const int b = c & 1, slot = c % TC_DEN;
             if (!group_wait(ot == 0, 3, &o_done[b], (c >> 1) & 1, &den_full[slot], (c / TC_DEN) & 1,
                             NORM, ctl))
                 break;
             tc_fence_after();
-            // the output tile must have been read by the previous chunk's TMA store
-            if (ot == 0 && c >= 1) tma_wait_read_all();
-            named_bar(3, 128);
+            const int row0 = (tile0 + c) * C;
+            const int nrow = min(C, a.L - row0);  // rows of this tile inside the sequence
+            const size_t rbase = (size_t)head * a.L + row0;
             const uint32_t tO = tmem + Lay::T_O + b * C + lane_off;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -857,57 +886,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&o_free[b]);
                 }
-                float rd[32];
-                if (NORM || DK) {
-                    // 1 / den per row, or (decay, no normaliser) gamma^(i+1-C) gamma^(C m)
-                    const float4 *rp = (const float4 *)(rden + (NORM ? slot * C : 0) + 32 * h);
-                    const float mf = (DK && !NORM) ? ex2(a.l2g * (float)(C * (c % a.period))) : 1.f;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 v = rp[q];
-                        rd[4 * q] = mf * v.x; rd[4 * q + 1] = mf * v.y;
-                        rd[4 * q + 2] = mf * v.z; rd[4 * q + 3] = mf * v.w;
-                    }
-                }
+                // 1 / den per row, or (decay, no normaliser) gamma^(i+1-C) gamma^(C m), read
+                // per pair of rows from shared memory
+                const float2 *rp = (const float2 *)(rden + (NORM ? slot * C : 0) + 32 * h);
+                const float mf = (DK && !NORM) ? ex2(a.l2g * (float)(C * (c % a.period))) : 1.f;
                 if constexpr (FO) {
-                    // fp32 rows: column j of token tt in 32-column box j / 32, 128-byte swizzle
-                    uint8_t *const fb = o_tile + (j >> 5) * C * 128 + ((j & 3) << 2);
+                    // fp32 rows: column j of token tt
+                    float *const o = (float *)a.out + rbase * DV + j;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int tt = 32 * h + u;
-                        if (live) *(uint32_t *)(fb + tt * 128 + ((((j & 31) >> 2) ^ (tt & 7)) << 4)) = r[u];
+                        if (live && tt < nrow) o[(size_t)tt * DV] = __uint_as_float(r[u]);
                     }
                 } else {
                     // Lanes j, j^1 swap one value per pair of rows so that each writes two
                     // neighbouring columns of one row as a single 32-bit word.
+                    uint32_t *const o = (uint32_t *)((__nv_bfloat16 *)a.out + rbase * DV + (j & ~1));
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
                         if (NORM || DK) {
-                            a0 *= rd[2 * u];
-                            a1 *= rd[2 * u + 1];
+                            const float2 f = rp[u];
+                            a0 *= mf * f.x;
+                            a1 *= mf * f.y;
                         }
                         const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
                         const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
                         const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-                        if (live) *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
+                        if (live && tt < nrow) o[(size_t)tt * (DV / 2)] = wv;
                     }
                 }
             }
-            fence_async_smem();
-            named_bar(3, 128);
-            if (ot == 0) {
-                if (FO)
-                    for (int jb = 0; jb < DV / 32; ++jb)
-                        tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 32, (tile0 + c) * C, head);
-                else
-                    for (int jb = 0; jb < DV / 64; ++jb)
-                        tma_store_3d(&a.tm_o, o_tile + jb * C * 128, jb * 64, (tile0 + c) * C, head);
-                tma_commit_group();
-                if (NORM) mbar_arrive(&den_empty[slot]);
+            if (NORM) {
+                // every thread has read this chunk's 1/den
+                named_bar(3, 128);
+                if (ot == 0) mbar_arrive(&den_empty[slot]);
             }
         }
-        if (ot == 0) tma_wait_all();
     }
 
     tc_fence_before();
@@ -941,11 +956,10 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     TcArgs a;
     memset(&a, 0, sizeof(a));
     const int BH = p.B * p.H;
-    const bool fo = mode == TC_F32OUT;
     if (!make_map(&a.tm_q, p.q, BH, p.L, p.dk, C) || !make_map(&a.tm_k, p.k, BH, p.L, p.dk, C) ||
-        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, C) ||
-        !(fo ? make_map_f32(&a.tm_o, p.out, BH, p.L, p.dv, C) : make_map(&a.tm_o, p.out, BH, p.L, p.dv, C)))
+        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, C))
         return LA_ERR_CUDA;
+    a.out = p.out;
     a.L = p.L;
     a.nch = (p.L + C - 1) / C;
     a.nsub = (p.L + CH - 1) / CH;

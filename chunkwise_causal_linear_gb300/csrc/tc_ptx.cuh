@@ -277,6 +277,15 @@ LA_DEV uint32_t elu1_bf16x2(uint32_t x)
     return r;
 }
 
+// fp32 column sums of bf16 pairs: c0 += lo half of w, c1 += hi half (mixed-precision adds,
+// no separate unpacking)
+LA_DEV void add_bf16x2_to_f32(float &c0, float &c1, uint32_t w)
+{
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.bf16 %0, l, %0; add.rn.f32.bf16 %1, h, %1; }"
+        : "+f"(c0), "+f"(c1)
+        : "r"(w));
+}
+
 LA_DEV uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;

@@ -457,10 +457,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         if (PHI) wv[e] = elu1_bf16x2(wv[e]);
-                        if (NORM) {
-                            colsum[2 * e] += bf_lo(wv[e]);
-                            colsum[2 * e + 1] += bf_hi(wv[e]);
-                        }
+                        if (NORM) add_bf16x2_to_f32(colsum[2 * e], colsum[2 * e + 1], wv[e]);
                     }
                 }
                 if (PHI) {
