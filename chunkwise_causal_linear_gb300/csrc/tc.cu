@@ -251,23 +251,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (NORM) {
-        // the z rows of every stage's K tile: rows C, C+1 rewritten per chunk, the rest zero
-        for (int e = tid; e < ST * (D / 64) * 8 * 8; e += TC_THREADS) {
-            const int st = e / ((D / 64) * 64), r = e % ((D / 64) * 64);
-            const int kb = r / 64, row = C + (r % 64) / 8, chn = r % 8;
-            *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
+    // Segments after the first start from the (decay-weighted) sum of the earlier segments'
+    // totals, plus a given initial state.  Every thread takes part: the sums go through an
+    // fp32 scratch in the stage ring (unused until the producer starts), with independent,
+    // coalesced loads, so the start-up does not wait on one serial chain of global loads.
+    const int nprev = totals ? 0 : (NC ? a.nseg_all : seg);
+    const bool has_prefix = !totals && (nprev > 0 || a.S0 != nullptr);
+    if (totals) pdl_trigger();  // the main pass may be scheduled now
+    else pdl_wait();            // the totals pass (if any) has completed
+    constexpr int SCR_LD = D + 4;  // scratch row stride in floats (padding against bank conflicts)
+    float *const scr = (float *)(sm + Lay::OFF_STAGE);
+    static_assert(DV * (D + 4) * 4 <= ST * Lay::STAGE_BYTES, "prefix scratch fits the stage ring");
+    if (has_prefix) {
+        for (int e4 = tid; e4 < DV * D / 4; e4 += TC_THREADS) {
+            const int j = e4 / (D / 4), i = 4 * (e4 % (D / 4));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int g = 0; g < nprev; ++g) {
+                const float4 v4 = __ldcg((const float4 *)(a.ws_T + ((size_t)g * a.BH + head) * DV * D) + e4);
+                const float w = seg_w(g);
+                acc.x += w * v4.x; acc.y += w * v4.y; acc.z += w * v4.z; acc.w += w * v4.w;
+            }
+            if (a.S0) {
+                // the given state before row 0 (S[i][j] at S0 + (head D + i) DV + j), decayed
+                // over the rows of the earlier segments
+                const float w = seg_w(-1);
+                const float *s0 = a.S0 + ((size_t)head * D + i) * DV + j;
+                acc.x += w * s0[0]; acc.y += w * s0[DV]; acc.z += w * s0[2 * DV]; acc.w += w * s0[3 * DV];
+            }
+            *(float4 *)(scr + j * SCR_LD + i) = acc;
         }
+    }
+    if (NORM)
         for (int i = tid; i < D; i += TC_THREADS) {
             float z0 = 0.f;
             if (!totals) {
-                for (int g = 0; g < (NC ? a.nseg_all : seg); ++g)
-                    z0 += seg_w(g) * a.ws_z[((size_t)g * a.BH + head) * D + i];
+#pragma unroll 4
+                for (int g = 0; g < nprev; ++g) z0 += seg_w(g) * __ldcg(a.ws_z + ((size_t)g * a.BH + head) * D + i);
                 if (a.z0) z0 += seg_w(-1) * a.z0[(size_t)head * D + i];  // the given state
             }
             zs[i] = z0;
         }
-    }
     if (DK && !NORM)
         for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
     if (CH == C)
@@ -283,59 +307,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (NC && NORM && !totals) {
-        // non-causal main pass: z of the whole sequence as a bf16 hi / lo pair in key rows C and
-        // C+1 of every stage (no keys are loaded in this pass, so they stay)
-        for (int e = tid; e < ST * (D / 8) * 2; e += TC_THREADS) {
-            const int st = e / ((D / 8) * 2), zr = e & 1, cg = (e >> 1) % (D / 8);
-            const int zkb = cg >> 3, zch = cg & 7, row = C + zr;
-            uint32_t pk[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float z0 = zs[8 * cg + 2 * u], z1 = zs[8 * cg + 2 * u + 1];
-                const float h0 = __bfloat162float(__float2bfloat16_rn(z0));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(z1));
-                pk[u] = zr ? pack_bf16x2(z0 - h0, z1 - h1) : pack_bf16x2(h0, h1);
-            }
-            *(uint4 *)(stage_k(st) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        fence_async_smem();
-    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + Lay::T_S, tSB = tmem + Lay::T_SB, tSL = tmem + Lay::T_SL;
     // fp32-output mode: bf16 hi / lo split of fp32 values (x = hi + lo to ~2^-16 relative)
     auto lo_of = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
     if (warp >= 4 + TC_FWARPS && warp < 8 + TC_FWARPS) {
-        // the state and its bf16 copy start at the sum of the earlier segments' totals (zero
-        // for the first segment and for the totals pass)
+        // the state and its bf16 copy start at the prefix in the scratch (zero for the first
+        // segment and for the totals pass)
         const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
         const int jr = (DV == 128) ? 32 * (warp & 3) + lane : 16 * (warp & 3) + (lane & 15);
         const bool live = (DV == 128) || lane < 16;
-        const int nprev = totals ? 0 : (NC ? a.nseg_all : seg);
 #pragma unroll 1
         for (int col = 0; col < D; col += 16) {
             float acc[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-            if (live)
-                for (int g = 0; g < nprev; ++g) {
-                    const float4 *src = (const float4 *)(a.ws_T + (((size_t)g * a.BH + head) * DV + jr) * D + col);
-                    const float w = seg_w(g);
+            if (live && has_prefix)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 v4 = src[q];
-                        acc[4 * q] += w * v4.x; acc[4 * q + 1] += w * v4.y;
-                        acc[4 * q + 2] += w * v4.z; acc[4 * q + 3] += w * v4.w;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v4 = *(const float4 *)(scr + jr * SCR_LD + col + 4 * q);
+                    acc[4 * q] = v4.x; acc[4 * q + 1] = v4.y; acc[4 * q + 2] = v4.z; acc[4 * q + 3] = v4.w;
                 }
-            if (live && a.S0 && !totals) {
-                // the given state before row 0 (S[i][j] at S0 + (head D + i) DV + j), decayed
-                // over the rows of the earlier segments
-                const float w = seg_w(-1);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) acc[e] += w * a.S0[((size_t)head * D + col + e) * DV + jr];
-            }
             if (DK)  // the first chunk reads gamma^C S and accumulates onto it
 #pragma unroll
                 for (int e = 0; e < 16; ++e) acc[e] *= gC;
@@ -354,6 +346,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         }
         tmem_wait_st();
     }
+    // the scratch has been read: the stage ring's z rows can now be written
+    __syncthreads();
+    if (NORM) {
+        // the z rows of every stage's K tile: rows C, C+1 rewritten per chunk, the rest zero
+        for (int e = tid; e < ST * (D / 64) * 8 * 8; e += TC_THREADS) {
+            const int st = e / ((D / 64) * 64), r = e % ((D / 64) * 64);
+            const int kb = r / 64, row = C + (r % 64) / 8, chn = r % 8;
+            *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (NC && NORM && !totals) {
+        // non-causal main pass: z of the whole sequence as a bf16 hi / lo pair in key rows C and
+        // C+1 of every stage (no keys are loaded in this pass, so they stay); written after the
+        // zero rows above
+        __syncthreads();
+        for (int e = tid; e < ST * (D / 8) * 2; e += TC_THREADS) {
+            const int st = e / ((D / 8) * 2), zr = e & 1, cg = (e >> 1) % (D / 8);
+            const int zkb = cg >> 3, zch = cg & 7, row = C + zr;
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float z0 = zs[8 * cg + 2 * u], z1 = zs[8 * cg + 2 * u + 1];
+                const float h0 = __bfloat162float(__float2bfloat16_rn(z0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(z1));
+                pk[u] = zr ? pack_bf16x2(z0 - h0, z1 - h1) : pack_bf16x2(h0, h1);
+            }
+            *(uint4 *)(stage_k(st) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1015,6 +1038,11 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     }
     a.totals = 0;
     a.grid_seg = nseg;
+    if (ntot > 0) {
+        // starts its set-up while the totals pass drains
+        if (launch_dependent(kern, BH * nseg, TC_THREADS, alloc, p.stream, a) != cudaSuccess) return LA_ERR_CUDA;
+        return LA_OK;
+    }
     kern<<<BH * nseg, TC_THREADS, alloc, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }

@@ -52,6 +52,14 @@ __device__ __forceinline__ bool group_wait(bool leader, int bar_id, uint64_t *b1
     return named_bar_and(bar_id, nthreads, ok);
 }
 
+// Programmatic dependent launch.  A pass that produces segment totals lets the pass that
+// reads them be scheduled early (its CTAs start their set-up on free SMs as soon as every
+// producer CTA has signalled); the reader waits for the producer grid to complete, with its
+// memory visible, before it touches the totals.  Both are no-ops for a launch without the
+// attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // bf16 (raw 16-bit) -> fp32 for the two halves of a 32-bit word
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -106,6 +114,26 @@ inline bool make_map_f32(CUtensorMap *m, const void *ptr, int BH, int L, int d, 
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches `kern` on `stream` with programmatic stream serialization: it may start while the
+// kernel before it in the stream is still running, and must call pdl_wait() before reading
+// what that kernel writes.
+template <typename Kern, typename Args>
+inline cudaError_t launch_dependent(Kern kern, int grid, int block, int smem, cudaStream_t stream,
+                                    const Args &args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 // Segments per head for a sequence of `tiles` 64-row tiles: split when the heads alone leave

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
     const int nch = min(a.seg_tiles, a.nch - tile0);
     const bool totals = a.totals != 0;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
+    if (totals) pdl_trigger();  // the main pass may be scheduled now
+    else pdl_wait();            // the totals pass (if any) has completed
     auto stage_q = [&](int s) { return sm + FV_STAGE + s * FV_STAGE_BYTES; };
     auto stage_k = [&](int s) { return stage_q(s) + FV_TILE; };
     auto stage_v = [&](int s) { return stage_k(s) + FV_TILE; };
@@ -604,6 +606,11 @@ int launch_fv(const Problem &p, int num_sms, bool noncausal = false)
     }
     a.totals = 0;
     a.grid_seg = nseg;
+    if (ntot > 0) {
+        // starts while the totals pass drains
+        if (launch_dependent(kern, BH * nseg, FV_THREADS, FV_ALLOC, p.stream, a) != cudaSuccess) return LA_ERR_CUDA;
+        return LA_OK;
+    }
     kern<<<BH * nseg, FV_THREADS, FV_ALLOC, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     const int nst = totals ? LL_STAGES_TOT : LL_STAGES_MAIN;
     const int sbytes = totals ? 2 * LL_TILE : 4 * LL_TILE;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
+    if (totals) pdl_trigger();  // the main pass may be scheduled now
+    else pdl_wait();            // the totals pass (if any) has completed
     // stage layout: main [Q | K | V | lambda], totals [K | V]
     auto stage_q = [&](int s) { return sm + s * sbytes; };
     auto stage_k = [&](int s) { return sm + s * sbytes + (totals ? 0 : LL_TILE); };
@@ -605,6 +607,12 @@ int tcl_launch(const Problem &p, int num_sms)
     }
     a.totals = 0;
     a.grid_seg = a.nseg;
+    if (a.nseg > 1) {
+        // starts while the totals pass drains
+        if (launch_dependent(tc_loglinear_kernel, BH * a.nseg, LL_THREADS, a.lay.alloc, p.stream, a) != cudaSuccess)
+            return LA_ERR_CUDA;
+        return LA_OK;
+    }
     tc_loglinear_kernel<<<BH * a.nseg, LL_THREADS, a.lay.alloc, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }

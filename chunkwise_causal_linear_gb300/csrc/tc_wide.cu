@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
     const int nt = min(a.seg_tiles, a.nch - tile0);   // tiles of this CTA
     const bool totals = a.totals != 0;
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
+    if (totals) pdl_trigger();  // the main pass may be scheduled now
+    else pdl_wait();            // the totals pass (if any) has completed
 
     auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
     auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
@@ -752,6 +754,11 @@ int launch_w(const Problem &p, int num_sms)
     }
     a.totals = 0;
     a.grid_seg = nseg;
+    if (nseg > 1) {
+        // starts while the totals pass drains
+        if (launch_dependent(kern, BH * nseg, TW_THREADS, Lay::ALLOC, p.stream, a) != cudaSuccess) return LA_ERR_CUDA;
+        return LA_OK;
+    }
     kern<<<BH * nseg, TW_THREADS, Lay::ALLOC, p.stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
