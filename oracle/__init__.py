@@ -73,6 +73,9 @@ def lib():
             L.orc_backward_features.argtypes = [_dp, _dp, _dp, _dp, c_long, c_int, c_int, c_int,
                                                 ctypes.c_double, _dp, _dp, _dp]
             L.orc_phi_grad.argtypes = [_dp, c_long, c_int, c_int, _dp, c_int, _dp, _dp]
+            L.orc_backward_features_ll.argtypes = [_dp, _dp, _dp, _dp, _dp, c_int, c_long, c_int,
+                                                   c_int, c_int, _dp, _dp, _dp]
+            L.orc_backward_features_ll.restype = c_int
             for name in ("orc_state_flops", "orc_score_flops", "orc_total_flops"):
                 getattr(L, name).argtypes = [c_ll, c_ll, c_ll]
                 getattr(L, name).restype = c_ll
@@ -225,13 +228,24 @@ def decay_scores_first(fq, fk, v, gamma, normalize=False, rows=None):
 _FM_CODE = {"identity": 0, "elu1": 1, "favor": 2}
 
 
-def backward_features(fq, fk, v, dout, normalize=False, gamma=None):
+def backward_features(fq, fk, v, dout, normalize=False, gamma=None, lam=None):
     """Gradients (dphi(q), dphi(k), dv) of the causal output, by the chain rule on the plain
-    definition (gamma: Retention decay, None for none)."""
+    definition (gamma: Retention decay, None for none; lam [L, NL]: the log-linear level
+    weights of each query row, None for none)."""
     fq, fk, v, dout = _c(fq), _c(fk), _c(v), _c(dout)
     L, D = fq.shape
     dv = v.shape[1]
     dfq, dfk, dvo = np.empty((L, D)), np.empty((L, D)), np.empty((L, dv))
+    if lam is not None:
+        if gamma is not None:
+            raise ValueError("the decay is defined for the plain causal mask only")
+        lam = _c(lam)
+        rc = lib().orc_backward_features_ll(_p(fq), _p(fk), _p(v), _p(dout), _p(lam),
+                                            lam.shape[1], L, D, dv, int(normalize), _p(dfq),
+                                            _p(dfk), _p(dvo))
+        if rc != 0:
+            raise ValueError("level weights have too few levels for this sequence length")
+        return dfq, dfk, dvo
     lib().orc_backward_features(_p(fq), _p(fk), _p(v), _p(dout), L, D, dv, int(normalize),
                                 -1.0 if gamma is None else float(gamma), _p(dfq), _p(dfk),
                                 _p(dvo))
@@ -249,21 +263,24 @@ def phi_grad(x, dphi, kind, omega=None):
     return dx
 
 
-def head_backward(q, k, v, dout, fm="identity", omega=None, normalize=False, gamma=None):
+def head_backward(q, k, v, dout, fm="identity", omega=None, normalize=False, gamma=None,
+                  lam=None):
     """(dq, dk, dv) of one head from raw q, k [L, dk], v, dout [L, dv] (float64)."""
     fq, fk = phi(q, fm, omega), phi(k, fm, omega)
-    dfq, dfk, dvo = backward_features(fq, fk, v, dout, normalize, gamma)
+    dfq, dfk, dvo = backward_features(fq, fk, v, dout, normalize, gamma, lam)
     return phi_grad(q, dfq, fm, omega), phi_grad(k, dfk, fm, omega), dvo
 
 
 def backward(q, k, v, dout, fm="identity", omega=None, normalize=False, gamma=None,
-             threads=None):
-    """All heads: q, k [n, L, dk], v, dout [n, L, dv] -> (dq, dk, dv) stacked over heads."""
+             threads=None, lam=None):
+    """All heads: q, k [n, L, dk], v, dout [n, L, dv] -> (dq, dk, dv) stacked over heads
+    (lam [n, L, NL]: log-linear level weights)."""
     n = q.shape[0]
     res = [None] * n
 
     def one(h):
-        res[h] = head_backward(q[h], k[h], v[h], dout[h], fm, omega, normalize, gamma)
+        res[h] = head_backward(q[h], k[h], v[h], dout[h], fm, omega, normalize, gamma,
+                               None if lam is None else lam[h])
 
     threads = threads or min(n, os.cpu_count() or 1)
     if threads <= 1 or n == 1:

@@ -428,6 +428,54 @@ void orc_backward_features(const double *fq, const double *fk, const double *v, 
     free(o);
 }
 
+/* The same chain rule under the log-linear mask of [loglinear] slide 17:
+ * M_ts = lambda_t^(l(t,s)), l from orc_fenwick_level, lam [L, nl] per query row t.
+ * With a_ts = phi(q_t).phi(k_s) and the forward out_t = sum_{s<=t} M_ts a_ts v_s (/ den_t,
+ * den_t = sum_{s<=t} M_ts a_ts):
+ *   G_ts = M_ts (dout_t . v_s - dout_t . out_t) / den_t      (normalised; else M_ts dout_t . v_s)
+ *   dphi(q)_t = sum_{s<=t} G_ts phi(k_s),  dphi(k)_s = sum_{t>=s} G_ts phi(q_t),
+ *   dv_s = sum_{t>=s} M_ts a_ts dout_t (/ den_t).
+ * The level weights are data here (their own gradient is not formed).  Returns -1 when nl
+ * does not cover the levels of L rows, else 0. */
+int orc_backward_features_ll(const double *fq, const double *fk, const double *v,
+                             const double *dout, const double *lam, int nl, long L, int D,
+                             int dv, int normalize, double *dfq, double *dfk, double *dvo)
+{
+    if (L > 1 && orc_fenwick_level(L - 1, 0) >= nl) return -1;
+    double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+    memset(dfq, 0, sizeof(double) * (size_t)L * D);
+    memset(dfk, 0, sizeof(double) * (size_t)L * D);
+    memset(dvo, 0, sizeof(double) * (size_t)L * dv);
+    for (long t = 0; t < L; ++t) {
+        const double *qt = fq + t * D, *dt = dout + t * dv, *lt = lam + t * nl;
+        double den = 0.0;
+        for (int j = 0; j < dv; ++j) o[j] = 0.0;
+        for (long s = 0; s <= t; ++s) {
+            double a = lt[orc_fenwick_level(t, s)] * dot(qt, fk + s * D, D);
+            for (int j = 0; j < dv; ++j) o[j] += a * v[s * dv + j];
+            den += a;
+        }
+        double scale = 1.0, dto = 0.0;
+        if (normalize) {
+            for (int j = 0; j < dv; ++j) o[j] /= den;
+            scale = 1.0 / den;
+            dto = dot(dt, o, dv);
+        }
+        for (long s = 0; s <= t; ++s) {
+            double m = lt[orc_fenwick_level(t, s)];
+            double a = m * dot(qt, fk + s * D, D);
+            double g = m * (dot(dt, v + s * dv, dv) - dto) * scale;
+            for (int i = 0; i < D; ++i) {
+                dfq[t * D + i] += g * fk[s * D + i];
+                dfk[s * D + i] += g * qt[i];
+            }
+            for (int j = 0; j < dv; ++j) dvo[s * dv + j] += a * scale * dt[j];
+        }
+    }
+    free(o);
+    return 0;
+}
+
 /* Chain rule through the feature map: dx from dphi for rows x [rows, d].
  *   identity: dx = dphi;
  *   elu+1:    dx = dphi * (x >= 0 ? 1 : e^x)   ([perf] ELU feature map);

@@ -555,3 +555,76 @@ def test_backward_identity_unnormalised_is_masked_matmuls():
     assert np.array_equal(dvv[0], A.T @ dout[0])
     assert np.array_equal(dq[0], G @ k[0])
     assert np.array_equal(dk[0], G.T @ q[0])
+
+
+# backward under the log-linear mask ("論文紹介：Log Linear Attention", slide 17): the chain
+# rule on the masked definition, pinned by finite differences of the Fenwick recurrence
+def _fd_grads_ll(q, k, v, dout, lam, fm, omega, normalize, eps=1e-6):
+    def loss(qq, kk, vv):
+        out = oracle.forward(qq[None], kk[None], vv[None], fm=fm, omega=omega,
+                             normalize=normalize, lam=lam[None], method="recurrence")[0]
+        return float((out * dout).sum())
+    grads = []
+    for which in range(3):
+        base = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(base[which])
+        for idx in np.ndindex(*g.shape):
+            plus = [b.copy() for b in base]
+            minus = [b.copy() for b in base]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            g[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("fm", ["identity", "elu1", "favor"])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_loglinear_backward_matches_finite_differences(fm, normalize):
+    rng = np.random.default_rng(37)
+    L, d, dv = 11, 3, 2                     # levels 0..4, three of them inter-pair levels
+    q, k = rng.normal(size=(L, d)) * 0.7, rng.normal(size=(L, d)) * 0.7
+    if fm == "identity" and normalize:
+        q, k = np.abs(q) + 0.2, np.abs(k) + 0.2
+    v, dout = rng.normal(size=(L, dv)), rng.normal(size=(L, dv))
+    lam = rng.uniform(0.1, 1.0, size=(L, 5))
+    omega = synth.block_orthogonal_gaussian(5, 8, d) if fm == "favor" else None
+    dq, dk, dvv = oracle.backward(q[None], k[None], v[None], dout[None], fm=fm, omega=omega,
+                                  normalize=normalize, lam=lam[None])
+    fq, fk, fv = _fd_grads_ll(q, k, v, dout, lam, fm, omega, normalize)
+    for got, want in ((dq[0], fq), (dk[0], fk), (dvv[0], fv)):
+        assert np.allclose(got, want, rtol=1e-6, atol=1e-7), np.abs(got - want).max()
+
+
+def test_loglinear_backward_all_ones_is_plain_backward():
+    """lambda == 1 is plain linear attention (slide 17), so its gradients are the plain
+    chain rule's."""
+    rng = np.random.default_rng(38)
+    L, d, dv = 40, 4, 3
+    fq, fk = np.abs(rng.normal(size=(L, d))), np.abs(rng.normal(size=(L, d)))
+    v, dout = rng.normal(size=(L, dv)), rng.normal(size=(L, dv))
+    for normalize in (False, True):
+        a = oracle.backward_features(fq, fk, v, dout, normalize, lam=np.ones((L, 7)))
+        b = oracle.backward_features(fq, fk, v, dout, normalize)
+        for x, y in zip(a, b):
+            assert np.allclose(x, y, rtol=1e-13, atol=1e-13)
+
+
+def test_loglinear_backward_level_zero_only_is_diagonal():
+    """Only lambda^(0) nonzero: out_t = lambda_t^(0) (phi(q_t).phi(k_t)) v_t, whose gradients
+    are dphi(q)_t = lambda_t^(0) (dout_t.v_t) phi(k_t), dphi(k)_t = lambda_t^(0) (dout_t.v_t)
+    phi(q_t) and dv_t = lambda_t^(0) (phi(q_t).phi(k_t)) dout_t, exactly on integers."""
+    rng = np.random.default_rng(39)
+    L, d, dv = 33, 4, 3
+    fq = rng.integers(-3, 4, size=(L, d)).astype(float)
+    fk = rng.integers(-3, 4, size=(L, d)).astype(float)
+    v = rng.integers(-3, 4, size=(L, dv)).astype(float)
+    dout = rng.integers(-3, 4, size=(L, dv)).astype(float)
+    lam = np.zeros((L, 7))
+    lam[:, 0] = rng.integers(1, 4, size=L)
+    dfq, dfk, dvo = oracle.backward_features(fq, fk, v, dout, False, lam=lam)
+    g = lam[:, 0] * (dout * v).sum(1)
+    a = lam[:, 0] * (fq * fk).sum(1)
+    assert np.array_equal(dfq, g[:, None] * fk)
+    assert np.array_equal(dfk, g[:, None] * fq)
+    assert np.array_equal(dvo, a[:, None] * dout)
