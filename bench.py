@@ -655,8 +655,9 @@ def run_decode(args):
 
 
 def run_backward(args):
-    """Backward passes: each timed step is one la_chunked_bwd over the whole workload.
-    Algorithmic bytes per step: q, k, v, dout read and dq, dk, dv written once each."""
+    """Backward passes: each timed step is one la_chunked_bwd (la_chunked_bwd_ll for the
+    log-linear mask) over the whole workload.  Algorithmic bytes per step: q, k, v, dout (and
+    the level weights) read and dq, dk, dv written once each."""
     import torch
 
     import chunkwise_causal_linear_gb300 as la
@@ -668,8 +669,7 @@ def run_backward(args):
     for key in ("B", "H", "L"):
         if getattr(args, key):
             w[key] = getattr(args, key)
-    if w.get("loglinear"):
-        raise SystemExit("--op backward: the log-linear mask has no backward pass")
+    ll = bool(w.get("loglinear"))
     B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
     C = args.C if args.C is not None else w["C"]
     gamma = w.get("gamma") or 1.0
@@ -688,7 +688,13 @@ def run_backward(args):
     omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
     fm = la.make_feature_map(w["fm"], w["m"], omega.data_ptr() if omega is not None else 0)
     dtype = la.LA_BF16 if w["dtype"] == "bf16" else la.LA_F32
-    need = la.la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), dtype)
+    lam = None if inp["lam"] is None else torch.from_numpy(inp["lam"]).reshape(B, H, L, -1).cuda()
+    nl = 0 if lam is None else lam.shape[-1]
+    if ll:
+        need = la.la_chunked_bwd_ll_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), nl,
+                                                    dtype)
+    else:
+        need = la.la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, fm, int(w["normalize"]), dtype)
     if need == 0:
         raise SystemExit("--op backward: unsupported sizes")
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
@@ -696,12 +702,18 @@ def run_backward(args):
     stream = torch.cuda.current_stream()
 
     def step():
-        r = la.la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
-                              dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H,
-                              L, dk, dv, C, fm, int(w["normalize"]), float(gamma), dtype,
-                              ws.data_ptr(), need, stream.cuda_stream)
+        if ll:
+            r = la.la_chunked_bwd_ll(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                     dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H, L, dk,
+                                     dv, C, fm, int(w["normalize"]), lam.data_ptr(), nl, dtype,
+                                     ws.data_ptr(), need, stream.cuda_stream)
+        else:
+            r = la.la_chunked_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                  dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H,
+                                  L, dk, dv, C, fm, int(w["normalize"]), float(gamma), dtype,
+                                  ws.data_ptr(), need, stream.cuda_stream)
         if r != la.LA_OK:
-            raise la.LAError(r, "la_chunked_bwd")
+            raise la.LAError(r, "la_chunked_bwd_ll" if ll else "la_chunked_bwd")
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -721,7 +733,7 @@ def run_backward(args):
     clk = clocks.stop()
     t_ms = sum(a.elapsed_time(b) for a, b in evs)
     ms = t_ms / args.steps
-    byts = B * H * L * es * (4 * dk + 3 * dv)
+    byts = B * H * L * (es * (4 * dk + 3 * dv) + 4 * nl)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = byts / (ms / 1e3) / 1e9
@@ -729,9 +741,12 @@ def run_backward(args):
     # prep, chain, and 3 passes (+ 3 for the normaliser, one launch each without a sequence
     # split); the generic route: 2 features, v', prep, 3 passes, 2 chain, 1 cast (+ 1 pass)
     tc_route = (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1") and gamma == 1.0
-                and L >= 128 and dk == dv and dk in (64, 128))
+                and L >= 128 and dk == dv and dk in (64, 128) and not ll)
     launches = (6 + (3 if w["normalize"] else 0)) if tc_route else (10 + (1 if w["normalize"] else 0))
-    line = {"metric": "backward tokens/sec (B·H·L/s, la_chunked_bwd)", "op": "backward",
+    if ll:  # two anti-causal sums of two launches each instead of one pass each
+        launches += 2
+    line = {"metric": "backward tokens/sec (B·H·L/s, %s)" % ("la_chunked_bwd_ll" if ll else "la_chunked_bwd"),
+            "op": "backward",
             "value": B * H * L * args.steps / (t_ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

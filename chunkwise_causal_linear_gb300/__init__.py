@@ -40,7 +40,8 @@ EXPORTS = ("la_chunked_fwd", "la_chunked_fwd_path", "la_chunked_fwd_host",
            "la_last_device_status", "la_status_string", "la_cost_model", "la_decode_step",
            "la_decode_state_elems", "la_noncausal_fwd", "la_noncausal_workspace_bytes",
            "la_decay_fwd", "la_decay_decode_step", "la_decay_workspace_bytes", "la_decay_plan",
-           "la_chunked_bwd", "la_chunked_bwd_workspace_bytes", "la_chunked_state",
+           "la_chunked_bwd", "la_chunked_bwd_workspace_bytes", "la_chunked_bwd_ll",
+           "la_chunked_bwd_ll_workspace_bytes", "la_chunked_state",
            "la_state_combine", "la_chunked_fwd_init", "la_version")
 
 
@@ -125,6 +126,11 @@ def lib() -> ctypes.CDLL:
             L.la_chunked_bwd.restype = i
             L.la_chunked_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i]
             L.la_chunked_bwd_workspace_bytes.restype = sz
+            L.la_chunked_bwd_ll.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, fmp, i, p, i, i,
+                                            p, sz, p, i]
+            L.la_chunked_bwd_ll.restype = i
+            L.la_chunked_bwd_ll_workspace_bytes.argtypes = [i, i, i, i, i, i, fmp, i, i, i]
+            L.la_chunked_bwd_ll_workspace_bytes.restype = sz
             L.la_chunked_state.argtypes = [p, p, p, p, i, i, i, i, i, fmp, f, i, p]
             L.la_chunked_state.restype = i
             L.la_state_combine.argtypes = [p, p, p, p, i, i, i, i, f, p]
@@ -263,6 +269,20 @@ def la_chunked_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map,
     return lib().la_chunked_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C,
                                 _fm(feature_map), normalize, gamma, dtype, workspace,
                                 workspace_bytes, stream, path)
+
+
+def la_chunked_bwd_ll(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C, feature_map, normalize,
+                      level_weights, num_levels, dtype, workspace, workspace_bytes, stream,
+                      path=LA_PATH_AUTO) -> int:
+    return lib().la_chunked_bwd_ll(q, k, v, dout, dq, dk, dv, B, H, L, dk_, dv_, C,
+                                   _fm(feature_map), normalize, level_weights, num_levels, dtype,
+                                   workspace, workspace_bytes, stream, path)
+
+
+def la_chunked_bwd_ll_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, num_levels,
+                                      dtype) -> int:
+    return lib().la_chunked_bwd_ll_workspace_bytes(B, H, L, dk, dv, C, _fm(feature_map),
+                                                   normalize, num_levels, dtype)
 
 
 def la_chunked_bwd_workspace_bytes(B, H, L, dk, dv, C, feature_map, normalize, dtype) -> int:
@@ -429,6 +449,33 @@ def chunked_bwd(q, k, v, dout, C=64, feature_map="identity", omega=None, normali
                         path)
     if rc != LA_OK:
         raise LAError(rc, "la_chunked_bwd")
+    return dq, dk_t, dv_t
+
+
+def chunked_bwd_ll(q, k, v, dout, level_weights, C=64, feature_map="identity", omega=None,
+                   normalize=False, workspace=None, stream=None, path=LA_PATH_AUTO):
+    """(dq, dk, dv) of the log-linear forward (level_weights [B,H,L,NL] fp32 CUDA tensor)."""
+    import torch
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    dtype = _dtype_code(q)
+    nl = level_weights.shape[-1]
+    fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
+                          omega.data_ptr() if omega is not None else 0)
+    need = la_chunked_bwd_ll_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), nl, dtype)
+    if need == 0:
+        raise LAError(LA_ERR_UNSUPPORTED, "la_chunked_bwd_ll_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = la_chunked_bwd_ll(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                           dq.data_ptr(), dk_t.data_ptr(), dv_t.data_ptr(), B, H, L, dk, dv, C, fm,
+                           int(normalize), level_weights.data_ptr(), nl, dtype,
+                           workspace.data_ptr(), need, stream, path)
+    if rc != LA_OK:
+        raise LAError(rc, "la_chunked_bwd_ll")
     return dq, dk_t, dv_t
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblachunked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "simt.cu", "tc.cu", "tc_favor.cu", "tc_loglinear.cu", "tc_wide.cu", "decode.cu", "noncausal.cu", "noalloc.cu", "bwd.cu"]
+SOURCES = ["api.cu", "simt.cu", "tc.cu", "tc_favor.cu", "tc_loglinear.cu", "tc_wide.cu", "decode.cu", "noncausal.cu", "noalloc.cu", "bwd.cu", "bwd_ll.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

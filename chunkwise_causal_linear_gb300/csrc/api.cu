@@ -595,6 +595,55 @@ int la_chunked_bwd(const void *q, const void *k, const void *v, const void *dout
     return bwd_launch(p, sms, path, dout, dq, dk_, dv_);
 }
 
+// ---- backward pass under the log-linear mask (generic route)
+static int bwd_ll_problem(int B, int H, int L, int dk, int dv, int C, const la_feature_map *fm,
+                          int normalize, int num_levels, int dtype, Problem *p)
+{
+    int rc = check_problem(B, H, L, dk, dv, C, fm, normalize, true, num_levels, dtype, p);
+    if (rc != LA_OK) return rc;
+    p->lam = (const float *)1;  // marks the mask for the support check; set to the caller's below
+    if (!bwd_supported(*p)) return LA_ERR_UNSUPPORTED;
+    p->lam = nullptr;
+    return LA_OK;
+}
+
+size_t la_chunked_bwd_ll_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                         const la_feature_map *feature_map, int normalize,
+                                         int num_levels, int dtype)
+{
+    Problem p;
+    if (bwd_ll_problem(B, H, L, dk, dv, C, feature_map, normalize, num_levels, dtype, &p) != LA_OK) return 0;
+    p.lam = (const float *)1;
+    const int sms = device_sms();
+    return bwd_workspace_bytes(p, sms > 0 ? sms : 152);
+}
+
+int la_chunked_bwd_ll(const void *q, const void *k, const void *v, const void *dout, void *dq,
+                      void *dk_, void *dv_, int B, int H, int L, int dk, int dv, int C,
+                      const la_feature_map *feature_map, int normalize, const float *level_weights,
+                      int num_levels, int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                      int path)
+{
+    if (!q || !k || !v || !dout || !dq || !dk_ || !dv_ || !level_weights) return LA_ERR_NULL;
+    Problem p;
+    int rc = bwd_ll_problem(B, H, L, dk, dv, C, feature_map, normalize, num_levels, dtype, &p);
+    if (rc != LA_OK) return rc;
+    if (p.fm == LA_FM_FAVOR && !p.omega) return LA_ERR_NULL;
+    if (path == LA_PATH_TC) return LA_ERR_UNSUPPORTED;
+    if (path != LA_PATH_AUTO && path != LA_PATH_SIMT) return LA_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return LA_ERR_CUDA;
+    p.lam = level_weights;
+    if (!workspace || workspace_bytes < bwd_workspace_bytes(p, sms)) return LA_ERR_WORKSPACE;
+    p.q = q; p.k = k; p.v = v;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes;
+    p.stream = (cudaStream_t)stream;
+    p.err = err_ptr();
+    if (!p.err) return LA_ERR_CUDA;
+    return bwd_launch(p, sms, LA_PATH_SIMT, dout, dq, dk_, dv_);
+}
+
 // ---- carried state: final state of a pass, combining segment states, a pass from a state
 int la_chunked_state(const void *k, const void *v, float *state, float *zstate, int B, int H, int L,
                      int dk, int dv, const la_feature_map *feature_map, float gamma, int dtype,

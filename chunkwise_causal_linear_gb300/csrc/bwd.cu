@@ -46,6 +46,11 @@
 namespace la {
 
 int simt_launch(const Problem &p, int n_inter, int log2C);
+int simt_inter_levels(int L, int C);
+size_t simt_workspace_bytes(int B, int H, int L, int D, int dv, int C, bool loglinear);
+size_t ll_anti_state_floats(int L, int C, int Da, int Wc);
+int ll_anti_pass(int BH, int L, int C, const float *a, const float *b, const float *c,
+                 const float *lam, int nl, float *out, int Da, int Wc, float *W, cudaStream_t st);
 bool tc_supported(const Problem &p, int num_sms);
 int tc_plan(const Problem &p, int num_sms, la_plan_info *info);
 int tc_launch(const Problem &p, int num_sms);
@@ -78,6 +83,31 @@ size_t bwd_floats(long rows, int D, int dv, int normalize, float *base, BwdBufs 
     take(&t->dfk, (size_t)rows * D);
     take(&t->dvf, (size_t)rows * dv);
     return off;
+}
+
+// The log-linear mask's passes use chunks of this many rows (the result does not depend on
+// it), a level-state buffer for the causal passes and the block states of the anti-causal
+// sums (bwd_ll.cu), placed after the per-row buffers.
+constexpr int BW_LL_C = 64;
+
+// level states of the causal passes (bytes, rounded to 256)
+size_t bwd_ll_level_bytes(const Problem &p)
+{
+    const int D = p.D, w = p.dv + (p.normalize ? 1 : 0);
+    size_t lv = simt_workspace_bytes(p.B, p.H, p.L, w, D, BW_LL_C, true);        // dphi(q)
+    if (p.normalize) {
+        const size_t l2 = simt_workspace_bytes(p.B, p.H, p.L, D, w, BW_LL_C, true);  // [num, den]
+        lv = lv > l2 ? lv : l2;
+    }
+    return ((lv + 255) / 256) * 256;
+}
+
+size_t bwd_ll_extra_bytes(const Problem &p)
+{
+    if (!p.lam) return 0;
+    const int w = p.dv + (p.normalize ? 1 : 0);
+    const size_t s1 = ll_anti_state_floats(p.L, BW_LL_C, w, p.D), s2 = ll_anti_state_floats(p.L, BW_LL_C, p.D, p.dv);
+    return bwd_ll_level_bytes(p) + (size_t)p.B * p.H * (s1 > s2 ? s1 : s2) * sizeof(float);
 }
 
 // phi of every row of x [rows, dk] (storage T) into f [rows, D] fp32
@@ -240,6 +270,24 @@ int pass(const Problem &base, const float *q, const float *k, const float *v, fl
     return simt_launch(p, 0, 0);
 }
 
+// one identity-feature, unnormalised causal pass under the log-linear mask (the caller's
+// level weights, query-side as in the forward) on the generic kernel, levels in `lv`
+int pass_ll(const Problem &base, const float *q, const float *k, const float *v, float *out, int dk,
+            int dv, void *lv)
+{
+    Problem p = base;
+    p.q = q; p.k = k; p.v = v; p.out = out;
+    p.dk = dk; p.dv = dv; p.D = dk;
+    p.C = BW_LL_C;
+    p.fm = LA_FM_IDENTITY; p.m = 0; p.omega = nullptr;
+    p.normalize = 0;
+    p.dtype = LA_F32;
+    p.rev = 0;
+    p.workspace = lv;
+    p.workspace_bytes = simt_workspace_bytes(p.B, p.H, p.L, dk, dv, BW_LL_C, true);
+    return simt_launch(p, simt_inter_levels(p.L, BW_LL_C), ilog2(BW_LL_C));
+}
+
 template <typename T>
 int bwd_t(const Problem &p, const void *dout, void *dq, void *dk_, void *dv_)
 {
@@ -254,13 +302,31 @@ int bwd_t(const Problem &p, const void *dout, void *dq, void *dk_, void *dv_)
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     int rc;
     bw_vw_kernel<T><<<1024, 256, 0, st>>>((const T *)p.v, b.vw, rows, p.dv, p.normalize);
-    if (p.normalize && (rc = pass(p, b.fq, b.fk, b.vw, b.nd, D, w, 0)) != LA_OK) return rc;  // [num, den]
-    bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
-                                                 p.normalize);
-    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
-    if ((rc = pass(p, b.dw, b.vw, b.fk, b.dfq, w, D, 0)) != LA_OK) return rc;   // dphi(q)
-    if ((rc = pass(p, b.vw, b.dw, b.fq, b.dfk, w, D, 1)) != LA_OK) return rc;   // dphi(k)
-    if ((rc = pass(p, b.fk, b.fq, b.dn, b.dvf, D, p.dv, 1)) != LA_OK) return rc;  // dv
+    if (p.lam) {
+        // log-linear mask: the causal passes carry the level weights of the query rows; the
+        // anti-causal sums weigh each pair by the later row's level weight (bwd_ll.cu)
+        uint8_t *extra = (uint8_t *)p.workspace + bwd_floats(rows, D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float);
+        void *lv = extra;
+        float *W = (float *)(extra + bwd_ll_level_bytes(p));
+        const int BH = p.B * p.H;
+        if (p.normalize && (rc = pass_ll(p, b.fq, b.fk, b.vw, b.nd, D, w, lv)) != LA_OK) return rc;  // [num, den]
+        bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
+                                                     p.normalize);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+        if ((rc = pass_ll(p, b.dw, b.vw, b.fk, b.dfq, w, D, lv)) != LA_OK) return rc;  // dphi(q)
+        if ((rc = ll_anti_pass(BH, p.L, BW_LL_C, b.vw, b.dw, b.fq, p.lam, p.nl, b.dfk, w, D, W, st)) != LA_OK)
+            return rc;  // dphi(k)
+        if ((rc = ll_anti_pass(BH, p.L, BW_LL_C, b.fk, b.fq, b.dn, p.lam, p.nl, b.dvf, D, p.dv, W, st)) != LA_OK)
+            return rc;  // dv
+    } else {
+        if (p.normalize && (rc = pass(p, b.fq, b.fk, b.vw, b.nd, D, w, 0)) != LA_OK) return rc;  // [num, den]
+        bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
+                                                     p.normalize);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+        if ((rc = pass(p, b.dw, b.vw, b.fk, b.dfq, w, D, 0)) != LA_OK) return rc;   // dphi(q)
+        if ((rc = pass(p, b.vw, b.dw, b.fq, b.dfk, w, D, 1)) != LA_OK) return rc;   // dphi(k)
+        if ((rc = pass(p, b.fk, b.fq, b.dn, b.dvf, D, p.dv, 1)) != LA_OK) return rc;  // dv
+    }
     bw_chain_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)p.q, b.dfq, (T *)dq, rows, p.dk, D, p.fm,
                                                   p.omega, p.m);
     bw_chain_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)p.k, b.dfk, (T *)dk_, rows, p.dk, D, p.fm,
@@ -559,13 +625,20 @@ bool bwd_tc_supported(const Problem &p, int sms)
 
 size_t bwd_workspace_bytes(const Problem &p, int sms)
 {
-    const size_t simt = bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float);
+    const size_t simt = bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float) +
+                        bwd_ll_extra_bytes(p);
     const size_t tc = bwd_tc_supported(p, sms) ? tc_bufs(p, sms, nullptr, nullptr) : 0;
     return simt > tc ? simt : tc;
 }
 
-// D, dk <= 512 and dv < 512 (the generic kernel's shared-memory rows); no level weights
-bool bwd_supported(const Problem &p) { return p.D <= 512 && p.dk <= 512 && p.dv < 512 && !p.lam; }
+// D, dk <= 512 and dv < 512 (the generic kernel's shared-memory rows); with level weights
+// no decay, and levels enough for the sequence (the generic route only)
+bool bwd_supported(const Problem &p)
+{
+    if (!(p.D <= 512 && p.dk <= 512 && p.dv < 512)) return false;
+    if (p.lam && (p.decay || p.nl < 1 + simt_inter_levels(p.L, 1))) return false;
+    return true;
+}
 
 int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, void *dk, void *dv)
 {

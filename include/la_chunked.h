@@ -355,6 +355,39 @@ size_t la_chunked_bwd_workspace_bytes(int B, int H, int L, int dk, int dv, int C
                                       int dtype);
 
 /*
+ * la_chunked_bwd_ll -- backward pass of the causal forward under the log-linear mask
+ * (la_chunked_fwd with level_weights; "論文紹介：Log Linear Attention", slide 17, mask
+ * M_ts = lambda_t^(l(t,s))): given dout, writes dq, dk, dv.  The level weights are treated as
+ * data: their own gradient is not formed.  By the chain rule, with G_ts = M_ts (dout_t . v_s)
+ * (normalised: M_ts (dout_t . v_s - dout_t . out_t) / den_t):
+ *   dphi(q)_t = sum_{s<=t} G_ts phi(k_s)    -- a causal log-linear pass with the roles swapped;
+ *   dphi(k)_s = sum_{t>=s} G_ts phi(q_t),   dv_s = sum_{t>=s} M_ts (phi(q_t).phi(k_s)) dout_t
+ *                                            (/ den_t) -- anti-causal sums in which each pair is
+ *                                            weighted by the LATER row's lambda; they are grouped
+ *                                            by the aligned dyadic blocks of the level rule, one
+ *                                            weighted state per block,
+ * then through the feature map.  Generic fp32 route (path LA_PATH_AUTO or LA_PATH_SIMT;
+ * LA_PATH_TC returns LA_ERR_UNSUPPORTED), any feature map, with or without the normaliser.
+ *   level_weights  device [B, H, L, num_levels] fp32, as la_chunked_fwd's (1 + ceil(log2 L)
+ *                  levels at least)
+ *   C              ignored beyond la_chunked_fwd's checks (the passes use 64-row chunks)
+ *   workspace      at least la_chunked_bwd_ll_workspace_bytes(...) bytes (fp32 rows of about
+ *                  4 (D + dv) floats per row, level states, and one D x dv state per aligned
+ *                  block of chunks per head)
+ * Other arguments and errors as la_chunked_bwd (no decay).
+ */
+int la_chunked_bwd_ll(const void *q, const void *k, const void *v, const void *dout,
+                      void *grad_q, void *grad_k, void *grad_v, int B, int H, int L, int dk,
+                      int dv, int C, const la_feature_map *feature_map, int normalize,
+                      const float *level_weights, int num_levels, int dtype, void *workspace,
+                      size_t workspace_bytes, void *stream, int path);
+
+/* Workspace bytes la_chunked_bwd_ll needs (0 on an invalid or unsupported combination). */
+size_t la_chunked_bwd_ll_workspace_bytes(int B, int H, int L, int dk, int dv, int C,
+                                         const la_feature_map *feature_map, int normalize,
+                                         int num_levels, int dtype);
+
+/*
  * Carried state.  The state a causal pass ends with seeds a decoding loop (prefill, then
  * la_decode_step / la_decay_decode_step) or the next segment of a sequence cut into
  * segments (one per stream, thread or rank): each segment's own final state T_r, an

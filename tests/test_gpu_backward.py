@@ -140,3 +140,101 @@ def test_backward_rejects_bad_arguments():
                              ws.numel(), s) == la.LA_ERR_ARG
     assert la.la_chunked_bwd(p, p, p, p, p, p, p, *args, 0, 1.0, la.LA_BF16, ws.data_ptr(), 16,
                              s) == la.LA_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------------------
+# log-linear mask ("論文紹介：Log Linear Attention", slide 17): la_chunked_bwd_ll
+# ---------------------------------------------------------------------------------------
+LL_CASES = [
+    # (base workload, overrides): ragged lengths, several levels of chunk blocks, every map
+    ("loglinear-d64-L65536", dict(B=1, H=2, L=1000)),
+    ("loglinear-d64-L65536", dict(B=2, H=1, L=333, dk=32, dv=48)),
+    ("loglinear-d64-L65536", dict(B=1, H=1, L=4096)),                       # 64 chunks, 6 block levels
+    ("loglinear-d64-L65536", dict(B=1, H=2, L=700, fm="elu1", normalize=True, scale=1.0)),
+    ("loglinear-d64-L65536", dict(B=1, H=2, L=200, fm="favor", m=256, normalize=True, scale=1.0)),
+    ("loglinear-d64-L65536", dict(B=1, H=1, L=50)),                          # one chunk
+    ("loglinear-d64-L65536", dict(B=1, H=2, L=300, dtype="f32")),
+]
+
+
+def run_bwd_ll(w, inp, dout_bits):
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    B, H, L, dk, dv = w["B"], w["H"], w["L"], w["dk"], w["dv"]
+    q = to_device(inp["q"], w["dtype"], (B, H, L, dk))
+    k = to_device(inp["k"], w["dtype"], (B, H, L, dk))
+    v = to_device(inp["v"], w["dtype"], (B, H, L, dv))
+    do = to_device(dout_bits, w["dtype"], (B, H, L, dv))
+    lam = torch.from_numpy(inp["lam"]).reshape(B, H, L, -1).cuda()
+    omega = None if inp["omega"] is None else torch.from_numpy(inp["omega"]).cuda()
+    dq, dk_, dv_ = la.chunked_bwd_ll(q, k, v, do, lam, C=64, feature_map=w["fm"], omega=omega,
+                                     normalize=w["normalize"])
+    torch.cuda.synchronize()
+    st = la.la_last_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == la.LA_OK, la.la_status_string(st)
+    n = B * H
+    return (from_device(dq).reshape(n, L, dk), from_device(dk_).reshape(n, L, dk),
+            from_device(dv_).reshape(n, L, dv))
+
+
+@pytest.mark.parametrize("base,over", LL_CASES)
+def test_loglinear_backward_matches_oracle(base, over):
+    import oracle
+    w = workload(base, **over)
+    inp = synth.make_inputs(w, seed=61)
+    do = dout_for(w, 61)
+    f = lambda x: synth.as_f64(x, w["dtype"])  # noqa: E731
+    om = None if inp["omega"] is None else inp["omega"].astype(np.float64)
+    ref = oracle.backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(do), fm=w["fm"], omega=om,
+                          normalize=w["normalize"], lam=inp["lam"].astype(np.float64))
+    got = run_bwd_ll(w, inp, do)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        if w["dtype"] == "f32":
+            # fp32 storage: errors at fp32 rounding level
+            assert np.abs(g - r).max() <= 1e-4 * np.abs(r).max(), (name, np.abs(g - r).max())
+        else:
+            assert_close(g, r, f"{name} log-linear {over}")
+
+
+def test_loglinear_backward_all_ones_equals_plain_backward():
+    """lambda == 1 is the plain mask: la_chunked_bwd_ll equals la_chunked_bwd (generic path)
+    to fp32 rounding."""
+    import torch
+    w = workload("loglinear-d64-L65536", B=1, H=2, L=900, dtype="f32")
+    inp = synth.make_inputs(w, seed=62)
+    inp["lam"] = np.ones_like(inp["lam"])
+    do = dout_for(w, 62)
+    a = run_bwd_ll(w, inp, do)
+    b = run_bwd(dict(w, loglinear=False), dict(inp, lam=None), do, 64, 1.0, 1)
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() <= 1e-5 * np.abs(y).max()
+    torch.cuda.synchronize()
+
+
+def test_loglinear_backward_rejects_bad_arguments():
+    import torch
+
+    import chunkwise_causal_linear_gb300 as la
+    fm = la.make_feature_map("identity")
+    x = torch.zeros(1, 1, 256, 64, dtype=torch.bfloat16, device="cuda")
+    lam = torch.ones(1, 1, 256, 9, device="cuda")
+    p = x.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    need = la.la_chunked_bwd_ll_workspace_bytes(1, 1, 256, 64, 64, 64, fm, 0, 9, la.LA_BF16)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    # too few levels for 256 rows (1 + 8 = 9 needed)
+    assert la.la_chunked_bwd_ll_workspace_bytes(1, 1, 256, 64, 64, 64, fm, 0, 8, la.LA_BF16) == 0
+    rc = la.la_chunked_bwd_ll(p, p, p, p, p, p, p, 1, 1, 256, 64, 64, 64, fm, 0, lam.data_ptr(), 8,
+                              la.LA_BF16, ws.data_ptr(), need, s)
+    assert rc != la.LA_OK
+    rc = la.la_chunked_bwd_ll(p, p, p, p, p, p, p, 1, 1, 256, 64, 64, 64, fm, 0, None, 9,
+                              la.LA_BF16, ws.data_ptr(), need, s)
+    assert rc == la.LA_ERR_NULL
+    rc = la.la_chunked_bwd_ll(p, p, p, p, p, p, p, 1, 1, 256, 64, 64, 64, fm, 0, lam.data_ptr(), 9,
+                              la.LA_BF16, ws.data_ptr(), need - 1, s)
+    assert rc == la.LA_ERR_WORKSPACE
+    rc = la.la_chunked_bwd_ll(p, p, p, p, p, p, p, 1, 1, 256, 64, 64, 64, fm, 0, lam.data_ptr(), 9,
+                              la.LA_BF16, ws.data_ptr(), need, s, la.LA_PATH_TC)
+    assert rc == la.LA_ERR_UNSUPPORTED
