@@ -613,7 +613,7 @@ size_t la_chunked_bwd_ll_workspace_bytes(int B, int H, int L, int dk, int dv, in
 {
     Problem p;
     if (bwd_ll_problem(B, H, L, dk, dv, C, feature_map, normalize, num_levels, dtype, &p) != LA_OK) return 0;
-    p.lam = (const float *)1;
+    p.lam = (const float *)256;  // a 16-byte aligned stand-in: the size is that of aligned weights
     const int sms = device_sms();
     return bwd_workspace_bytes(p, sms > 0 ? sms : 152);
 }

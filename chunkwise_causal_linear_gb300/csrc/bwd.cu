@@ -102,12 +102,46 @@ size_t bwd_ll_level_bytes(const Problem &p)
     return ((lv + 255) / 256) * 256;
 }
 
+// Identity features, no normaliser, bf16 storage: the causal gradient pass dphi(q) =
+// sum_{s<=t} M_ts (dout_t . v_s) k_s has bf16 inputs exactly (q' = dout, k' = v, v' = k) and
+// is dq itself, so it runs on the tensor-core log-linear forward when that covers the
+// shape.  Returns false (and leaves *tp alone) otherwise.
+bool bwd_ll_tc_dq(const Problem &p, int sms, Problem *tp)
+{
+    if (!p.lam || p.dtype != LA_BF16 || p.fm != LA_FM_IDENTITY || p.normalize || p.decay) return false;
+    if (((uintptr_t)p.lam & 15) != 0) return false;
+    Problem t = p;
+    t.dk = p.dv; t.dv = p.dk; t.D = p.dv;
+    t.C = 64;
+    t.rev = 0; t.out_f32 = 0; t.S0 = nullptr; t.z0 = nullptr;
+    if (!tc_supported(t, sms)) return false;
+    *tp = t;
+    return true;
+}
+
+size_t bwd_ll_tc_bytes(const Problem &p, int sms)
+{
+    Problem t;
+    if (!bwd_ll_tc_dq(p, sms, &t)) return 0;
+    la_plan_info info;
+    if (tc_plan(t, sms, &info) != LA_OK) return 0;
+    return ((info.workspace_bytes + 255) / 256) * 256;
+}
+
 size_t bwd_ll_extra_bytes(const Problem &p)
 {
     if (!p.lam) return 0;
     const int w = p.dv + (p.normalize ? 1 : 0);
     const size_t s1 = ll_anti_state_floats(p.L, BW_LL_C, w, p.D), s2 = ll_anti_state_floats(p.L, BW_LL_C, p.D, p.dv);
     return bwd_ll_level_bytes(p) + (size_t)p.B * p.H * (s1 > s2 ? s1 : s2) * sizeof(float);
+}
+
+// the part of the workspace after the per-row buffers and the log-linear buffers: the
+// tensor-core dq pass's own workspace (segment totals, snapshot stack)
+size_t bwd_ll_tail_bytes(const Problem &p, int sms)
+{
+    const size_t t = p.lam ? bwd_ll_tc_bytes(p, sms) : 0;
+    return t ? t + 256 : 0;  // + alignment of its start
 }
 
 // phi of every row of x [rows, dk] (storage T) into f [rows, D] fp32
@@ -289,7 +323,7 @@ int pass_ll(const Problem &base, const float *q, const float *k, const float *v,
 }
 
 template <typename T>
-int bwd_t(const Problem &p, const void *dout, void *dq, void *dk_, void *dv_)
+int bwd_t(const Problem &p, int sms, const void *dout, void *dq, void *dk_, void *dv_)
 {
     const long rows = (long)p.B * p.H * p.L;
     const int D = p.D, w = p.dv + (p.normalize ? 1 : 0);
@@ -313,11 +347,27 @@ int bwd_t(const Problem &p, const void *dout, void *dq, void *dk_, void *dv_)
         bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
                                                      p.normalize);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
-        if ((rc = pass_ll(p, b.dw, b.vw, b.fk, b.dfq, w, D, lv)) != LA_OK) return rc;  // dphi(q)
+        Problem tq;
+        const bool tc_dq = bwd_ll_tc_dq(p, sms, &tq);
+        if (tc_dq) {
+            // dq = the tensor-core log-linear forward of (q' = dout, k' = v, v' = k)
+            tq.q = dout; tq.k = p.v; tq.v = p.k; tq.out = dq;
+            tq.workspace = (void *)(((uintptr_t)(extra + bwd_ll_extra_bytes(p)) + 255) & ~(uintptr_t)255);
+            tq.workspace_bytes = bwd_ll_tc_bytes(p, sms);
+            if ((rc = tc_launch(tq, sms)) != LA_OK) return rc;
+        } else if ((rc = pass_ll(p, b.dw, b.vw, b.fk, b.dfq, w, D, lv)) != LA_OK) {
+            return rc;  // dphi(q)
+        }
         if ((rc = ll_anti_pass(BH, p.L, BW_LL_C, b.vw, b.dw, b.fq, p.lam, p.nl, b.dfk, w, D, W, st)) != LA_OK)
             return rc;  // dphi(k)
         if ((rc = ll_anti_pass(BH, p.L, BW_LL_C, b.fk, b.fq, b.dn, p.lam, p.nl, b.dvf, D, p.dv, W, st)) != LA_OK)
             return rc;  // dv
+        if (tc_dq) {
+            bw_chain_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)p.k, b.dfk, (T *)dk_, rows, p.dk, D, p.fm,
+                                                          p.omega, p.m);
+            bw_cast_kernel<T><<<1024, 256, 0, st>>>(b.dvf, (T *)dv_, rows * p.dv);
+            return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+        }
     } else {
         if (p.normalize && (rc = pass(p, b.fq, b.fk, b.vw, b.nd, D, w, 0)) != LA_OK) return rc;  // [num, den]
         bw_prep_kernel<T><<<grid, BW_THREADS, 0, st>>>((const T *)dout, b.nd, b.dn, b.dw, rows, p.dv,
@@ -626,7 +676,7 @@ bool bwd_tc_supported(const Problem &p, int sms)
 size_t bwd_workspace_bytes(const Problem &p, int sms)
 {
     const size_t simt = bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float) +
-                        bwd_ll_extra_bytes(p);
+                        bwd_ll_extra_bytes(p) + bwd_ll_tail_bytes(p, sms);
     const size_t tc = bwd_tc_supported(p, sms) ? tc_bufs(p, sms, nullptr, nullptr) : 0;
     return simt > tc ? simt : tc;
 }
@@ -650,8 +700,8 @@ int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, 
     const bool tc = bwd_tc_supported(p, sms) && (al & 15) == 0;
     if (path == LA_PATH_TC && !tc) return LA_ERR_UNSUPPORTED;
     if (path != LA_PATH_SIMT && tc) return tc_route(p, sms, dout, dq, dk, dv);
-    if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, dout, dq, dk, dv);
-    return bwd_t<float>(p, dout, dq, dk, dv);
+    if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, sms, dout, dq, dk, dv);
+    return bwd_t<float>(p, sms, dout, dq, dk, dv);
 }
 
 }  // namespace la
