@@ -539,6 +539,28 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+_GENERIC_WARN_TOKENS = 1 << 20
+_warned_shapes = set()
+
+
+def _warn_if_generic(B, H, L, dk, dv, C, fm, normalize, nl, dtype, path):
+    """The automatic path falls back to the generic CUDA-core kernel for shapes outside the
+    tensor-core kernels' coverage; on large bf16 problems that is 100-1000x slower, so say so
+    (once per shape) instead of staying silent."""
+    if path != LA_PATH_AUTO or dtype != LA_BF16 or B * H * L < _GENERIC_WARN_TOKENS:
+        return
+    rc, info = la_chunked_plan(B, H, L, dk, dv, C, fm, normalize, int(nl > 0), nl, dtype,
+                               LA_PATH_AUTO, 0)
+    key = (B, H, L, dk, dv, C, fm.kind, fm.m, normalize, nl)
+    if rc == LA_OK and info["path"] == LA_PATH_SIMT and key not in _warned_shapes:
+        import warnings
+        _warned_shapes.add(key)
+        warnings.warn(f"la_chunked_fwd: B={B} H={H} L={L} dk={dk} dv={dv} C={C} runs on the generic "
+                      "CUDA-core path (outside the tensor-core kernels' coverage, see "
+                      "la_chunked_fwd_path in la_chunked.h); expect it to be 100-1000x slower",
+                      RuntimeWarning, stacklevel=3)
+
+
 def chunked_fwd(q, k, v, C=64, feature_map="identity", omega=None, normalize=False,
                 level_weights=None, out=None, workspace=None, stream=None, path=LA_PATH_AUTO):
     """out[B,H,L,dv] = chunkwise causal linear attention of CUDA tensors q,k [B,H,L,dk],
@@ -557,6 +579,7 @@ def chunked_fwd(q, k, v, C=64, feature_map="identity", omega=None, normalize=Fal
     fm = make_feature_map(feature_map, omega.shape[0] if omega is not None else 0,
                           omega.data_ptr() if omega is not None else 0)
     nl = level_weights.shape[-1] if level_weights is not None else 0
+    _warn_if_generic(B, H, L, dk, dv, C, fm, int(normalize), nl, dtype, path)
     need = la_chunked_workspace_bytes(B, H, L, dk, dv, C, fm, int(normalize), nl, dtype)
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -216,3 +216,22 @@ def test_backward_workspace_and_errors(lib):
     # the CUDA failure instead -- either way nothing runs
     assert la.la_chunked_bwd(ok, ok, ok, ok, ok, ok, ok, *args, 0, 1.0, la.LA_F32, ok,
                              16, None) in (la.LA_ERR_WORKSPACE, la.LA_ERR_CUDA)
+
+
+def test_generic_fallback_warns_on_large_bf16_problems(monkeypatch):
+    """The binding names the slow generic path when the automatic plan picks it for a large
+    bf16 problem (the plan query is host-only here: a fixed SM count)."""
+    import warnings
+
+    import chunkwise_causal_linear_gb300 as la
+    real_plan = la.la_chunked_plan
+    monkeypatch.setattr(la, "la_chunked_plan",
+                        lambda *a: real_plan(*a[:-1], 152))
+    fm = la.make_feature_map("elu1")
+    with warnings.catch_warnings(record=True) as rec:
+        warnings.simplefilter("always")
+        # d = 96 is outside the tensor-core coverage
+        la._warn_if_generic(8, 16, 8192, 96, 96, 64, fm, 1, 0, la.LA_BF16, la.LA_PATH_AUTO)
+        # the headline shape is covered: no warning
+        la._warn_if_generic(8, 16, 8192, 128, 128, 64, fm, 1, 0, la.LA_BF16, la.LA_PATH_AUTO)
+    assert len(rec) == 1 and "generic" in str(rec[0].message)
