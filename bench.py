@@ -107,15 +107,18 @@ def flops_per_token(w, C):
     return f
 
 
-def kernel_sha1(w):
-    """Hash of the tensor-core kernel source that serves workload `w` (plus the shared
-    headers): a committed DRAM-traffic figure is only used while this is unchanged."""
+def kernel_sha1(w, C=64):
+    """Hash of the tensor-core kernel source that serves workload `w` at chunk size C (plus
+    the shared headers): a committed DRAM-traffic figure is only used while this is
+    unchanged."""
     import hashlib
     d = os.path.join(ROOT, "chunkwise_causal_linear_gb300", "csrc")
     if w.get("loglinear"):
         main = "tc_loglinear.cu"
     elif w["fm"] == "favor":
         main = "tc_favor.cu"
+    elif C > 64:
+        main = "tc_wide.cu"
     else:
         main = "tc.cu"
     h = hashlib.sha1()
@@ -134,7 +137,7 @@ def ncu_traffic(workload, C, path, B, H, L=None):
     except Exception:
         return None
     w = synth.WORKLOADS[workload]
-    if not rec or rec.get("kernel_sha1") != kernel_sha1(w) or (B, H) != (w["B"], w["H"]):
+    if not rec or rec.get("kernel_sha1") != kernel_sha1(w, C) or (B, H) != (w["B"], w["H"]):
         return None
     if L is not None and L != w["L"]:
         return None
