@@ -743,7 +743,8 @@ def run_backward(args):
     # the tensor-core route (bf16, identity / elu+1, no decay, dk = dv in {64, 128}): features,
     # prep, chain, and 3 passes (+ 3 for the normaliser, one launch each without a sequence
     # split); the generic route: 2 features, v', prep, 3 passes, 2 chain, 1 cast (+ 1 pass)
-    tc_route = (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1") and gamma == 1.0
+    tc_route = (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
+                and (gamma == 1.0 or (gamma >= 0.5 and not w["normalize"]))
                 and L >= 128 and dk == dv and dk in (64, 128) and not ll)
     launches = (6 + (3 if w["normalize"] else 0)) if tc_route else (10 + (1 if w["normalize"] else 0))
     if ll:  # two anti-causal sums of two launches each instead of one pass each

@@ -125,8 +125,9 @@ struct TcArgs {
     int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
 
-// kernel modes (TC_F32OUT: causal, output stored as fp32 rows)
-constexpr int TC_CAUSAL = 0, TC_NONCAUSAL = 1, TC_DECAY = 2, TC_F32OUT = 3;
+// kernel modes (TC_F32OUT: causal, output stored as fp32 rows; TC_DECAY_F32OUT: both, for the
+// backward pass of the decayed forward)
+constexpr int TC_CAUSAL = 0, TC_NONCAUSAL = 1, TC_DECAY = 2, TC_F32OUT = 3, TC_DECAY_F32OUT = 4;
 
 template <int D, int DV, int C, bool NORM, bool F32O = false>
 struct TcLayout {
@@ -185,8 +186,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     constexpr int C = 64;           // rows per tile
     constexpr int NSUB = C / CH;    // chunks per tile
     constexpr bool NC = MODE == TC_NONCAUSAL;
-    constexpr bool DK = MODE == TC_DECAY;
-    constexpr bool FO = MODE == TC_F32OUT;
+    constexpr bool DK = MODE == TC_DECAY || MODE == TC_DECAY_F32OUT;
+    constexpr bool FO = MODE == TC_F32OUT || MODE == TC_DECAY_F32OUT;
     static_assert(!DK || CH == C, "decay: one chunk per tile");
     static_assert(!FO || (FM == LA_FM_IDENTITY && !NORM), "fp32 output: identity features, no normaliser");
     using Lay = TcLayout<D, DV, C, NORM, FO>;
@@ -914,12 +915,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const float2 *rp = (const float2 *)(rden + (NORM ? slot * C : 0) + 32 * h);
                 const float mf = (DK && !NORM) ? ex2(a.l2g * (float)(C * (c % a.period))) : 1.f;
                 if constexpr (FO) {
-                    // fp32 rows: column j of token tt
+                    // fp32 rows: column j of token tt (decay: times gamma^(i+1-C) gamma^(C m))
                     float *const o = (float *)a.out + rbase * DV + j;
+                    const float *rf = (const float *)rp;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int tt = 32 * h + u;
-                        if (live && tt < nrow) o[(size_t)tt * DV] = __uint_as_float(r[u]);
+                        const float x = DK ? __uint_as_float(r[u]) * (mf * rf[u]) : __uint_as_float(r[u]);
+                        if (live && tt < nrow) o[(size_t)tt * DV] = x;
                     }
                 } else {
                     // Lanes j, j^1 swap one value per pair of rows so that each writes two
@@ -998,7 +1001,7 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     }
     a.noncausal = noncausal ? 1 : 0;
     a.nseg_all = nseg;
-    a.l2g = mode == TC_DECAY ? p.l2g : 0.f;
+    a.l2g = (mode == TC_DECAY || mode == TC_DECAY_F32OUT) ? p.l2g : 0.f;
     a.S0 = p.S0;
     a.z0 = p.z0;
     // largest period P with C P |log2 gamma| <= 64 (gamma^(C P) >= 2^-64); tc_supported keeps
@@ -1016,9 +1019,10 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     if constexpr (CH == C) {
         if (mode == TC_NONCAUSAL) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_NONCAUSAL>;
         if (mode == TC_DECAY) kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_DECAY>;
-        if (mode == TC_F32OUT) {
+        if (mode == TC_F32OUT || mode == TC_DECAY_F32OUT) {
             if constexpr (FM == LA_FM_IDENTITY && !NORM) {
-                kern = tc_chunked_kernel<D, DV, CH, FM, NORM, TC_F32OUT>;
+                kern = mode == TC_F32OUT ? tc_chunked_kernel<D, DV, CH, FM, NORM, TC_F32OUT>
+                                         : tc_chunked_kernel<D, DV, CH, FM, NORM, TC_DECAY_F32OUT>;
                 alloc = TcLayout<D, DV, C, NORM, true>::ALLOC;
             } else {
                 return LA_ERR_UNSUPPORTED;
@@ -1061,7 +1065,7 @@ int launch_dc(const Problem &p, int sms, int mode = TC_CAUSAL)
 template <int D, int DV>
 int launch_d(const Problem &p, int sms)
 {
-    if (p.decay) return launch_dc<D, DV, 64>(p, sms, TC_DECAY);
+    if (p.decay) return launch_dc<D, DV, 64>(p, sms, p.out_f32 ? TC_DECAY_F32OUT : TC_DECAY);
     if (p.out_f32) return launch_dc<D, DV, 64>(p, sms, TC_F32OUT);
     if (p.C == 16) return launch_dc<D, DV, 16>(p, sms);
     if (p.C == 32) return launch_dc<D, DV, 32>(p, sms);
@@ -1092,7 +1096,7 @@ bool tc_supported(const Problem &p, int num_sms)
         if (p.lam || p.C != 64 || p.l2g < -1.f) return false;
         if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     }
-    if (p.out_f32 && (p.decay || p.lam || p.C != 64 || p.fm != LA_FM_IDENTITY || p.normalize))
+    if (p.out_f32 && (p.lam || p.C != 64 || p.fm != LA_FM_IDENTITY || p.normalize))
         return false;
     // a given initial state: the identity / elu+1 kernel with C <= 64 (or the decay mode)
     if ((p.S0 || p.z0) && (p.lam || p.fm == LA_FM_FAVOR || p.C > 64)) return false;

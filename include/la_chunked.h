@@ -322,7 +322,8 @@ int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_m
  * backward formulas; these follow from the chain rule on the causal definition (mask 1 or
  * gamma^(t-s), with or without the normaliser), then through the feature map.  They are
  * linear-attention passes with the roles swapped, two of them anti-causal:
- *   - LA_PATH_TC: bf16, identity / elu+1 features, no decay, L >= 128, 16-byte aligned
+ *   - LA_PATH_TC: bf16, identity / elu+1 features, no decay, or gamma >= 0.5 without the
+ *     normaliser (the same gamma^|t-s| mask in every pass), L >= 128, 16-byte aligned
  *     q, k, v, dout and gradient buffers, and pass shapes the tensor-core forward covers
  *     ((dk, dv) in {(64, 64), (128, 128)}); the anti-causal
  *     passes run over reversed rows and the normaliser adds two passes; pass outputs are

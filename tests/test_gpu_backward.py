@@ -69,12 +69,17 @@ CASES = [
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=2048), 64, 1.0),  # d128, 32 tiles per head
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=700, normalize=False), 64, 1.0),
     ("identity-d64-L2048", dict(B=1, H=3, L=1000, normalize=True, fm="elu1", scale=1.0), 64, 1.0),
+    # the decay without the normaliser on the tensor-core route: split sequence, d128, d64
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=2048, normalize=False), 64, 0.98),
+    ("elu1-norm-d128-L8192", dict(B=1, H=2, L=700, normalize=False), 64, 0.9),
+    ("identity-d64-L2048", dict(B=2, H=2, L=777), 64, 0.75),
 ]
 
 
 def bwd_path(w, gamma):
     """1 (generic) or 2 (tensor cores): the path la_chunked_bwd takes on AUTO."""
-    return 2 if (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1") and gamma == 1.0
+    return 2 if (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
+                 and (gamma == 1.0 or (gamma >= 0.5 and not w["normalize"]))
                  and w["L"] >= 128 and w["dk"] == w["dv"] and w["dk"] in (64, 128)) else 1
 
 
@@ -100,8 +105,12 @@ def test_backward_tensor_core_route_is_taken():
     inp = synth.make_inputs(w, seed=43)
     do = dout_for(w, 43)
     run_bwd(w, inp, do, 64, 1.0, path=2)
+    wn = dict(w, normalize=False)
+    run_bwd(wn, inp, do, 64, 0.9, path=2)      # decay with gamma >= 0.5, no normaliser: tensor cores
     with pytest.raises(la.LAError):
-        run_bwd(w, inp, do, 64, 0.9, path=2)  # decay: generic path only
+        run_bwd(w, inp, do, 64, 0.9, path=2)   # decay with the normaliser: generic path only
+    with pytest.raises(la.LAError):
+        run_bwd(wn, inp, do, 64, 0.4, path=2)  # gamma^64 below 2^-64: generic path only
     wf = workload("elu1-norm-d128-L8192", B=1, H=1, L=256, dtype="f32")
     inpf = synth.make_inputs(wf, seed=43)
     with pytest.raises(la.LAError):
