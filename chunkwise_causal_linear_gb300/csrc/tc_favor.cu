@@ -51,7 +51,8 @@ using namespace tcc;
 namespace {
 
 constexpr int FV_THREADS = 640;
-constexpr int FV_STAGES = 2;
+constexpr int FV_STAGES = 2;      // main pass: Q, K, V per stage
+constexpr int FV_STAGES_TOT = 3;  // totals pass: K, V per stage, in the same bytes
 constexpr int FV_DK = 64, FV_M = 256, FV_DV = 64, FV_C = 64;
 constexpr int FV_DEN = 4;
 
@@ -70,7 +71,8 @@ constexpr int FV_P = FV_SBAR + (FV_M / 64) * FV_SBLK;           // P [64 t][64 s
 constexpr int FV_F32 = FV_P + FV_TILE;
 constexpr int FV_N_F32 = 2 * FV_C /*nrm q,k*/ + FV_DEN * FV_C /*den_intra*/;
 constexpr int FV_BAR = FV_F32 + FV_N_F32 * 4;
-constexpr int FV_N_BAR = 2 * FV_STAGES + 16 + 2 * FV_DEN;
+constexpr int FV_N_BAR = 2 * FV_STAGES_TOT + 17 + 2 * FV_DEN;
+static_assert(FV_STAGES_TOT * 2 * FV_C * 128 <= FV_STAGES * 3 * FV_C * 128, "totals stages fit the stage area");
 constexpr int FV_MISC = FV_BAR + FV_N_BAR * 8;
 constexpr int FV_BYTES = FV_MISC + 16;
 constexpr int FV_ALLOC = FV_BYTES + 1024;
@@ -108,11 +110,12 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
     float *den_intra = nrm + 2 * FV_C;             // [FV_DEN][64]
     uint64_t *bars = (uint64_t *)(sm + FV_BAR);
     uint64_t *full = bars;                         // [S]
-    uint64_t *stage_free = full + FV_STAGES;       // [S]
-    uint64_t *p_done = stage_free + FV_STAGES;     // projection of the chunk in TMEM
+    uint64_t *stage_free = full + FV_STAGES_TOT;   // [S]
+    uint64_t *p_done = stage_free + FV_STAGES_TOT; // projection of the chunk in TMEM (totals
+                                                   // pass: [2] by chunk parity)
     uint64_t *phi_ready = p_done + 3;              // phi(Q), phi(K), z rows written (and the
-                                                   // projection read)
-    uint64_t *scores_done = phi_ready + 1;
+                                                   // projection read); totals pass: [2]
+    uint64_t *scores_done = phi_ready + 2;
     uint64_t *a_free = scores_done + 1;            // scores read (their columns reusable)
     uint64_t *p_ready = a_free + 1;
     uint64_t *state_done = p_ready + 1;
@@ -134,17 +137,21 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
     Ctl ctl{abort_flag, a.err, a.timeout_ns};
     if (totals) pdl_trigger();  // the main pass may be scheduled now
     else pdl_wait();            // the totals pass (if any) has completed
+    // stages: main pass [Q | K | V] x 2, totals pass [K | V] x 3 (no Q), in the same bytes
+    const int NST = totals ? FV_STAGES_TOT : FV_STAGES;
     auto stage_q = [&](int s) { return sm + FV_STAGE + s * FV_STAGE_BYTES; };
-    auto stage_k = [&](int s) { return stage_q(s) + FV_TILE; };
+    auto stage_k = [&](int s) { return totals ? sm + FV_STAGE + s * 2 * FV_TILE : stage_q(s) + FV_TILE; };
     auto stage_v = [&](int s) { return stage_k(s) + FV_TILE; };
 
     if (tid == 0) {
-        for (int i = 0; i < FV_STAGES; ++i) {
+        for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&stage_free[i], 1);
         }
-        mbar_init(p_done, 1);
-        mbar_init(phi_ready, 1);
+        mbar_init(&p_done[0], 1);
+        mbar_init(&p_done[1], 1);
+        mbar_init(&phi_ready[0], 1);
+        mbar_init(&phi_ready[1], 1);
         mbar_init(scores_done, 1);
         mbar_init(a_free, 4);
         mbar_init(p_ready, 1);
@@ -229,8 +236,8 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
-                const int s = c % FV_STAGES;
-                if (c >= FV_STAGES && !wait_phase(&stage_free[s], ((c / FV_STAGES) - 1) & 1, ctl)) break;
+                const int s = c % NST;
+                if (c >= NST && !wait_phase(&stage_free[s], ((c / NST) - 1) & 1, ctl)) break;
                 const int row = (tile0 + c) * FV_C;
                 mbar_arrive_expect_tx(&full[s], totals ? 2 * FV_TILE : 3 * FV_TILE);
                 if (!totals) tma_load_3d(stage_q(s), &a.tm_q, 0, row, head, &full[s]);
@@ -238,9 +245,9 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 tma_load_3d(stage_v(s), &a.tm_v, 0, row, head, &full[s]);
                 issued = c + 1;
             }
-            for (int c = (issued > FV_STAGES ? issued - FV_STAGES : 0); c < issued; ++c) {
+            for (int c = (issued > NST ? issued - NST : 0); c < issued; ++c) {
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_sleep(&full[c % FV_STAGES], (c / FV_STAGES) & 1, 200000u))
+                while (!mbar_try_sleep(&full[c % NST], (c / NST) & 1, 200000u))
                     if (globaltimer() - t0 > ctl.timeout_ns) break;
             }
         }
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                            dSb = smem_desc(sb, 16, 1024), dPa = smem_desc(pa, 16, 1024);
             // projection of raw rows into TMEM (features on lanes), omega hi + lo: the 128 rows
             // Q, K of the stage (main pass) or the 64 K rows (totals pass)
-            auto project = [&](uint32_t xa, uint32_t idesc) {
+            auto project = [&](uint32_t xa, uint32_t idesc, uint32_t col) {
                 const uint64_t dX = smem_desc(xa, 16, 1024);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -270,38 +277,60 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tmem + FT_P + 128 * h,
+                            mma_ss(tmem + FT_P + 128 * h + col,
                                    desc_add(dOm, part * FV_M * 128 + h * 128 * 128 + ks * 32),
                                    desc_add(dX, ks * 32), idesc, (part | ks) != 0);
             };
-            for (int c = 0; c < nch; ++c) {
+            if (totals) {
+                // Totals pass, pipelined over two buffers (chunk parity b): the projection of K
+                // into TMEM columns FT_P + 128 h + 64 b, phi(K)^T into the phi(K) tile (b = 0) or
+                // the otherwise idle phi(Q) tile (b = 1).  The projection of chunk c is issued
+                // before the state update of chunk c-1 waits for its phi, so the feature-map
+                // warps exponentiate one chunk while the next one is projected.
+                bool tok = true;
+                auto state_of = [&](int c) -> bool {
+                    const int b = c & 1, s = c % NST;
+                    if (!wait_phase(&phi_ready[b], (c >> 1) & 1, ctl)) return false;
+                    tc_fence_after();
+                    const uint64_t dPh = smem_desc(b ? phq : phk, 16, 1024);
+                    const uint64_t dV = smem_desc(smem_u32(stage_v(s)), FV_C * 128, 1024);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tmem + FT_S + 64 * h, desc_add(dPh, h * 128 * 128 + ks * 32),
+                                   desc_add(dV, ks * 2048), ID_STATE, (c > 0) || (ks > 0));
+                    mma_commit(&stage_free[s]);
+                    return true;
+                };
+                for (int c = 0; tok && c < nch; ++c) {
+                    const int s = c % NST, b = c & 1;
+                    if (!wait_phase(&full[s], (c / NST) & 1, ctl)) {
+                        tok = false;
+                        break;
+                    }
+                    // TMEM buffer b was read for chunk c-2: its phi_ready was waited on below
+                    tc_fence_after();
+                    project(smem_u32(stage_k(s)), ID_PROJ, 64u * b);
+                    mma_commit(&p_done[b]);
+                    if (c >= 1) tok = state_of(c - 1);
+                }
+                if (tok && nch > 0 && state_of(nch - 1)) mma_commit(totals_done);
+            }
+            for (int c = 0; c < nch && !totals; ++c) {
                 const int s = c % FV_STAGES;
                 const int g = tile0 + c;  // chunk index in the sequence
                 if (!wait_phase(&full[s], (c / FV_STAGES) & 1, ctl)) break;
                 // the projection's columns hold the previous chunk's scores until the P warps
                 // have read them; the previous projection itself was read before phi_ready
                 if (!totals && c >= 1 && !wait_phase(a_free, (c - 1) & 1, ctl)) break;
-                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
+                const uint32_t qa = smem_u32(stage_q(s)), va = smem_u32(stage_v(s));
                 const uint64_t dVmn = smem_desc(va, FV_C * 128, 1024);
                 tc_fence_after();
-                if (totals)
-                    project(ka, ID_PROJ);
-                else
-                    project(qa, ID_PROJ2);  // K follows Q in the stage: rows 0-63 Q, 64-127 K
-                mma_commit(p_done);
-                if (!wait_phase(phi_ready, c & 1, ctl)) break;
+                project(qa, ID_PROJ2, 0);  // K follows Q in the stage: rows 0-63 Q, 64-127 K
+                mma_commit(&p_done[0]);
+                if (!wait_phase(&phi_ready[0], c & 1, ctl)) break;
                 tc_fence_after();
-                if (totals) {
-                    // state only
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tmem + FT_S + 64 * h, desc_add(dPhk, h * 128 * 128 + ks * 32),
-                                   desc_add(dVmn, ks * 2048), ID_STATE, (c > 0) || (ks > 0));
-                    mma_commit(&stage_free[s]);
-                    continue;
-                }
                 // scores: phi(Q) (MN-major A) x phi(K)^T (MN-major B), K = 256 features, into
                 // the projection's columns (read by now: phi_ready)
 #pragma unroll
@@ -336,7 +365,6 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 mma_commit(o_done);
                 mma_commit(&stage_free[s]);
             }
-            if (totals) mma_commit(totals_done);
             mma_commit(drain);
             const uint64_t t0 = globaltimer();
             while (!mbar_try_sleep(drain, 0, 200000u))
@@ -387,9 +415,9 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
             return zs;
         };
         for (int c = 0; c < nch; ++c) {
-            const int s = c % FV_STAGES;
+            const int s = c % NST;
             const int g = tile0 + c;
-            if (!group_wait(l == 0, 1, &full[s], (c / FV_STAGES) & 1, nullptr, 0, false, ctl, 256)) break;
+            if (!group_wait(l == 0, 1, &full[s], (c / NST) & 1, nullptr, 0, false, ctl, 256)) break;
             // |x^|^2 = |x|^2 / sqrt(dk) of the Q and K rows: two threads per row
             {
                 const int r = l >> 1, part = l & 1;
@@ -413,7 +441,10 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 }
             }
             named_bar(1, 256);
-            if (!group_wait(l == 0, 1, p_done, c & 1, nullptr, 0, false, ctl, 256)) break;
+            // totals pass: projection buffer and phi(K) tile by chunk parity
+            const int tb = totals ? (c & 1) : 0;
+            if (!group_wait(l == 0, 1, &p_done[tb], totals ? (c >> 1) & 1 : c & 1, nullptr, 0, false, ctl, 256))
+                break;
             tc_fence_after();
             if (!totals) {
                 phi_row(0, nrm, rowq, false, 0);
@@ -424,12 +455,13 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                 *(__nv_bfloat16 *)(sblk + 65 * 128 + ((lch ^ 1) << 4)) = zl;
             }
             {
-                const float zk = phi_row(totals ? 0 : 64, nrm + 64, rowk, totals || !NC, a.L - g * FV_C);
+                const float zk = phi_row(totals ? 64 * tb : 64, nrm + 64, tb ? rowq : rowk, totals || !NC,
+                                         a.L - g * FV_C);
                 if (totals || !NC) zreg += zk;
             }
             fence_async_smem();
             named_bar(1, 256);
-            if (l == 0) mbar_arrive(phi_ready);
+            if (l == 0) mbar_arrive(&phi_ready[tb]);
             // bf16 copy of the state (S~ rows 0..63, column l) for the next chunk
             if (!totals && !NC && g + 1 < a.nch) {
                 if (!group_wait(l == 0, 1, state_done, c & 1, nullptr, 0, false, ctl, 256)) break;
