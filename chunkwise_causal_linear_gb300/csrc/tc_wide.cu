@@ -7,11 +7,13 @@
 //
 // Rows still move in 64-row tiles.  Query tile r of a chunk (r = 0 .. R-1) is processed as
 // 1 + r score blocks against the key tiles of its chunk:
-//   * the diagonal block (its own keys, causal mask, plus the z rows for phi(q).z), from the
-//     tile's own stage;
-//   * the r blocks against the chunk's earlier key tiles, unmasked; those K, V tiles are
-//     fetched again (from L2, where they were read a few tiles earlier) into a two-slot key
-//     ring, and phi is applied to them again.
+//   * the diagonal block (its own keys, causal mask, plus the z rows for phi(q).z);
+//   * the r blocks against the chunk's earlier key tiles, unmasked.
+// Q tiles and (K, V) tiles live in two shared-memory rings.  A Q slot is released as soon as
+// its tile's scores and inter product are done; a K/V slot holds phi(K) and V until the last
+// tile of its chunk is done, so the earlier key tiles are read from HBM once and phi is
+// applied to them once.  The K/V ring has room for more than one chunk (2R slots where they
+// fit, else R + 1), so the next chunk's tiles load while the current one computes.
 // The inter product reads the bf16 state copy made at the chunk start; the fp32 state takes
 // every tile's update, and its bf16 copy is refreshed once per chunk, after the chunk's last
 // tile.  z (phi(q).z in the denominator) is likewise the value at the chunk start.  So the
@@ -19,7 +21,7 @@
 // page's cost model (section 3).
 //
 // Warp roles (as in the one-tile kernel): 0 TMA producer, 1 MMA issuer, 4-11 feature map,
-// 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue.
+// 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue (rows stored from registers).
 //
 // MMAs per query tile (bf16 in, fp32 accumulate), D = feature dim, T = 64:
 //   scores  A_k   = phi(Q) [phi(K_k); z]^T       M=T   N=T(+8)  K=D   per block k
@@ -45,12 +47,12 @@ namespace {
 
 constexpr int TW_THREADS = 640;
 constexpr int TW_FWARPS = 8;
-constexpr int TW_STAGES = 2;   // main stages (Q, K, V of a query tile)
-constexpr int TW_KR = 2;       // key ring (K, V of an earlier tile of the chunk)
 constexpr int TW_DEN = 4;
+constexpr int TW_SMEM = 232448 - 1024;   // opt-in shared memory less the alignment slack
 
 struct TwArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
+    void *out;           // bf16 [BH][L][dv]
     int L, nch;          // nch: 64-row tiles of a head
     int seg_tiles;       // a multiple of R: segments start on chunk edges
     int grid_seg, totals, BH;
@@ -60,44 +62,62 @@ struct TwArgs {
     unsigned long long timeout_ns;
 };
 
-template <int D, int DV, bool NORM>
+// K/V slots: 2R (a whole chunk ahead) where that fits beside two Q slots, else fewer, at
+// least R + 1; then as many Q slots (2 to 4) as the rest allows.
+constexpr int tw_pick_nkv(int R, int kv, int q, int fixed)
+{
+    int n = 2 * R;
+    while (n > R + 1 && n * kv + 2 * q + fixed > TW_SMEM) --n;
+    return n;
+}
+
+constexpr int tw_pick_nq(int nkv, int kv, int q, int fixed)
+{
+    int n = 4;
+    while (n > 2 && nkv * kv + n * q + fixed > TW_SMEM) --n;
+    return n;
+}
+
+template <int D, int DV, int R, bool NORM>
 struct TwLayout {
     static constexpr int T = 64;
     static constexpr int KROWS = NORM ? T + 8 : T;
     static constexpr int NSC = KROWS;
-    static constexpr int K_BLK = KROWS * 128;        // 64-feature block of a stage's K tile
+    static constexpr int K_BLK = KROWS * 128;        // 64-feature block of a slot's K tile
     static constexpr int Q_BYTES = T * D * 2;
     static constexpr int K_BYTES = (D / 64) * K_BLK;
     static constexpr int V_BYTES = T * DV * 2;
-    static constexpr int STAGE_BYTES = Q_BYTES + K_BYTES + V_BYTES;
-    static constexpr int STAGE_TX = Q_BYTES + T * D * 2 + V_BYTES;
-    static constexpr int RK_BYTES = T * D * 2;       // key ring: K (64-row blocks), V
-    static constexpr int RING_BYTES = RK_BYTES + V_BYTES;
+    static constexpr int KV_BYTES = K_BYTES + V_BYTES;
+    static constexpr int KV_TX = T * D * 2 + V_BYTES;   // bytes TMA writes into a K/V slot
     static constexpr int P_BYTES = T * T * 2;
-    static constexpr int O_BYTES = T * DV * 2;
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_RING = TW_STAGES * STAGE_BYTES;
-    static constexpr int OFF_P = OFF_RING + TW_KR * RING_BYTES;   // two P tiles
-    static constexpr int OFF_O = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_F32 = OFF_O + O_BYTES;
     // floats: rden[TW_DEN][T], z (running), z at the chunk start, zpart[TW_FWARPS][D]
     static constexpr int N_F32 = TW_DEN * T + 2 * D + TW_FWARPS * D;
-    static constexpr int OFF_BAR = OFF_F32 + ((N_F32 * 4 + 15) / 16) * 16;
-    static constexpr int N_BAR = 3 * TW_STAGES + 3 * TW_KR + 2 * 3 + 2 * 2 + 2 * TW_DEN + 3;
+    static constexpr int F32_BYTES = ((N_F32 * 4 + 15) / 16) * 16;
+    static constexpr int MAX_BAR = 3 * 2 * R + 4 + 2 * 5 + 2 * TW_DEN + 3;
+    static constexpr int FIXED = 2 * P_BYTES + F32_BYTES + MAX_BAR * 8 + 16;
+    static constexpr int NKV = tw_pick_nkv(R, KV_BYTES, Q_BYTES, FIXED);
+    static constexpr int NQ = tw_pick_nq(NKV, KV_BYTES, Q_BYTES, FIXED);
+    static constexpr int OFF_KV = 0;
+    static constexpr int OFF_Q = OFF_KV + NKV * KV_BYTES;
+    static constexpr int OFF_P = OFF_Q + NQ * Q_BYTES;     // two P tiles
+    static constexpr int OFF_F32 = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_BAR = OFF_F32 + F32_BYTES;
+    static constexpr int N_BAR = 3 * NKV + NQ + 2 * 5 + 2 * TW_DEN + 3;
     static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;
     static constexpr uint32_t T_S = 0, T_SB = 128, T_O = 192, T_A = 320, A_STRIDE = 80;
     static_assert(D <= 128 && (DV == 64 || DV == 128), "D <= 128, dv 64 or 128");
-    static_assert(K_BLK % 1024 == 0 && STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "swizzle atoms");
-    static_assert(ALLOC <= 232448, "shared memory budget");
+    static_assert(K_BLK % 1024 == 0 && KV_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms");
+    static_assert(NKV > R && N_BAR <= MAX_BAR && BYTES <= TW_SMEM, "shared memory budget");
 };
 
 template <int D, int DV, int R, int FM, bool NORM>
 __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_constant__ TwArgs a)
 {
-    using Lay = TwLayout<D, DV, NORM>;
+    using Lay = TwLayout<D, DV, R, NORM>;
     constexpr int T = Lay::T;
+    constexpr int NKV = Lay::NKV, NQ = Lay::NQ;
     constexpr bool PHI = FM != LA_FM_IDENTITY;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -107,13 +127,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
     float *zcs = zs + D;                // [D] z at the chunk start
     float *zpart = zcs + D;             // [TW_FWARPS][D]
     uint64_t *bars = (uint64_t *)(sm + Lay::OFF_BAR);
-    uint64_t *full = bars;                          // [S] TMA -> feature map
-    uint64_t *phi_ready = full + TW_STAGES;         // [S] feature map -> MMA
-    uint64_t *stage_free = phi_ready + TW_STAGES;   // [S] MMA -> TMA
-    uint64_t *kfull = stage_free + TW_STAGES;       // [KR] TMA -> feature map
-    uint64_t *kready = kfull + TW_KR;               // [KR] feature map -> MMA
-    uint64_t *kfree = kready + TW_KR;               // [KR] MMA -> TMA
-    uint64_t *scores_done = kfree + TW_KR;          // [2] by block parity
+    uint64_t *kv_full = bars;                       // [NKV] TMA -> feature map (Q, K, V of a tile)
+    uint64_t *phi_ready = kv_full + NKV;            // [NKV] feature map -> MMA
+    uint64_t *kv_free = phi_ready + NKV;            // [NKV] MMA -> TMA, at the end of the slot's chunk
+    uint64_t *q_free = kv_free + NKV;               // [NQ] MMA -> TMA
+    uint64_t *scores_done = q_free + NQ;            // [2] by block parity
     uint64_t *a_free = scores_done + 2;             // [2]
     uint64_t *p_ready = a_free + 2;                 // [2]
     uint64_t *o_done = p_ready + 2;                 // [2] by tile parity
@@ -135,25 +153,19 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
     if (totals) pdl_trigger();  // the main pass may be scheduled now
     else pdl_wait();            // the totals pass (if any) has completed
 
-    auto stage_q = [&](int s) { return sm + Lay::OFF_STAGE + s * Lay::STAGE_BYTES; };
-    auto stage_k = [&](int s) { return stage_q(s) + Lay::Q_BYTES; };
-    auto stage_v = [&](int s) { return stage_k(s) + Lay::K_BYTES; };
-    auto ring_k = [&](int k) { return sm + Lay::OFF_RING + k * Lay::RING_BYTES; };
-    auto ring_v = [&](int k) { return ring_k(k) + Lay::RK_BYTES; };
+    // local tile c: Q in slot c % NQ, K and V in slot c % NKV
+    auto q_tile = [&](int s) { return sm + Lay::OFF_Q + s * Lay::Q_BYTES; };
+    auto k_tile = [&](int s) { return sm + Lay::OFF_KV + s * Lay::KV_BYTES; };
+    auto v_tile = [&](int s) { return k_tile(s) + Lay::K_BYTES; };
     auto p_tile = [&](int bb) { return sm + Lay::OFF_P + bb * Lay::P_BYTES; };
-    uint8_t *const o_tile = sm + Lay::OFF_O;
 
     if (tid == 0) {
-        for (int i = 0; i < TW_STAGES; ++i) {
-            mbar_init(&full[i], 1);
+        for (int i = 0; i < NKV; ++i) {
+            mbar_init(&kv_full[i], 1);
             mbar_init(&phi_ready[i], 1);
-            mbar_init(&stage_free[i], 1);
+            mbar_init(&kv_free[i], 1);
         }
-        for (int i = 0; i < TW_KR; ++i) {
-            mbar_init(&kfull[i], 1);
-            mbar_init(&kready[i], 1);
-            mbar_init(&kfree[i], 1);
-        }
+        for (int i = 0; i < NQ; ++i) mbar_init(&q_free[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&scores_done[i], 1);
             mbar_init(&a_free[i], 4);
@@ -172,10 +184,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
         mbar_init_fence();
     }
     if (NORM) {
-        for (int e = tid; e < TW_STAGES * (D / 64) * 8 * 8; e += TW_THREADS) {
+        // rows T .. T+7 of every K block: z hi, z lo, then zeros (TMA writes rows 0 .. T-1)
+        for (int e = tid; e < NKV * (D / 64) * 8 * 8; e += TW_THREADS) {
             const int st = e / ((D / 64) * 64), r = e % ((D / 64) * 64);
             const int kb = r / 64, row = T + (r % 64) / 8, chn = r % 8;
-            *(uint4 *)(stage_k(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
+            *(uint4 *)(k_tile(st) + kb * Lay::K_BLK + row * 128 + chn * 16) = make_uint4(0, 0, 0, 0);
         }
         for (int i = tid; i < D; i += TW_THREADS) {
             float z0 = 0.f;
@@ -229,50 +242,26 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int s = 0, sph = 0, kslot = 0, kuse = 0;
-            bool ok = true;
-            for (int c = 0; c < nt && ok; ++c) {
-                if (c >= TW_STAGES && !wait_phase(&stage_free[s], sph ^ 1, ctl)) break;
+            for (int c = 0; c < nt; ++c) {
+                const int ks = c % NKV, qs = c % NQ;
+                // the slot's previous tile: its chunk is done (K/V), its own products are done (Q)
+                if (c >= NKV && !wait_phase(&kv_free[ks], ((c / NKV) - 1) & 1, ctl)) break;
+                if (!totals && c >= NQ && !wait_phase(&q_free[qs], ((c / NQ) - 1) & 1, ctl)) break;
                 const int row = (tile0 + c) * T;
-                mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES : Lay::STAGE_TX);
+                mbar_arrive_expect_tx(&kv_full[ks], totals ? Lay::KV_TX : Lay::KV_TX + Lay::Q_BYTES);
                 for (int kb = 0; kb < D / 64; ++kb) {
-                    if (!totals) tma_load_3d(stage_q(s) + kb * T * 128, &a.tm_q, kb * 64, row, head, &full[s]);
-                    tma_load_3d(stage_k(s) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &full[s]);
+                    if (!totals) tma_load_3d(q_tile(qs) + kb * T * 128, &a.tm_q, kb * 64, row, head, &kv_full[ks]);
+                    tma_load_3d(k_tile(ks) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &kv_full[ks]);
                 }
                 for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_load_3d(stage_v(s) + jb * T * 128, &a.tm_v, jb * 64, row, head, &full[s]);
-                if (++s == TW_STAGES) { s = 0; sph ^= 1; }
-                if (totals) continue;
-                // the chunk's earlier key tiles, for this query tile's off-diagonal blocks
-                const int r = c % R;
-                for (int k = c - r; k < c; ++k) {
-                    if (kuse >= TW_KR && !wait_phase(&kfree[kslot], ((kuse / TW_KR) - 1) & 1, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    const int krow = (tile0 + k) * T;
-                    mbar_arrive_expect_tx(&kfull[kslot], Lay::RK_BYTES + Lay::V_BYTES);
-                    for (int kb = 0; kb < D / 64; ++kb)
-                        tma_load_3d(ring_k(kslot) + kb * T * 128, &a.tm_k, kb * 64, krow, head, &kfull[kslot]);
-                    for (int jb = 0; jb < DV / 64; ++jb)
-                        tma_load_3d(ring_v(kslot) + jb * T * 128, &a.tm_v, jb * 64, krow, head, &kfull[kslot]);
-                    ++kuse;
-                    if (++kslot == TW_KR) kslot = 0;
-                }
+                    tma_load_3d(v_tile(ks) + jb * T * 128, &a.tm_v, jb * 64, row, head, &kv_full[ks]);
             }
-            // never leave with loads in flight: the last uses of every stage and ring slot
+            // never leave with loads in flight: slot i was filled ceil((nt - i) / NKV) times
             const uint64_t t0 = globaltimer();
-            for (int i = 0; i < TW_STAGES; ++i) {
-                // stage i was used ceil((nt - i) / S) times; wait for its last completion
-                const int uses = nt > i ? (nt - i + TW_STAGES - 1) / TW_STAGES : 0;
+            for (int i = 0; i < NKV; ++i) {
+                const int uses = nt > i ? (nt - i + NKV - 1) / NKV : 0;
                 if (uses > 0)
-                    while (!mbar_try_sleep(&full[i], (uses - 1) & 1, 200000u))
-                        if (globaltimer() - t0 > ctl.timeout_ns) break;
-            }
-            for (int i = 0; i < TW_KR; ++i) {
-                const int uses = kuse > i ? (kuse - i + TW_KR - 1) / TW_KR : 0;
-                if (uses > 0)
-                    while (!mbar_try_sleep(&kfull[i], (uses - 1) & 1, 200000u))
+                    while (!mbar_try_sleep(&kv_full[i], (uses - 1) & 1, 200000u))
                         if (globaltimer() - t0 > ctl.timeout_ns) break;
             }
         }
@@ -285,61 +274,47 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
             constexpr uint32_t ID_STATE = idesc_bf16_f32(DV, D, 1, 1);
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(DV, T, 1, 0);
             bool ok = true;
-            int s = 0, sph = 0;
             if (totals) {
                 for (int c = 0; c < nt; ++c) {
-                    uint64_t *ph = (!PHI && !NORM) ? &full[s] : &phi_ready[s];
-                    if (!wait_phase(ph, sph, ctl)) { ok = false; break; }
+                    const int ks = c % NKV;
+                    uint64_t *ph = (!PHI && !NORM) ? &kv_full[ks] : &phi_ready[ks];
+                    if (!wait_phase(ph, (c / NKV) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
+                    const uint32_t ka = smem_u32(k_tile(ks)), va = smem_u32(v_tile(ks));
 #pragma unroll
-                    for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), ks * 2048),
-                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), ks * 2048), ID_STATE, 1);
-                    mma_commit(&stage_free[s]);
-                    if (++s == TW_STAGES) { s = 0; sph ^= 1; }
+                    for (int kk = 0; kk < T / 16; ++kk)
+                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), kk * 2048),
+                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), kk * 2048), ID_STATE, 1);
+                    mma_commit(&kv_free[ks]);
                 }
                 if (ok) mma_commit(state_done);
                 ok = false;
             }
             int kb = 0;                   // score blocks issued so far (A / P parity)
-            int kuse = 0;                 // key-ring loads consumed so far
             int nref = 0;                 // bf16 state refreshes consumed
             for (int c = 0; ok && c < nt; ++c) {
-                const int b = c & 1, r = c % R, gt = tile0 + c;
-                uint64_t *ph = (!PHI && !NORM) ? &full[s] : &phi_ready[s];
-                if (!wait_phase(ph, sph, ctl)) break;
+                const int b = c & 1, r = c % R, gt = tile0 + c, ks = c % NKV, qs = c % NQ;
+                uint64_t *ph = (!PHI && !NORM) ? &kv_full[ks] : &phi_ready[ks];
+                if (!wait_phase(ph, (c / NKV) & 1, ctl)) break;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)), va = smem_u32(stage_v(s));
+                const uint32_t qa = smem_u32(q_tile(qs)), ka = smem_u32(k_tile(ks)), va = smem_u32(v_tile(ks));
                 const uint32_t tO = tmem + Lay::T_O + b * T;
-                // blocks: n = 0 is the diagonal, n = 1..r the key tiles c - r .. c - 1 (ring)
+                // blocks: n = 0 is the diagonal, n = 1..r the key tiles c - r .. c - 1, still resident
                 const int nblk = 1 + r;
+                auto kv_slot = [&](int n) { return n == 0 ? ks : (c - r + n - 1) % NKV; };
                 // scores of block n into A[(kb + n) & 1]
                 auto scores = [&](int n) -> bool {
                     const int bb = (kb + n) & 1, use = (kb + n) >> 1;
                     if (kb + n >= 2 && !wait_phase(&a_free[bb], (use - 1) & 1, ctl)) return false;
                     const uint32_t tA = tmem + Lay::T_A + bb * Lay::A_STRIDE;
-                    if (n == 0) {
-                        tc_fence_after();
+                    const uint32_t kk = smem_u32(k_tile(kv_slot(n)));
+                    tc_fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
-                            const uint32_t ko = (ks >> 2) * Lay::K_BLK + (ks & 3) * 32;
-                            mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(ka, 16, 1024), ko),
-                                   ID_SCD, ks > 0);
-                        }
-                    } else {
-                        const int slot = (kuse + n - 1) % TW_KR, u = (kuse + n - 1) / TW_KR;
-                        uint64_t *kr = PHI ? &kready[slot] : &kfull[slot];
-                        if (!wait_phase(kr, u & 1, ctl)) return false;
-                        tc_fence_after();
-                        const uint32_t rk = smem_u32(ring_k(slot));
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
-                            mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(rk, 16, 1024), qo),
-                                   ID_SCO, ks > 0);
-                        }
+                    for (int ki = 0; ki < D / 16; ++ki) {
+                        const uint32_t qo = (ki >> 2) * T * 128 + (ki & 3) * 32;
+                        const uint32_t ko = (ki >> 2) * Lay::K_BLK + (ki & 3) * 32;
+                        mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(kk, 16, 1024), ko),
+                               n == 0 ? ID_SCD : ID_SCO, ki > 0);
                     }
                     mma_commit(&scores_done[bb]);
                     return true;
@@ -350,12 +325,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     if (!wait_phase(&p_ready[bb], use & 1, ctl)) return false;
                     tc_fence_after();
                     const uint32_t pa = smem_u32(p_tile(bb));
-                    const uint32_t vv = n == 0 ? va : smem_u32(ring_v((kuse + n - 1) % TW_KR));
+                    const uint32_t vv = smem_u32(v_tile(kv_slot(n)));
 #pragma unroll
-                    for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tO, desc_add(smem_desc(vv, T * 128, 1024), ks * 2048), desc_add(smem_desc(pa, 16, 1024), ks * 32),
+                    for (int ki = 0; ki < T / 16; ++ki)
+                        mma_ss(tO, desc_add(smem_desc(vv, T * 128, 1024), ki * 2048), desc_add(smem_desc(pa, 16, 1024), ki * 32),
                                ID_INTRA, 1);
-                    if (n > 0) mma_commit(&kfree[(kuse + n - 1) % TW_KR]);
                     return true;
                 };
                 if (!scores(0)) break;
@@ -367,16 +341,16 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t qo = (ks >> 2) * T * 128 + (ks & 3) * 32;
-                    mma_ts(tO, tSB + ks * 8, desc_add(smem_desc(qa, 16, 1024), qo), ID_INTER, ks > 0);
+                for (int ki = 0; ki < D / 16; ++ki) {
+                    const uint32_t qo = (ki >> 2) * T * 128 + (ki & 3) * 32;
+                    mma_ts(tO, tSB + ki * 8, desc_add(smem_desc(qa, 16, 1024), qo), ID_INTER, ki > 0);
                 }
                 // state: every tile joins the fp32 state; the copy is refreshed at chunk ends
                 if (gt + 1 < a.nch) {
 #pragma unroll
-                    for (int ks = 0; ks < T / 16; ++ks)
-                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), ks * 2048),
-                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), ks * 2048), ID_STATE, 1);
+                    for (int ki = 0; ki < T / 16; ++ki)
+                        mma_ss(tS, desc_add(smem_desc(va, T * 128, 1024), ki * 2048),
+                               desc_add(smem_desc(ka, Lay::K_BLK, 1024), ki * 2048), ID_STATE, 1);
                     if (r == R - 1) mma_commit(state_done);
                 }
                 // scores run one block ahead of the intra products (P is double-buffered)
@@ -387,10 +361,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 }
                 if (!bok) break;
                 kb += nblk;
-                kuse += r;
                 mma_commit(&o_done[b]);
-                mma_commit(&stage_free[s]);
-                if (++s == TW_STAGES) { s = 0; sph ^= 1; }
+                mma_commit(&q_free[qs]);
+                // the chunk's last tile: its K/V slots may be refilled
+                if (r == R - 1)
+                    for (int n = 0; n < R; ++n) mma_commit(&kv_free[(c - r + n) % NKV]);
             }
             mma_commit(drain);
             const uint64_t t0 = globaltimer();
@@ -408,18 +383,17 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
         const int kbk = g >> 3, ch = g & 7;
         const int q_swz = kbk * T * 128 + ((ch ^ (rg & 7)) << 4) + rg * 128;
         const int k_swz = kbk * Lay::K_BLK + ((ch ^ (rg & 7)) << 4) + rg * 128;
-        int s = 0, sph = 0, kuse = 0;
         if (PHI || NORM) {
             for (int c = 0; c < nt; ++c) {
-                const int r = c % R;
-                if (!group_wait(ft == 0, 1, &full[s], sph, nullptr, 0, false, ctl, NF)) break;
+                const int r = c % R, ks = c % NKV, qs = c % NQ;
+                if (!group_wait(ft == 0, 1, &kv_full[ks], (c / NKV) & 1, nullptr, 0, false, ctl, NF)) break;
                 if (NORM && !totals && r == 0) {
                     // a new chunk: its phi(q).z uses z at the chunk start
                     for (int i = ft; i < D; i += NF) zcs[i] = zs[i];
                     named_bar(1, NF);
                 }
-                uint4 *qp = (uint4 *)(stage_q(s) + q_swz);
-                uint4 *kp = (uint4 *)(stage_k(s) + k_swz);
+                uint4 *qp = (uint4 *)(q_tile(qs) + q_swz);
+                uint4 *kp = (uint4 *)(k_tile(ks) + k_swz);
                 uint4 wq[NR], wk[NR];
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
@@ -439,7 +413,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                         pk[e] = zr ? pack_bf16x2(zz[2 * e] - h0, zz[2 * e + 1] - h1) : pack_bf16x2(h0, h1);
                     }
                     const int row = T + zr;
-                    *(uint4 *)(stage_k(s) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
+                    *(uint4 *)(k_tile(ks) + zkb * Lay::K_BLK + row * 128 + ((zch ^ (row & 7)) << 4)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 if (PHI && !totals) {
@@ -483,7 +457,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     }
                 }
                 named_bar(1, NF);
-                if (ft == 0) mbar_arrive(&phi_ready[s]);
+                if (ft == 0) mbar_arrive(&phi_ready[ks]);
                 if (zupd) {
                     for (int i = ft; i < D; i += NF) {
                         float acc = 0.f;
@@ -492,31 +466,6 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                         zs[i] += acc;
                     }
                     named_bar(1, NF);
-                }
-                if (++s == TW_STAGES) { s = 0; sph ^= 1; }
-                // phi of the chunk's earlier key tiles, fetched again into the key ring
-                if (PHI && !totals) {
-                    bool ok = true;
-                    for (int k = 0; k < r; ++k, ++kuse) {
-                        const int slot = kuse % TW_KR;
-                        if (!group_wait(ft == 0, 1, &kfull[slot], (kuse / TW_KR) & 1, nullptr, 0, false, ctl, NF)) {
-                            ok = false;
-                            break;
-                        }
-                        uint4 *rp = (uint4 *)(ring_k(slot) + q_swz);
-#pragma unroll
-                        for (int n = 0; n < NR; ++n) {
-                            uint4 w = rp[n * RG * 8];
-                            uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) wv[e] = elu1_bf16x2(wv[e]);
-                            rp[n * RG * 8] = w;
-                        }
-                        fence_async_smem();
-                        named_bar(1, NF);
-                        if (ft == 0) mbar_arrive(&kready[slot]);
-                    }
-                    if (!ok) break;
                 }
             }
             if (totals && NORM)
@@ -635,21 +584,23 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
         }
     } else if (warp >= 8 + TW_FWARPS) {
         // ------------------------------------------------------------ output epilogue
+        // For each token a warp writes 32 neighbouring output columns (64 contiguous bytes)
+        // straight from registers; rows past L are skipped.
         const int q4 = warp & 3;
         const int ot = tid - 32 * (8 + TW_FWARPS);
+        // row j of O^T: lane j (dv = 128), or lane j%16 of quadrant j/16 (dv = 64)
         const int j = (DV == 128) ? 32 * q4 + lane : 16 * q4 + (lane & 15);
         const bool live = (DV == 128) || lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const bool odd = lane & 1;
-        uint8_t *const ob = o_tile + (j >> 6) * T * 128 + (((j & 7) & ~1) << 1);
-        const int jc = (j & 63) >> 3;
         for (int c = 0; c < nt && !totals; ++c) {
             const int b = c & 1, slot = c % TW_DEN;
             if (!group_wait(ot == 0, 3, &o_done[b], (c >> 1) & 1, &den_full[slot], (c / TW_DEN) & 1, NORM, ctl))
                 break;
             tc_fence_after();
-            if (ot == 0 && c >= 1) tma_wait_read_all();
-            named_bar(3, 128);
+            const int row0 = (tile0 + c) * T;
+            const int nrow = min(T, a.L - row0);   // rows of this tile inside the sequence
+            uint32_t *const o = (uint32_t *)((__nv_bfloat16 *)a.out + ((size_t)head * a.L + row0) * DV + (j & ~1));
             const uint32_t tO = tmem + Lay::T_O + b * T + lane_off;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -661,38 +612,29 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&o_free[b]);
                 }
-                float rd[32];
-                if (NORM) {
-                    const float4 *rp = (const float4 *)(rden + slot * T + 32 * h);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 v = rp[q];
-                        rd[4 * q] = v.x; rd[4 * q + 1] = v.y; rd[4 * q + 2] = v.z; rd[4 * q + 3] = v.w;
-                    }
-                }
+                const float2 *rp = (const float2 *)(rden + slot * T + 32 * h);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
                     if (NORM) {
-                        a0 *= rd[2 * u];
-                        a1 *= rd[2 * u + 1];
+                        const float2 f = rp[u];
+                        a0 *= f.x;
+                        a1 *= f.y;
                     }
+                    // lanes j, j^1 swap one value per pair of rows: each writes two neighbouring
+                    // columns of one row as a 32-bit word
                     const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
                     const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
                     const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-                    if (live) *(uint32_t *)(ob + tt * 128 + ((jc ^ (tt & 7)) << 4)) = wv;
+                    if (live && tt < nrow) o[(size_t)tt * (DV / 2)] = wv;
                 }
             }
-            fence_async_smem();
-            named_bar(3, 128);
-            if (ot == 0) {
-                for (int jb = 0; jb < DV / 64; ++jb)
-                    tma_store_3d(&a.tm_o, o_tile + jb * T * 128, jb * 64, (tile0 + c) * T, head);
-                tma_commit_group();
-                if (NORM) mbar_arrive(&den_empty[slot]);
+            if (NORM) {
+                // every thread has read this tile's 1/den
+                named_bar(3, 128);
+                if (ot == 0) mbar_arrive(&den_empty[slot]);
             }
         }
-        if (ot == 0) tma_wait_all();
     }
 
     tc_fence_before();
@@ -723,13 +665,14 @@ size_t tw_workspace(const Problem &p, int nseg)
 template <int D, int DV, int R, int FM, bool NORM>
 int launch_w(const Problem &p, int num_sms)
 {
-    using Lay = TwLayout<D, DV, NORM>;
+    using Lay = TwLayout<D, DV, R, NORM>;
     TwArgs a;
     memset(&a, 0, sizeof(a));
     const int BH = p.B * p.H;
     if (!make_map(&a.tm_q, p.q, BH, p.L, p.dk, 64) || !make_map(&a.tm_k, p.k, BH, p.L, p.dk, 64) ||
-        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, 64) || !make_map(&a.tm_o, p.out, BH, p.L, p.dv, 64))
+        !make_map(&a.tm_v, p.v, BH, p.L, p.dv, 64))
         return LA_ERR_CUDA;
+    a.out = p.out;
     a.L = p.L;
     a.nch = (p.L + 63) / 64;
     const int nseg = tw_segments(p, R, num_sms, &a.seg_tiles);
@@ -799,7 +742,8 @@ int tcw_plan(const Problem &p, int num_sms, la_plan_info *info)
     info->block = TW_THREADS;
     auto alloc = [&](auto d, auto dv) {
         constexpr int D = decltype(d)::value, DV = decltype(dv)::value;
-        return p.normalize ? TwLayout<D, DV, true>::ALLOC : TwLayout<D, DV, false>::ALLOC;
+        if (p.C == 128) return p.normalize ? TwLayout<D, DV, 2, true>::ALLOC : TwLayout<D, DV, 2, false>::ALLOC;
+        return p.normalize ? TwLayout<D, DV, 4, true>::ALLOC : TwLayout<D, DV, 4, false>::ALLOC;
     };
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;
