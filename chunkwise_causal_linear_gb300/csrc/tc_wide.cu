@@ -290,49 +290,58 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 if (ok) mma_commit(state_done);
                 ok = false;
             }
-            int kb = 0;                   // score blocks issued so far (A / P parity)
+            // Issue order of tile c: the first off-diagonal block's scores (the P warps need
+            // them next), inter, state, then the intra products, each block's scores issued
+            // ahead of the previous block's intra (the score accumulator and P are
+            // double-buffered); after the tile's commits, the next tile's diagonal scores.
+            // (Issuing those before this tile's last intra product, as the one-tile kernel
+            // does, measured slower here: it delays the commits that free K/V slots.)
+            auto wait_phi = [&](int c) {
+                uint64_t *ph = (!PHI && !NORM) ? &kv_full[c % NKV] : &phi_ready[c % NKV];
+                return wait_phase(ph, (c / NKV) & 1, ctl);
+            };
+            // scores of block n of local tile c into A[g & 1], g = the block's running index
+            auto scores = [&](int c, int n, int g) -> bool {
+                const int bb = g & 1, use = g >> 1;
+                if (g >= 2 && !wait_phase(&a_free[bb], (use - 1) & 1, ctl)) return false;
+                const uint32_t tA = tmem + Lay::T_A + bb * Lay::A_STRIDE;
+                const int ksn = n == 0 ? c % NKV : (c - c % R + n - 1) % NKV;
+                const uint32_t qa = smem_u32(q_tile(c % NQ)), kk = smem_u32(k_tile(ksn));
+                tc_fence_after();
+#pragma unroll
+                for (int ki = 0; ki < D / 16; ++ki) {
+                    const uint32_t qo = (ki >> 2) * T * 128 + (ki & 3) * 32;
+                    const uint32_t ko = (ki >> 2) * Lay::K_BLK + (ki & 3) * 32;
+                    mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(kk, 16, 1024), ko),
+                           n == 0 ? ID_SCD : ID_SCO, ki > 0);
+                }
+                mma_commit(&scores_done[bb]);
+                return true;
+            };
+            int kb = 0;                   // score blocks of the tiles before this one
             int nref = 0;                 // bf16 state refreshes consumed
+            if (ok && nt > 0) ok = wait_phi(0) && scores(0, 0, 0);
             for (int c = 0; ok && c < nt; ++c) {
                 const int b = c & 1, r = c % R, gt = tile0 + c, ks = c % NKV, qs = c % NQ;
-                uint64_t *ph = (!PHI && !NORM) ? &kv_full[ks] : &phi_ready[ks];
-                if (!wait_phase(ph, (c / NKV) & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(q_tile(qs)), ka = smem_u32(k_tile(ks)), va = smem_u32(v_tile(ks));
                 const uint32_t tO = tmem + Lay::T_O + b * T;
                 // blocks: n = 0 is the diagonal, n = 1..r the key tiles c - r .. c - 1, still resident
                 const int nblk = 1 + r;
-                auto kv_slot = [&](int n) { return n == 0 ? ks : (c - r + n - 1) % NKV; };
-                // scores of block n into A[(kb + n) & 1]
-                auto scores = [&](int n) -> bool {
-                    const int bb = (kb + n) & 1, use = (kb + n) >> 1;
-                    if (kb + n >= 2 && !wait_phase(&a_free[bb], (use - 1) & 1, ctl)) return false;
-                    const uint32_t tA = tmem + Lay::T_A + bb * Lay::A_STRIDE;
-                    const uint32_t kk = smem_u32(k_tile(kv_slot(n)));
-                    tc_fence_after();
-#pragma unroll
-                    for (int ki = 0; ki < D / 16; ++ki) {
-                        const uint32_t qo = (ki >> 2) * T * 128 + (ki & 3) * 32;
-                        const uint32_t ko = (ki >> 2) * Lay::K_BLK + (ki & 3) * 32;
-                        mma_ss(tA, desc_add(smem_desc(qa, 16, 1024), qo), desc_add(smem_desc(kk, 16, 1024), ko),
-                               n == 0 ? ID_SCD : ID_SCO, ki > 0);
-                    }
-                    mma_commit(&scores_done[bb]);
-                    return true;
-                };
                 // intra of block n: O^T += V_n^T P^T
                 auto intra = [&](int n) -> bool {
                     const int bb = (kb + n) & 1, use = (kb + n) >> 1;
                     if (!wait_phase(&p_ready[bb], use & 1, ctl)) return false;
                     tc_fence_after();
                     const uint32_t pa = smem_u32(p_tile(bb));
-                    const uint32_t vv = smem_u32(v_tile(kv_slot(n)));
+                    const uint32_t vv = smem_u32(v_tile(n == 0 ? ks : (c - r + n - 1) % NKV));
 #pragma unroll
                     for (int ki = 0; ki < T / 16; ++ki)
-                        mma_ss(tO, desc_add(smem_desc(vv, T * 128, 1024), ki * 2048), desc_add(smem_desc(pa, 16, 1024), ki * 32),
-                               ID_INTRA, 1);
+                        mma_ss(tO, desc_add(smem_desc(vv, T * 128, 1024), ki * 2048),
+                               desc_add(smem_desc(pa, 16, 1024), ki * 32), ID_INTRA, 1);
                     return true;
                 };
-                if (!scores(0)) break;
+                if (r >= 1 && !scores(c, 1, kb + 1)) break;
                 // inter from the chunk-start state copy (refreshed after the previous chunk)
                 if (c >= 2 && !wait_phase(&o_free[b], ((c >> 1) - 1) & 1, ctl)) break;
                 if (r == 0 && c >= 1) {
@@ -353,19 +362,19 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                                desc_add(smem_desc(ka, Lay::K_BLK, 1024), ki * 2048), ID_STATE, 1);
                     if (r == R - 1) mma_commit(state_done);
                 }
-                // scores run one block ahead of the intra products (P is double-buffered)
                 bool bok = true;
                 for (int n = 0; n < nblk && bok; ++n) {
-                    if (n + 1 < nblk) bok = scores(n + 1);
+                    if (n >= 1 && n + 1 < nblk) bok = scores(c, n + 1, kb + n + 1);
                     if (bok) bok = intra(n);
+                    // the chunk's last tile: key tile n - 1 of the chunk has had its last use
+                    if (bok && r == R - 1 && n >= 1) mma_commit(&kv_free[(c - r + n - 1) % NKV]);
                 }
                 if (!bok) break;
                 kb += nblk;
                 mma_commit(&o_done[b]);
                 mma_commit(&q_free[qs]);
-                // the chunk's last tile: its K/V slots may be refilled
-                if (r == R - 1)
-                    for (int n = 0; n < R; ++n) mma_commit(&kv_free[(c - r + n) % NKV]);
+                if (r == R - 1) mma_commit(&kv_free[ks]);
+                if (c + 1 < nt && !(wait_phi(c + 1) && scores(c + 1, 0, kb))) break;
             }
             mma_commit(drain);
             const uint64_t t0 = globaltimer();
