@@ -20,8 +20,9 @@
 // intra work per row grows with C and the state work per row shrinks with 1/C, as in the
 // page's cost model (section 3).
 //
-// Warp roles (as in the one-tile kernel): 0 TMA producer, 1 MMA issuer, 4-11 feature map,
-// 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue (rows stored from registers).
+// Warp roles (as in the one-tile kernel): 0 TMA producer, 1 MMA issuer, 2-4, 6-8, 10-11
+// feature map, 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue (rows stored
+// from registers).
 //
 // MMAs per query tile (bf16 in, fp32 accumulate), D = feature dim, T = 64:
 //   scores  A_k   = phi(Q) [phi(K_k); z]^T       M=T   N=T(+8)  K=D   per block k
@@ -47,6 +48,15 @@ namespace {
 
 constexpr int TW_THREADS = 640;
 constexpr int TW_FWARPS = 8;
+
+// The feature-map group is warps 2, 3, 4, 6, 7, 8, 10, 11, so that none shares a
+// sub-partition (warp % 4) with the MMA issuer (warp 1) and takes its issue slots.
+// Returns the warp's rank in the group, or -1.
+__device__ __forceinline__ int tw_phi_rank(int warp)
+{
+    if (warp < 2 || warp >= 12 || (warp & 3) == 1) return -1;
+    return warp - 2 - (warp > 5) - (warp > 9);
+}
 constexpr int TW_DEN = 4;
 constexpr int TW_SMEM = 232448 - 1024;   // opt-in shared memory less the alignment slack
 
@@ -381,9 +391,9 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
             while (!mbar_try_sleep(drain, 0, 200000u))
                 if (globaltimer() - t0 > ctl.timeout_ns) break;
         }
-    } else if (warp >= 4 && warp < 4 + TW_FWARPS) {
+    } else if (tw_phi_rank(warp) >= 0) {
         // ------------------------------------------------------------ feature map / z
-        const int ft = tid - 128;
+        const int ft = 32 * tw_phi_rank(warp) + lane;
         constexpr int NF = 32 * TW_FWARPS;
         constexpr int G = D / 8;
         constexpr int RG = NF / G;
