@@ -56,7 +56,7 @@ constexpr int LL_STAGES_TOT = 6;    // K, V (16 KB each)
 constexpr int LL_STAGE_AREA = LL_STAGES_MAIN * 4 * LL_TILE;
 static_assert(LL_STAGES_TOT * 2 * LL_TILE <= LL_STAGE_AREA, "stage area");
 static_assert(LL_C * LL_MAXNL * 4 <= LL_TILE, "lambda tile");
-constexpr int LL_N_BAR = 2 * LL_STAGES_TOT + 2 * LL_RING + 16;
+constexpr int LL_N_BAR = 2 * LL_STAGES_TOT + 2 * LL_RING + 16;   // all used
 
 // TMEM columns (M = 64 layout: row m at lane (m % 16) + 32 (m / 16))
 constexpr uint32_t LT_PS = 0;     // running segment state PS [d_k rows][d_v]
@@ -72,7 +72,9 @@ inline LlLayout ll_layout(int nlev)
 {
     LlLayout l;
     l.off_T = LL_STAGE_AREA;
-    l.off_P = l.off_T + nlev * LL_TILE;   // two P tiles (chunk parity)
+    // nlev block tiles, plus a second tile for level 0 (the block of one chunk closes after
+    // every other chunk, and is written while the previous one may still be read)
+    l.off_P = l.off_T + (nlev + 1) * LL_TILE;   // two P tiles (chunk parity)
     l.off_bar = l.off_P + 2 * LL_TILE;
     l.bytes = l.off_bar + LL_N_BAR * 8 + 16;
     l.alloc = l.bytes + 1024;
@@ -104,14 +106,15 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
     uint64_t *r_free = r_full + LL_RING;             // [RING]
     uint64_t *scores_done = r_free + LL_RING;
     uint64_t *a_free = scores_done + 1;
-    // p_ready and t_formed alternate by chunk parity: their producers may finish chunk i + 1
-    // before the MMA issuer waits for chunk i, and one barrier would then be two phases ahead
+    // p_ready alternates by chunk parity, t_formed and c_done by chunk mod 4: their producers
+    // may run one (p_ready) or two chunks (t_formed, c_done) ahead of the waiter, and one
+    // barrier must never be two phases ahead of it.
     uint64_t *p_ready = a_free + 1;                  // [2]
     uint64_t *state_done = p_ready + 2;
     uint64_t *ps_read = state_done + 1;              // PS copied out by the block-closing warps
-    uint64_t *t_formed = ps_read + 1;                // [2] the block closed after a chunk is in smem
-    uint64_t *c_done = t_formed + 2;                 // [2] every product of a chunk is in TMEM
-    uint64_t *drain = c_done + 2;
+    uint64_t *t_formed = ps_read + 1;                // [4] the block closed after a chunk is in smem
+    uint64_t *c_done = t_formed + 4;                 // [4] every product of a chunk is in TMEM
+    uint64_t *drain = c_done + 4;
     uint64_t *totals_done = drain + 1;
     uint32_t *tmem_slot = (uint32_t *)(sm + a.lay.off_bar + LL_N_BAR * 8);
     volatile int *abort_flag = (volatile int *)(sm + a.lay.off_bar + LL_N_BAR * 8 + 4);
@@ -149,10 +152,10 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
         mbar_init(&p_ready[1], 1);
         mbar_init(state_done, 1);
         mbar_init(ps_read, 4);
-        mbar_init(&t_formed[0], 1);
-        mbar_init(&t_formed[1], 1);
-        mbar_init(&c_done[0], 1);
-        mbar_init(&c_done[1], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&t_formed[i], 1);
+            mbar_init(&c_done[i], 1);
+        }
         mbar_init(drain, 1);
         mbar_init(totals_done, 1);
         *abort_flag = 0;
@@ -271,17 +274,23 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 };
                 int s = 0;                           // stage of chunk i
                 int s1 = 1 % nst, ph1 = (1 == nst) ? 1 : 0;  // stage of chunk i + 1
-                int kr = 0, slot = 0, rph = 0;       // ring uses so far, next slot and its phase
-                // one product into the next ring slot: 4 x K16 MMAs
-                auto product = [&](uint64_t dA, uint64_t dB) -> bool {
-                    if (kr >= LL_RING && !wait_phase(&r_free[slot], rph ^ 1, ctl)) return false;
-                    tc_fence_after();
+                int kr = 0, slot = 0;                // ring uses so far, next slot
+                // one product into the next ring slot (4 x K16 MMAs), its slot known to be free
+                auto issue = [&](uint64_t dA, uint64_t dB) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_ss(tmem + LT_R + 64 * slot, dA + 2 * ks, dB + 128 * ks, ID_AB, ks > 0);
                     mma_commit(&r_full[slot]);
                     ++kr;
-                    if (++slot == LL_RING) { slot = 0; rph ^= 1; }
+                    if (++slot == LL_RING) slot = 0;
+                };
+                // wait until the slots of the next n products are free: the output warps free
+                // the slots in order, so the last one being free means all of them are
+                auto slots_free = [&](int n) -> bool {
+                    const int kl = kr + n - 1;
+                    if (kl >= LL_RING && !wait_phase(&r_free[kl % LL_RING], ((kl / LL_RING) - 1) & 1, ctl))
+                        return false;
+                    tc_fence_after();
                     return true;
                 };
                 ok = front(0, 0, 0);
@@ -291,13 +300,24 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                     const uint64_t dQ = dQ_k(s), dVm = dV_m(s);
                     // P V first: its P was written a chunk ahead
                     if (!wait_phase(&p_ready[b], (i >> 1) & 1, ctl)) { ok = false; break; }
-                    if (!product(dP0 + (uint64_t)(b * (LL_TILE >> 4)), dVm)) { ok = false; break; }
-                    if (i >= 1 && !wait_phase(&t_formed[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl)) { ok = false; break; }
-                    // set bits of the chunk index, lowest first (one product each)
-                    for (uint32_t bits = (uint32_t)(tile0 + i) & ((1u << a.nlev) - 1u); bits && ok; bits &= bits - 1u)
-                        ok = product(dQ, dT0 + (uint64_t)((__ffs(bits) - 1) * (LL_TILE >> 4)));
+                    if (!slots_free(1)) { ok = false; break; }
+                    issue(dP0 + (uint64_t)(b * (LL_TILE >> 4)), dVm);
+                    if (i >= 1 && !wait_phase(&t_formed[(i - 1) & 3], ((i - 1) >> 2) & 1, ctl)) { ok = false; break; }
+                    // set bits of the chunk index, lowest first (one product each), in batches of
+                    // up to LL_RING behind one wait; the block of level 0 (chunk i - 1, i odd)
+                    // sits in its second tile when bit 1 of i is set
+                    uint32_t bits = (uint32_t)(tile0 + i) & ((1u << a.nlev) - 1u);
+                    while (bits && ok) {
+                        const int nb = min(__popc(bits), LL_RING);
+                        if (!slots_free(nb)) { ok = false; break; }
+                        for (int n = 0; n < nb; ++n, bits &= bits - 1u) {
+                            const int j = __ffs(bits) - 1;
+                            const int jt = (j == 0 && ((i >> 1) & 1)) ? a.nlev : j;
+                            issue(dQ, dT0 + (uint64_t)(jt * (LL_TILE >> 4)));
+                        }
+                    }
                     if (!ok) break;
-                    mma_commit(&c_done[b]);
+                    mma_commit(&c_done[i & 3]);
                     mma_commit(&stage_free[s]);
                     s = s1;
                     if (++s1 == nst) { s1 = 0; ph1 ^= 1; }
@@ -405,11 +425,13 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ps_read);
                 const int x = i + 1;  // position after this chunk
-                // the level MMAs of chunk i - 1 (issued after this chunk's state update) may
-                // still read the tile about to be overwritten: wait until they are done.  (Waiting on every chunk also keeps t_formed
-                // at most one phase ahead of the MMA issuer.)
-                if (i >= 1 &&
-                    !group_wait(ct == 0, 4, &c_done[(i - 1) & 1], ((i - 1) >> 1) & 1, nullptr, 0, false, ctl))
+                // The tile about to be overwritten was last read by the level products of chunk
+                // x - 2^r - 1 <= i - 2 (r >= 1), or, for level 0 with its two tiles, of chunk
+                // i - 3: wait until chunk i - 2's products are done.  (Waiting on every chunk also
+                // keeps t_formed at most two chunks ahead of the MMA issuer, which its four
+                // barriers allow.)
+                if (i >= 2 &&
+                    !group_wait(ct == 0, 4, &c_done[(i - 2) & 3], ((i - 2) >> 2) & 1, nullptr, 0, false, ctl))
                     break;
                 if (x < nloc && row_lane) {
                     const int d = __popc(x), r = __ffs(x) - 1;
@@ -418,7 +440,8 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                     // it closes at a position one level below x (none does if x is odd).
                     const float4 *src = (const float4 *)(stack + (size_t)(d >= 2 ? d - 2 : 0) * LL_D * LL_D);
                     float4 *dst = (float4 *)(stack + (size_t)(d - 1) * LL_D * LL_D);
-                    uint8_t *row = tbuf(r) + m * 128;
+                    // level 0 alternates between its two tiles (bit 1 of x)
+                    uint8_t *row = tbuf((r == 0 && ((x >> 1) & 1)) ? a.nlev : r) + m * 128;
 #pragma unroll
                     for (int ck = 0; ck < 8; ++ck) {
                         const uint32_t *rr = ck < 4 ? r0 : r1;
@@ -442,7 +465,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 }
                 fence_async_smem();
                 named_bar(4, 128);
-                if (ct == 0) mbar_arrive(&t_formed[i & 1]);
+                if (ct == 0) mbar_arrive(&t_formed[i & 3]);
             }
         }
     } else if (warp >= 12 && !totals) {
