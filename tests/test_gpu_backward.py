@@ -96,6 +96,31 @@ def test_backward_matches_oracle(base, over, C, gamma):
             assert_close(g, r, f"{name} {base} {over} C={C} gamma={gamma} path={path}")
 
 
+FULL_CASES = [
+    # (benchmark workload, heads compared row by row; None: every head)
+    ("elu1-norm-d128-L8192", (0, 63, 127)),
+    ("identity-d64-L2048", None),
+]
+
+
+@pytest.mark.parametrize("base,heads", FULL_CASES)
+def test_backward_full_size(base, heads):
+    """The benchmark's backward workloads at full size, on the path AUTO takes (the tensor
+    cores), against the oracle's gradients: every row and every output of the listed heads.
+    The oracle's plain chain rule costs O(L^2 d) per head, about 20 s at L = 8192 and
+    d = 128, so the default workload compares its first, a middle and its last head; the
+    short-sequence workload compares all of them."""
+    w = workload(base)
+    inp = synth.make_inputs(w, seed=43)
+    do = dout_for(w, 43)
+    got = run_bwd(w, inp, do, 64, 1.0, 0)
+    n = w["B"] * w["H"]
+    hs = list(range(n)) if heads is None else list(heads)
+    ref = oracle_bwd(w, synth.make_inputs(w, seed=43, heads=hs), do[hs])
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g[hs], r, f"{name} {base} full size, heads {hs}")
+
+
 def test_backward_tensor_core_route_is_taken():
     """LA_PATH_TC succeeds where the route applies and is refused where it does not."""
     import torch
