@@ -66,6 +66,8 @@ CASES = [
     ("favor-m256-d64-L16384", dict(B=1, H=1, L=30, normalize=False)),
     ("loglinear-d64-L65536", dict(B=1, H=2, L=100)),
     ("loglinear-d64-L65536", dict(B=1, H=1, L=64, dv=40)),
+    # the benchmark's decoding configuration: all 128 heads of B8 H16 d128 per step
+    ("elu1-norm-d128-L8192", dict(L=48)),
 ]
 
 
