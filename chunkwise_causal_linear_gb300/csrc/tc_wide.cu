@@ -49,6 +49,31 @@ namespace {
 constexpr int TW_THREADS = 640;
 constexpr int TW_FWARPS = 8;
 
+// TMEM loads of 16 lanes spread over all 32 threads of a warp (shape 16x256b): thread i
+// gets lane i/4 in registers 4k, 4k+1 and lane 8 + i/4 in registers 4k+2, 4k+3, at columns
+// 8k + 2 (i % 4) and the next one (k = 0 .. repetitions-1).  An M = 64 accumulator keeps its
+// 16 rows of a lane quadrant in that quadrant's first 16 lanes.
+__device__ __forceinline__ void tw_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tw_ld16x256_x1(uint32_t taddr, uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // The feature-map group is warps 2, 3, 4, 6, 7, 8, 10, 11, so that none shares a
 // sub-partition (warp % 4) with the MMA issuer (warp 1) and takes its issue slots.
 // Returns the warp's rank in the group, or -1.
@@ -494,8 +519,6 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
         // ------------------------------------------------------------ scores -> P, state copy
         const int q4 = warp & 3;
         const int pt = tid - 32 * (4 + TW_FWARPS);
-        const int t = 16 * q4 + (lane & 15);
-        const bool row_lane = lane < 16;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         if (totals) {
             const int jr = (DV == 128) ? 32 * q4 + lane : 16 * q4 + (lane & 15);
@@ -518,10 +541,15 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 }
             }
         }
+        // Each thread owns half of two rows of the block: rows ta = 16 q4 + lane/4 and tb = ta + 8,
+        // columns 8k + 2 (lane % 4) and the next one (k = 0..7), as a 16x256b TMEM load
+        // delivers them; the four threads of a row pool their row sums with shuffles.
+        const int ta = 16 * q4 + (lane >> 2), tb = ta + 8, cpos = lane & 3;
         int kb = 0, nref = 0;
         for (int c = 0; c < nt && !totals; ++c) {
             const int slot = c % TW_DEN, r = c % R, gt = tile0 + c;
-            float rsa[4] = {0.f, 0.f, 0.f, 0.f}, dz = 0.f;  // row sum: four short chains
+            float rsa[2] = {0.f, 0.f}, rsb[2] = {0.f, 0.f};  // this thread's part of the row sums
+            float dza = 0.f, dzb = 0.f;                      // phi(q).z at the chunk start (cpos 0)
             bool ok = true;
             for (int n = 0; n <= r && ok; ++n, ++kb) {
                 const int bb = kb & 1;
@@ -534,44 +562,44 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 tc_fence_after();
                 const uint32_t tA = tmem + Lay::T_A + bb * Lay::A_STRIDE + lane_off;
                 if (NORM && n == 0) {
-                    uint32_t rz[8];
-                    tmem_ld8(tA + T, rz);
+                    uint32_t rz[4];
+                    tw_ld16x256_x1(tA + T, rz);  // columns T, T+1: the z rows (hi, lo)
                     tmem_wait_ld();
-                    dz = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);  // phi(q_t).z at the chunk start
+                    dza = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);
+                    dzb = __uint_as_float(rz[2]) + __uint_as_float(rz[3]);
                 }
+                uint32_t rr[32];
+                tw_ld16x256_x8(tA, rr);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_free[bb]);
+                uint8_t *pa = p_tile(bb) + ta * 128 + 4 * cpos, *pb = p_tile(bb) + tb * 128 + 4 * cpos;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t rr[32];
-                    tmem_ld32(tA + 32 * h, rr);
-                    tmem_wait_ld();
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&a_free[bb]);
-                    }
-                    if (row_lane) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            // diagonal block: keys s <= t; earlier key tiles: all keys
-                            const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
-                            const float v0 = (n > 0 || s0 <= t) ? __uint_as_float(rr[2 * e]) : 0.f;
-                            const float v1 = (n > 0 || s1 <= t) ? __uint_as_float(rr[2 * e + 1]) : 0.f;
-                            rsa[e & 3] += v0 + v1;
-                            pk[e] = pack_bf16x2(v0, v1);
-                        }
-                        uint8_t *prow = p_tile(bb) + t * 128;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int chn = 4 * h + q;
-                            *(uint4 *)(prow + ((chn ^ (t & 7)) << 4)) =
-                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        }
+                for (int k = 0; k < 8; ++k) {
+                    // diagonal block: keys s <= t; earlier key tiles: all keys
+                    const int s0 = 8 * k + 2 * cpos, s1 = s0 + 1;
+                    const float a0 = (n > 0 || s0 <= ta) ? __uint_as_float(rr[4 * k]) : 0.f;
+                    const float a1 = (n > 0 || s1 <= ta) ? __uint_as_float(rr[4 * k + 1]) : 0.f;
+                    const float b0 = (n > 0 || s0 <= tb) ? __uint_as_float(rr[4 * k + 2]) : 0.f;
+                    const float b1 = (n > 0 || s1 <= tb) ? __uint_as_float(rr[4 * k + 3]) : 0.f;
+                    rsa[k & 1] += a0 + a1;
+                    rsb[k & 1] += b0 + b1;
+                    *(uint32_t *)(pa + ((k ^ (ta & 7)) << 4)) = pack_bf16x2(a0, a1);
+                    *(uint32_t *)(pb + ((k ^ (tb & 7)) << 4)) = pack_bf16x2(b0, b1);
+                }
+                if (NORM && n == r) {
+                    float sa = rsa[0] + rsa[1], sb = rsb[0] + rsb[1];
+                    sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+                    sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+                    sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+                    sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+                    // fast division: 1/den only scales the fp32 row before its bf16 rounding
+                    if (cpos == 0) {
+                        rden[slot * T + ta] = __fdividef(1.f, dza + sa);
+                        rden[slot * T + tb] = __fdividef(1.f, dzb + sb);
                     }
                 }
-                // fast division: 1/den only scales the fp32 row before its bf16 rounding
-                if (NORM && n == r && row_lane)
-                    rden[slot * T + t] = __fdividef(1.f, dz + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])));
                 fence_async_smem();
                 named_bar(2, 128);
                 if (pt == 0) {
