@@ -714,6 +714,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
         const int pt = tid - 32 * (4 + TC_FWARPS);
         const int t = 16 * q4 + (lane & 15);  // M = 64 TMEM layout: row t at lane t%16 of quadrant t/16
         const bool row_lane = lane < 16;
+        const int ta = 16 * q4 + (lane >> 2), tb = ta + 8, cpos = lane & 3;  // 16x256b loads
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         if (totals) {
             // this segment's total: S^T rows (fp32) to the workspace
@@ -761,72 +762,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                             ((c / TC_DEN) - 1) & 1, NORM && c >= TC_DEN, ctl))
                 break;
             tc_fence_after();
-            // one 32-column half of the scores row at a time (register budget).  With one chunk
-            // per tile, rows 0-31 (warps 0, 1 of the group) keep nothing from columns 32-63: their
-            // P there is the zero block written at the start, and they load only the first half.
+            // Each thread owns half of two rows: ta = 16 q4 + lane/4 and tb = ta + 8, columns
+            // 8k + 2 (lane % 4) and the next one, as a 16x256b TMEM load delivers them; the four
+            // threads of a row pool their row sums with shuffles.  With one chunk per tile,
+            // rows 0-31 (warps 0, 1 of the group) keep nothing from columns 32-63: their P there
+            // is the zero block written at the start, and they load only the first half.
             const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off;
-            const int nh = (CH == C && q4 < 2) ? 1 : 2;
-            float rsa[4] = {0.f, 0.f, 0.f, 0.f}, dz = 0.f;  // row sum: four short chains
+            const int nh = (CH == C && q4 < 2) ? 1 : 2;  // 32-column halves to read
+            float rsa[2] = {0.f, 0.f}, rsb[2] = {0.f, 0.f};  // this thread's part of the row sums
+            uint32_t rz[4];
+            uint8_t *pa = p_tile + b * Lay::P_SET + ta * 128 + 4 * cpos;
+            uint8_t *pb = p_tile + b * Lay::P_SET + tb * 128 + 4 * cpos;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (h >= nh) break;
-                uint32_t r[32];
-                tmem_ld32(tA + 32 * h, r);
-                if (NORM && h == 0) {
-                    // phi(q_t).z_c (hi + lo), loaded with the first half
-                    uint32_t rz[8];
-                    tmem_ld8(tA + C, rz);
-                    tmem_wait_ld();
-                    dz = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);
-                } else {
-                    tmem_wait_ld();
-                }
+                uint32_t r[32];  // r[0..15]: columns 32h .. 32h+31
+                tmem_ld16x256_x4(tA + 32 * h, r);
+                if (NORM && h == 0) tmem_ld16x256_x1(tA + C, rz);  // columns C, C+1: phi(q_t).z_c (hi, lo)
+                tmem_wait_ld();
                 if (h == nh - 1) tc_fence_before();  // scores buffer b read (see the MMA issuer)
-                if (row_lane) {
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        // P keeps s in t's chunk with s <= t (block-diagonal causal mask at
-                        // CH); the normaliser's row sum keeps every s <= t of the tile
-                        const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
-                        const float v0 = (s0 <= t && !NC) ? __uint_as_float(r[2 * e]) : 0.f;
-                        const float v1 = (s1 <= t && !NC) ? __uint_as_float(r[2 * e + 1]) : 0.f;
-                        rsa[e & 3] += v0 + v1;
-                        if (CH == C) {
-                            pk[e] = pack_bf16x2(v0, v1);
-                        } else {
-                            const int tlo = t & ~(CH - 1);
-                            pk[e] = pack_bf16x2(s0 >= tlo ? v0 : 0.f, s1 >= tlo ? v1 : 0.f);
-                        }
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    // P keeps s in t's chunk with s <= t (block-diagonal causal mask at CH); the
+                    // normaliser's row sum keeps every s <= t of the tile
+                    const int k = 4 * h + k4, s0 = 8 * k + 2 * cpos, s1 = s0 + 1;
+                    const float a0 = s0 <= ta ? __uint_as_float(r[4 * k4]) : 0.f;
+                    const float a1 = s1 <= ta ? __uint_as_float(r[4 * k4 + 1]) : 0.f;
+                    const float b0 = s0 <= tb ? __uint_as_float(r[4 * k4 + 2]) : 0.f;
+                    const float b1 = s1 <= tb ? __uint_as_float(r[4 * k4 + 3]) : 0.f;
+                    rsa[k4 & 1] += a0 + a1;
+                    rsb[k4 & 1] += b0 + b1;
+                    uint32_t wa, wb;
+                    if (CH == C) {
+                        wa = pack_bf16x2(a0, a1);
+                        wb = pack_bf16x2(b0, b1);
+                    } else {
+                        const int la = ta & ~(CH - 1), lb = tb & ~(CH - 1);
+                        wa = pack_bf16x2(s0 >= la ? a0 : 0.f, s1 >= la ? a1 : 0.f);
+                        wb = pack_bf16x2(s0 >= lb ? b0 : 0.f, s1 >= lb ? b1 : 0.f);
                     }
-                    uint8_t *prow = p_tile + b * Lay::P_SET + t * 128;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chn = 4 * h + q;
-                        *(uint4 *)(prow + ((chn ^ (t & 7)) << 4)) =
-                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                    }
+                    const int oa = (k ^ (ta & 7)) << 4, ob = (k ^ (tb & 7)) << 4;
+                    *(uint32_t *)(pa + oa) = wa;
+                    *(uint32_t *)(pb + ob) = wb;
                     if (FO) {
                         // P's lo tile: the rounding residue of each kept score (CH == C here)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int s0 = 32 * h + 2 * e, s1 = s0 + 1;
-                            const float v0 = s0 <= t ? __uint_as_float(r[2 * e]) : 0.f;
-                            const float v1 = s1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
-                            pk[e] = pack_bf16x2(lo_of(v0), lo_of(v1));
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int chn = 4 * h + q;
-                            *(uint4 *)(prow + Lay::P_BYTES + ((chn ^ (t & 7)) << 4)) =
-                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        }
+                        *(uint32_t *)(pa + Lay::P_BYTES + oa) = pack_bf16x2(lo_of(a0), lo_of(a1));
+                        *(uint32_t *)(pb + Lay::P_BYTES + ob) = pack_bf16x2(lo_of(b0), lo_of(b1));
                     }
                 }
             }
             // den = phi(q_t).z_c + masked row sum
             // (fast division: 1/den only scales the fp32 row before its bf16 rounding)
-            if (NORM && row_lane) rden[slot * C + t] = __fdividef(1.f, dz + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])));
+            if (NORM) {
+                float sa = rsa[0] + rsa[1], sb = rsb[0] + rsb[1];
+                sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+                sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+                sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+                sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+                if (cpos == 0) {
+                    rden[slot * C + ta] = __fdividef(1.f, __uint_as_float(rz[0]) + __uint_as_float(rz[1]) + sa);
+                    rden[slot * C + tb] = __fdividef(1.f, __uint_as_float(rz[2]) + __uint_as_float(rz[3]) + sb);
+                }
+            }
             fence_async_smem();
             named_bar(2, 128);
             if (pt == 0) {

@@ -49,31 +49,6 @@ namespace {
 constexpr int TW_THREADS = 640;
 constexpr int TW_FWARPS = 8;
 
-// TMEM loads of 16 lanes spread over all 32 threads of a warp (shape 16x256b): thread i
-// gets lane i/4 in registers 4k, 4k+1 and lane 8 + i/4 in registers 4k+2, 4k+3, at columns
-// 8k + 2 (i % 4) and the next one (k = 0 .. repetitions-1).  An M = 64 accumulator keeps its
-// 16 rows of a lane quadrant in that quadrant's first 16 lanes.
-__device__ __forceinline__ void tw_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tw_ld16x256_x1(uint32_t taddr, uint32_t (&r)[4])
-{
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr)
-                 : "memory");
-}
-
 // The feature-map group is warps 2, 3, 4, 6, 7, 8, 10, 11, so that none shares a
 // sub-partition (warp % 4) with the MMA issuer (warp 1) and takes its issue slots.
 // Returns the warp's rank in the group, or -1.
@@ -563,13 +538,13 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 const uint32_t tA = tmem + Lay::T_A + bb * Lay::A_STRIDE + lane_off;
                 if (NORM && n == 0) {
                     uint32_t rz[4];
-                    tw_ld16x256_x1(tA + T, rz);  // columns T, T+1: the z rows (hi, lo)
+                    tmem_ld16x256_x1(tA + T, rz);  // columns T, T+1: the z rows (hi, lo)
                     tmem_wait_ld();
                     dza = __uint_as_float(rz[0]) + __uint_as_float(rz[1]);
                     dzb = __uint_as_float(rz[2]) + __uint_as_float(rz[3]);
                 }
                 uint32_t rr[32];
-                tw_ld16x256_x8(tA, rr);
+                tmem_ld16x256_x8(tA, rr);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
