@@ -506,9 +506,11 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         }
     } else if (warp >= 12 && warp < 16 && !totals) {
         // ------------------------------------------------------------ scores -> P (M = 64 rows)
+        // Each thread owns half of two rows: ta = 16 q4 + lane/4 and tb = ta + 8, columns
+        // 8k + 2 (lane % 4) and the next one, as a 16x256b TMEM load delivers them; the four
+        // threads of a row pool their row sums with shuffles.
         const int q4 = warp & 3, pt = tid - 384;
-        const int t = 16 * q4 + (lane & 15);
-        const bool row_lane = lane < 16;
+        const int ta = 16 * q4 + (lane >> 2), tb = ta + 8, cpos = lane & 3;
         const uint32_t tA = tmem + FT_A + ((uint32_t)(32 * q4) << 16);
         for (int c = 0; c < nch; ++c) {
             const int slot = c % FV_DEN;
@@ -516,31 +518,36 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
                             NORM && c >= FV_DEN, ctl))
                 break;
             tc_fence_after();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tA, r0);
-            tmem_ld32(tA + 32, r1);
+            uint32_t r[32];
+            tmem_ld16x256_x8(tA, r);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_free);
-            if (row_lane) {
-                float rsa[4] = {0.f, 0.f, 0.f, 0.f};  // row sum: four short chains
-                uint8_t *prow = sm + FV_P + t * 128;
+            float rsa[2] = {0.f, 0.f}, rsb[2] = {0.f, 0.f};  // row sums: two short chains each
+            uint8_t *pa = sm + FV_P + ta * 128 + 4 * cpos, *pb = sm + FV_P + tb * 128 + 4 * cpos;
 #pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = 8 * ck + 2 * e, s1 = s0 + 1;
-                        const uint32_t *rr = s0 < 32 ? r0 : r1;
-                        const float v0 = (!NC && s0 <= t) ? __uint_as_float(rr[s0 & 31]) : 0.f;
-                        const float v1 = (!NC && s1 <= t) ? __uint_as_float(rr[s1 & 31]) : 0.f;
-                        rsa[e] += v0 + v1;
-                        w[e] = pack_bf16x2(v0, v1);
-                    }
-                    *(uint4 *)(prow + ((ck ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int k = 0; k < 8; ++k) {
+                const int s0 = 8 * k + 2 * cpos, s1 = s0 + 1;
+                const float a0 = (!NC && s0 <= ta) ? __uint_as_float(r[4 * k]) : 0.f;
+                const float a1 = (!NC && s1 <= ta) ? __uint_as_float(r[4 * k + 1]) : 0.f;
+                const float b0 = (!NC && s0 <= tb) ? __uint_as_float(r[4 * k + 2]) : 0.f;
+                const float b1 = (!NC && s1 <= tb) ? __uint_as_float(r[4 * k + 3]) : 0.f;
+                rsa[k & 1] += a0 + a1;
+                rsb[k & 1] += b0 + b1;
+                *(uint32_t *)(pa + ((k ^ (ta & 7)) << 4)) = pack_bf16x2(a0, a1);
+                *(uint32_t *)(pb + ((k ^ (tb & 7)) << 4)) = pack_bf16x2(b0, b1);
+            }
+            if (NORM) {
+                float sa = rsa[0] + rsa[1], sb = rsb[0] + rsb[1];
+                sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+                sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+                sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+                sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+                if (cpos == 0) {
+                    den_intra[slot * FV_C + ta] = sa;
+                    den_intra[slot * FV_C + tb] = sb;
                 }
-                if (NORM) den_intra[slot * FV_C + t] = (rsa[0] + rsa[1]) + (rsa[2] + rsa[3]);
             }
             fence_async_smem();
             named_bar(2, 128);
@@ -551,43 +558,44 @@ __global__ void __launch_bounds__(FV_THREADS, 1) tc_favor_kernel(const __grid_co
         }
     } else if (warp >= 16 && !totals) {
         // ------------------------------------------------------------ output rows -> global
+        // Each thread owns half of two rows, ta = 16 q4 + lane/4 and tb = ta + 8 (columns
+        // 8k + 2 (lane % 4) and the next one), as a 16x256b TMEM load delivers them.
         const int q4 = warp & 3, ot = tid - 512;
-        const int t = 16 * q4 + (lane & 15);
-        const bool row_lane = lane < 16;
+        const int ta = 16 * q4 + (lane >> 2), tb = ta + 8, cpos = lane & 3;
         for (int c = 0; c < nch; ++c) {
             const int slot = c % FV_DEN;
-            const int row = (tile0 + c) * FV_C + t;
+            const int row0 = (tile0 + c) * FV_C;
             if (!group_wait(ot == 0, 3, o_done, c & 1, &den_full[slot], (c / FV_DEN) & 1, NORM, ctl))
                 break;
             tc_fence_after();
             const uint32_t tO = tmem + FT_O + ((uint32_t)(32 * q4) << 16);
-            uint32_t r0[32], r1[32], rz[8];
-            tmem_ld32(tO, r0);
-            tmem_ld32(tO + 32, r1);
-            tmem_ld8(tO + 64, rz);
+            uint32_t r[32], rz[4];
+            tmem_ld16x256_x8(tO, r);
+            if (NORM) tmem_ld16x256_x1(tO + 64, rz);  // columns 64, 65: phi(q_t).z (hi, lo)
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-            float inv = 1.f;
-            if (NORM && row_lane)
-                // fast division: 1/den only scales the fp32 row before its bf16 rounding
-                inv = __fdividef(1.f, __uint_as_float(rz[0]) + __uint_as_float(rz[1]) + den_intra[slot * FV_C + t]);
+            float inva = 1.f, invb = 1.f;
+            if (NORM) {
+                // fast division: 1/den only scales the fp32 row before its bf16 rounding; the
+                // thread with the z columns (lane % 4 == 0) shares it with its row's others
+                if (cpos == 0) {
+                    inva = __fdividef(1.f, __uint_as_float(rz[0]) + __uint_as_float(rz[1]) + den_intra[slot * FV_C + ta]);
+                    invb = __fdividef(1.f, __uint_as_float(rz[2]) + __uint_as_float(rz[3]) + den_intra[slot * FV_C + tb]);
+                }
+                inva = __shfl_sync(0xffffffffu, inva, lane & ~3);
+                invb = __shfl_sync(0xffffffffu, invb, lane & ~3);
+            }
             named_bar(3, 128);
             if (NORM && ot == 0) mbar_arrive(&den_empty[slot]);
-            if (row_lane && row < a.L) {
-                uint4 *dst = (uint4 *)(a.out + ((size_t)head * a.L + row) * FV_DV);
+            uint32_t *da = (uint32_t *)(a.out + ((size_t)head * a.L + row0 + ta) * FV_DV) + cpos;
+            uint32_t *db = (uint32_t *)(a.out + ((size_t)head * a.L + row0 + tb) * FV_DV) + cpos;
+            const bool va = row0 + ta < a.L, vb = row0 + tb < a.L;
 #pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    const uint32_t *rr = ck < 4 ? r0 : r1;
-                    const int i0 = (8 * ck) & 31;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(rr[i0 + 2 * e]) * inv,
-                                           __uint_as_float(rr[i0 + 2 * e + 1]) * inv);
-                    dst[ck] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
+            for (int k = 0; k < 8; ++k) {
+                if (va) da[4 * k] = pack_bf16x2(__uint_as_float(r[4 * k]) * inva, __uint_as_float(r[4 * k + 1]) * inva);
+                if (vb) db[4 * k] = pack_bf16x2(__uint_as_float(r[4 * k + 2]) * invb, __uint_as_float(r[4 * k + 3]) * invb);
             }
         }
     }
