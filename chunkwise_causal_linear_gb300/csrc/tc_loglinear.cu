@@ -330,56 +330,52 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
         }
     } else if (warp >= 4 && warp < 8 && !totals) {
         // ------------------------------------------------------------ scores -> P (intra mask)
+        // Each thread owns half of two rows, ta = 16 q4 + lane/4 and tb = ta + 8: columns
+        // 8k + 2 (lane % 4) and the next one (k = 0..7), as a 16x256b TMEM load delivers them.
         const int q4 = warp & 3, pt = tid - 128;
-        const int t = 16 * q4 + (lane & 15);
-        const int t8 = t >> 3, t7 = t & 7;
-        const bool row_lane = lane < 16;
+        const int cpos = lane & 3;
+        const int trow[2] = {16 * q4 + (lane >> 2), 16 * q4 + 8 + (lane >> 2)};
         const uint32_t tA = tmem + LT_A + ((uint32_t)(32 * q4) << 16);
         int s = 0, ph = 0;
         for (int i = 0; i < nloc; ++i) {
             if (!group_wait(pt == 0, 2, scores_done, i & 1, &full[s], ph, true, ctl)) break;
             tc_fence_after();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tA, r0);
-            tmem_ld32(tA + 32, r1);
+            uint32_t r[32];
+            tmem_ld16x256_x8(tA, r);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_free);
-            if (row_lane) {
-                // lambda_t^(l) for the intra levels 0..6.  Column block ck (8 keys) against
-                // row block t8: below the diagonal the level is 4 + floor(log2(ck ^ t8)),
-                // on it 1 + floor(log2(e ^ t7)) (0 on the diagonal element).
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                // lambda_t^(l) for the intra levels 0..6.  Column block k (8 keys) against row
+                // block t8: below the diagonal the level is 4 + floor(log2(k ^ t8)), on it
+                // 1 + floor(log2(e ^ t7)) (0 on the diagonal element).
+                const int t = trow[hr], t8 = t >> 3, t7 = t & 7;
                 const bool valid = (tile0 + i) * LL_C + t < a.L;
                 const float *lrow = stage_l(s) + t * NL;
                 float lw[LL_LOG2C + 1];
 #pragma unroll
                 for (int l = 0; l <= LL_LOG2C; ++l) lw[l] = valid ? lrow[l] : 0.f;
-                uint8_t *prow = sm + a.lay.off_P + (i & 1) * LL_TILE + t * 128;
+                uint8_t *prow = sm + a.lay.off_P + (i & 1) * LL_TILE + t * 128 + 4 * cpos;
 #pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    const uint32_t *rr = ck < 4 ? r0 : r1;
-                    const int i0 = (8 * ck) & 31;
-                    float v[8];
-                    if (ck < t8) {
-                        const int x = ck ^ t8;
+                for (int k = 0; k < 8; ++k) {
+                    const float x0 = __uint_as_float(r[4 * k + 2 * hr]), x1 = __uint_as_float(r[4 * k + 2 * hr + 1]);
+                    float v0 = 0.f, v1 = 0.f;
+                    if (k < t8) {
+                        const int x = k ^ t8;
                         const float w = x >= 4 ? lw[6] : (x >= 2 ? lw[5] : lw[4]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i0 + e]) * w;
-                    } else if (ck == t8) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int y = e ^ t7;
-                            const float w = y == 0 ? lw[0] : (y >= 4 ? lw[3] : (y >= 2 ? lw[2] : lw[1]));
-                            v[e] = e <= t7 ? __uint_as_float(rr[i0 + e]) * w : 0.f;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                        v0 = x0 * w;
+                        v1 = x1 * w;
+                    } else if (k == t8) {
+                        const int e0 = 2 * cpos, e1 = e0 + 1;
+                        const int y0 = e0 ^ t7, y1 = e1 ^ t7;
+                        const float w0 = y0 == 0 ? lw[0] : (y0 >= 4 ? lw[3] : (y0 >= 2 ? lw[2] : lw[1]));
+                        const float w1 = y1 == 0 ? lw[0] : (y1 >= 4 ? lw[3] : (y1 >= 2 ? lw[2] : lw[1]));
+                        v0 = e0 <= t7 ? x0 * w0 : 0.f;
+                        v1 = e1 <= t7 ? x1 * w1 : 0.f;
                     }
-                    *(uint4 *)(prow + ((ck ^ (t & 7)) << 4)) =
-                        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                   pack_bf16x2(v[6], v[7]));
+                    *(uint32_t *)(prow + ((k ^ (t & 7)) << 4)) = pack_bf16x2(v0, v1);
                 }
             }
             fence_async_smem();
@@ -393,7 +389,6 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
         const int m = 16 * q4 + (lane & 15);
         const bool row_lane = lane < 16;
         const uint32_t tP = tmem + LT_PS + ((uint32_t)(32 * q4) << 16);
-        float *stack = a.ws_stack + (size_t)blockIdx.x * a.p * LL_D * LL_D + (size_t)m * LL_D;
         if (totals) {
             if (group_wait(ct == 0, 4, totals_done, 0, nullptr, 0, false, ctl)) {
                 tc_fence_after();
@@ -414,12 +409,14 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 }
             }
         } else {
+            // each thread: half of rows ma = 16 q4 + lane/4 and mb = ma + 8 (16x256b loads)
+            const int cpos = lane & 3;
+            const int mrow[2] = {16 * q4 + (lane >> 2), 16 * q4 + 8 + (lane >> 2)};
             for (int i = 0; i < nloc; ++i) {
                 if (!group_wait(ct == 0, 4, state_done, i & 1, nullptr, 0, false, ctl)) break;
                 tc_fence_after();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tP, r0);
-                tmem_ld32(tP + 32, r1);
+                uint32_t r[32];
+                tmem_ld16x256_x8(tP, r);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
@@ -433,34 +430,30 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                 if (i >= 2 &&
                     !group_wait(ct == 0, 4, &c_done[(i - 2) & 3], ((i - 2) >> 2) & 1, nullptr, 0, false, ctl))
                     break;
-                if (x < nloc && row_lane) {
-                    const int d = __popc(x), r = __ffs(x) - 1;
+                if (x < nloc) {
+                    const int d = __popc(x), r_ = __ffs(x) - 1;
                     // T_r = PS(x) - PS(x - 2^r); PS(x - 2^r) is the snapshot at depth d - 1.
                     // PS(x) becomes the snapshot at depth d: a later block reads it back when
                     // it closes at a position one level below x (none does if x is odd).
-                    const float4 *src = (const float4 *)(stack + (size_t)(d >= 2 ? d - 2 : 0) * LL_D * LL_D);
-                    float4 *dst = (float4 *)(stack + (size_t)(d - 1) * LL_D * LL_D);
-                    // level 0 alternates between its two tiles (bit 1 of x)
-                    uint8_t *row = tbuf((r == 0 && ((x >> 1) & 1)) ? a.nlev : r) + m * 128;
 #pragma unroll
-                    for (int ck = 0; ck < 8; ++ck) {
-                        const uint32_t *rr = ck < 4 ? r0 : r1;
-                        const int i0 = (8 * ck) & 31;
-                        float v[8];
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int m = mrow[hr];
+                        const float *stk = a.ws_stack + (size_t)blockIdx.x * a.p * LL_D * LL_D + (size_t)m * LL_D + 2 * cpos;
+                        const float *src = stk + (size_t)(d >= 2 ? d - 2 : 0) * LL_D * LL_D;
+                        float *dst = (float *)stk + (size_t)(d - 1) * LL_D * LL_D;
+                        // level 0 alternates between its two tiles (bit 1 of x)
+                        uint8_t *row = tbuf((r_ == 0 && ((x >> 1) & 1)) ? a.nlev : r_) + m * 128 + 4 * cpos;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i0 + e]);
-                        if (r >= 1) {
-                            dst[2 * ck] = make_float4(v[0], v[1], v[2], v[3]);
-                            dst[2 * ck + 1] = make_float4(v[4], v[5], v[6], v[7]);
+                        for (int k = 0; k < 8; ++k) {
+                            float v0 = __uint_as_float(r[4 * k + 2 * hr]), v1 = __uint_as_float(r[4 * k + 2 * hr + 1]);
+                            if (r_ >= 1) *(float2 *)(dst + 8 * k) = make_float2(v0, v1);
+                            if (d >= 2) {
+                                const float2 u = *(const float2 *)(src + 8 * k);
+                                v0 -= u.x;
+                                v1 -= u.y;
+                            }
+                            *(uint32_t *)(row + ((k ^ (m & 7)) << 4)) = pack_bf16x2(v0, v1);
                         }
-                        if (d >= 2) {
-                            const float4 u0 = src[2 * ck], u1 = src[2 * ck + 1];
-                            v[0] -= u0.x; v[1] -= u0.y; v[2] -= u0.z; v[3] -= u0.w;
-                            v[4] -= u1.x; v[5] -= u1.y; v[6] -= u1.z; v[7] -= u1.w;
-                        }
-                        *(uint4 *)(row + ((ck ^ (m & 7)) << 4)) =
-                            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                       pack_bf16x2(v[6], v[7]));
                     }
                 }
                 fence_async_smem();
@@ -470,21 +463,26 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
         }
     } else if (warp >= 12 && !totals) {
         // ------------------------------------------------------------ combine + store rows
+        // Each thread owns half of two rows, ta = 16 q4 + lane/4 and tb = ta + 8: columns
+        // 8k + 2 (lane % 4) and the next one (k = 0..7), as a 16x256b TMEM load delivers them.
         const int q4 = warp & 3, ot = tid - 384;
-        const int t = 16 * q4 + (lane & 15);
-        const bool row_lane = lane < 16;
+        const int cpos = lane & 3;
+        const int trow[2] = {16 * q4 + (lane >> 2), 16 * q4 + 8 + (lane >> 2)};
         const uint32_t lq = (uint32_t)(32 * q4) << 16;
         int slot = 0, rph = 0, s = 0, ph = 0;
         for (int i = 0; i < nloc; ++i) {
             const int c = tile0 + i;
-            const int row = c * LL_C + t;
-            const bool valid = row_lane && row < a.L;
+            bool valid[2];
+            const float *lrow[2];
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) valid[hr] = c * LL_C + trow[hr] < a.L;
             // the stage holds this chunk's lambda rows
             if (!group_wait(ot == 0, 3, &full[s], ph, nullptr, 0, false, ctl)) break;
-            const float *lrow = stage_l(s) + t * NL + 1 + LL_LOG2C;  // lambda_t^(7 + j) at [j]
-            float acc[64];
 #pragma unroll
-            for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+            for (int hr = 0; hr < 2; ++hr) lrow[hr] = stage_l(s) + trow[hr] * NL + 1 + LL_LOG2C;  // lambda_t^(7 + j) at [j]
+            float acc[32];  // register 4k + 2 hr + e of the loads: row trow[hr], column 8k + 2 cpos + e
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
             bool ok = true;
             // products in issue order: P V (weight 1), then R_j for the set bits j of c
             uint32_t bits = (uint32_t)c & ((1u << a.nlev) - 1u);
@@ -494,20 +492,21 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
                     break;
                 }
                 tc_fence_after();
-                const float w = j < 0 ? 1.f : (valid ? lrow[j] : 0.f);
-                const uint32_t tR = tmem + LT_R + 64 * slot + lq;
+                const float wa = j < 0 ? 1.f : (valid[0] ? lrow[0][j] : 0.f);
+                const float wb = j < 0 ? 1.f : (valid[1] ? lrow[1][j] : 0.f);
                 uint32_t r[32];
-                tmem_ld32(tR, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = fmaf(w, __uint_as_float(r[e]), acc[e]);
-                tmem_ld32(tR + 32, r);
+                tmem_ld16x256_x8(tmem + LT_R + 64 * slot + lq, r);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&r_free[slot]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[32 + e] = fmaf(w, __uint_as_float(r[e]), acc[32 + e]);
+                for (int k = 0; k < 8; ++k) {
+                    acc[4 * k] = fmaf(wa, __uint_as_float(r[4 * k]), acc[4 * k]);
+                    acc[4 * k + 1] = fmaf(wa, __uint_as_float(r[4 * k + 1]), acc[4 * k + 1]);
+                    acc[4 * k + 2] = fmaf(wb, __uint_as_float(r[4 * k + 2]), acc[4 * k + 2]);
+                    acc[4 * k + 3] = fmaf(wb, __uint_as_float(r[4 * k + 3]), acc[4 * k + 3]);
+                }
                 if (++slot == LL_RING) { slot = 0; rph ^= 1; }
                 if (!bits) break;
                 j = __ffs(bits) - 1;
@@ -517,13 +516,12 @@ __global__ void __launch_bounds__(LL_THREADS, 1) tc_loglinear_kernel(const __gri
             // every output thread is past its lambda reads: the stage may be refilled
             named_bar(3, 128);
             if (ot == 0) mbar_arrive(&stage_free[s]);
-            if (valid) {
-                uint4 *dst = (uint4 *)(a.out + ((size_t)head * a.L + row) * LL_D);
 #pragma unroll
-                for (int ck = 0; ck < 8; ++ck)
-                    dst[ck] = make_uint4(pack_bf16x2(acc[8 * ck], acc[8 * ck + 1]), pack_bf16x2(acc[8 * ck + 2], acc[8 * ck + 3]),
-                                         pack_bf16x2(acc[8 * ck + 4], acc[8 * ck + 5]),
-                                         pack_bf16x2(acc[8 * ck + 6], acc[8 * ck + 7]));
+            for (int hr = 0; hr < 2; ++hr) {
+                if (!valid[hr]) continue;
+                uint32_t *dst = (uint32_t *)(a.out + ((size_t)head * a.L + c * LL_C + trow[hr]) * LL_D) + cpos;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dst[4 * k] = pack_bf16x2(acc[4 * k + 2 * hr], acc[4 * k + 2 * hr + 1]);
             }
             if (++s == nst) { s = 0; ph ^= 1; }
         }
