@@ -20,9 +20,10 @@
 // intra work per row grows with C and the state work per row shrinks with 1/C, as in the
 // page's cost model (section 3).
 //
-// Warp roles (as in the one-tile kernel): 0 TMA producer, 1 MMA issuer, 2-4, 6-8, 10-11
-// feature map, 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue (rows stored
-// from registers).
+// Warp roles (as in the one-tile kernel): 0 TMA producer (K, V; and Q unless warp 5 loads
+// it), 5 TMA producer of Q when the Q ring is shorter than the K/V ring, 1 MMA issuer, 2-4,
+// 6-8, 10-11 feature map, 12-15 scores -> P (+ bf16 state copy), 16-19 output epilogue (rows
+// stored from registers).
 //
 // MMAs per query tile (bf16 in, fp32 accumulate), D = feature dim, T = 64:
 //   scores  A_k   = phi(Q) [phi(K_k); z]^T       M=T   N=T(+8)  K=D   per block k
@@ -120,6 +121,7 @@ struct TwLayout {
     static_assert(D <= 128 && (DV == 64 || DV == 128), "D <= 128, dv 64 or 128");
     static_assert(K_BLK % 1024 == 0 && KV_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms");
     static_assert(NKV > R && N_BAR <= MAX_BAR && BYTES <= TW_SMEM, "shared memory budget");
+    static_assert(NQ <= NKV, "a Q load must not reach a K/V barrier's previous phase");
 };
 
 template <int D, int DV, int R, int FM, bool NORM>
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
     using Lay = TwLayout<D, DV, R, NORM>;
     constexpr int T = Lay::T;
     constexpr int NKV = Lay::NKV, NQ = Lay::NQ;
+    constexpr bool QP = NQ < NKV;  // Q loads from their own producer thread
     constexpr bool PHI = FM != LA_FM_IDENTITY;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -251,16 +254,23 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // With a Q ring shorter than the K/V ring (QP), a tile's K and V load as soon as its
+        // K/V slot is free and its Q (main pass) is loaded by warp 5 once its Q slot is free,
+        // completing on the same barrier, which this thread arms with the bytes of all three.
+        // (The Q bytes may land before the arming: the transaction count goes negative
+        // meanwhile.  The Q slot of tile c frees only after tile c - NQ is done, NQ <= NKV, so
+        // the barrier's previous phase is complete by then.)  Otherwise this thread loads all
+        // three when both slots are free.
         if (lane == 0) {
             for (int c = 0; c < nt; ++c) {
                 const int ks = c % NKV, qs = c % NQ;
                 // the slot's previous tile: its chunk is done (K/V), its own products are done (Q)
                 if (c >= NKV && !wait_phase(&kv_free[ks], ((c / NKV) - 1) & 1, ctl)) break;
-                if (!totals && c >= NQ && !wait_phase(&q_free[qs], ((c / NQ) - 1) & 1, ctl)) break;
+                if (!QP && !totals && c >= NQ && !wait_phase(&q_free[qs], ((c / NQ) - 1) & 1, ctl)) break;
                 const int row = (tile0 + c) * T;
                 mbar_arrive_expect_tx(&kv_full[ks], totals ? Lay::KV_TX : Lay::KV_TX + Lay::Q_BYTES);
                 for (int kb = 0; kb < D / 64; ++kb) {
-                    if (!totals) tma_load_3d(q_tile(qs) + kb * T * 128, &a.tm_q, kb * 64, row, head, &kv_full[ks]);
+                    if (!QP && !totals) tma_load_3d(q_tile(qs) + kb * T * 128, &a.tm_q, kb * 64, row, head, &kv_full[ks]);
                     tma_load_3d(k_tile(ks) + kb * Lay::K_BLK, &a.tm_k, kb * 64, row, head, &kv_full[ks]);
                 }
                 for (int jb = 0; jb < DV / 64; ++jb)
@@ -273,6 +283,20 @@ __global__ void __launch_bounds__(TW_THREADS, 1) tc_wide_kernel(const __grid_con
                 if (uses > 0)
                     while (!mbar_try_sleep(&kv_full[i], (uses - 1) & 1, 200000u))
                         if (globaltimer() - t0 > ctl.timeout_ns) break;
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ TMA producer (Q, QP only)
+        // (warp 5 is otherwise idle: it shares a sub-partition with the MMA issuer, so it does
+        // no feature-map work, and this thread mostly sleeps in its waits)
+        if (QP && lane == 0 && !totals) {
+            for (int c = 0; c < nt; ++c) {
+                const int qs = c % NQ;
+                // the slot's previous tile: its scores and inter product are done
+                if (c >= NQ && !wait_phase(&q_free[qs], ((c / NQ) - 1) & 1, ctl)) break;
+                const int row = (tile0 + c) * T;
+                for (int kb = 0; kb < D / 64; ++kb)
+                    tma_load_3d(q_tile(qs) + kb * T * 128, &a.tm_q, kb * 64, row, head, &kv_full[c % NKV]);
             }
         }
     } else if (warp == 1) {
