@@ -25,16 +25,17 @@
 // Workspace (fp32, per (b, h) head, rows of L): phi(q), phi(k) [D]; [num, den] [w];
 // D' [w = dv + normalise]; v' [w]; D [dv]; dphi(q), dphi(k) [D]; dv [dv].
 //
-// Tensor-core route (bf16, identity / elu+1, plain or decayed): the same passes run on the causal
-// tensor-core forward with identity features.  An anti-causal pass is the causal pass over
-// reversed rows R(x)_t = x_{L-1-t}: the elementwise kernels write the reversed operands and
-// the last one reads the reversed results back.  The normaliser's extra column becomes two
+// Tensor-core route (bf16, identity / elu+1, plain or decayed): the same passes run on the
+// tensor-core forward with identity features, the anti-causal ones in its anti-causal mode
+// (the causal pass over the mirrored sequence, read and written in place, so no reversed
+// copies are made).  The normaliser's extra column becomes two
 // more passes against constant rows e = (1, 0, ..., 0): Z_t = sum_{s<=t} phi(k_s) (so den_t =
 // phi(q_t).Z_t and dphi(q)_t -= g_t Z_t) and the suffix sums sum_{t>=s} g_t phi(q_t)
 // (subtracted from dphi(k)_s); the forward output is recomputed by one more pass, num =
 // causal(phi(q), phi(k), v), over the same bf16 features, so that out = num / den and the
-// other sums cancel exactly for those features.  The feature-gradient passes run in the
-// kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows out).
+// other sums cancel exactly for those features.  With the normaliser the feature-gradient
+// passes run in the kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows
+// out); without it every pass writes its gradient rows in place, in bf16.
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -389,19 +390,18 @@ int bwd_t(const Problem &p, int sms, const void *dout, void *dq, void *dk_, void
 typedef __nv_bfloat16 bf16;
 
 struct TcBufs {
-    bf16 *fq, *fk, *rfq, *rfk, *rv, *dn, *rd, *rgq, *e;  // operands
-    float *zc, *num, *dqm, *dkr, *zsr;                   // pass outputs (fp32 rows)
-    bf16 *dvr;
+    bf16 *fq, *fk, *dn, *gq, *e;          // operands
+    float *zc, *num, *dqm, *dkm, *zsu;    // pass outputs (fp32 rows, normaliser)
     float *g;
     void *ws;                                            // tensor-core pass workspace
     size_t ws_bytes;
 };
 
-// one identity-feature, unnormalised causal pass on the tensor cores (bf16 rows), with the
-// caller's Retention decay if any (gamma^|t-s| is the same mask over reversed rows, so the
-// anti-causal passes keep it too)
+// one identity-feature, unnormalised pass on the tensor cores (bf16 rows), causal or (rev)
+// anti-causal, with the caller's Retention decay if any (gamma^|t-s| is the same mask read
+// in either direction)
 Problem tc_pass(const Problem &base, const void *q, const void *k, const void *v, void *out, int dk,
-                int dv)
+                int dv, int rev = 0)
 {
     Problem p = base;
     p.q = q; p.k = k; p.v = v; p.out = out;
@@ -411,26 +411,30 @@ Problem tc_pass(const Problem &base, const void *q, const void *k, const void *v
     p.normalize = 0;
     p.lam = nullptr; p.nl = 0;
     p.dtype = LA_BF16;
-    p.rev = 0;
+    p.rev = rev;
     p.out_f32 = 0;
     p.S0 = nullptr; p.z0 = nullptr;
     return p;
 }
 
-// the passes of the route, in order (unused ones have out == nullptr when !normalize)
-int tc_passes(const Problem &p, const TcBufs &b, const void *dout, Problem *ps)
+// the passes of the route, in order.  dv is written by its pass; without the normaliser so
+// are dphi(q), dphi(k), into dq, dk (bf16; the chain kernel then applies elu+1's derivative
+// in place).  With it the feature-gradient passes store fp32: dphi(q) = pass - g Z and
+// dphi(k) = pass - suffix can cancel, so those terms are not rounded to bf16 before the
+// subtraction.
+int tc_passes(const Problem &p, const TcBufs &b, const void *dout, void *dq, void *dk, void *dv, Problem *ps)
 {
-    const int D = p.D, dv = p.dv;
+    const int D = p.D, w = p.dv;
+    const bool nz = p.normalize != 0;
     int n = 0;
-    // the feature-gradient passes store fp32: dphi(q) = pass - g Z and dphi(k) = pass - suffix
-    // can cancel, so those terms are not rounded to bf16 before the subtraction
-    if (p.normalize) ps[n++] = tc_pass(p, b.e, b.e, b.fk, b.zc, 64, D);                  // Z
-    if (p.normalize) ps[n++] = tc_pass(p, b.fq, b.fk, p.v, b.num, D, dv);                 // num
-    ps[n++] = tc_pass(p, p.normalize ? (const void *)b.dn : dout, p.v, b.fk, b.dqm, dv, D);  // dphi(q)
-    ps[n++] = tc_pass(p, b.rv, b.rd, b.rfq, b.dkr, dv, D);                                // R dphi(k)
-    if (p.normalize) ps[n++] = tc_pass(p, b.e, b.e, b.rgq, b.zsr, 64, D);                 // R suffix
-    for (int i = 0; i < n; ++i) ps[i].out_f32 = 1;
-    ps[n++] = tc_pass(p, b.rfk, b.rfq, b.rd, b.dvr, D, dv);                               // R dv
+    if (nz) ps[n++] = tc_pass(p, b.e, b.e, b.fk, b.zc, 64, D);                            // Z
+    if (nz) ps[n++] = tc_pass(p, b.fq, b.fk, p.v, b.num, D, w);                           // num
+    const void *dd = nz ? (const void *)b.dn : dout;                                     // D
+    ps[n++] = tc_pass(p, dd, p.v, b.fk, nz ? (void *)b.dqm : dq, w, D);                   // dphi(q)
+    ps[n++] = tc_pass(p, p.v, dd, b.fq, nz ? (void *)b.dkm : dk, w, D, 1);                // dphi(k), anti
+    if (nz) ps[n++] = tc_pass(p, b.e, b.e, b.gq, b.zsu, 64, D, 1);                        // suffix, anti
+    for (int i = 0; i < n && nz; ++i) ps[i].out_f32 = 1;
+    ps[n++] = tc_pass(p, b.fk, b.fq, dd, dv, D, w, 1);                                    // dv, anti
     return n;
 }
 
@@ -445,27 +449,22 @@ size_t tc_bufs(const Problem &p, int sms, char *base, TcBufs *b)
         if (b) *ptr = (std::remove_reference_t<decltype(**ptr)> *)(base + off);
         off += (bytes + 1023) / 1024 * 1024;
     };
-    const size_t N = p.normalize ? 1 : 0;
-    take(&t->fq, rows * D * 2);
-    take(&t->fk, rows * D * 2);
-    take(&t->rfq, rows * D * 2);
-    take(&t->rfk, rows * D * 2);
-    take(&t->rv, rows * dv * 2);
+    const size_t N = p.normalize ? 1 : 0, F = p.fm == LA_FM_IDENTITY ? 0 : 1;
+    take(&t->fq, F * rows * D * 2);  // identity features: the passes read q, k themselves
+    take(&t->fk, F * rows * D * 2);
     take(&t->dn, N * rows * dv * 2);
-    take(&t->rd, rows * dv * 2);
-    take(&t->rgq, N * rows * D * 2);
+    take(&t->gq, N * rows * D * 2);
     take(&t->e, N * rows * 64 * 2);
     take(&t->zc, N * rows * D * 4);
     take(&t->num, N * rows * dv * 4);
-    take(&t->dqm, rows * D * 4);
-    take(&t->dkr, rows * D * 4);
-    take(&t->zsr, N * rows * D * 4);
-    take(&t->dvr, rows * dv * 2);
+    take(&t->dqm, N * rows * D * 4);
+    take(&t->dkm, N * rows * D * 4);
+    take(&t->zsu, N * rows * D * 4);
     take(&t->g, N * rows * 4);
     // the passes run one after another on the stream and share one workspace
     Problem ps[6];
     TcBufs nb{};
-    const int n = tc_passes(p, nb, nullptr, ps);
+    const int n = tc_passes(p, nb, nullptr, nullptr, nullptr, nullptr, ps);
     size_t wmax = 0;
     for (int i = 0; i < n; ++i) {
         la_plan_info info;
@@ -509,51 +508,38 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// phi(q), phi(k) as bf16 rows and reversed rows; reversed v; constant rows e (normaliser)
-__global__ void __launch_bounds__(32 * TB_ROWS) tb_feat_kernel(const bf16 *q, const bf16 *k, const bf16 *v,
-                                                             TcBufs b, long rows, int L, int dk, int dv,
-                                                             int fm, int normalize)
+// phi(q), phi(k) as bf16 rows (elu+1); constant rows e (normaliser)
+__global__ void __launch_bounds__(32 * TB_ROWS) tb_feat_kernel(const bf16 *q, const bf16 *k, TcBufs b,
+                                                             long rows, int dk, int fm, int normalize)
 {
     const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
-    const long head = r / L, t = r % L;
-    const long rr = head * L + (L - 1 - t);
-    for (int i = 4 * lane; i < dk; i += 128) {
+    for (int i = 4 * lane; i < dk && fm == LA_FM_ELU1; i += 128) {
         float xq[4], xk[4];
         ld4(q + r * dk + i, xq);
         ld4(k + r * dk + i, xk);
-        if (fm == LA_FM_ELU1)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                xq[e] = phi_elu1(xq[e]);
-                xk[e] = phi_elu1(xk[e]);
-            }
+        for (int e = 0; e < 4; ++e) {
+            xq[e] = phi_elu1(xq[e]);
+            xk[e] = phi_elu1(xk[e]);
+        }
         st4(b.fq + r * dk + i, xq);
         st4(b.fk + r * dk + i, xk);
-        st4(b.rfq + rr * dk + i, xq);
-        st4(b.rfk + rr * dk + i, xk);
     }
-    for (int j = 4 * lane; j < dv; j += 128) *(uint2 *)(b.rv + rr * dv + j) = *(const uint2 *)(v + r * dv + j);
     if (normalize && lane < 16) {
         const float ev[4] = {lane == 0 ? 1.f : 0.f, 0.f, 0.f, 0.f};
         st4(b.e + r * 64 + 4 * lane, ev);
     }
 }
 
-// D = dout (/ den, den = phi(q).Z), reversed D; normaliser: g = D . num / den and R(g phi(q))
-__global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout, TcBufs b, long rows, int L,
-                                                             int D, int dv, int normalize)
+// With the normaliser: D = dout / den (den = phi(q).Z), g = D . num / den and g phi(q)
+__global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout, TcBufs b, long rows, int D,
+                                                             int dv)
 {
     const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
-    const long head = r / L, t = r % L;
-    const long rr = head * L + (L - 1 - t);
-    if (!normalize) {
-        for (int j = 4 * lane; j < dv; j += 128) *(uint2 *)(b.rd + rr * dv + j) = *(const uint2 *)(dout + r * dv + j);
-        return;
-    }
     float part = 0.f;
     for (int i = 4 * lane; i < D; i += 128) {
         float f[4], z[4];
@@ -572,7 +558,6 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout,
 #pragma unroll
         for (int e = 0; e < 4; ++e) d[e] = __bfloat162float(__float2bfloat16_rn(d[e] * inv));
         st4(b.dn + r * dv + j, d);
-        st4(b.rd + rr * dv + j, d);
 #pragma unroll
         for (int e = 0; e < 4; ++e) gp += d[e] * (n[e] * inv);
     }
@@ -583,29 +568,33 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout,
         ld4(b.fq + r * D + i, f);
 #pragma unroll
         for (int e = 0; e < 4; ++e) f[e] *= g;
-        st4(b.rgq + rr * D + i, f);
+        st4(b.gq + r * D + i, f);
     }
 }
 
-// dq, dk through the feature map from the pass outputs (reversed ones read back), dv
+// dq, dk through the feature map from dphi(q), dphi(k): the fp32 pass outputs less the
+// normaliser's terms, or (no normaliser, elu+1) the bf16 rows already in dq, dk, in place
 __global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, const bf16 *k, TcBufs b,
-                                                              bf16 *dq, bf16 *dk, bf16 *dv, long rows,
-                                                              int L, int D, int dvn, int fm, int normalize)
+                                                              bf16 *dq, bf16 *dk, long rows, int D, int fm,
+                                                              int normalize)
 {
     const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
-    const long head = r / L, t = r % L;
-    const long rr = head * L + (L - 1 - t);
     const float g = normalize ? b.g[r] : 0.f;
     for (int i = 4 * lane; i < D; i += 128) {
         float a[4], c[4];
-        ld4(b.dqm + r * D + i, a);
-        ld4(b.dkr + rr * D + i, c);
+        if (normalize) {
+            ld4(b.dqm + r * D + i, a);
+            ld4(b.dkm + r * D + i, c);
+        } else {
+            ld4(dq + r * D + i, a);
+            ld4(dk + r * D + i, c);
+        }
         if (normalize) {
             float z[4], zs[4];
             ld4(b.zc + r * D + i, z);
-            ld4(b.zsr + rr * D + i, zs);
+            ld4(b.zsu + r * D + i, zs);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 a[e] -= g * z[e];
@@ -625,21 +614,26 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, c
         st4(dq + r * D + i, a);
         st4(dk + r * D + i, c);
     }
-    for (int j = 4 * lane; j < dvn; j += 128) *(uint2 *)(dv + r * dvn + j) = *(const uint2 *)(b.dvr + rr * dvn + j);
 }
 
 int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, void *dv)
 {
     TcBufs b;
     tc_bufs(p, sms, (char *)p.workspace, &b);
+    if (p.fm == LA_FM_IDENTITY) {
+        b.fq = (bf16 *)p.q;  // read only
+        b.fk = (bf16 *)p.k;
+    }
     const long rows = (long)p.B * p.H * p.L;
     cudaStream_t st = p.stream;
     const unsigned tgrid = (unsigned)((rows + TB_ROWS - 1) / TB_ROWS);
-    tb_feat_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, (const bf16 *)p.v, b,
-                                                  rows, p.L, p.dk, p.dv, p.fm, p.normalize);
-    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    if (p.fm != LA_FM_IDENTITY || p.normalize) {
+        tb_feat_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b, rows, p.dk,
+                                                      p.fm, p.normalize);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    }
     Problem ps[6];
-    const int n = tc_passes(p, b, dout, ps);
+    const int n = tc_passes(p, b, dout, dq, dk, dv, ps);
     for (int i = 0; i < n; ++i) {
         ps[i].workspace = b.ws;
         ps[i].workspace_bytes = b.ws_bytes;
@@ -649,14 +643,15 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
         for (; i < 2; ++i)
             if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
     }
-    tb_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, p.L, p.D, p.dv,
-                                                  p.normalize);
-    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    if (p.normalize) {
+        tb_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, p.D, p.dv);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    }
     for (; i < n; ++i)
         if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
+    if (p.fm == LA_FM_IDENTITY && !p.normalize) return LA_OK;  // the passes wrote dq, dk, dv
     tb_chain_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b, (bf16 *)dq,
-                                                   (bf16 *)dk, (bf16 *)dv, rows, p.L, p.D, p.dv, p.fm,
-                                                   p.normalize);
+                                                   (bf16 *)dk, rows, p.D, p.fm, p.normalize);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
@@ -674,7 +669,7 @@ bool bwd_tc_supported(const Problem &p, int sms)
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     Problem ps[6];
     TcBufs nb{};
-    const int n = tc_passes(p, nb, nullptr, ps);
+    const int n = tc_passes(p, nb, nullptr, nullptr, nullptr, nullptr, ps);
     for (int i = 0; i < n; ++i)
         if (!tc_supported(ps[i], sms)) return false;
     return true;

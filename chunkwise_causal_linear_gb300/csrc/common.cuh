@@ -58,8 +58,9 @@ struct Problem {
     int decay;               // 1: Retention decay S_t = gamma S_{t-1} + phi(k_t) v_t^T
     float gamma;             // decay factor, 0 < gamma <= 1
     float l2g;               // log2(gamma), rounded from the double value
-    int rev;                 // 1: anti-causal (generic path only): row t reads the rows s >= t,
-                             // computed as the causal pass over the reversed sequence
+    int rev;                 // 1: anti-causal: row t reads the rows s >= t, computed as the
+                             // causal pass over the reversed sequence (generic path; the
+                             // tensor-core path for identity features, no normaliser, C = 64)
     int out_f32;             // 1: out is fp32 rows (tensor-core path, identity features, no
                              // normaliser; the backward pass's internal passes)
     const float *S0, *z0;    // NULL, or the state (and normaliser) before row 0: fp32

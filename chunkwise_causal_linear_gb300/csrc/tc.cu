@@ -121,6 +121,7 @@ struct TcArgs {
     // phi(q) S_total (/ phi(q) z_total).
     int noncausal, nseg_all;
     float l2g;  // decay: log2(gamma)
+    int anti;   // anti-causal pass (identity features, no normaliser, C = 64): see the kernel
     const float *S0, *z0;  // NULL, or the state before row 0 ([BH][D][DV], [BH][D])
     int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
@@ -190,6 +191,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     constexpr bool FO = MODE == TC_F32OUT || MODE == TC_DECAY_F32OUT;
     static_assert(!DK || CH == C, "decay: one chunk per tile");
     static_assert(!FO || (FM == LA_FM_IDENTITY && !NORM), "fp32 output: identity features, no normaliser");
+    // Anti-causal pass (row t reads the rows s >= t; used by the backward pass).  It is the
+    // causal pass over the mirrored sequence v = L-1-t, run in mirrored order: virtual tile c
+    // is the box of rows L - 64 (c+1) .. L - 64 c - 1 (a negative start reads zeros), and
+    // smem row r of a tile is virtual row 63 - r of it.  Segments, totals, their prefix and the
+    // decay periods all stay in virtual order; only the loads, the causal mask (s >= t in smem
+    // order), the decay's in-tile factors and the rows stored change.
+    const bool anti = FM == LA_FM_IDENTITY && !NORM && !NC && CH == C && a.anti != 0;
     using Lay = TcLayout<D, DV, C, NORM, FO>;
     constexpr int ST = Lay::STAGES;  // TMA ring depth
     extern __shared__ uint8_t smem_raw[];
@@ -294,7 +302,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             zs[i] = z0;
         }
     if (DK && !NORM)
-        for (int i = tid; i < C; i += TC_THREADS) rden[i] = ex2(a.l2g * (float)(i + 1 - C));  // gamma^(i+1-C)
+        for (int i = tid; i < C; i += TC_THREADS)  // gamma^(i'+1-C), i' the row's in-tile virtual index
+            rden[i] = ex2(a.l2g * (float)(anti ? -i : i + 1 - C));
     if (CH == C)
         // P rows 0-31, columns 32-63: always zero (causal mask), written once in every P tile
         // (both buffers; hi and lo tiles in the fp32-output mode)
@@ -392,7 +401,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const int s = c % ST;
                 if (c >= ST && !wait_phase(&stage_free[s], ((c / ST) - 1) & 1, ctl))
                     break;
-                const int row = (tile0 + c) * C;
+                const int row = anti ? a.L - (tile0 + c + 1) * C : (tile0 + c) * C;
                 mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES
                                                 : (qonly ? Lay::Q_BYTES : Lay::STAGE_TX));
                 for (int kb = 0; kb < D / 64; ++kb) {
@@ -595,7 +604,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // gamma^(C (nch-1-c)) (totals pass)
             float rowf[NR];
 #pragma unroll
-            for (int n = 0; n < NR; ++n) rowf[n] = DK ? ex2(a.l2g * (float)(C - 1 - rg - n * RG)) : 1.f;
+            for (int n = 0; n < NR; ++n)  // (the in-tile virtual index is C-1-r in the anti-causal pass)
+                rowf[n] = DK ? ex2(a.l2g * (float)(anti ? rg + n * RG : C - 1 - rg - n * RG)) : 1.f;
             int pm = 0;  // c mod period
             for (int c = 0; c < nch; ++c, pm = (pm + 1 == a.period) ? 0 : pm + 1) {
                 const int s = c % ST;
@@ -768,7 +778,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
             // rows 0-31 (warps 0, 1 of the group) keep nothing from columns 32-63: their P there
             // is the zero block written at the start, and they load only the first half.
             const uint32_t tA = tmem + Lay::T_A + b * Lay::A_STRIDE + lane_off;
-            const int nh = (CH == C && q4 < 2) ? 1 : 2;  // 32-column halves to read
+            const int nh = (CH == C && q4 < 2 && !anti) ? 1 : 2;  // 32-column halves to read
             float rsa[2] = {0.f, 0.f}, rsb[2] = {0.f, 0.f};  // this thread's part of the row sums
             uint32_t rz[4];
             uint8_t *pa = p_tile + b * Lay::P_SET + ta * 128 + 4 * cpos;
@@ -786,10 +796,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                     // P keeps s in t's chunk with s <= t (block-diagonal causal mask at CH); the
                     // normaliser's row sum keeps every s <= t of the tile
                     const int k = 4 * h + k4, s0 = 8 * k + 2 * cpos, s1 = s0 + 1;
-                    const float a0 = s0 <= ta ? __uint_as_float(r[4 * k4]) : 0.f;
-                    const float a1 = s1 <= ta ? __uint_as_float(r[4 * k4 + 1]) : 0.f;
-                    const float b0 = s0 <= tb ? __uint_as_float(r[4 * k4 + 2]) : 0.f;
-                    const float b1 = s1 <= tb ? __uint_as_float(r[4 * k4 + 3]) : 0.f;
+                    // (anti-causal: s >= t in smem order, which is s <= t in virtual rows)
+                    const float a0 = (anti ? s0 >= ta : s0 <= ta) ? __uint_as_float(r[4 * k4]) : 0.f;
+                    const float a1 = (anti ? s1 >= ta : s1 <= ta) ? __uint_as_float(r[4 * k4 + 1]) : 0.f;
+                    const float b0 = (anti ? s0 >= tb : s0 <= tb) ? __uint_as_float(r[4 * k4 + 2]) : 0.f;
+                    const float b1 = (anti ? s1 >= tb : s1 <= tb) ? __uint_as_float(r[4 * k4 + 3]) : 0.f;
                     rsa[k4 & 1] += a0 + a1;
                     rsb[k4 & 1] += b0 + b1;
                     uint32_t wa, wb;
@@ -893,9 +904,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                             NORM, ctl))
                 break;
             tc_fence_after();
-            const int row0 = (tile0 + c) * C;
-            const int nrow = min(C, a.L - row0);  // rows of this tile inside the sequence
-            const size_t rbase = (size_t)head * a.L + row0;
+            // rows of this tile inside the sequence: smem rows tlo .. thi-1 at rows row0 + tt
+            const int row0 = anti ? a.L - (tile0 + c + 1) * C : (tile0 + c) * C;
+            const int tlo = anti ? max(0, -row0) : 0, thi = anti ? C : min(C, a.L - row0);
+            const long rbase = (long)head * a.L + row0;
             const uint32_t tO = tmem + Lay::T_O + b * C + lane_off;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -913,18 +925,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 const float mf = (DK && !NORM) ? ex2(a.l2g * (float)(C * (c % a.period))) : 1.f;
                 if constexpr (FO) {
                     // fp32 rows: column j of token tt (decay: times gamma^(i+1-C) gamma^(C m))
-                    float *const o = (float *)a.out + rbase * DV + j;
                     const float *rf = (const float *)rp;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int tt = 32 * h + u;
                         const float x = DK ? __uint_as_float(r[u]) * (mf * rf[u]) : __uint_as_float(r[u]);
-                        if (live && tt < nrow) o[(size_t)tt * DV] = x;
+                        if (live && tt >= tlo && tt < thi) ((float *)a.out)[(rbase + tt) * DV + j] = x;
                     }
                 } else {
                     // Lanes j, j^1 swap one value per pair of rows so that each writes two
                     // neighbouring columns of one row as a single 32-bit word.
-                    uint32_t *const o = (uint32_t *)((__nv_bfloat16 *)a.out + rbase * DV + (j & ~1));
+                    uint32_t *const o = (uint32_t *)a.out + (j >> 1);  // column pair j & ~1
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
@@ -936,7 +947,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                         const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
                         const int tt = 32 * h + 2 * u + (odd ? 1 : 0);
                         const uint32_t wv = odd ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-                        if (live && tt < nrow) o[(size_t)tt * (DV / 2)] = wv;
+                        if (live && tt >= tlo && tt < thi) o[(rbase + tt) * (DV / 2)] = wv;
                     }
                 }
             }
@@ -999,6 +1010,7 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     a.noncausal = noncausal ? 1 : 0;
     a.nseg_all = nseg;
     a.l2g = (mode == TC_DECAY || mode == TC_DECAY_F32OUT) ? p.l2g : 0.f;
+    a.anti = p.rev ? 1 : 0;
     a.S0 = p.S0;
     a.z0 = p.z0;
     // largest period P with C P |log2 gamma| <= 64 (gamma^(C P) >= 2^-64); tc_supported keeps
@@ -1087,6 +1099,8 @@ int tcw_launch(const Problem &p, int num_sms);
 bool tc_supported(const Problem &p, int num_sms)
 {
     (void)num_sms;
+    // the anti-causal pass: identity features, no normaliser, one 64-row chunk per tile
+    if (p.rev && (p.fm != LA_FM_IDENTITY || p.normalize || p.lam || p.C != 64 || p.S0 || p.z0)) return false;
     if (p.decay) {
         // one 64-row chunk per tile; gamma^64 >= 2^-64 keeps the scaled keys and the
         // output factor gamma^(i+1-64) well inside the fp32 / bf16 range
