@@ -28,14 +28,16 @@
 // Tensor-core route (bf16, identity / elu+1, plain or decayed): the same passes run on the
 // tensor-core forward with identity features, the anti-causal ones in its anti-causal mode
 // (the causal pass over the mirrored sequence, read and written in place, so no reversed
-// copies are made).  The normaliser's extra column becomes two
-// more passes against constant rows e = (1, 0, ..., 0): Z_t = sum_{s<=t} phi(k_s) (so den_t =
+// copies are made).  The normaliser's extra column becomes two more passes against constant
+// rows e = (1, 0, ..., 0), which the kernel keeps in shared memory instead of reading them:
+// Z_t = sum_{s<=t} phi(k_s) (so den_t =
 // phi(q_t).Z_t and dphi(q)_t -= g_t Z_t) and the suffix sums sum_{t>=s} g_t phi(q_t)
 // (subtracted from dphi(k)_s); the forward output is recomputed by one more pass, num =
 // causal(phi(q), phi(k), v), over the same bf16 features, so that out = num / den and the
-// other sums cancel exactly for those features.  With the normaliser the feature-gradient
-// passes run in the kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows
-// out); without it every pass writes its gradient rows in place, in bf16.
+// other sums cancel exactly for those features.  With the normaliser these passes run in
+// the kernel's fp32-output mode (bf16 hi / lo state copy and P, fp32 rows out) and the
+// last elementwise kernel forms dq, dk; without it every pass writes its gradient rows in
+// place, in bf16.
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -390,8 +392,8 @@ int bwd_t(const Problem &p, int sms, const void *dout, void *dq, void *dk_, void
 typedef __nv_bfloat16 bf16;
 
 struct TcBufs {
-    bf16 *fq, *fk, *dn, *gq, *e;          // operands
-    float *zc, *num, *dqm, *dkm, *zsu;    // pass outputs (fp32 rows, normaliser)
+    bf16 *fq, *fk, *dn, *gq;              // operands
+    float *zc, *num, *zsu, *dqm, *dkm;    // pass outputs (fp32 rows, normaliser)
     float *g;
     void *ws;                                            // tensor-core pass workspace
     size_t ws_bytes;
@@ -414,27 +416,41 @@ Problem tc_pass(const Problem &base, const void *q, const void *k, const void *v
     p.rev = rev;
     p.out_f32 = 0;
     p.S0 = nullptr; p.z0 = nullptr;
+    p.esyn = 0;
     return p;
 }
 
-// the passes of the route, in order.  dv is written by its pass; without the normaliser so
-// are dphi(q), dphi(k), into dq, dk (bf16; the chain kernel then applies elu+1's derivative
-// in place).  With it the feature-gradient passes store fp32: dphi(q) = pass - g Z and
-// dphi(k) = pass - suffix can cancel, so those terms are not rounded to bf16 before the
-// subtraction.
+// a pass whose q and k are the constant rows e = (1, 0, ..., 0) (dk = 64): out_t = the sum of
+// the rows v_s, s <= t (causal) or s >= t (anti-causal).  The kernel writes e into shared
+// memory itself; the tensor maps of q and k only need a valid, aligned address.
+Problem e_pass(const Problem &base, const void *v, void *out, int dv, int rev)
+{
+    Problem p = tc_pass(base, base.v, base.v, v, out, 64, dv, rev);
+    p.esyn = 1;
+    return p;
+}
+
+// The passes of the route, in order.  Without the normaliser dphi(q), dphi(k) and dv go
+// straight into dq, dk, dv (bf16; with elu+1 the chain kernel then applies its derivative
+// to dq, dk in place).  With it: Z, num and (after the prep kernel) the suffix sums, then
+// dphi(q), dphi(k) in fp32, since dphi(q) = pass - g Z and dphi(k) = pass - suffix can
+// cancel and so are formed (by the chain kernel) before any rounding to bf16; then dv.
 int tc_passes(const Problem &p, const TcBufs &b, const void *dout, void *dq, void *dk, void *dv, Problem *ps)
 {
     const int D = p.D, w = p.dv;
-    const bool nz = p.normalize != 0;
     int n = 0;
-    if (nz) ps[n++] = tc_pass(p, b.e, b.e, b.fk, b.zc, 64, D);                            // Z
-    if (nz) ps[n++] = tc_pass(p, b.fq, b.fk, p.v, b.num, D, w);                           // num
-    const void *dd = nz ? (const void *)b.dn : dout;                                     // D
-    ps[n++] = tc_pass(p, dd, p.v, b.fk, nz ? (void *)b.dqm : dq, w, D);                   // dphi(q)
-    ps[n++] = tc_pass(p, p.v, dd, b.fq, nz ? (void *)b.dkm : dk, w, D, 1);                // dphi(k), anti
-    if (nz) ps[n++] = tc_pass(p, b.e, b.e, b.gq, b.zsu, 64, D, 1);                        // suffix, anti
-    for (int i = 0; i < n && nz; ++i) ps[i].out_f32 = 1;
-    ps[n++] = tc_pass(p, b.fk, b.fq, dd, dv, D, w, 1);                                    // dv, anti
+    if (p.normalize) {
+        ps[n++] = e_pass(p, b.fk, b.zc, D, 0);                             // Z
+        ps[n++] = tc_pass(p, b.fq, b.fk, p.v, b.num, D, w);                // num
+        ps[n++] = e_pass(p, b.gq, b.zsu, D, 1);                            // suffix, anti
+        ps[n++] = tc_pass(p, b.dn, p.v, b.fk, b.dqm, w, D);                // dphi(q)
+        ps[n++] = tc_pass(p, p.v, b.dn, b.fq, b.dkm, w, D, 1);             // dphi(k), anti
+        for (int i = 0; i < n; ++i) ps[i].out_f32 = 1;
+    } else {
+        ps[n++] = tc_pass(p, dout, p.v, b.fk, dq, w, D);                   // dphi(q)
+        ps[n++] = tc_pass(p, p.v, dout, b.fq, dk, w, D, 1);                // dphi(k), anti
+    }
+    ps[n++] = tc_pass(p, b.fk, b.fq, p.normalize ? (const void *)b.dn : dout, dv, D, w, 1);  // dv, anti
     return n;
 }
 
@@ -454,12 +470,11 @@ size_t tc_bufs(const Problem &p, int sms, char *base, TcBufs *b)
     take(&t->fk, F * rows * D * 2);
     take(&t->dn, N * rows * dv * 2);
     take(&t->gq, N * rows * D * 2);
-    take(&t->e, N * rows * 64 * 2);
     take(&t->zc, N * rows * D * 4);
     take(&t->num, N * rows * dv * 4);
+    take(&t->zsu, N * rows * D * 4);
     take(&t->dqm, N * rows * D * 4);
     take(&t->dkm, N * rows * D * 4);
-    take(&t->zsu, N * rows * D * 4);
     take(&t->g, N * rows * 4);
     // the passes run one after another on the stream and share one workspace
     Problem ps[6];
@@ -508,14 +523,14 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// phi(q), phi(k) as bf16 rows (elu+1); constant rows e (normaliser)
+// phi(q), phi(k) as bf16 rows (elu+1)
 __global__ void __launch_bounds__(32 * TB_ROWS) tb_feat_kernel(const bf16 *q, const bf16 *k, TcBufs b,
-                                                             long rows, int dk, int fm, int normalize)
+                                                             long rows, int dk)
 {
     const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
-    for (int i = 4 * lane; i < dk && fm == LA_FM_ELU1; i += 128) {
+    for (int i = 4 * lane; i < dk; i += 128) {
         float xq[4], xk[4];
         ld4(q + r * dk + i, xq);
         ld4(k + r * dk + i, xk);
@@ -526,10 +541,6 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_feat_kernel(const bf16 *q, co
         }
         st4(b.fq + r * dk + i, xq);
         st4(b.fk + r * dk + i, xk);
-    }
-    if (normalize && lane < 16) {
-        const float ev[4] = {lane == 0 ? 1.f : 0.f, 0.f, 0.f, 0.f};
-        st4(b.e + r * 64 + 4 * lane, ev);
     }
 }
 
@@ -572,8 +583,9 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_prep_kernel(const bf16 *dout,
     }
 }
 
-// dq, dk through the feature map from dphi(q), dphi(k): the fp32 pass outputs less the
-// normaliser's terms, or (no normaliser, elu+1) the bf16 rows already in dq, dk, in place
+// dq, dk through the feature map: with the normaliser from the fp32 pass outputs,
+// dphi(q) = dqm - g Z and dphi(k) = dkm - suffix; without it (elu+1 only) from the bf16
+// dphi rows the passes left in dq, dk, in place
 __global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, const bf16 *k, TcBufs b,
                                                               bf16 *dq, bf16 *dk, long rows, int D, int fm,
                                                               int normalize)
@@ -585,14 +597,9 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, c
     for (int i = 4 * lane; i < D; i += 128) {
         float a[4], c[4];
         if (normalize) {
+            float z[4], zs[4];
             ld4(b.dqm + r * D + i, a);
             ld4(b.dkm + r * D + i, c);
-        } else {
-            ld4(dq + r * D + i, a);
-            ld4(dk + r * D + i, c);
-        }
-        if (normalize) {
-            float z[4], zs[4];
             ld4(b.zc + r * D + i, z);
             ld4(b.zsu + r * D + i, zs);
 #pragma unroll
@@ -600,6 +607,9 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tb_chain_kernel(const bf16 *q, c
                 a[e] -= g * z[e];
                 c[e] -= zs[e];
             }
+        } else {
+            ld4(dq + r * D + i, a);
+            ld4(dk + r * D + i, c);
         }
         if (fm == LA_FM_ELU1) {
             float xq[4], xk[4];
@@ -627,9 +637,8 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     const long rows = (long)p.B * p.H * p.L;
     cudaStream_t st = p.stream;
     const unsigned tgrid = (unsigned)((rows + TB_ROWS - 1) / TB_ROWS);
-    if (p.fm != LA_FM_IDENTITY || p.normalize) {
-        tb_feat_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b, rows, p.dk,
-                                                      p.fm, p.normalize);
+    if (p.fm == LA_FM_ELU1) {
+        tb_feat_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)p.q, (const bf16 *)p.k, b, rows, p.dk);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }
     Problem ps[6];
@@ -639,11 +648,9 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
         ps[i].workspace_bytes = b.ws_bytes;
     }
     int i = 0, rc;
-    if (p.normalize) {  // Z, num
+    if (p.normalize) {  // Z, num, then D, g and g phi(q) from them
         for (; i < 2; ++i)
             if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
-    }
-    if (p.normalize) {
         tb_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, p.D, p.dv);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }

@@ -65,6 +65,10 @@ struct Problem {
                              // normaliser; the backward pass's internal passes)
     const float *S0, *z0;    // NULL, or the state (and normaliser) before row 0: fp32
                              // [B*H][D][dv] and [B*H][D] (the decoding state's layout)
+    // The backward pass's internal passes on the tensor-core path (identity features, no
+    // normaliser, no decay):
+    int esyn;                // 1: q and k are the constant rows e = (1, 0, ..., 0), dk = 64;
+                             // q, k are not read
 };
 
 // Host-side queries used by the planner.

@@ -122,6 +122,7 @@ struct TcArgs {
     int noncausal, nseg_all;
     float l2g;  // decay: log2(gamma)
     int anti;   // anti-causal pass (identity features, no normaliser, C = 64): see the kernel
+    int esyn;   // q = k = e (1, 0, ..., 0) rows: constant tiles, only V loaded (see the kernel)
     const float *S0, *z0;  // NULL, or the state before row 0 ([BH][D][DV], [BH][D])
     int period; // decay: chunks between rescalings of the fp32 state accumulator (P)
 };
@@ -198,6 +199,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
     // decay periods all stay in virtual order; only the loads, the causal mask (s >= t in smem
     // order), the decay's in-tile factors and the rows stored change.
     const bool anti = FM == LA_FM_IDENTITY && !NORM && !NC && CH == C && a.anti != 0;
+    // Constant rows e = (1, 0, ..., 0) as both Q and K (the backward pass's prefix and suffix
+    // sums, sum_{s<=t} v_s): written once into every stage, never loaded.  No decay (its
+    // feature-map warps would rescale the K tiles in place).
+    const bool esyn = FM == LA_FM_IDENTITY && !NORM && !NC && !DK && a.esyn != 0;
     using Lay = TcLayout<D, DV, C, NORM, FO>;
     constexpr int ST = Lay::STAGES;  // TMA ring depth
     extern __shared__ uint8_t smem_raw[];
@@ -386,6 +391,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
     }
+    if (esyn)
+        // e in every row of every stage's Q and K tiles: element 0 lies in the row's first
+        // 16-byte chunk, which the 128B swizzle puts at chunk position row % 8
+        for (int e = tid; e < ST * 2 * (D / 64) * C * 8; e += TC_THREADS) {
+            const int chn = e & 7, row = (e >> 3) % C, blk = (e >> 3) / C;
+            const int kb = blk % (D / 64), isk = (blk / (D / 64)) & 1, st = blk / (2 * (D / 64));
+            uint8_t *const t = isk ? stage_k(st) + kb * Lay::K_BLK : stage_q(st) + kb * C * 128;
+            *(uint4 *)(t + row * 128 + ((chn ^ (row & 7)) << 4)) =
+                make_uint4((kb == 0 && chn == 0) ? 0x3F80u : 0u, 0u, 0u, 0u);  // bf16 1.0
+        }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -402,9 +417,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_chunked_kernel(const __grid_
                 if (c >= ST && !wait_phase(&stage_free[s], ((c / ST) - 1) & 1, ctl))
                     break;
                 const int row = anti ? a.L - (tile0 + c + 1) * C : (tile0 + c) * C;
-                mbar_arrive_expect_tx(&full[s], totals ? Lay::STAGE_TX - Lay::Q_BYTES
-                                                : (qonly ? Lay::Q_BYTES : Lay::STAGE_TX));
-                for (int kb = 0; kb < D / 64; ++kb) {
+                mbar_arrive_expect_tx(&full[s], esyn ? Lay::V_BYTES
+                                                : totals ? Lay::STAGE_TX - Lay::Q_BYTES
+                                                         : (qonly ? Lay::Q_BYTES : Lay::STAGE_TX));
+                for (int kb = 0; kb < D / 64 && !esyn; ++kb) {
                     if (!totals)
                         tma_load_3d(stage_q(s) + kb * C * 128, &a.tm_q, kb * 64, row, head, &full[s]);
                     if (!qonly)
@@ -1011,6 +1027,7 @@ int launch_t(const Problem &p, int num_sms, int mode = TC_CAUSAL)
     a.nseg_all = nseg;
     a.l2g = (mode == TC_DECAY || mode == TC_DECAY_F32OUT) ? p.l2g : 0.f;
     a.anti = p.rev ? 1 : 0;
+    a.esyn = p.esyn;
     a.S0 = p.S0;
     a.z0 = p.z0;
     // largest period P with C P |log2 gamma| <= 64 (gamma^(C P) >= 2^-64); tc_supported keeps
@@ -1101,6 +1118,9 @@ bool tc_supported(const Problem &p, int num_sms)
     (void)num_sms;
     // the anti-causal pass: identity features, no normaliser, one 64-row chunk per tile
     if (p.rev && (p.fm != LA_FM_IDENTITY || p.normalize || p.lam || p.C != 64 || p.S0 || p.z0)) return false;
+    // constant e rows: dk = 64, identity, no normaliser, no decay
+    if (p.esyn && (p.dk != 64 || p.fm != LA_FM_IDENTITY || p.normalize || p.lam || p.decay || p.C != 64))
+        return false;
     if (p.decay) {
         // one 64-row chunk per tile; gamma^64 >= 2^-64 keeps the scaled keys and the
         // output factor gamma^(i+1-64) well inside the fp32 / bf16 range
