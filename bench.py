@@ -740,13 +740,32 @@ def run_backward(args):
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = byts / (ms / 1e3) / 1e9
-    # the tensor-core route (bf16, identity / elu+1, no decay, dk = dv in {64, 128}): features,
-    # prep, chain, and 3 passes (+ 3 for the normaliser, one launch each without a sequence
-    # split); the generic route: 2 features, v', prep, 3 passes, 2 chain, 1 cast (+ 1 pass)
-    tc_route = (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
-                and (gamma == 1.0 or (gamma >= 0.5 and not w["normalize"]))
-                and L >= 128 and dk == dv and dk in (64, 128) and not ll)
-    launches = (6 + (3 if w["normalize"] else 0)) if tc_route else (10 + (1 if w["normalize"] else 0))
+    # Launches per step.  Tensor-core routes: every pass is one launch, or two where the plan
+    # splits the sequence (a totals launch first), as for a forward of the same B, H, L.
+    # Identity / elu+1 (dk = dv in {64, 128}; the decay without the normaliser): 3 passes
+    # (+ Z, num, suffix and a prep kernel with the normaliser), elu+1's feature kernel, and a
+    # chain kernel for elu+1 or the normaliser.  FAVOR+ (dk = dv = 64, m a multiple of 128):
+    # 2 feature kernels, 3 passes per 128-feature half (+ 3 and a prep kernel with the
+    # normaliser), 1 chain kernel.  The generic route: 2 features, v', prep, 3 passes, 2
+    # chain, 1 cast (+ 1 pass).
+    nz = bool(w["normalize"])
+    favor_tc = (w["dtype"] == "bf16" and w["fm"] == "favor" and gamma == 1.0 and L >= 128
+                and dk == dv == 64 and w["m"] % 128 == 0 and w["m"] <= 512 and not ll)
+    tc_route = favor_tc or (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
+                            and (gamma == 1.0 or (gamma >= 0.5 and not nz))
+                            and L >= 128 and dk == dv and dk in (64, 128) and not ll)
+    if tc_route:
+        _, pplan = la.la_chunked_plan(B, H, L, 64, 64, 64, la.make_feature_map("identity"), 0, 0, 0,
+                                      dtype, la.LA_PATH_TC, 0)
+        per_pass = pplan["n_launches"]
+        if favor_tc:
+            nh = w["m"] // 128
+            launches = 3 + (1 if nz else 0) + per_pass * nh * (6 if nz else 3)
+        else:
+            launches = per_pass * (6 if nz else 3) + (1 if nz else 0)
+            launches += (1 if w["fm"] == "elu1" else 0) + (1 if (nz or w["fm"] == "elu1") else 0)
+    else:
+        launches = 10 + (1 if nz else 0)
     if ll:  # two anti-causal sums of two launches each instead of one pass each
         launches += 2
     line = {"metric": "backward tokens/sec (B·H·L/s, %s)" % ("la_chunked_bwd_ll" if ll else "la_chunked_bwd"),

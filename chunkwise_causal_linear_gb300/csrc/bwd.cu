@@ -662,16 +662,310 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- FAVOR+ tensor-core route
+// FAVOR+ features ("Linear Attention / Performerの理論と実装", the FAVOR+ section): phi(x)_l =
+// exp(w_l . x - |x s|^2 / 2) / sqrt(m) with w_l = s omega_l and s = dk^(-1/4).  The m features
+// are cut into NH = m / 128 halves of 128 columns (bf16 rows, one buffer each), and every pass
+// of the identity route runs once per half: the passes whose scores are phi(q).phi(k) (num,
+// dv) add their halves' fp32 outputs, the others (Z, suffix, dphi) give a half of their
+// m-wide output each.  All passes store fp32; the last kernel forms dphi, contracts it with
+// the features' derivative and sums dv.
+struct TfBufs {
+    bf16 *fq, *fk;           // [NH][rows][128]
+    bf16 *dn, *gq;           // [rows][dv], [NH][rows][128] (normaliser)
+    float *zc, *num, *zsu;   // [NH][rows][128], [NH][rows][dv], [NH][rows][128] (normaliser)
+    float *dqm, *dkm, *dvp;  // [NH][rows][128], [NH][rows][128], [NH][rows][dv]
+    float *g;                // [rows] (normaliser)
+    void *ws;
+    size_t ws_bytes;
+};
+constexpr int TF_MAXP = 6 * 4;  // passes: six per half, m <= 512
+
+int tf_passes(const Problem &p, const TfBufs &b, const void *dout, Problem *ps)
+{
+    const long rows = (long)p.B * p.H * p.L;
+    const int NH = p.m / 128, w = p.dv;
+    const bool nz = p.normalize != 0;
+    const void *dd = nz ? (const void *)b.dn : dout;
+    auto fq = [&](int h) { return b.fq ? b.fq + h * rows * 128 : nullptr; };
+    auto fk = [&](int h) { return b.fk ? b.fk + h * rows * 128 : nullptr; };
+    auto f32 = [&](float *x, int h, int width) { return x ? x + h * rows * width : nullptr; };
+    auto b16 = [&](bf16 *x, int h) { return x ? x + h * rows * 128 : nullptr; };
+    int n = 0;
+    for (int h = 0; h < NH && nz; ++h) ps[n++] = e_pass(p, fk(h), f32(b.zc, h, 128), 128, 0);          // Z
+    for (int h = 0; h < NH && nz; ++h) ps[n++] = tc_pass(p, fq(h), fk(h), p.v, f32(b.num, h, w), 128, w);  // num
+    for (int h = 0; h < NH && nz; ++h) ps[n++] = e_pass(p, b16(b.gq, h), f32(b.zsu, h, 128), 128, 1);  // suffix
+    for (int h = 0; h < NH; ++h) ps[n++] = tc_pass(p, dd, p.v, fk(h), f32(b.dqm, h, 128), w, 128);     // dphi(q)
+    for (int h = 0; h < NH; ++h) ps[n++] = tc_pass(p, p.v, dd, fq(h), f32(b.dkm, h, 128), w, 128, 1);  // dphi(k)
+    for (int h = 0; h < NH; ++h) ps[n++] = tc_pass(p, fk(h), fq(h), dd, f32(b.dvp, h, w), 128, w, 1);  // dv
+    for (int i = 0; i < n; ++i) ps[i].out_f32 = 1;
+    return n;
+}
+
+size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
+{
+    const size_t rows = (size_t)p.B * p.H * p.L, NH = p.m / 128, w = p.dv;
+    const size_t N = p.normalize ? 1 : 0;
+    size_t off = 0;
+    TfBufs dummy;
+    TfBufs *t = b ? b : &dummy;
+    auto take = [&](auto **ptr, size_t bytes) {
+        if (b) *ptr = (std::remove_reference_t<decltype(**ptr)> *)(base + off);
+        off += (bytes + 1023) / 1024 * 1024;
+    };
+    take(&t->fq, NH * rows * 128 * 2);
+    take(&t->fk, NH * rows * 128 * 2);
+    take(&t->dn, N * rows * w * 2);
+    take(&t->gq, N * NH * rows * 128 * 2);
+    take(&t->zc, N * NH * rows * 128 * 4);
+    take(&t->num, N * NH * rows * w * 4);
+    take(&t->zsu, N * NH * rows * 128 * 4);
+    take(&t->dqm, NH * rows * 128 * 4);
+    take(&t->dkm, NH * rows * 128 * 4);
+    take(&t->dvp, NH * rows * w * 4);
+    take(&t->g, N * rows * 4);
+    Problem ps[TF_MAXP];
+    TfBufs nb{};
+    const int n = tf_passes(p, nb, nullptr, ps);
+    size_t wmax = 0;
+    for (int i = 0; i < n; ++i) {
+        la_plan_info info;
+        if (tc_plan(ps[i], sms, &info) == LA_OK && info.workspace_bytes > wmax) wmax = info.workspace_bytes;
+    }
+    if (b) {
+        t->ws = base + off;
+        t->ws_bytes = wmax;
+    }
+    off += (wmax + 1023) / 1024 * 1024;
+    return off;
+}
+
+// FAVOR+ features of TF_RB rows per block, one thread per feature l: w_l (64 floats) stays
+// in registers, the rows' x in shared memory (broadcast reads); phi as bf16 into its half.
+constexpr int TF_RB = 32;
+constexpr int TF_DK = 64;
+__global__ void __launch_bounds__(512) tf_feat_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
+                                                      int m)
+{
+    __shared__ float4 xs[TF_RB][TF_DK / 4];
+    __shared__ float n2[TF_RB];
+    const int l = threadIdx.x;
+    const long r0 = (long)blockIdx.x * TF_RB;
+    const float s = rsqrtf(8.f);  // dk^(-1/4), dk = 64
+    for (int e = threadIdx.x; e < TF_RB * TF_DK / 4; e += blockDim.x) {
+        const int r = e / (TF_DK / 4), c4 = e % (TF_DK / 4);
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r0 + r < rows) ld4(x + (r0 + r) * TF_DK + 4 * c4, v);
+        xs[r][c4] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    if (threadIdx.x < TF_RB) {
+        float a = 0.f;
+        for (int c4 = 0; c4 < TF_DK / 4; ++c4) {
+            const float4 v = xs[threadIdx.x][c4];
+            a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        n2[threadIdx.x] = 0.5f * s * s * a;
+    }
+    __syncthreads();
+    if (l >= m) return;
+    float wl[TF_DK];
+#pragma unroll
+    for (int i = 0; i < TF_DK; ++i) wl[i] = s * __ldg(omega + (size_t)l * TF_DK + i);
+    const float inv = rsqrtf((float)m);
+    bf16 *const fo = f + (size_t)(l >> 7) * rows * 128 + (l & 127);
+    for (int r = 0; r < TF_RB && r0 + r < rows; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < TF_DK / 4; ++c4) {
+            const float4 v = xs[r][c4];
+            acc = fmaf(wl[4 * c4], v.x, acc);
+            acc = fmaf(wl[4 * c4 + 1], v.y, acc);
+            acc = fmaf(wl[4 * c4 + 2], v.z, acc);
+            acc = fmaf(wl[4 * c4 + 3], v.w, acc);
+        }
+        fo[(r0 + r) * 128] = __float2bfloat16_rn(expf(acc - n2[r]) * inv);
+    }
+}
+
+// Normaliser, one warp per row: den = phi(q).Z over all halves, D = bf16(dout / den),
+// g = D . num / den (num summed over the halves), g phi(q) by half
+__global__ void __launch_bounds__(32 * TB_ROWS) tf_prep_kernel(const bf16 *dout, TfBufs b, long rows, int NH,
+                                                             int dv)
+{
+    const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    float part = 0.f;
+    for (int h = 0; h < NH; ++h) {
+        float f[4], z[4];
+        ld4(b.fq + (h * rows + r) * 128 + 4 * lane, f);
+        ld4(b.zc + (h * rows + r) * 128 + 4 * lane, z);
+        part += f[0] * z[0] + f[1] * z[1] + f[2] * z[2] + f[3] * z[3];
+    }
+    const float inv = 1.f / warp_sum(part);
+    float gp = 0.f;
+    for (int j = 4 * lane; j < dv; j += 128) {
+        float d[4], nm[4] = {0.f, 0.f, 0.f, 0.f};
+        ld4(dout + r * dv + j, d);
+        for (int h = 0; h < NH; ++h) {
+            float x[4];
+            ld4(b.num + (h * rows + r) * dv + j, x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) nm[e] += x[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[e] = __bfloat162float(__float2bfloat16_rn(d[e] * inv));
+        st4(b.dn + r * dv + j, d);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gp += d[e] * (nm[e] * inv);
+    }
+    const float g = warp_sum(gp);
+    if (lane == 0) b.g[r] = g;
+    for (int h = 0; h < NH; ++h) {
+        float f[4];
+        ld4(b.fq + (h * rows + r) * 128 + 4 * lane, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] *= g;
+        st4(b.gq + (h * rows + r) * 128 + 4 * lane, f);
+    }
+}
+
+// dq (blockIdx.y = 0) or dk (1) through the FAVOR+ derivative, TF_RB rows per block:
+// u_l = dphi_l phi_l with dphi = dqm - g Z or dkm - suffix (normaliser), then
+// dx_i = s sum_l u_l omega_li - s^2 x_i sum_l u_l.  The dv halves are summed by the y = 0 blocks.
+__global__ void __launch_bounds__(256) tf_chain_kernel(const bf16 *q, const bf16 *k, const float *omega, TfBufs b,
+                                                       bf16 *dq, bf16 *dk, bf16 *dv, long rows, int m, int dvn,
+                                                       int normalize)
+{
+    extern __shared__ float4 tf_sm[];
+    float *u = (float *)tf_sm;             // [TF_RB][m]
+    __shared__ float usum[TF_RB];
+    const bool isq = blockIdx.y == 0;
+    const long r0 = (long)blockIdx.x * TF_RB;
+    const int NH = m / 128;
+    const bf16 *feat = isq ? b.fq : b.fk;
+    const float *dm = isq ? b.dqm : b.dkm;
+    const float *sub = normalize ? (isq ? b.zc : b.zsu) : nullptr;
+    for (int e = threadIdx.x; e < TF_RB * m; e += blockDim.x) {
+        const int r = e / m, l = e % m;
+        float x = 0.f;
+        if (r0 + r < rows) {
+            const size_t at = ((size_t)(l >> 7) * rows + r0 + r) * 128 + (l & 127);
+            float d = dm[at];
+            if (sub) d -= (isq ? b.g[r0 + r] : 1.f) * sub[at];
+            x = d * __bfloat162float(feat[at]);
+        }
+        u[r * m + l] = x;
+    }
+    __syncthreads();
+    {
+        const int wp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int r = wp; r < TF_RB; r += 8) {
+            float a = 0.f;
+            for (int l = lane; l < m; l += 32) a += u[r * m + l];
+            a = warp_sum(a);
+            if (lane == 0) usum[r] = a;
+        }
+    }
+    __syncthreads();
+    const float s = rsqrtf(8.f);
+    const int i = threadIdx.x & (TF_DK - 1), rg = threadIdx.x >> 6;  // 4 row groups of 8 rows
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int l = 0; l < m; l += 4) {
+        const float w0 = __ldg(omega + (size_t)l * TF_DK + i), w1 = __ldg(omega + (size_t)(l + 1) * TF_DK + i);
+        const float w2 = __ldg(omega + (size_t)(l + 2) * TF_DK + i), w3 = __ldg(omega + (size_t)(l + 3) * TF_DK + i);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 uv = *(const float4 *)(u + (8 * rg + e) * m + l);
+            acc[e] = fmaf(uv.x, w0, fmaf(uv.y, w1, fmaf(uv.z, w2, fmaf(uv.w, w3, acc[e]))));
+        }
+    }
+    const bf16 *x = isq ? q : k;
+    bf16 *dx = isq ? dq : dk;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const long r = r0 + 8 * rg + e;
+        if (r >= rows) continue;
+        const float xv = __bfloat162float(x[r * TF_DK + i]);
+        dx[r * TF_DK + i] = __float2bfloat16_rn(s * acc[e] - s * s * xv * usum[8 * rg + e]);
+    }
+    if (!isq) return;
+    for (int e = threadIdx.x; e < TF_RB * dvn; e += blockDim.x) {
+        const long r = r0 + e / dvn;
+        const int j = e % dvn;
+        if (r >= rows) continue;
+        float a = 0.f;
+        for (int h = 0; h < NH; ++h) a += b.dvp[((size_t)h * rows + r) * dvn + j];
+        dv[r * dvn + j] = __float2bfloat16_rn(a);
+    }
+}
+
+int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, void *dv)
+{
+    TfBufs b;
+    tf_bufs(p, sms, (char *)p.workspace, &b);
+    const long rows = (long)p.B * p.H * p.L;
+    const int NH = p.m / 128;
+    cudaStream_t st = p.stream;
+    const unsigned fgrid = (unsigned)((rows + TF_RB - 1) / TF_RB);
+    const int fthreads = (p.m + 31) / 32 * 32;
+    tf_feat_kernel<<<fgrid, fthreads, 0, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m);
+    tf_feat_kernel<<<fgrid, fthreads, 0, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    Problem ps[TF_MAXP];
+    const int n = tf_passes(p, b, dout, ps);
+    for (int i = 0; i < n; ++i) {
+        ps[i].workspace = b.ws;
+        ps[i].workspace_bytes = b.ws_bytes;
+    }
+    int i = 0, rc;
+    if (p.normalize) {  // Z and num halves, then D, g and g phi(q)
+        for (; i < 2 * NH; ++i)
+            if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
+        const unsigned tgrid = (unsigned)((rows + TB_ROWS - 1) / TB_ROWS);
+        tf_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, NH, p.dv);
+        if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    }
+    for (; i < n; ++i)
+        if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
+    const size_t smem = (size_t)TF_RB * p.m * sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(tf_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LA_ERR_CUDA;
+    tf_chain_kernel<<<dim3(fgrid, 2), 256, smem, st>>>((const bf16 *)p.q, (const bf16 *)p.k, p.omega, b, (bf16 *)dq,
+                                                        (bf16 *)dk, (bf16 *)dv, rows, p.m, p.dv, p.normalize);
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+// bf16 FAVOR+ with dk = dv = 64, m a multiple of 128 (at most 512), no decay, every pass on
+// the tensor cores
+bool tf_supported(const Problem &p, int sms)
+{
+    if (p.dtype != LA_BF16 || p.fm != LA_FM_FAVOR || p.lam || p.decay || p.L < 128) return false;
+    if (p.dk != TF_DK || p.dv != 64 || p.m % 128 != 0 || p.m > 512 || !p.omega) return false;
+    Problem ps[TF_MAXP];
+    TfBufs nb{};
+    const int n = tf_passes(p, nb, nullptr, ps);
+    for (int i = 0; i < n; ++i)
+        if (!tc_supported(ps[i], sms)) return false;
+    return true;
+}
+
 }  // namespace
 
-// The tensor-core route: bf16, identity / elu+1 features, plain or decayed, and every pass of a
-// shape the tensor-core forward covers (with the decay: gamma >= 0.5).  The decay with the
+// The tensor-core routes: bf16, identity / elu+1 features, plain or decayed, and every pass of
+// a shape the tensor-core forward covers (with the decay: gamma >= 0.5); FAVOR+ with dk = dv =
+// 64 and m a multiple of 128, without the decay.  The decay with the
 // normaliser stays on the generic route: dphi(q) is then the difference of two passes, and the
 // decay mode rounds its gamma-scaled key rows to bf16 differently in each, so the sums no
 // longer cancel to the bf16 bar (measured relative RMS 5.5e-3 on dq at gamma = 0.95).
 bool bwd_tc_supported(const Problem &p, int sms)
 {
     if (p.dtype != LA_BF16 || p.lam || p.L < 128) return false;
+    if (p.fm == LA_FM_FAVOR) return tf_supported(p, sms);
     if (p.decay && p.normalize) return false;
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     Problem ps[6];
@@ -686,7 +980,9 @@ size_t bwd_workspace_bytes(const Problem &p, int sms)
 {
     const size_t simt = bwd_floats((long)p.B * p.H * p.L, p.D, p.dv, p.normalize, nullptr, nullptr) * sizeof(float) +
                         bwd_ll_extra_bytes(p) + bwd_ll_tail_bytes(p, sms);
-    const size_t tc = bwd_tc_supported(p, sms) ? tc_bufs(p, sms, nullptr, nullptr) : 0;
+    const size_t tc = !bwd_tc_supported(p, sms) ? 0
+                      : p.fm == LA_FM_FAVOR ? tf_bufs(p, sms, nullptr, nullptr)
+                                            : tc_bufs(p, sms, nullptr, nullptr);
     return simt > tc ? simt : tc;
 }
 
@@ -708,7 +1004,8 @@ int bwd_launch(const Problem &p, int sms, int path, const void *dout, void *dq, 
                          (uintptr_t)dq | (uintptr_t)dk | (uintptr_t)dv;
     const bool tc = bwd_tc_supported(p, sms) && (al & 15) == 0;
     if (path == LA_PATH_TC && !tc) return LA_ERR_UNSUPPORTED;
-    if (path != LA_PATH_SIMT && tc) return tc_route(p, sms, dout, dq, dk, dv);
+    if (path != LA_PATH_SIMT && tc)
+        return p.fm == LA_FM_FAVOR ? tf_route(p, sms, dout, dq, dk, dv) : tc_route(p, sms, dout, dq, dk, dv);
     if (p.dtype == LA_BF16) return bwd_t<__nv_bfloat16>(p, sms, dout, dq, dk, dv);
     return bwd_t<float>(p, sms, dout, dq, dk, dv);
 }

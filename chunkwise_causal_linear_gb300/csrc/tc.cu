@@ -1137,8 +1137,10 @@ bool tc_supported(const Problem &p, int num_sms)
     if (p.dtype != LA_BF16) return false;
     if (p.fm != LA_FM_IDENTITY && p.fm != LA_FM_ELU1) return false;
     if (p.dk != p.D) return false;
-    // (D, dv) in {(64, 64), (64, 128), (128, 128)}
-    if (!((p.D == 64 && (p.dv == 64 || p.dv == 128)) || (p.D == 128 && p.dv == 128))) return false;
+    // (D, dv) in {(64, 64), (64, 128), (128, 128)}; (128, 64) for the fp32-output mode
+    // without the decay (the backward pass's FAVOR+ route)
+    const bool d128v64 = p.D == 128 && p.dv == 64 && p.out_f32 && !p.decay;
+    if (!((p.D == 64 && (p.dv == 64 || p.dv == 128)) || (p.D == 128 && p.dv == 128) || d128v64)) return false;
     if (p.C != 16 && p.C != 32 && p.C != 64) return false;
     if (p.L < 2 * 64) return false;  // short sequences: the generic path is as fast
     return true;
@@ -1160,7 +1162,8 @@ int tc_plan(const Problem &p, int num_sms, la_plan_info *info)
     };
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;
-    info->smem_bytes = p.D == 128 ? alloc(I128{}, I128{}) : (p.dv == 128 ? alloc(I64{}, I128{}) : alloc(I64{}, I64{}));
+    info->smem_bytes = p.D == 128 ? (p.dv == 128 ? alloc(I128{}, I128{}) : TcLayout<128, 64, 64, false, true>::ALLOC)
+                                  : (p.dv == 128 ? alloc(I64{}, I128{}) : alloc(I64{}, I64{}));
     info->n_launches = nseg > 1 ? 2 : 1;
     info->workspace_bytes = tc_workspace(p, nseg);
     return LA_OK;
@@ -1172,6 +1175,8 @@ int tc_launch(const Problem &p, int num_sms)
     if (p.lam) return tcl_launch(p, num_sms);
     if (p.fm == LA_FM_FAVOR) return tcf_launch(p, num_sms);
     if (p.C == 128 || p.C == 256) return tcw_launch(p, num_sms);
+    if (p.D == 128 && p.dv == 64)  // the fp32-output mode only (tc_supported)
+        return launch_t<128, 64, 64, LA_FM_IDENTITY, false>(p, num_sms, TC_F32OUT);
     if (p.D == 128) return launch_d<128, 128>(p, num_sms);
     return p.dv == 128 ? launch_d<64, 128>(p, num_sms) : launch_d<64, 64>(p, num_sms);
 }

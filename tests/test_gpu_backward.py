@@ -73,14 +73,23 @@ CASES = [
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=2048, normalize=False), 64, 0.98),
     ("elu1-norm-d128-L8192", dict(B=1, H=2, L=700, normalize=False), 64, 0.9),
     ("identity-d64-L2048", dict(B=2, H=2, L=777), 64, 0.75),
+    # FAVOR+ on the tensor-core route: split sequence, m = 128 and 256, with and without the
+    # normaliser
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=1500), 64, 1.0),
+    ("favor-m256-d64-L16384", dict(B=2, H=1, L=700, m=128, normalize=False), 64, 1.0),
 ]
 
 
 def bwd_path(w, gamma):
     """1 (generic) or 2 (tensor cores): the path la_chunked_bwd takes on AUTO."""
-    return 2 if (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
+    if w["dtype"] != "bf16" or w["L"] < 128:
+        return 1
+    if w["fm"] == "favor":
+        return 2 if (gamma == 1.0 and w["dk"] == w["dv"] == 64 and w["m"] % 128 == 0
+                     and w["m"] <= 512) else 1
+    return 2 if (w["fm"] in ("identity", "elu1")
                  and (gamma == 1.0 or (gamma >= 0.5 and not w["normalize"]))
-                 and w["L"] >= 128 and w["dk"] == w["dv"] and w["dk"] in (64, 128)) else 1
+                 and w["dk"] == w["dv"] and w["dk"] in (64, 128)) else 1
 
 
 @pytest.mark.parametrize("base,over,C,gamma", CASES)
