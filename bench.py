@@ -744,13 +744,13 @@ def run_backward(args):
     # splits the sequence (a totals launch first), as for a forward of the same B, H, L.
     # Identity / elu+1 (dk = dv in {64, 128}; the decay without the normaliser): 3 passes
     # (+ Z, num, suffix and a prep kernel with the normaliser), elu+1's feature kernel, and a
-    # chain kernel for elu+1 or the normaliser.  FAVOR+ (dk = dv = 64, m a multiple of 128):
+    # chain kernel for elu+1 or the normaliser.  FAVOR+ (dk = dv = 64, m = 128, 256 or 512):
     # 2 feature kernels, 3 passes per 128-feature half (+ 3 and a prep kernel with the
     # normaliser), 1 chain kernel.  The generic route: 2 features, v', prep, 3 passes, 2
     # chain, 1 cast (+ 1 pass).
     nz = bool(w["normalize"])
     favor_tc = (w["dtype"] == "bf16" and w["fm"] == "favor" and gamma == 1.0 and L >= 128
-                and dk == dv == 64 and w["m"] % 128 == 0 and w["m"] <= 512 and not ll)
+                and dk == dv == 64 and w["m"] in (128, 256, 512) and not ll)
     tc_route = favor_tc or (w["dtype"] == "bf16" and w["fm"] in ("identity", "elu1")
                             and (gamma == 1.0 or (gamma >= 0.5 and not nz))
                             and L >= 128 and dk == dv and dk in (64, 128) and not ll)

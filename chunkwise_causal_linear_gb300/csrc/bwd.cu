@@ -740,53 +740,7 @@ size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
     return off;
 }
 
-// FAVOR+ features of TF_RB rows per block, one thread per feature l: w_l (64 floats) stays
-// in registers, the rows' x in shared memory (broadcast reads); phi as bf16 into its half.
-constexpr int TF_RB = 32;
 constexpr int TF_DK = 64;
-__global__ void __launch_bounds__(512) tf_feat_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
-                                                      int m)
-{
-    __shared__ float4 xs[TF_RB][TF_DK / 4];
-    __shared__ float n2[TF_RB];
-    const int l = threadIdx.x;
-    const long r0 = (long)blockIdx.x * TF_RB;
-    const float s = rsqrtf(8.f);  // dk^(-1/4), dk = 64
-    for (int e = threadIdx.x; e < TF_RB * TF_DK / 4; e += blockDim.x) {
-        const int r = e / (TF_DK / 4), c4 = e % (TF_DK / 4);
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r0 + r < rows) ld4(x + (r0 + r) * TF_DK + 4 * c4, v);
-        xs[r][c4] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    __syncthreads();
-    if (threadIdx.x < TF_RB) {
-        float a = 0.f;
-        for (int c4 = 0; c4 < TF_DK / 4; ++c4) {
-            const float4 v = xs[threadIdx.x][c4];
-            a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-        n2[threadIdx.x] = 0.5f * s * s * a;
-    }
-    __syncthreads();
-    if (l >= m) return;
-    float wl[TF_DK];
-#pragma unroll
-    for (int i = 0; i < TF_DK; ++i) wl[i] = s * __ldg(omega + (size_t)l * TF_DK + i);
-    const float inv = rsqrtf((float)m);
-    bf16 *const fo = f + (size_t)(l >> 7) * rows * 128 + (l & 127);
-    for (int r = 0; r < TF_RB && r0 + r < rows; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int c4 = 0; c4 < TF_DK / 4; ++c4) {
-            const float4 v = xs[r][c4];
-            acc = fmaf(wl[4 * c4], v.x, acc);
-            acc = fmaf(wl[4 * c4 + 1], v.y, acc);
-            acc = fmaf(wl[4 * c4 + 2], v.z, acc);
-            acc = fmaf(wl[4 * c4 + 3], v.w, acc);
-        }
-        fo[(r0 + r) * 128] = __float2bfloat16_rn(expf(acc - n2[r]) * inv);
-    }
-}
 
 // Normaliser, one warp per row: den = phi(q).Z over all halves, D = bf16(dout / den),
 // g = D . num / den (num summed over the halves), g phi(q) by half
@@ -831,75 +785,222 @@ __global__ void __launch_bounds__(32 * TB_ROWS) tf_prep_kernel(const bf16 *dout,
     }
 }
 
-// dq (blockIdx.y = 0) or dk (1) through the FAVOR+ derivative, TF_RB rows per block:
-// u_l = dphi_l phi_l with dphi = dqm - g Z or dkm - suffix (normaliser), then
-// dx_i = s sum_l u_l omega_li - s^2 x_i sum_l u_l.  The dv halves are summed by the y = 0 blocks.
-__global__ void __launch_bounds__(256) tf_chain_kernel(const bf16 *q, const bf16 *k, const float *omega, TfBufs b,
-                                                       bf16 *dq, bf16 *dk, bf16 *dv, long rows, int m, int dvn,
-                                                       int normalize)
+// The two contractions with omega (features: x omega^T; chain: u omega) on the warp-level
+// tensor-core instruction, m16n8k16 bf16 in, fp32 accumulate.  omega enters as a bf16 hi / lo
+// pair (omega = hi + lo to about 2^-16 relative): x is exact in bf16, u is split the same
+// way, and the products hi.hi + hi.lo (+ lo.hi) keep the contraction at fp32 accuracy.
+// Fragment layout of the instruction (PTX ISA, mma.m16n8k16 with 16-bit operands), with
+// g = lane / 4 and t = lane % 4: A holds rows g and g+8 at columns 2t, 2t+1 and 2t+8, 2t+9;
+// B holds column g at rows 2t, 2t+1 and 2t+8, 2t+9; the accumulator holds rows g and g+8 at
+// columns 2t, 2t+1.  The lower half of each 32-bit register is the lower index.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-    extern __shared__ float4 tf_sm[];
-    float *u = (float *)tf_sm;             // [TF_RB][m]
-    __shared__ float usum[TF_RB];
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t bf2(float lo, float hi)
+{
+    const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *(const uint32_t *)&t;
+}
+__device__ __forceinline__ float bf_to(bf16 x) { return __bfloat162float(x); }
+
+// Features: persistent blocks of 4 warps, one 16-row tile per warp at a time; W = s omega
+// as bf16 hi / lo rows [m][TFM_WS] in shared memory (the padded stride makes the B loads
+// conflict-free); 64 features per accumulator pass.
+constexpr int TFM_WS = 72;
+__global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
+                                                          int m)
+{
+    extern __shared__ uint4 tfm_sm[];
+    bf16 *const Whi = (bf16 *)tfm_sm, *const Wlo = Whi + m * TFM_WS;
+    const float s = rsqrtf(8.f);  // dk^(-1/4), dk = 64
+    for (int e = threadIdx.x; e < m * TF_DK; e += blockDim.x) {
+        const float w = s * __ldg(omega + e);
+        const bf16 h = __float2bfloat16_rn(w);
+        Whi[(e >> 6) * TFM_WS + (e & 63)] = h;
+        Wlo[(e >> 6) * TFM_WS + (e & 63)] = __float2bfloat16_rn(w - bf_to(h));
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float inv = rsqrtf((float)m);
+    const long ntiles = (rows + 15) / 16;
+    for (long tile = (long)blockIdx.x * 4 + warp; tile < ntiles; tile += (long)gridDim.x * 4) {
+        const long ra = tile * 16 + g, rb = ra + 8;
+        uint32_t a[4][4];
+        float sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int c = kk * 16 + 2 * t;
+            a[kk][0] = ra < rows ? *(const uint32_t *)(x + ra * TF_DK + c) : 0u;
+            a[kk][1] = rb < rows ? *(const uint32_t *)(x + rb * TF_DK + c) : 0u;
+            a[kk][2] = ra < rows ? *(const uint32_t *)(x + ra * TF_DK + c + 8) : 0u;
+            a[kk][3] = rb < rows ? *(const uint32_t *)(x + rb * TF_DK + c + 8) : 0u;
+#pragma unroll
+            for (int h = 0; h < 4; h += 2) {
+                const float x0 = __uint_as_float(a[kk][h] << 16), x1 = __uint_as_float(a[kk][h] & 0xFFFF0000u);
+                const float y0 = __uint_as_float(a[kk][h + 1] << 16), y1 = __uint_as_float(a[kk][h + 1] & 0xFFFF0000u);
+                sa += x0 * x0 + x1 * x1;
+                sb += y0 * y0 + y1 * y1;
+            }
+        }
+        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+        sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+        const float ha = 0.5f * s * s * sa, hb = 0.5f * s * s * sb;
+        for (int c0 = 0; c0 < m; c0 += 64) {
+            float acc[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    const int at = (c0 + nt * 8 + g) * TFM_WS + kk * 16 + 2 * t;
+                    const uint32_t *wh = (const uint32_t *)(Whi + at), *wl = (const uint32_t *)(Wlo + at);
+                    mma_bf16(acc[nt], a[kk], wh[0], wh[4]);
+                    mma_bf16(acc[nt], a[kk], wl[0], wl[4]);
+                }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int col = c0 + nt * 8 + 2 * t;
+                bf16 *const fo = f + (size_t)(col >> 7) * rows * 128 + (col & 127);
+                if (ra < rows)
+                    *(uint32_t *)(fo + ra * 128) = bf2(expf(acc[nt][0] - ha) * inv, expf(acc[nt][1] - ha) * inv);
+                if (rb < rows)
+                    *(uint32_t *)(fo + rb * 128) = bf2(expf(acc[nt][2] - hb) * inv, expf(acc[nt][3] - hb) * inv);
+            }
+        }
+    }
+}
+
+// Chain: persistent blocks of 8 warps over tiles of TFC_RB rows, blockIdx.y = 0 for dq, 1 for
+// dk.  The block first forms u = dphi phi (as bf16 hi / lo rows) and sum_l u_l for its rows in
+// shared memory; then warp w takes rows 16 (w / 4) .. +15 and output columns 16 (w % 4) .. +15:
+// sum_l u_l omega_li with omega^T as bf16 hi / lo rows [64][m + 8].  The y = 0 blocks also
+// sum the dv halves of their rows.
+constexpr int TFC_RB = 32;
+__global__ void __launch_bounds__(256) tf_chain_mma_kernel(const bf16 *q, const bf16 *k, const float *omega,
+                                                           TfBufs b, bf16 *dq, bf16 *dk, bf16 *dv, long rows,
+                                                           int m, int dvn, int normalize)
+{
+    extern __shared__ uint4 tfc_sm[];
+    const int OS = m + 8;  // bf16 stride of the omega^T and u rows
+    bf16 *const Ohi = (bf16 *)tfc_sm, *const Olo = Ohi + TF_DK * OS;
+    bf16 *const Uhi = Olo + TF_DK * OS, *const Ulo = Uhi + TFC_RB * OS;
+    float *const usum = (float *)(Ulo + TFC_RB * OS);
+    for (int e = threadIdx.x; e < m * TF_DK; e += blockDim.x) {
+        const float w = __ldg(omega + e);
+        const bf16 h = __float2bfloat16_rn(w);
+        Ohi[(e & 63) * OS + (e >> 6)] = h;
+        Olo[(e & 63) * OS + (e >> 6)] = __float2bfloat16_rn(w - bf_to(h));
+    }
     const bool isq = blockIdx.y == 0;
-    const long r0 = (long)blockIdx.x * TF_RB;
-    const int NH = m / 128;
-    const bf16 *feat = isq ? b.fq : b.fk;
-    const float *dm = isq ? b.dqm : b.dkm;
-    const float *sub = normalize ? (isq ? b.zc : b.zsu) : nullptr;
-    for (int e = threadIdx.x; e < TF_RB * m; e += blockDim.x) {
-        const int r = e / m, l = e % m;
-        float x = 0.f;
-        if (r0 + r < rows) {
-            const size_t at = ((size_t)(l >> 7) * rows + r0 + r) * 128 + (l & 127);
-            float d = dm[at];
-            if (sub) d -= (isq ? b.g[r0 + r] : 1.f) * sub[at];
-            x = d * __bfloat162float(feat[at]);
-        }
-        u[r * m + l] = x;
-    }
-    __syncthreads();
-    {
-        const int wp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int r = wp; r < TF_RB; r += 8) {
-            float a = 0.f;
-            for (int l = lane; l < m; l += 32) a += u[r * m + l];
-            a = warp_sum(a);
-            if (lane == 0) usum[r] = a;
-        }
-    }
-    __syncthreads();
+    const bf16 *const feat = isq ? b.fq : b.fk;
+    const float *const dm = isq ? b.dqm : b.dkm;
+    const float *const sub = normalize ? (isq ? b.zc : b.zsu) : nullptr;
+    const bf16 *const x = isq ? q : k;
+    bf16 *const dx = isq ? dq : dk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int NH = m / 128, lm = 31 - __clz(m);  // m: a power of two
     const float s = rsqrtf(8.f);
-    const int i = threadIdx.x & (TF_DK - 1), rg = threadIdx.x >> 6;  // 4 row groups of 8 rows
-    float acc[8];
+    const long ntiles = (rows + TFC_RB - 1) / TFC_RB;
+    for (long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const long r0 = tile * TFC_RB;
+        __syncthreads();  // omega^T written; the previous tile's u read
+        if (threadIdx.x < TFC_RB) usum[threadIdx.x] = 0.f;
+        __syncthreads();
+        // u rows in groups of four columns: item e = r (m / 4) + l4, eight per thread with
+        // their loads in flight together; a warp's 32 items share one row (m / 4 is a multiple
+        // of 32), so each row sum is one shuffle reduction per warp
+        const int lg = lm - 2;  // log2(m / 4)
+        for (int e0 = 0; e0 < TFC_RB << lg; e0 += 8 * 256) {
+            float4 d4[8], s4[8];
+            uint2 f4[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int l = 0; l < m; l += 4) {
-        const float w0 = __ldg(omega + (size_t)l * TF_DK + i), w1 = __ldg(omega + (size_t)(l + 1) * TF_DK + i);
-        const float w2 = __ldg(omega + (size_t)(l + 2) * TF_DK + i), w3 = __ldg(omega + (size_t)(l + 3) * TF_DK + i);
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * 256 + threadIdx.x, r = e >> lg, l = (e & ((1 << lg) - 1)) << 2;
+                const long row = r0 + r;
+                d4[j] = s4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                f4[j] = make_uint2(0u, 0u);
+                if (r < TFC_RB && row < rows) {
+                    const size_t at = ((size_t)(l >> 7) * rows + row) * 128 + (l & 127);
+                    d4[j] = *(const float4 *)(dm + at);
+                    if (sub) {
+                        const float c = isq ? b.g[row] : 1.f;
+                        const float4 z = *(const float4 *)(sub + at);
+                        s4[j] = make_float4(c * z.x, c * z.y, c * z.z, c * z.w);
+                    }
+                    f4[j] = *(const uint2 *)(feat + at);
+                }
+            }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 uv = *(const float4 *)(u + (8 * rg + e) * m + l);
-            acc[e] = fmaf(uv.x, w0, fmaf(uv.y, w1, fmaf(uv.z, w2, fmaf(uv.w, w3, acc[e]))));
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * 256 + threadIdx.x, r = e >> lg, l = (e & ((1 << lg) - 1)) << 2;
+                const float u0 = (d4[j].x - s4[j].x) * __uint_as_float(f4[j].x << 16);
+                const float u1 = (d4[j].y - s4[j].y) * __uint_as_float(f4[j].x & 0xFFFF0000u);
+                const float u2 = (d4[j].z - s4[j].z) * __uint_as_float(f4[j].y << 16);
+                const float u3 = (d4[j].w - s4[j].w) * __uint_as_float(f4[j].y & 0xFFFF0000u);
+                if (r < TFC_RB) {
+                    const uint2 h = make_uint2(bf2(u0, u1), bf2(u2, u3));
+                    const float h0 = __uint_as_float(h.x << 16), h1 = __uint_as_float(h.x & 0xFFFF0000u);
+                    const float h2 = __uint_as_float(h.y << 16), h3 = __uint_as_float(h.y & 0xFFFF0000u);
+                    *(uint2 *)(Uhi + r * OS + l) = h;
+                    *(uint2 *)(Ulo + r * OS + l) = make_uint2(bf2(u0 - h0, u1 - h1), bf2(u2 - h2, u3 - h3));
+                }
+                const float part = warp_sum(u0 + u1 + u2 + u3);
+                if (lane == 0 && r < TFC_RB) atomicAdd(&usum[r], part);
+            }
         }
-    }
-    const bf16 *x = isq ? q : k;
-    bf16 *dx = isq ? dq : dk;
+        __syncthreads();
+        const int rt = 16 * (warp >> 2), n0 = 2 * (warp & 3);  // row tile, first of two n-tiles
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int kk = 0; kk < m / 16; ++kk) {
+            const int c = kk * 16 + 2 * t;
+            const int ua = (rt + g) * OS + c, ub = ua + 8 * OS;
+            const uint32_t ah[4] = {*(const uint32_t *)(Uhi + ua), *(const uint32_t *)(Uhi + ub),
+                                    *(const uint32_t *)(Uhi + ua + 8), *(const uint32_t *)(Uhi + ub + 8)};
+            const uint32_t al[4] = {*(const uint32_t *)(Ulo + ua), *(const uint32_t *)(Ulo + ub),
+                                    *(const uint32_t *)(Ulo + ua + 8), *(const uint32_t *)(Ulo + ub + 8)};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const long r = r0 + 8 * rg + e;
-        if (r >= rows) continue;
-        const float xv = __bfloat162float(x[r * TF_DK + i]);
-        dx[r * TF_DK + i] = __float2bfloat16_rn(s * acc[e] - s * s * xv * usum[8 * rg + e]);
-    }
-    if (!isq) return;
-    for (int e = threadIdx.x; e < TF_RB * dvn; e += blockDim.x) {
-        const long r = r0 + e / dvn;
-        const int j = e % dvn;
-        if (r >= rows) continue;
-        float a = 0.f;
-        for (int h = 0; h < NH; ++h) a += b.dvp[((size_t)h * rows + r) * dvn + j];
-        dv[r * dvn + j] = __float2bfloat16_rn(a);
+            for (int j = 0; j < 2; ++j) {
+                const int at = ((n0 + j) * 8 + g) * OS + c;
+                const uint32_t *oh = (const uint32_t *)(Ohi + at), *ol = (const uint32_t *)(Olo + at);
+                mma_bf16(acc[j], ah, oh[0], oh[4]);
+                mma_bf16(acc[j], ah, ol[0], ol[4]);
+                mma_bf16(acc[j], al, oh[0], oh[4]);
+            }
+        }
+        const long ra = r0 + rt + g, rb = ra + 8;
+        const float sa = usum[rt + g], sb = usum[rt + g + 8];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = (n0 + j) * 8 + 2 * t;
+            if (ra < rows) {
+                const uint32_t xv = *(const uint32_t *)(x + ra * TF_DK + i);
+                *(uint32_t *)(dx + ra * TF_DK + i) =
+                    bf2(s * acc[j][0] - s * s * __uint_as_float(xv << 16) * sa,
+                        s * acc[j][1] - s * s * __uint_as_float(xv & 0xFFFF0000u) * sa);
+            }
+            if (rb < rows) {
+                const uint32_t xv = *(const uint32_t *)(x + rb * TF_DK + i);
+                *(uint32_t *)(dx + rb * TF_DK + i) =
+                    bf2(s * acc[j][2] - s * s * __uint_as_float(xv << 16) * sb,
+                        s * acc[j][3] - s * s * __uint_as_float(xv & 0xFFFF0000u) * sb);
+            }
+        }
+        if (isq)
+            for (int e = threadIdx.x; e < TFC_RB * dvn; e += blockDim.x) {
+                const long row = r0 + e / dvn;
+                const int j = e % dvn;
+                if (row >= rows) continue;
+                float a = 0.f;
+                for (int h = 0; h < NH; ++h) a += b.dvp[((size_t)h * rows + row) * dvn + j];
+                dv[row * dvn + j] = __float2bfloat16_rn(a);
+            }
     }
 }
 
@@ -910,10 +1011,13 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     const long rows = (long)p.B * p.H * p.L;
     const int NH = p.m / 128;
     cudaStream_t st = p.stream;
-    const unsigned fgrid = (unsigned)((rows + TF_RB - 1) / TF_RB);
-    const int fthreads = (p.m + 31) / 32 * 32;
-    tf_feat_kernel<<<fgrid, fthreads, 0, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m);
-    tf_feat_kernel<<<fgrid, fthreads, 0, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m);
+    const size_t fsm = (size_t)2 * p.m * TFM_WS * sizeof(bf16);
+    if (cudaFuncSetAttribute(tf_feat_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm) != cudaSuccess)
+        return LA_ERR_CUDA;
+    const long ftiles = (rows + 63) / 64;
+    const unsigned fgrid = (unsigned)(ftiles < 2L * sms ? ftiles : 2L * sms);
+    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m);
+    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     Problem ps[TF_MAXP];
     const int n = tf_passes(p, b, dout, ps);
@@ -931,21 +1035,23 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     }
     for (; i < n; ++i)
         if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
-    const size_t smem = (size_t)TF_RB * p.m * sizeof(float);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(tf_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    const size_t csm = (size_t)(2 * TF_DK + 2 * TFC_RB) * (p.m + 8) * sizeof(bf16) + TFC_RB * sizeof(float);
+    if (cudaFuncSetAttribute(tf_chain_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm) != cudaSuccess)
         return LA_ERR_CUDA;
-    tf_chain_kernel<<<dim3(fgrid, 2), 256, smem, st>>>((const bf16 *)p.q, (const bf16 *)p.k, p.omega, b, (bf16 *)dq,
-                                                        (bf16 *)dk, (bf16 *)dv, rows, p.m, p.dv, p.normalize);
+    const long ctiles = (rows + TFC_RB - 1) / TFC_RB;
+    const unsigned cgrid = (unsigned)(ctiles < 2L * sms ? ctiles : 2L * sms);
+    tf_chain_mma_kernel<<<dim3(cgrid, 2), 256, csm, st>>>((const bf16 *)p.q, (const bf16 *)p.k, p.omega, b,
+                                                          (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, rows, p.m, p.dv,
+                                                          p.normalize);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-// bf16 FAVOR+ with dk = dv = 64, m a multiple of 128 (at most 512), no decay, every pass on
-// the tensor cores
+// bf16 FAVOR+ with dk = dv = 64, m = 128, 256 or 512, no decay, every pass on the tensor
+// cores
 bool tf_supported(const Problem &p, int sms)
 {
     if (p.dtype != LA_BF16 || p.fm != LA_FM_FAVOR || p.lam || p.decay || p.L < 128) return false;
-    if (p.dk != TF_DK || p.dv != 64 || p.m % 128 != 0 || p.m > 512 || !p.omega) return false;
+    if (p.dk != TF_DK || p.dv != 64 || (p.m != 128 && p.m != 256 && p.m != 512) || !p.omega) return false;
     Problem ps[TF_MAXP];
     TfBufs nb{};
     const int n = tf_passes(p, nb, nullptr, ps);
@@ -958,7 +1064,7 @@ bool tf_supported(const Problem &p, int sms)
 
 // The tensor-core routes: bf16, identity / elu+1 features, plain or decayed, and every pass of
 // a shape the tensor-core forward covers (with the decay: gamma >= 0.5); FAVOR+ with dk = dv =
-// 64 and m a multiple of 128, without the decay.  The decay with the
+// 64 and m = 128, 256 or 512, without the decay.  The decay with the
 // normaliser stays on the generic route: dphi(q) is then the difference of two passes, and the
 // decay mode rounds its gamma-scaled key rows to bf16 differently in each, so the sums no
 // longer cancel to the bf16 bar (measured relative RMS 5.5e-3 on dq at gamma = 0.95).

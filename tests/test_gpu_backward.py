@@ -85,8 +85,7 @@ def bwd_path(w, gamma):
     if w["dtype"] != "bf16" or w["L"] < 128:
         return 1
     if w["fm"] == "favor":
-        return 2 if (gamma == 1.0 and w["dk"] == w["dv"] == 64 and w["m"] % 128 == 0
-                     and w["m"] <= 512) else 1
+        return 2 if (gamma == 1.0 and w["dk"] == w["dv"] == 64 and w["m"] in (128, 256, 512)) else 1
     return 2 if (w["fm"] in ("identity", "elu1")
                  and (gamma == 1.0 or (gamma >= 0.5 and not w["normalize"]))
                  and w["dk"] == w["dv"] and w["dk"] in (64, 128)) else 1
