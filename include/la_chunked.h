@@ -322,12 +322,13 @@ int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_m
  * backward formulas; these follow from the chain rule on the causal definition (mask 1 or
  * gamma^(t-s), with or without the normaliser), then through the feature map.  They are
  * linear-attention passes with the roles swapped, two of them anti-causal:
- *   - LA_PATH_TC: bf16, identity / elu+1 features, no decay, or gamma >= 0.5 without the
- *     normaliser (the same gamma^|t-s| mask in every pass), L >= 128, 16-byte aligned
- *     q, k, v, dout and gradient buffers, and pass shapes the tensor-core forward covers
- *     ((dk, dv) in {(64, 64), (128, 128)}); the anti-causal
- *     passes run over reversed rows and the normaliser adds two passes; pass outputs are
- *     bf16 like the forward's;
+ *   - LA_PATH_TC: bf16, L >= 128, 16-byte aligned q, k, v, dout and gradient buffers, and
+ *     either identity / elu+1 features with (dk, dv) in {(64, 64), (128, 128)}, no decay or
+ *     gamma >= 0.5 without the normaliser (the same gamma^|t-s| mask in every pass), or
+ *     FAVOR+ with dk = dv = 64, m in {128, 256, 512} and no decay.  Every pass runs on the
+ *     tensor-core forward with identity features (the anti-causal ones in its anti-causal
+ *     mode, in place; FAVOR+ once per 128 features); the normaliser adds three passes and
+ *     its feature-gradient passes keep fp32 rows;
  *   - LA_PATH_SIMT: every supported case, in fp32 on the generic kernel;
  *   - LA_PATH_AUTO picks the first that applies.
  *   q, k, v, dout   device, as la_chunked_fwd's q, k, v and out ([B, H, L, d], dtype).
@@ -339,8 +340,10 @@ int la_decay_plan(int B, int H, int L, int dk, int dv, int C, const la_feature_m
  *   gamma           1 for the plain mask, else the decay (0 < gamma < 1; LA_ERR_ARG outside)
  *   C               chunk size of the generic path's passes (any value; the result does
  *                   not depend on it beyond rounding); the tensor-core passes use 64
- *   workspace       at least la_chunked_bwd_workspace_bytes(...) bytes (fp32 intermediates,
- *                   about 4 (D + dv) floats per row)
+ *   workspace       at least la_chunked_bwd_workspace_bytes(...) bytes (intermediates:
+ *                   about 4 (D + dv) floats per row on the generic route, at most about
+ *                   6 (D + dv) on the tensor-core route, none there for identity features
+ *                   without the normaliser)
  * D (dk, or m for FAVOR+) and dk must be at most 512 and dv below 512.  Returns LA_OK or a
  * negative status before any launch.
  */
