@@ -676,10 +676,12 @@ struct TfBufs {
     float *zc, *num, *zsu;   // [NH][rows][128], [NH][rows][dv], [NH][rows][128] (normaliser)
     float *dqm, *dkm, *dvp;  // [NH][rows][128], [NH][rows][128], [NH][rows][dv]
     float *g;                // [rows] (normaliser)
+    bf16 *omt;               // omega^T as bf16 hi / lo rows: [2][64][m + 8]
     void *ws;
     size_t ws_bytes;
 };
 constexpr int TF_MAXP = 6 * 4;  // passes: six per half, m <= 512
+constexpr int TF_DK = 64;        // dk = dv of the route
 
 int tf_passes(const Problem &p, const TfBufs &b, const void *dout, Problem *ps)
 {
@@ -724,6 +726,7 @@ size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
     take(&t->dkm, NH * rows * 128 * 4);
     take(&t->dvp, NH * rows * w * 4);
     take(&t->g, N * rows * 4);
+    take(&t->omt, (size_t)2 * TF_DK * (p.m + 8) * 2);
     Problem ps[TF_MAXP];
     TfBufs nb{};
     const int n = tf_passes(p, nb, nullptr, ps);
@@ -739,8 +742,6 @@ size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
     off += (wmax + 1023) / 1024 * 1024;
     return off;
 }
-
-constexpr int TF_DK = 64;
 
 // Normaliser, one warp per row: den = phi(q).Z over all halves, D = bf16(dout / den),
 // g = D . num / den (num summed over the halves), g phi(q) by half
@@ -812,7 +813,7 @@ __device__ __forceinline__ float bf_to(bf16 x) { return __bfloat162float(x); }
 // conflict-free); 64 features per accumulator pass.
 constexpr int TFM_WS = 72;
 __global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
-                                                          int m)
+                                                          int m, bf16 *omt)
 {
     extern __shared__ uint4 tfm_sm[];
     bf16 *const Whi = (bf16 *)tfm_sm, *const Wlo = Whi + m * TFM_WS;
@@ -822,6 +823,13 @@ __global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const f
         const bf16 h = __float2bfloat16_rn(w);
         Whi[(e >> 6) * TFM_WS + (e & 63)] = h;
         Wlo[(e >> 6) * TFM_WS + (e & 63)] = __float2bfloat16_rn(w - bf_to(h));
+        if (omt && blockIdx.x == 0) {
+            // omega^T hi / lo rows for the chain kernel (unscaled)
+            const float o = __ldg(omega + e);
+            const bf16 oh = __float2bfloat16_rn(o);
+            omt[(e & 63) * (m + 8) + (e >> 6)] = oh;
+            omt[(TF_DK + (e & 63)) * (m + 8) + (e >> 6)] = __float2bfloat16_rn(o - bf_to(oh));
+        }
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -880,24 +888,20 @@ __global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const f
 // Chain: persistent blocks of 8 warps over tiles of TFC_RB rows, blockIdx.y = 0 for dq, 1 for
 // dk.  The block first forms u = dphi phi (as bf16 hi / lo rows) and sum_l u_l for its rows in
 // shared memory; then warp w takes rows 16 (w / 4) .. +15 and output columns 16 (w % 4) .. +15:
-// sum_l u_l omega_li with omega^T as bf16 hi / lo rows [64][m + 8].  The y = 0 blocks also
-// sum the dv halves of their rows.
+// sum_l u_l omega_li with omega^T as bf16 hi / lo rows [64][m + 8], read through the L1 (it is
+// the same 2 x 64 x (m + 8) values for every block), which leaves shared memory to u alone
+// and so lets four blocks share an SM.  The y = 0 blocks also sum the dv halves of their rows.
 constexpr int TFC_RB = 32;
-__global__ void __launch_bounds__(256) tf_chain_mma_kernel(const bf16 *q, const bf16 *k, const float *omega,
+constexpr int TFC_IT = 4;  // staged items in flight per thread
+__global__ void __launch_bounds__(256, 4) tf_chain_mma_kernel(const bf16 *q, const bf16 *k, const float *omega,
                                                            TfBufs b, bf16 *dq, bf16 *dk, bf16 *dv, long rows,
                                                            int m, int dvn, int normalize)
 {
     extern __shared__ uint4 tfc_sm[];
     const int OS = m + 8;  // bf16 stride of the omega^T and u rows
-    bf16 *const Ohi = (bf16 *)tfc_sm, *const Olo = Ohi + TF_DK * OS;
-    bf16 *const Uhi = Olo + TF_DK * OS, *const Ulo = Uhi + TFC_RB * OS;
+    const bf16 *const Ohi = b.omt, *const Olo = b.omt + TF_DK * OS;
+    bf16 *const Uhi = (bf16 *)tfc_sm, *const Ulo = Uhi + TFC_RB * OS;
     float *const usum = (float *)(Ulo + TFC_RB * OS);
-    for (int e = threadIdx.x; e < m * TF_DK; e += blockDim.x) {
-        const float w = __ldg(omega + e);
-        const bf16 h = __float2bfloat16_rn(w);
-        Ohi[(e & 63) * OS + (e >> 6)] = h;
-        Olo[(e & 63) * OS + (e >> 6)] = __float2bfloat16_rn(w - bf_to(h));
-    }
     const bool isq = blockIdx.y == 0;
     const bf16 *const feat = isq ? b.fq : b.fk;
     const float *const dm = isq ? b.dqm : b.dkm;
@@ -910,18 +914,18 @@ __global__ void __launch_bounds__(256) tf_chain_mma_kernel(const bf16 *q, const 
     const long ntiles = (rows + TFC_RB - 1) / TFC_RB;
     for (long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const long r0 = tile * TFC_RB;
-        __syncthreads();  // omega^T written; the previous tile's u read
+        __syncthreads();  // the previous tile's u read
         if (threadIdx.x < TFC_RB) usum[threadIdx.x] = 0.f;
         __syncthreads();
-        // u rows in groups of four columns: item e = r (m / 4) + l4, eight per thread with
+        // u rows in groups of four columns: item e = r (m / 4) + l4, TFC_IT per thread with
         // their loads in flight together; a warp's 32 items share one row (m / 4 is a multiple
         // of 32), so each row sum is one shuffle reduction per warp
         const int lg = lm - 2;  // log2(m / 4)
-        for (int e0 = 0; e0 < TFC_RB << lg; e0 += 8 * 256) {
-            float4 d4[8], s4[8];
-            uint2 f4[8];
+        for (int e0 = 0; e0 < TFC_RB << lg; e0 += TFC_IT * 256) {
+            float4 d4[TFC_IT], s4[TFC_IT];
+            uint2 f4[TFC_IT];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < TFC_IT; ++j) {
                 const int e = e0 + j * 256 + threadIdx.x, r = e >> lg, l = (e & ((1 << lg) - 1)) << 2;
                 const long row = r0 + r;
                 d4[j] = s4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -938,7 +942,7 @@ __global__ void __launch_bounds__(256) tf_chain_mma_kernel(const bf16 *q, const 
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < TFC_IT; ++j) {
                 const int e = e0 + j * 256 + threadIdx.x, r = e >> lg, l = (e & ((1 << lg) - 1)) << 2;
                 const float u0 = (d4[j].x - s4[j].x) * __uint_as_float(f4[j].x << 16);
                 const float u1 = (d4[j].y - s4[j].y) * __uint_as_float(f4[j].x & 0xFFFF0000u);
@@ -969,9 +973,10 @@ __global__ void __launch_bounds__(256) tf_chain_mma_kernel(const bf16 *q, const 
             for (int j = 0; j < 2; ++j) {
                 const int at = ((n0 + j) * 8 + g) * OS + c;
                 const uint32_t *oh = (const uint32_t *)(Ohi + at), *ol = (const uint32_t *)(Olo + at);
-                mma_bf16(acc[j], ah, oh[0], oh[4]);
-                mma_bf16(acc[j], ah, ol[0], ol[4]);
-                mma_bf16(acc[j], al, oh[0], oh[4]);
+                const uint32_t h0 = __ldg(oh), h1 = __ldg(oh + 4), l0 = __ldg(ol), l1 = __ldg(ol + 4);
+                mma_bf16(acc[j], ah, h0, h1);
+                mma_bf16(acc[j], ah, l0, l1);
+                mma_bf16(acc[j], al, h0, h1);
             }
         }
         const long ra = r0 + rt + g, rb = ra + 8;
@@ -1016,8 +1021,8 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
         return LA_ERR_CUDA;
     const long ftiles = (rows + 63) / 64;
     const unsigned fgrid = (unsigned)(ftiles < 2L * sms ? ftiles : 2L * sms);
-    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m);
-    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m);
+    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m, b.omt);
+    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m, nullptr);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     Problem ps[TF_MAXP];
     const int n = tf_passes(p, b, dout, ps);
@@ -1035,11 +1040,12 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     }
     for (; i < n; ++i)
         if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
-    const size_t csm = (size_t)(2 * TF_DK + 2 * TFC_RB) * (p.m + 8) * sizeof(bf16) + TFC_RB * sizeof(float);
-    if (cudaFuncSetAttribute(tf_chain_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm) != cudaSuccess)
+    const size_t csm = (size_t)2 * TFC_RB * (p.m + 8) * sizeof(bf16) + TFC_RB * sizeof(float);
+    if (csm > 48 * 1024 &&
+        cudaFuncSetAttribute(tf_chain_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm) != cudaSuccess)
         return LA_ERR_CUDA;
     const long ctiles = (rows + TFC_RB - 1) / TFC_RB;
-    const unsigned cgrid = (unsigned)(ctiles < 2L * sms ? ctiles : 2L * sms);
+    const unsigned cgrid = (unsigned)(ctiles < 4L * sms ? ctiles : 4L * sms);
     tf_chain_mma_kernel<<<dim3(cgrid, 2), 256, csm, st>>>((const bf16 *)p.q, (const bf16 *)p.k, p.omega, b,
                                                           (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, rows, p.m, p.dv,
                                                           p.normalize);
