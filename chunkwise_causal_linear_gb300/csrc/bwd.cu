@@ -808,11 +808,11 @@ __device__ __forceinline__ uint32_t bf2(float lo, float hi)
 }
 __device__ __forceinline__ float bf_to(bf16 x) { return __bfloat162float(x); }
 
-// Features: persistent blocks of 4 warps, one 16-row tile per warp at a time; W = s omega
+// Features: persistent blocks of 8 warps, one 16-row tile per warp at a time; W = s omega
 // as bf16 hi / lo rows [m][TFM_WS] in shared memory (the padded stride makes the B loads
 // conflict-free); 64 features per accumulator pass.
 constexpr int TFM_WS = 72;
-__global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
+__global__ void __launch_bounds__(256) tf_feat_mma_kernel(const bf16 *x, const float *omega, bf16 *f, long rows,
                                                           int m, bf16 *omt)
 {
     extern __shared__ uint4 tfm_sm[];
@@ -835,7 +835,7 @@ __global__ void __launch_bounds__(128) tf_feat_mma_kernel(const bf16 *x, const f
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const float inv = rsqrtf((float)m);
     const long ntiles = (rows + 15) / 16;
-    for (long tile = (long)blockIdx.x * 4 + warp; tile < ntiles; tile += (long)gridDim.x * 4) {
+    for (long tile = (long)blockIdx.x * 8 + warp; tile < ntiles; tile += (long)gridDim.x * 8) {
         const long ra = tile * 16 + g, rb = ra + 8;
         uint32_t a[4][4];
         float sa = 0.f, sb = 0.f;
@@ -1019,10 +1019,10 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     const size_t fsm = (size_t)2 * p.m * TFM_WS * sizeof(bf16);
     if (cudaFuncSetAttribute(tf_feat_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm) != cudaSuccess)
         return LA_ERR_CUDA;
-    const long ftiles = (rows + 63) / 64;
-    const unsigned fgrid = (unsigned)(ftiles < 2L * sms ? ftiles : 2L * sms);
-    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m, b.omt);
-    tf_feat_mma_kernel<<<fgrid, 128, fsm, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m, nullptr);
+    const long ftiles = (rows + 127) / 128;
+    const unsigned fgrid = (unsigned)(ftiles < 3L * sms ? ftiles : 3L * sms);
+    tf_feat_mma_kernel<<<fgrid, 256, fsm, st>>>((const bf16 *)p.q, p.omega, b.fq, rows, p.m, b.omt);
+    tf_feat_mma_kernel<<<fgrid, 256, fsm, st>>>((const bf16 *)p.k, p.omega, b.fk, rows, p.m, nullptr);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     Problem ps[TF_MAXP];
     const int n = tf_passes(p, b, dout, ps);
