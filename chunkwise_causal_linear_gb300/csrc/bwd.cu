@@ -743,46 +743,59 @@ size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
     return off;
 }
 
-// Normaliser, one warp per row: den = phi(q).Z over all halves, D = bf16(dout / den),
-// g = D . num / den (num summed over the halves), g phi(q) by half
-__global__ void __launch_bounds__(32 * TB_ROWS) tf_prep_kernel(const bf16 *dout, TfBufs b, long rows, int NH,
-                                                             int dv)
+// Normaliser, RW rows per warp (their loads in flight together): den = phi(q).Z over all
+// NH halves, D = bf16(dout / den), g = D . num / den (num summed over the halves), g phi(q)
+// by half.  dv = 64: lanes 0-15 hold one group of four columns of D.
+template <int NH>
+__global__ void __launch_bounds__(32 * TB_ROWS) tf_prep_kernel(const bf16 *dout, TfBufs b, long rows)
 {
-    const long r = (long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    float part = 0.f;
-    for (int h = 0; h < NH; ++h) {
-        float f[4], z[4];
-        ld4(b.fq + (h * rows + r) * 128 + 4 * lane, f);
-        ld4(b.zc + (h * rows + r) * 128 + 4 * lane, z);
-        part += f[0] * z[0] + f[1] * z[1] + f[2] * z[2] + f[3] * z[3];
-    }
-    const float inv = 1.f / warp_sum(part);
-    float gp = 0.f;
-    for (int j = 4 * lane; j < dv; j += 128) {
-        float d[4], nm[4] = {0.f, 0.f, 0.f, 0.f};
-        ld4(dout + r * dv + j, d);
+    constexpr int RW = NH <= 2 ? 2 : 1, DV = 64;
+    const long r0 = ((long)blockIdx.x * TB_ROWS + (threadIdx.x >> 5)) * RW;
+    const int lane = threadIdx.x & 31, c = 4 * lane;
+    const bool dl = c < DV;
+    float f[RW][NH][4], z[RW][NH][4], d[RW][4], nm[RW][NH][4];
+#pragma unroll
+    for (int w = 0; w < RW; ++w) {
+        const long r = r0 + w < rows ? r0 + w : rows - 1;  // past the end: a valid row, not stored
+#pragma unroll
         for (int h = 0; h < NH; ++h) {
-            float x[4];
-            ld4(b.num + (h * rows + r) * dv + j, x);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) nm[e] += x[e];
+            ld4(b.fq + (h * rows + r) * 128 + c, f[w][h]);
+            ld4(b.zc + (h * rows + r) * 128 + c, z[w][h]);
+            if (dl) ld4(b.num + (h * rows + r) * DV + c, nm[w][h]);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d[e] = __bfloat162float(__float2bfloat16_rn(d[e] * inv));
-        st4(b.dn + r * dv + j, d);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) gp += d[e] * (nm[e] * inv);
+        if (dl) ld4(dout + r * DV + c, d[w]);
     }
-    const float g = warp_sum(gp);
-    if (lane == 0) b.g[r] = g;
-    for (int h = 0; h < NH; ++h) {
-        float f[4];
-        ld4(b.fq + (h * rows + r) * 128 + 4 * lane, f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) f[e] *= g;
-        st4(b.gq + (h * rows + r) * 128 + 4 * lane, f);
+    for (int w = 0; w < RW; ++w) {
+        const long r = r0 + w;
+        float part = 0.f;
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+            part += f[w][h][0] * z[w][h][0] + f[w][h][1] * z[w][h][1] + f[w][h][2] * z[w][h][2] +
+                    f[w][h][3] * z[w][h][3];
+        const float inv = 1.f / warp_sum(part);
+        float gp = 0.f;
+        if (dl) {
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s4[e] += nm[w][h][e];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[w][e] = __bfloat162float(__float2bfloat16_rn(d[w][e] * inv));
+            if (r < rows) st4(b.dn + r * DV + c, d[w]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gp += d[w][e] * (s4[e] * inv);
+        }
+        const float g = warp_sum(gp);
+        if (r >= rows) continue;
+        if (lane == 0) b.g[r] = g;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[w][h][e] *= g;
+            st4(b.gq + (h * rows + r) * 128 + c, f[w][h]);
+        }
     }
 }
 
@@ -1034,8 +1047,11 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
     if (p.normalize) {  // Z and num halves, then D, g and g phi(q)
         for (; i < 2 * NH; ++i)
             if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
-        const unsigned tgrid = (unsigned)((rows + TB_ROWS - 1) / TB_ROWS);
-        tf_prep_kernel<<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows, NH, p.dv);
+        const long rw = NH <= 2 ? 2 : 1;  // rows per warp of the prep kernel
+        const unsigned tgrid = (unsigned)((rows + TB_ROWS * rw - 1) / (TB_ROWS * rw));
+        if (NH == 1) tf_prep_kernel<1><<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows);
+        if (NH == 2) tf_prep_kernel<2><<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows);
+        if (NH == 4) tf_prep_kernel<4><<<tgrid, 32 * TB_ROWS, 0, st>>>((const bf16 *)dout, b, rows);
         if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     }
     for (; i < n; ++i)
