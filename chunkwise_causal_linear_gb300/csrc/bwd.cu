@@ -392,10 +392,10 @@ int bwd_t(const Problem &p, int sms, const void *dout, void *dq, void *dk_, void
 typedef __nv_bfloat16 bf16;
 
 struct TcBufs {
-    bf16 *fq, *fk, *dn, *gq;              // operands
-    float *zc, *num, *zsu, *dqm, *dkm;    // pass outputs (fp32 rows, normaliser)
-    float *g;
-    void *ws;                                            // tensor-core pass workspace
+    bf16 *fq, *fk, *dn, *gq;            // operands (fq, fk: elu+1 only; dn, gq: normaliser)
+    float *zc, *num, *zsu, *dqm, *dkm;  // pass outputs (fp32 rows, normaliser)
+    float *g;                           // normaliser: g_t = D_t . out_t
+    void *ws;                           // tensor-core pass workspace (segment totals)
     size_t ws_bytes;
 };
 
@@ -665,10 +665,10 @@ int tc_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
 // ---------------------------------------------------------------- FAVOR+ tensor-core route
 // FAVOR+ features ("Linear Attention / Performerの理論と実装", the FAVOR+ section): phi(x)_l =
 // exp(w_l . x - |x s|^2 / 2) / sqrt(m) with w_l = s omega_l and s = dk^(-1/4).  The m features
-// are cut into NH = m / 128 halves of 128 columns (bf16 rows, one buffer each), and every pass
-// of the identity route runs once per half: the passes whose scores are phi(q).phi(k) (num,
-// dv) add their halves' fp32 outputs, the others (Z, suffix, dphi) give a half of their
-// m-wide output each.  All passes store fp32; the last kernel forms dphi, contracts it with
+// are cut into NH = m / 128 blocks of 128 columns (bf16 rows, one buffer each), and every
+// pass of the identity route runs once per block: the passes whose scores are phi(q).phi(k)
+// (num, dv) add their blocks' fp32 outputs, the others (Z, suffix, dphi) give a block of
+// their m-wide output each.  All passes store fp32; the last kernel forms dphi, contracts it with
 // the features' derivative and sums dv.
 struct TfBufs {
     bf16 *fq, *fk;           // [NH][rows][128]
@@ -680,7 +680,7 @@ struct TfBufs {
     void *ws;
     size_t ws_bytes;
 };
-constexpr int TF_MAXP = 6 * 4;  // passes: six per half, m <= 512
+constexpr int TF_MAXP = 6 * 4;  // passes: six per feature block, m <= 512
 constexpr int TF_DK = 64;        // dk = dv of the route
 
 int tf_passes(const Problem &p, const TfBufs &b, const void *dout, Problem *ps)
@@ -744,8 +744,8 @@ size_t tf_bufs(const Problem &p, int sms, char *base, TfBufs *b)
 }
 
 // Normaliser, RW rows per warp (their loads in flight together): den = phi(q).Z over all
-// NH halves, D = bf16(dout / den), g = D . num / den (num summed over the halves), g phi(q)
-// by half.  dv = 64: lanes 0-15 hold one group of four columns of D.
+// NH feature blocks, D = bf16(dout / den), g = D . num / den (num summed over the blocks),
+// g phi(q) by block.  dv = 64: lanes 0-15 hold one group of four columns of D.
 template <int NH>
 __global__ void __launch_bounds__(32 * TB_ROWS) tf_prep_kernel(const bf16 *dout, TfBufs b, long rows)
 {
@@ -903,7 +903,7 @@ __global__ void __launch_bounds__(256) tf_feat_mma_kernel(const bf16 *x, const f
 // shared memory; then warp w takes rows 16 (w / 4) .. +15 and output columns 16 (w % 4) .. +15:
 // sum_l u_l omega_li with omega^T as bf16 hi / lo rows [64][m + 8], read through the L1 (it is
 // the same 2 x 64 x (m + 8) values for every block), which leaves shared memory to u alone
-// and so lets four blocks share an SM.  The y = 0 blocks also sum the dv halves of their rows.
+// and so lets four blocks share an SM.  The y = 0 blocks also sum the per-block dv parts of their rows.
 constexpr int TFC_RB = 32;
 constexpr int TFC_IT = 4;  // staged items in flight per thread
 __global__ void __launch_bounds__(256, 4) tf_chain_mma_kernel(const bf16 *q, const bf16 *k, const float *omega,
@@ -1044,7 +1044,7 @@ int tf_route(const Problem &p, int sms, const void *dout, void *dq, void *dk, vo
         ps[i].workspace_bytes = b.ws_bytes;
     }
     int i = 0, rc;
-    if (p.normalize) {  // Z and num halves, then D, g and g phi(q)
+    if (p.normalize) {  // Z and num of every feature block, then D, g and g phi(q)
         for (; i < 2 * NH; ++i)
             if ((rc = tc_launch(ps[i], sms)) != LA_OK) return rc;
         const long rw = NH <= 2 ? 2 : 1;  // rows per warp of the prep kernel
