@@ -77,6 +77,7 @@ CASES = [
     # normaliser
     ("favor-m256-d64-L16384", dict(B=1, H=2, L=1500), 64, 1.0),
     ("favor-m256-d64-L16384", dict(B=2, H=1, L=700, m=128, normalize=False), 64, 1.0),
+    ("favor-m256-d64-L16384", dict(B=1, H=2, L=400, m=512), 64, 1.0),
 ]
 
 
